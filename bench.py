@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Cascade decode benchmark: µs/step and effective KV GB/s on GB300.
+
+One step = one pass of the whole hot path over one batch of decode queries:
+the host plan (load-balanced KV chunks over CTAs), its upload, the prefix
+states on the tensor cores, the paged suffix decode, and the contraction +
+merge into the final O / LSE.  Inputs are resident in HBM before timing.
+
+Default workload "gqa_cascade_lb": batch 256, 32 query / 8 KV heads x 128,
+bf16, page size 16, 4 shared prefixes of 8192 tokens (64 requests each),
+suffix lengths clip(rint(lognormal(7, 1)), 16, 16384) (440,093 tokens at
+seed 5), plan over 148 CTAs with alpha = beta = 1.  One step reads 1.94 GB,
+more than the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  `--impl reference` times the float64 CPU
+oracle instead, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["pkc", "reference"], default="pkc")
+    ap.add_argument("--workload", default="gqa_cascade_lb",
+                    choices=["gqa_cascade_lb", "cascade_long_prompt", "tiny_cascade"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def workload_cfg(name):
+    cfg = dict(workloads.WORKLOADS[name])
+    cfg.setdefault("num_ctas", 148)
+    cfg.setdefault("alpha", 1.0)
+    cfg.setdefault("beta", 1.0)
+    return cfg
+
+
+def kv_bytes_per_token(p):
+    return 2 * p["num_kv_heads"] * p["q"].shape[2] * p["q"].dtype.itemsize
+
+
+def kernel_traffic(kernel):
+    """Per-launch DRAM bytes from a committed ncu summary, if its recorded
+    source hash matches the current kernel source; else None."""
+    import hashlib
+    src_file = {"paged_decode": "decode.cu", "prefix_state": "prefix.cu"}.get(kernel)
+    summ = os.path.join(ROOT, "profiles", f"{kernel}_traffic.md")
+    if not src_file or not os.path.exists(summ):
+        return None
+    src = os.path.join(ROOT, "paged_kv_cascade_gb300", "csrc", src_file)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    rec = {}
+    for line in open(summ):
+        if line.startswith("traffic_record:"):
+            for kv in line.split(":", 1)[1].split():
+                k, _, v = kv.partition("=")
+                rec[k] = v
+    if rec.get("source_sha") != sha or rec.get("workload") is None:
+        return None
+    try:
+        return {"bytes_per_launch": float(rec["dram_bytes_per_launch"]),
+                "workload": rec["workload"], "scaled": rec.get("scaled", "no")}
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pkc_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def gpu_smi_id(torch, local):
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[local] if vis else local
+
+
+def cpu_oracle_sample(p, target_s, rows_total_cap=None):
+    """Time the oracle on a bounded sample of (request, head) rows."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from pkc_testing import oracle_args
+    B, Hq, _ = p["q"].shape
+    args = oracle_args(p)
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(123)
+    order = rng.permutation(B * Hq)
+    n = min(32, B * Hq)
+    rows = np.stack([order[:n] // Hq, order[:n] % Hq], 1).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attention_rows(p["q"], rows=rows, **args)
+    t_cal = time.perf_counter() - t0
+    n2 = int(min(B * Hq, max(n, n * target_s / max(t_cal, 1e-6))))
+    rows = np.stack([order[:n2] // Hq, order[:n2] % Hq], 1).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attention_rows(p["q"], rows=rows, **args)
+    t = time.perf_counter() - t0
+    return n2, B * Hq, t, threads
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cfg = workload_cfg(args.workload)
+    p = workloads.workload(args.workload)
+    eff = workloads.effective_bytes(p)
+    per_step_s = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    times, fracs = [], []
+    n_rows = total = threads = 0
+    for i in range(args.warmup + args.steps):
+        n_rows, total, t, threads = cpu_oracle_sample(p, per_step_s)
+        if i >= args.warmup:
+            times.append(t)
+            fracs.append(n_rows / total)
+    # seconds for one full step, extrapolated from each sampled fraction
+    full = [t / f for t, f in zip(times, fracs)]
+    ms = 1e3 * sum(full) / len(full)
+    value = eff / (ms / 1e3) / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "cascade decode effective KV throughput",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": cfg["batch"],
+                   "num_qo_heads": cfg["hq"], "num_kv_heads": cfg["hkv"], "head_dim": cfg["d"],
+                   "page_size": cfg["page_size"], "prefix_lens": cfg["prefix_lens"],
+                   "suffix_tokens": int(p["cache_seqlens"].sum()), "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_rows} of {total} (request, head) rows per step, "
+                                   "extrapolated to the full step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    rank, world, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    if dist is None or rank == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+    import paged_kv_cascade_gb300 as pkc
+
+    cfg = workload_cfg(args.workload)
+    p = workloads.workload(args.workload)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from pkc_testing import to_device
+    d = to_device(p, f"cuda:{local}")
+    B, Hq, D = p["q"].shape
+    num_ctas = cfg["num_ctas"]
+    lens = p["cache_seqlens"]
+    ws = torch.empty(pkc.workspace_size(B, Hq, num_ctas, 64), dtype=torch.uint8, device=d["q"].device)
+    pkc.workspace_init(ws)
+    words = pkc.plan_words(B, num_ctas)
+    pinned = [torch.empty(words, dtype=torch.int32).pin_memory() for _ in range(2)]
+    plan_np = [t.numpy() for t in pinned]
+    o = torch.empty_like(d["q"])
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=d["q"].device)
+
+    host_plan_s = []
+
+    def step(i):
+        t0 = time.perf_counter()
+        buf = pkc.plan(lens, num_ctas, alpha=cfg["alpha"], beta=cfg["beta"], out=plan_np[i & 1])
+        host_plan_s.append(time.perf_counter() - t0)
+        pkc.plan_upload(buf, ws)
+        pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
+                           p["prefix_req_indptr"], d["k_cache"], d["v_cache"], d["block_table"],
+                           d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    status = pkc.device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status after warm-up: {pkc.STATUS_NAMES.get(status, status)}")
+    host_plan_s.clear()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e in ev:  # torch creates the CUDA event on first record
+        for x in e:
+            x.record()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_smi_id(torch, local))
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    start.record()
+    for i in range(K):
+        pkc.set_stage_events(ev[i])
+        step(i)
+    end.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = start.elapsed_time(end)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=d["q"].device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    status = pkc.device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status after timing: {pkc.STATUS_NAMES.get(status, status)}")
+
+    stage_ms = {
+        "prefix_state": statistics.mean(e[0].elapsed_time(e[1]) for e in ev),
+        "paged_decode": statistics.mean(e[1].elapsed_time(e[2]) for e in ev),
+        "contraction": statistics.mean(e[2].elapsed_time(e[3]) for e in ev),
+    }
+    eff = workloads.effective_bytes(p)
+    ms_per_step = elapsed_ms / K
+    value = world * eff * K / (elapsed_ms / 1e3) / 1e9
+
+    hbm_peak, tf_peak, peak_kind = load_peaks()
+    kvb = kv_bytes_per_token(p)
+    suffix_tokens = int(lens.sum())
+    prefix_tokens = int(p["prefix_kv_indptr"][-1])
+    dominant = max(stage_ms, key=stage_ms.get)
+    if dominant == "prefix_state":
+        alg_bytes = prefix_tokens * kvb
+        unit_desc = f"{kvb} B per shared-prefix token x {prefix_tokens} tokens"
+    else:
+        dominant = "paged_decode"
+        alg_bytes = suffix_tokens * kvb
+        unit_desc = f"{kvb} B per suffix token x {suffix_tokens} tokens"
+    achieved = alg_bytes / (stage_ms[dominant] / 1e3) / 1e9
+    tr = kernel_traffic(dominant)
+    # prefix stage on the tensor cores: FLOPs 4*D per (row, prefix token)
+    rows_per_prefix = np.diff(p["prefix_req_indptr"]) * (Hq // p["num_kv_heads"])
+    prefix_flops = float(4 * D * np.sum(rows_per_prefix * np.diff(p["prefix_kv_indptr"])) *
+                         p["num_kv_heads"])
+
+    # ---- e2e through host buffers ----
+    e2e = None
+    if args.e2e_steps > 0:
+        q_h = torch.from_numpy(p["q"].view(np.int16) if p["q"].dtype == np.uint16 else p["q"])
+        q_h = q_h.pin_memory()
+        bt_h = torch.from_numpy(p["block_table"]).pin_memory()
+        sl_h = torch.from_numpy(p["cache_seqlens"]).pin_memory()
+        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        q_d = d["q"].view(torch.int16) if d["q"].dtype == torch.bfloat16 else d["q"]
+        stream = torch.cuda.current_stream()
+
+        def e2e_step(i):
+            lens_host = sl_h.numpy()
+            buf = pkc.plan(lens_host, num_ctas, alpha=cfg["alpha"], beta=cfg["beta"],
+                           out=plan_np[i & 1])
+            q_d.copy_(q_h, non_blocking=True)
+            d["block_table"].copy_(bt_h, non_blocking=True)
+            d["cache_seqlens"].copy_(sl_h, non_blocking=True)
+            pkc.plan_upload(buf, ws)
+            pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
+                               p["prefix_req_indptr"], d["k_cache"], d["v_cache"],
+                               d["block_table"], d["cache_seqlens"], p["sm_scale"], ws,
+                               plan_buf=buf, o=o, lse=lse)
+            o_h.copy_(o, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+            stream.synchronize()
+
+        for i in range(3):
+            e2e_step(i)
+        if dist is not None:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        t_e2e = time.perf_counter() - t0
+        if dist is not None:
+            t = torch.tensor([t_e2e], device=d["q"].device, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4 + words * 4
+        d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * 4
+        e2e = {"value": world * eff * args.e2e_steps / t_e2e / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": 1e3 * t_e2e / args.e2e_steps, "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_rows, total, t, threads = cpu_oracle_sample(p, args.cpu_seconds)
+        full_s = t / (n_rows / total)
+        cpu = {"value": eff / full_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n_rows} of {total} (request, head) rows of one step in {t:.1f} s, "
+                         "extrapolated to the full step"}
+
+    if rank == 0:
+        line = {
+            "metric": "cascade decode effective KV throughput",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": 1e3 * ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg["dtype"], "data": "synthetic",
+            "config": {"workload": args.workload, "batch": B, "num_qo_heads": Hq,
+                       "num_kv_heads": p["num_kv_heads"], "head_dim": D,
+                       "page_size": cfg["page_size"], "prefix_lens": cfg["prefix_lens"],
+                       "suffix_tokens": suffix_tokens, "num_ctas": num_ctas,
+                       "effective_bytes_per_step": eff,
+                       "l2": "inputs larger than L2 (one step reads %.2f GB)" % (eff / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "hbm_fraction": value / world / hbm_peak,
+            "stages_us": {k: 1e3 * v for k, v in stage_ms.items()},
+            "host_plan_us": 1e6 * statistics.mean(host_plan_s) if host_plan_s else None,
+            "roofline": {"kernel": dominant, "bound": "hbm", "achieved": achieved,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "algorithmic_bytes_per_launch": alg_bytes, "per_unit": unit_desc,
+                         "traffic": tr["bytes_per_launch"] if tr else None},
+            "prefix_tensor": {"flops_per_launch": prefix_flops,
+                              "tflops": prefix_flops / (stage_ms["prefix_state"] / 1e3) / 1e12,
+                              "peak_tflops": tf_peak, "peak_source": f"{peak_kind} bf16_tflops"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

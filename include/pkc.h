@@ -1,0 +1,306 @@
+/*
+ * pkc.h -- C ABI of libpkc, shared-prefix ("cascade") batch-decode attention
+ * over a paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * Every attention call returns attention STATES: for a query q and a set I
+ * of cached keys/values,
+ *     s_i  = sm_scale * (q . k_i)
+ *     LSE  = s(I) = log sum_{i in I} exp(s_i)          (natural log)
+ *     O    = v(I) = sum_{i in I} exp(s_i - s(I)) v_i
+ * and states of disjoint sets combine with the merge operator (+)
+ * (FlashInfer tutorial "Attention States and Recursive Attention", the
+ * definitions of s(I), v(I) and the binary / n-ary merge equations; blog
+ * "Cascade Inference: Memory Bandwidth Efficient Shared Prefix Batch
+ * Decoding", section "Recursive Attention").  An empty set has the identity
+ * state O = 0, LSE = -inf.
+ *
+ * Conventions shared by all calls
+ *  - Pointers named *_host are host memory; every other tensor pointer is
+ *    device memory.  The caller owns every buffer; the library allocates no
+ *    device memory.
+ *  - Tensors are dense and row-major (C order) in the layouts stated below.
+ *    Device pointers to 16-bit tensors must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *    device work is enqueued on it asynchronously; no call synchronises the
+ *    host except pkc_device_status.
+ *  - Return value: PKC_OK or a pkc_status code; on error nothing has been
+ *    enqueued and pkc_last_error() describes the problem.  No call aborts
+ *    the process or traps on the device.  Faults found by kernels (a bad
+ *    page id, a plan that does not match cache_seqlens, a wait that timed
+ *    out) are recorded in the workspace status word, read with
+ *    pkc_device_status.
+ *  - head_dim must be 128 for the attention calls (PKC_ERR_UNSUPPORTED
+ *    otherwise).  num_qo_heads must be a multiple of num_kv_heads; query
+ *    head h reads KV head h / (num_qo_heads / num_kv_heads) (GQA head
+ *    groups, FlashInfer MLSys'25 notes, appendix A "head-group fusion").
+ */
+#ifndef PKC_H_
+#define PKC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKC_OK = 0,
+  PKC_ERR_INVALID_ARG = 1, /* bad pointer, size, stride or dtype */
+  PKC_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head_dim) */
+  PKC_ERR_WORKSPACE = 3,   /* workspace too small or misaligned */
+  PKC_ERR_BLOCK_TABLE = 4, /* device: page id < 0 or >= num_pages in use */
+  PKC_ERR_CUDA = 5,        /* a CUDA runtime call failed */
+  PKC_ERR_TIMEOUT = 6,     /* device: a bounded wait ran out */
+  PKC_ERR_PLAN = 7         /* plan buffer invalid or inconsistent */
+} pkc_status;
+
+/* Element types. */
+typedef enum { PKC_F32 = 0, PKC_F16 = 1, PKC_BF16 = 2 } pkc_dtype;
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkc_version(void);
+
+/* Message for the last error returned on the calling thread ("" if none). */
+const char* pkc_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * Merge operator
+ * ---------------------------------------------------------------------- */
+
+/*
+ * Binary merge of two attention states per (token, head):
+ *   v_out = (v_a e^{s_a} + v_b e^{s_b}) / (e^{s_a} + e^{s_b})
+ *   s_out = log(e^{s_a} + e^{s_b})
+ * ("Attention States and Recursive Attention", binary merge equation),
+ * evaluated with the larger s subtracted first; a side with s = -inf is
+ * empty and two empty sides give (0, -inf).
+ *
+ * v_a, v_b, v_out: [n_tokens, n_heads, head_dim] of v_dtype (F32, F16 or
+ * BF16); s_a, s_b, s_out: [n_tokens, n_heads] float32 natural-log LSE.
+ * v_out may be v_a (in place); s_out may be s_a.  head_dim * element size
+ * must be a multiple of 16 bytes and all pointers 16-byte aligned.
+ */
+int pkc_merge_state(const void* v_a, const float* s_a, const void* v_b,
+                    const float* s_b, void* v_out, float* s_out,
+                    int64_t n_tokens, int n_heads, int head_dim, int v_dtype,
+                    void* stream);
+
+/*
+ * n-ary merge over axis 1 ("Attention States and Recursive Attention",
+ * n-ary merge equation): v_out = sum_i softmax_i(s_i) v_i,
+ * s_out = log sum_i exp(s_i).  v: [n_tokens, n_states, n_heads, head_dim]
+ * of v_dtype; s: [n_tokens, n_states, n_heads] float32; v_out
+ * [n_tokens, n_heads, head_dim]; s_out [n_tokens, n_heads].  n_states >= 1.
+ */
+int pkc_merge_states(const void* v, const float* s, void* v_out, float* s_out,
+                     int64_t n_tokens, int n_states, int n_heads, int head_dim,
+                     int v_dtype, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Load-balanced plan (host only)
+ * ---------------------------------------------------------------------- */
+
+/*
+ * The plan is the CPU-side schedule of KV chunks onto CTAs (FlashInfer
+ * MLSys'25 notes, A3 "load-balanced scheduling", steps 1-7, and appendix D
+ * "split-K direct write"):
+ *   1. a work unit is a (request, query tile of tile_q rows), request-major;
+ *   2. L_kv = ceil(sum_i ceil(qo_len_i / tile_q) * kv_len_i / num_ctas), >= 1;
+ *   3. each unit's KV is cut into consecutive chunks of at most L_kv tokens,
+ *      numbered w unit by unit (a unit with kv_len 0 has no chunk);
+ *   4. chunks are sorted longest first (equal lengths keep ascending w);
+ *   5. a min-priority queue of (cost, CTA index) starts at (0, c) for every
+ *      CTA; each chunk goes to the popped CTA, whose cost grows by
+ *      alpha * l_q + beta * l_kv (l_q = the tile's query rows);
+ *   6. a unit with one chunk writes its output directly; chunks of units
+ *      with >= 2 chunks get partial slots numbered in w order, and a
+ *      contraction merges them in ascending KV order.
+ *
+ * The plan is an int32 buffer of pkc_plan_words(...) words; its layout is
+ * given by the PKC_PLAN_* header indices below (all offsets in words from
+ * the start of the buffer):
+ *   cta_indptr[num_ctas + 1]    CSR: CTA c runs work cta_work[...] in pop order
+ *   cta_work[n_work]            work index w
+ *   work_unit, work_kv_begin, work_kv_end, work_partial [n_work] each
+ *                               (work_partial = -1: direct write)
+ *   unit_req, unit_qtile, unit_kv_len, unit_n_chunks, unit_partial_begin
+ *                               [n_units] each (partial_begin -1 if unsplit)
+ *   unit_list[n_split + n_empty] split units then empty units, unit order
+ *   cta_cost[num_ctas]          final cost per CTA, as float64 (2 words each)
+ * The plan depends on lengths only: it is the same for every head.
+ */
+enum {
+  PKC_PLAN_MAGIC = 0, /* == PKC_PLAN_MAGIC_VALUE */
+  PKC_PLAN_TOTAL_WORDS,
+  PKC_PLAN_NUM_CTAS,
+  PKC_PLAN_TILE_Q,
+  PKC_PLAN_N_REQ,
+  PKC_PLAN_KV_CHUNK, /* L_kv */
+  PKC_PLAN_N_UNITS,
+  PKC_PLAN_N_WORK,
+  PKC_PLAN_N_PARTIALS,
+  PKC_PLAN_N_SPLIT,
+  PKC_PLAN_N_EMPTY,
+  PKC_PLAN_OFF_CTA_INDPTR,
+  PKC_PLAN_OFF_CTA_WORK,
+  PKC_PLAN_OFF_WORK_UNIT,
+  PKC_PLAN_OFF_WORK_KV_BEGIN,
+  PKC_PLAN_OFF_WORK_KV_END,
+  PKC_PLAN_OFF_WORK_PARTIAL,
+  PKC_PLAN_OFF_UNIT_REQ,
+  PKC_PLAN_OFF_UNIT_QTILE,
+  PKC_PLAN_OFF_UNIT_KV_LEN,
+  PKC_PLAN_OFF_UNIT_N_CHUNKS,
+  PKC_PLAN_OFF_UNIT_PARTIAL_BEGIN,
+  PKC_PLAN_OFF_UNIT_LIST,
+  PKC_PLAN_OFF_CTA_COST,
+  PKC_PLAN_HEADER_WORDS = 32
+};
+#define PKC_PLAN_MAGIC_VALUE 0x504b4331 /* "PKC1" */
+
+/*
+ * Words needed for a plan of n requests.  qo_len_host [n] may be NULL for
+ * decode (every request has one query row).  The bound uses
+ * n_work <= num_ctas + n_units.
+ */
+int pkc_plan_words(const int32_t* qo_len_host, int n, int tile_q,
+                   int num_ctas, size_t* words);
+
+/*
+ * Compute the plan on the host into plan_host [plan_words].  qo_len_host
+ * may be NULL (all 1); kv_len_host [n] >= 0.  Deterministic: equal inputs
+ * give bit-identical buffers.  Pinned host memory for plan_host makes the
+ * later upload truly asynchronous.
+ */
+int pkc_plan(const int32_t* qo_len_host, const int32_t* kv_len_host, int n,
+             int tile_q, int num_ctas, double alpha, double beta,
+             int32_t* plan_host, size_t plan_words);
+
+/*
+ * Copy a plan into the plan region of a workspace (cudaMemcpyAsync on
+ * `stream`).  plan_host must stay valid until the copy has run.
+ */
+int pkc_plan_upload(const int32_t* plan_host, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Workspace
+ * ---------------------------------------------------------------------- */
+
+/*
+ * Bytes of device workspace for a problem.  The workspace holds, in order
+ * and each 256-byte aligned: a status block (256 B); the plan region
+ * (pkc_plan_words for `batch` decode requests and num_ctas CTAs, 0 when
+ * num_ctas is 0); the suffix states [batch, Hq, D+1] float32; the suffix
+ * partials [2 * num_ctas, Hq, D+1] float32 (appendix D bound
+ * 2 * #CTA * T_q * H * (D+1) with T_q = 1); and prefix_splits copies of
+ * [batch, Hq, D+1] float32 for prefix partial states.
+ *   num_ctas: CTAs of the plan the calls will use (0 if none).
+ *   prefix_splits: most KV splits of the shared prefix (0 if no prefix;
+ *                  the calls use as many as fit, up to the SM count).
+ */
+int pkc_workspace_size(int batch, int num_qo_heads, int head_dim,
+                       int num_ctas, int prefix_splits, size_t* bytes);
+
+/* Zero the status block.  Call once after allocating a workspace. */
+int pkc_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Read (and clear) the device status word: *status = PKC_OK or the first
+ * PKC_ERR_BLOCK_TABLE / PKC_ERR_PLAN / PKC_ERR_TIMEOUT a kernel recorded
+ * since the last read.  Synchronises `stream`.
+ */
+int pkc_device_status(void* workspace, void* stream, int32_t* status);
+
+/* ------------------------------------------------------------------------
+ * Attention states
+ * ---------------------------------------------------------------------- */
+
+/*
+ * Single-query paged decode state (blog "Cascade Inference", step 2 of the
+ * algorithm; Hugging Face "Paged attention", decoding path).  For every
+ * request b and query head h, the state of q[b, h] over the
+ * cache_seqlens[b] cached tokens of b:
+ *   q        [batch, num_qo_heads, 128] of dtype (F16 or BF16)
+ *   k_cache, v_cache [num_pages, page_size, num_kv_heads, 128] of dtype
+ *   block_table [batch, block_table_stride] int32: token t of request b is
+ *            in page block_table[b, t / page_size], slot t % page_size;
+ *            entries past the last used page are never read (-1 allowed)
+ *   cache_seqlens [batch] int32 >= 0
+ *   plan_host: NULL, or a plan of these lengths (tile_q 1) that was
+ *            uploaded into this workspace with pkc_plan_upload.  NULL runs
+ *            one chunk per request.
+ *   o        [batch, num_qo_heads, 128] of dtype; lse [batch, num_qo_heads]
+ *            float32 natural log.  A request with 0 tokens gets (0, -inf).
+ */
+int pkc_paged_decode_state(const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* block_table,
+                           int block_table_stride,
+                           const int32_t* cache_seqlens, int batch,
+                           int num_qo_heads, int num_kv_heads, int head_dim,
+                           int page_size, int64_t num_pages, float sm_scale,
+                           const int32_t* plan_host, void* workspace,
+                           size_t workspace_bytes, void* o, float* lse,
+                           int dtype, void* stream);
+
+/*
+ * Multi-query prefix state (blog "Cascade Inference", step 1 of the
+ * algorithm): every request's queries against the KV of the shared prefix
+ * of its group, on the tensor cores (tcgen05, TMEM accumulators).
+ *   q [batch, num_qo_heads, 128] of dtype
+ *   k_prefix, v_prefix [L, num_kv_heads, 128] of dtype, L = last indptr
+ *   prefix_kv_indptr_host [n_prefix + 1]: prefix j is tokens
+ *            indptr[j] .. indptr[j+1]-1
+ *   prefix_req_indptr_host [n_prefix + 1]: requests indptr[j] ..
+ *            indptr[j+1]-1 share prefix j (cumulative-length convention of
+ *            Hugging Face "Paged attention", varlen path); requests outside
+ *            every group get the empty state
+ *   o [batch, num_qo_heads, 128] float32; lse [batch, num_qo_heads] float32
+ * 1 <= n_prefix <= 256.  Uses the prefix-partials region of the workspace.
+ */
+int pkc_prefix_attention_state(
+    const void* q, const void* k_prefix, const void* v_prefix,
+    const int32_t* prefix_kv_indptr_host,
+    const int32_t* prefix_req_indptr_host, int n_prefix, int batch,
+    int num_qo_heads, int num_kv_heads, int head_dim, float sm_scale,
+    void* workspace, size_t workspace_bytes, float* o, float* lse, int dtype,
+    void* stream);
+
+/*
+ * Cascade decode (blog "Cascade Inference", the three-step algorithm):
+ * prefix state (tensor cores) (+) paged suffix state (load-balanced split
+ * KV) -> final O [batch, num_qo_heads, 128] of dtype and LSE [batch,
+ * num_qo_heads] float32, equal to attention over prefix u suffix.
+ * Arguments as in the two calls above; cache_seqlens counts suffix tokens
+ * only; plan_host as in pkc_paged_decode_state.
+ */
+int pkc_cascade_decode(
+    const void* q, const void* k_prefix, const void* v_prefix,
+    const int32_t* prefix_kv_indptr_host,
+    const int32_t* prefix_req_indptr_host, int n_prefix, const void* k_cache,
+    const void* v_cache, const int32_t* block_table, int block_table_stride,
+    const int32_t* cache_seqlens, int batch, int num_qo_heads,
+    int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+    float sm_scale, const int32_t* plan_host, void* workspace,
+    size_t workspace_bytes, void* o, float* lse, int dtype, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Stage timing
+ * ---------------------------------------------------------------------- */
+
+/*
+ * Optional timing hook for the calling thread.  When events is non-NULL,
+ * the NEXT pkc_cascade_decode call on this thread records events[0] on its
+ * stream before its first kernel, then events[1], events[2], events[3]
+ * after the prefix, suffix-decode and contraction kernels; the hook is then
+ * cleared.  events: n_events >= 4 cudaEvent_t handles created by the
+ * caller; NULL clears the hook.
+ */
+int pkc_set_stage_events(void* const* events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKC_H_ */

@@ -1,0 +1,283 @@
+"""Python binding of libpkc (paged-KV cascade decode attention for GB300).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libpkc.so``.  torch tensors supply device memory and the
+current CUDA stream; their data pointers go straight to the C ABI declared
+in ``include/pkc.h``.  If the library has not been built, every call raises
+-- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpkc.so")
+
+PKC_OK = 0
+STATUS_NAMES = {0: "PKC_OK", 1: "PKC_ERR_INVALID_ARG", 2: "PKC_ERR_UNSUPPORTED",
+                3: "PKC_ERR_WORKSPACE", 4: "PKC_ERR_BLOCK_TABLE", 5: "PKC_ERR_CUDA",
+                6: "PKC_ERR_TIMEOUT", 7: "PKC_ERR_PLAN"}
+F32, F16, BF16 = 0, 1, 2
+
+# Header indices of the plan buffer (include/pkc.h).
+PLAN_FIELDS = ["MAGIC", "TOTAL_WORDS", "NUM_CTAS", "TILE_Q", "N_REQ", "KV_CHUNK",
+               "N_UNITS", "N_WORK", "N_PARTIALS", "N_SPLIT", "N_EMPTY",
+               "OFF_CTA_INDPTR", "OFF_CTA_WORK", "OFF_WORK_UNIT", "OFF_WORK_KV_BEGIN",
+               "OFF_WORK_KV_END", "OFF_WORK_PARTIAL", "OFF_UNIT_REQ", "OFF_UNIT_QTILE",
+               "OFF_UNIT_KV_LEN", "OFF_UNIT_N_CHUNKS", "OFF_UNIT_PARTIAL_BEGIN",
+               "OFF_UNIT_LIST", "OFF_CTA_COST"]
+PLAN = {name: i for i, name in enumerate(PLAN_FIELDS)}
+PLAN_MAGIC = 0x504B4331
+
+# Every symbol the C ABI exports, with (restype, argtypes).
+_c = ctypes
+_P, _I, _I64, _SZ, _F, _D = _c.c_void_p, _c.c_int, _c.c_int64, _c.c_size_t, _c.c_float, _c.c_double
+SIGNATURES = {
+    "pkc_version": (_I, []),
+    "pkc_last_error": (_c.c_char_p, []),
+    "pkc_merge_state": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _P]),
+    "pkc_merge_states": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P]),
+    "pkc_plan_words": (_I, [_P, _I, _I, _I, _c.POINTER(_SZ)]),
+    "pkc_plan": (_I, [_P, _P, _I, _I, _I, _D, _D, _P, _SZ]),
+    "pkc_plan_upload": (_I, [_P, _P, _SZ, _P]),
+    "pkc_workspace_size": (_I, [_I, _I, _I, _I, _I, _c.POINTER(_SZ)]),
+    "pkc_workspace_init": (_I, [_P, _SZ, _P]),
+    "pkc_device_status": (_I, [_P, _P, _c.POINTER(_c.c_int32)]),
+    "pkc_paged_decode_state": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I64, _F,
+                                    _P, _P, _SZ, _P, _P, _I, _P]),
+    "pkc_prefix_attention_state": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ,
+                                        _P, _P, _I, _P]),
+    "pkc_set_stage_events": (_I, [_c.POINTER(_P), _I]),
+    "pkc_cascade_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
+                                _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PkcError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def lib():
+    """The loaded libpkc.so.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libpkc.so not found at {LIB_PATH}; build it first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(rc):
+    if rc != PKC_OK:
+        raise PkcError(rc, lib().pkc_last_error().decode())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[t.dtype]
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _host_i32(a):
+    return np.ascontiguousarray(np.asarray(a), dtype=np.int32)
+
+
+def _hptr(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def version() -> int:
+    return lib().pkc_version()
+
+
+# ---------------------------------------------------------------------------
+# Merge operator
+# ---------------------------------------------------------------------------
+
+def merge_state(v_a, s_a, v_b, s_b, v_out=None, s_out=None, stream=None):
+    """(v_a, s_a) (+) (v_b, s_b); v [T, H, D], s [T, H] float32."""
+    import torch
+    T, H, D = v_a.shape
+    v_out = torch.empty_like(v_a) if v_out is None else v_out
+    s_out = torch.empty_like(s_a) if s_out is None else s_out
+    _check(lib().pkc_merge_state(_ptr(v_a), _ptr(s_a), _ptr(v_b), _ptr(s_b), _ptr(v_out),
+                                 _ptr(s_out), T, H, D, _dtype_code(v_a), _stream(stream)))
+    return v_out, s_out
+
+
+def merge_states(v, s, v_out=None, s_out=None, stream=None):
+    """n-ary (+) over axis 1: v [T, n, H, D], s [T, n, H] -> [T, H, D], [T, H]."""
+    import torch
+    T, n, H, D = v.shape
+    v_out = torch.empty((T, H, D), dtype=v.dtype, device=v.device) if v_out is None else v_out
+    s_out = torch.empty((T, H), dtype=torch.float32, device=v.device) if s_out is None else s_out
+    _check(lib().pkc_merge_states(_ptr(v), _ptr(s), _ptr(v_out), _ptr(s_out), T, n, H, D,
+                                  _dtype_code(v), _stream(stream)))
+    return v_out, s_out
+
+
+# ---------------------------------------------------------------------------
+# Plan and workspace
+# ---------------------------------------------------------------------------
+
+def plan_words(n, num_ctas, tile_q=1, qo_len=None) -> int:
+    q = None if qo_len is None else _host_i32(qo_len)
+    out = ctypes.c_size_t()
+    _check(lib().pkc_plan_words(_hptr(q), n, tile_q, num_ctas, ctypes.byref(out)))
+    return out.value
+
+
+def plan(kv_len, num_ctas, tile_q=1, qo_len=None, alpha=1.0, beta=1.0, out=None):
+    """Host-side load-balanced plan; returns the int32 plan buffer."""
+    kv = _host_i32(kv_len)
+    q = None if qo_len is None else _host_i32(qo_len)
+    words = plan_words(len(kv), num_ctas, tile_q, q)
+    if out is None:
+        out = np.zeros(words, np.int32)
+    assert out.dtype == np.int32 and out.flags.c_contiguous and out.size >= words
+    _check(lib().pkc_plan(_hptr(q), _hptr(kv), len(kv), tile_q, num_ctas, float(alpha),
+                          float(beta), _hptr(out), out.size))
+    return out
+
+
+def plan_upload(plan_buf, workspace, stream=None):
+    _check(lib().pkc_plan_upload(_hptr(plan_buf), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)))
+
+
+def workspace_size(batch, num_qo_heads, num_ctas=0, prefix_splits=0, head_dim=128) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().pkc_workspace_size(batch, num_qo_heads, head_dim, num_ctas, prefix_splits,
+                                    ctypes.byref(out)))
+    return out.value
+
+
+def workspace_init(workspace, stream=None):
+    _check(lib().pkc_workspace_init(_ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def device_status(workspace, stream=None) -> int:
+    st = ctypes.c_int32()
+    _check(lib().pkc_device_status(_ptr(workspace), _stream(stream), ctypes.byref(st)))
+    return st.value
+
+
+# ---------------------------------------------------------------------------
+# Attention states
+# ---------------------------------------------------------------------------
+
+def paged_decode_state(q, k_cache, v_cache, block_table, cache_seqlens, sm_scale, workspace,
+                       plan_buf=None, o=None, lse=None, stream=None):
+    """States of q [B, Hq, 128] over each request's paged cache."""
+    import torch
+    B, Hq, D = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().pkc_paged_decode_state(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(cache_seqlens), B, Hq, Hkv, D, ps, P, float(sm_scale), _hptr(plan_buf),
+        _ptr(workspace), workspace.numel(), _ptr(o), _ptr(lse), _dtype_code(q), _stream(stream)))
+    return o, lse
+
+
+def prefix_attention_state(q, k_prefix, v_prefix, prefix_kv_indptr, prefix_req_indptr, sm_scale,
+                           workspace, o=None, lse=None, stream=None):
+    """States of q [B, Hq, 128] over each request's shared prefix (fp32 O)."""
+    import torch
+    B, Hq, D = q.shape
+    Hkv = k_prefix.shape[1]
+    kv_ptr, req_ptr = _host_i32(prefix_kv_indptr), _host_i32(prefix_req_indptr)
+    o = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().pkc_prefix_attention_state(
+        _ptr(q), _ptr(k_prefix), _ptr(v_prefix), _hptr(kv_ptr), _hptr(req_ptr), len(kv_ptr) - 1,
+        B, Hq, Hkv, D, float(sm_scale), _ptr(workspace), workspace.numel(), _ptr(o), _ptr(lse),
+        _dtype_code(q), _stream(stream)))
+    return o, lse
+
+
+def cascade_decode(q, k_prefix, v_prefix, prefix_kv_indptr, prefix_req_indptr, k_cache, v_cache,
+                   block_table, cache_seqlens, sm_scale, workspace, plan_buf=None, o=None,
+                   lse=None, stream=None):
+    """Final O [B, Hq, 128] and LSE [B, Hq] over shared prefix + paged suffix."""
+    import torch
+    B, Hq, D = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    kv_ptr, req_ptr = _host_i32(prefix_kv_indptr), _host_i32(prefix_req_indptr)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().pkc_cascade_decode(
+        _ptr(q), _ptr(k_prefix), _ptr(v_prefix), _hptr(kv_ptr), _hptr(req_ptr), len(kv_ptr) - 1,
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens),
+        B, Hq, Hkv, D, ps, P, float(sm_scale), _hptr(plan_buf), _ptr(workspace),
+        workspace.numel(), _ptr(o), _ptr(lse), _dtype_code(q), _stream(stream)))
+    return o, lse
+
+
+def set_stage_events(events):
+    """Record 4 torch.cuda.Event objects around the stages of the next
+    cascade_decode call on this thread (None clears)."""
+    if events is None:
+        _check(lib().pkc_set_stage_events(None, 0))
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(lib().pkc_set_stage_events(arr, len(events)))
+
+
+def plan_dict(buf):
+    """Decode a plan buffer into Python lists (for inspection and tests)."""
+    h = {k: int(buf[v]) for k, v in PLAN.items()}
+    nc, nw, nu = h["NUM_CTAS"], h["N_WORK"], h["N_UNITS"]
+
+    def arr(off, n):
+        return buf[h[off]:h[off] + n].tolist()
+    indptr = arr("OFF_CTA_INDPTR", nc + 1)
+    cta_work_flat = arr("OFF_CTA_WORK", nw)
+    return {
+        "header": h,
+        "kv_chunk": h["KV_CHUNK"],
+        "cta_work": [cta_work_flat[indptr[c]:indptr[c + 1]] for c in range(nc)],
+        "work": list(zip(arr("OFF_WORK_UNIT", nw), arr("OFF_WORK_KV_BEGIN", nw),
+                         arr("OFF_WORK_KV_END", nw))),
+        "partial": arr("OFF_WORK_PARTIAL", nw),
+        "unit_req": arr("OFF_UNIT_REQ", nu),
+        "unit_qtile": arr("OFF_UNIT_QTILE", nu),
+        "unit_kv_len": arr("OFF_UNIT_KV_LEN", nu),
+        "unit_n_chunks": arr("OFF_UNIT_N_CHUNKS", nu),
+        "unit_partial_begin": arr("OFF_UNIT_PARTIAL_BEGIN", nu),
+        "split_units": arr("OFF_UNIT_LIST", h["N_SPLIT"]),
+        "empty_units": buf[h["OFF_UNIT_LIST"] + h["N_SPLIT"]:
+                           h["OFF_UNIT_LIST"] + h["N_SPLIT"] + h["N_EMPTY"]].tolist(),
+        "cta_cost": buf[h["OFF_CTA_COST"]:h["OFF_CTA_COST"] + 2 * nc].view(np.float64).tolist(),
+        "n_partials": h["N_PARTIALS"],
+    }

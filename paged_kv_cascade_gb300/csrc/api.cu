@@ -1,0 +1,409 @@
+// C ABI entry points: argument checks, workspace layout, and the launch
+// sequences that compose the kernels into the public calls.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "pkc.h"
+#include "pkc_internal.h"
+
+namespace pkc {
+
+static thread_local char g_err[1024] = "";
+static thread_local cudaEvent_t g_stage_events[4] = {nullptr, nullptr, nullptr, nullptr};
+
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_error(int e, const char* what) {
+  return set_error(PKC_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)e));
+}
+
+int num_sms() {
+  static int cache[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(int batch, int hq, int d, int num_ctas) {
+  WsLayout L;
+  size_t off = PKC_STATUS_BYTES;
+  L.plan = off;
+  off += al256(num_ctas > 0 ? 4 * (size_t)plan_layout(batch, num_ctas).total : 0);
+  const size_t rows = (size_t)batch * hq;
+  L.suffix_o = off;   off += al256(4 * rows * d);
+  L.suffix_lse = off; off += al256(4 * rows);
+  const size_t prow = (size_t)2 * num_ctas * hq;
+  L.part_o = off;     off += al256(4 * prow * d);
+  L.part_lse = off;   off += al256(4 * prow);
+  L.fixed_end = off;
+  L.prefix = off;
+  L.prefix_split = al256(4 * rows * d) + al256(4 * rows);
+  return L;
+}
+
+}  // namespace pkc
+
+using namespace pkc;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_attn_dims(int batch, int hq, int hkv, int head_dim, int dtype) {
+  if (batch < 0) return set_error(PKC_ERR_INVALID_ARG, "batch must be >= 0 (got %d)", batch);
+  if (head_dim != PKC_HEAD_DIM)
+    return set_error(PKC_ERR_UNSUPPORTED, "head_dim %d is not supported (only 128)", head_dim);
+  if (hkv <= 0 || hq <= 0 || hq % hkv != 0)
+    return set_error(PKC_ERR_INVALID_ARG, "num_qo_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                     hq, hkv);
+  const int g = hq / hkv;
+  if (g != 1 && g != 2 && g != 4 && g != 8)
+    return set_error(PKC_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8 (got %d)", g);
+  if (dtype != PKC_F16 && dtype != PKC_BF16)
+    return set_error(PKC_ERR_INVALID_ARG, "dtype must be PKC_F16 or PKC_BF16 (got %d)", dtype);
+  return PKC_OK;
+}
+
+int check_plan(const int32_t* plan, int batch) {
+  if (!plan) return PKC_OK;
+  if (plan[PKC_PLAN_MAGIC] != PKC_PLAN_MAGIC_VALUE) return set_error(PKC_ERR_PLAN, "plan: bad magic word");
+  if (plan[PKC_PLAN_N_REQ] != batch)
+    return set_error(PKC_ERR_PLAN, "plan was made for %d requests, call has batch %d", plan[PKC_PLAN_N_REQ], batch);
+  if (plan[PKC_PLAN_TILE_Q] != 1 || plan[PKC_PLAN_N_UNITS] != batch)
+    return set_error(PKC_ERR_PLAN, "decode needs a plan with tile_q 1 and one query row per request");
+  if (plan[PKC_PLAN_NUM_CTAS] < 1) return set_error(PKC_ERR_PLAN, "plan: num_ctas < 1");
+  return PKC_OK;
+}
+
+int check_ws(const void* ws, size_t bytes, size_t need) {
+  if (!ws) return set_error(PKC_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return set_error(PKC_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (bytes < need) return set_error(PKC_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", bytes, need);
+  return PKC_OK;
+}
+
+struct PrefixSetup {
+  PrefixParams pp;
+  int n_tiles = 0;
+  int64_t tokens = 0;
+};
+
+// Validate the prefix description and choose the KV split count: as many
+// splits as fill the SMs with one wave of row tiles, within the workspace.
+int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_indptr, int n_prefix, int batch,
+                 int hq, int hkv, float sm_scale, uint8_t* ws, size_t ws_bytes, const WsLayout& L,
+                 int32_t* status) {
+  if (n_prefix < 1 || n_prefix > PKC_MAX_PREFIX)
+    return set_error(PKC_ERR_INVALID_ARG, "n_prefix must be in [1, %d] (got %d)", PKC_MAX_PREFIX, n_prefix);
+  if (!kv_indptr || !req_indptr) return set_error(PKC_ERR_INVALID_ARG, "prefix indptr arrays are NULL");
+  if (kv_indptr[0] < 0 || req_indptr[0] < 0)
+    return set_error(PKC_ERR_INVALID_ARG, "prefix indptr arrays must start >= 0");
+  for (int j = 0; j < n_prefix; ++j)
+    if (kv_indptr[j + 1] < kv_indptr[j] || req_indptr[j + 1] < req_indptr[j])
+      return set_error(PKC_ERR_INVALID_ARG, "prefix indptr arrays must be non-decreasing (at %d)", j);
+  if (req_indptr[n_prefix] > batch)
+    return set_error(PKC_ERR_INVALID_ARG, "prefix_req_indptr ends at %d > batch %d", req_indptr[n_prefix], batch);
+  PrefixParams& p = S.pp;
+  std::memset(&p, 0, sizeof(p));
+  p.batch = batch;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.g = hq / hkv;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.n_prefix = n_prefix;
+  int tiles = 0;
+  int max_len = 0;
+  for (int j = 0; j <= n_prefix; ++j) {
+    p.kv_indptr[j] = kv_indptr[j];
+    p.req_indptr[j] = req_indptr[j];
+    p.tile_indptr[j] = tiles;
+    if (j < n_prefix) {
+      const int rows = (req_indptr[j + 1] - req_indptr[j]) * p.g;
+      tiles += (rows + 127) / 128;
+      max_len = std::max(max_len, kv_indptr[j + 1] - kv_indptr[j]);
+    }
+  }
+  S.n_tiles = tiles;
+  S.tokens = kv_indptr[n_prefix];
+  const size_t avail = ws_bytes > L.fixed_end ? (ws_bytes - L.fixed_end) / L.prefix_split : 0;
+  if (avail < 1) return set_error(PKC_ERR_WORKSPACE, "workspace has no room for prefix partial states");
+  const int per_split = std::max(1, tiles * hkv);
+  int splits = std::max(1, num_sms() / per_split);
+  const int max_useful = std::max(1, (max_len + 127) / 128);
+  splits = std::min({splits, max_useful, (int)std::min<size_t>(avail, PKC_MAX_PREFIX_SPLITS)});
+  p.splits = splits;
+  for (int j = 0; j < n_prefix; ++j) {
+    const int len = kv_indptr[j + 1] - kv_indptr[j];
+    const int c = (len + splits - 1) / splits;
+    p.chunk[j] = std::max(128, (c + 127) / 128 * 128);
+  }
+  p.out_o = reinterpret_cast<float*>(ws + L.prefix);
+  p.out_lse = reinterpret_cast<float*>(ws + L.prefix + al256(4 * (size_t)batch * hq * PKC_HEAD_DIM));
+  p.split_stride_o = (int64_t)(L.prefix_split / 4);
+  p.split_stride_lse = (int64_t)(L.prefix_split / 4);
+  p.status = status;
+  return PKC_OK;
+}
+
+void fill_contract_prefix(ContractParams& c, const PrefixSetup& S) {
+  c.prefix_o = S.pp.out_o;
+  c.prefix_lse = S.pp.out_lse;
+  c.prefix_stride_o = S.pp.split_stride_o;
+  c.prefix_stride_lse = S.pp.split_stride_lse;
+  c.prefix_splits = S.pp.splits;
+  c.n_prefix = S.pp.n_prefix;
+  std::memcpy(c.req_indptr, S.pp.req_indptr, sizeof(c.req_indptr));
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkc_version(void) { return PKC_VERSION; }
+
+int pkc_set_stage_events(void* const* events, int n_events) {
+  if (events && n_events < 4) return set_error(PKC_ERR_INVALID_ARG, "set_stage_events: need 4 events");
+  for (int i = 0; i < 4; ++i) g_stage_events[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  return PKC_OK;
+}
+
+const char* pkc_last_error(void) { return g_err; }
+
+int pkc_merge_state(const void* v_a, const float* s_a, const void* v_b, const float* s_b, void* v_out,
+                    float* s_out, int64_t n_tokens, int n_heads, int head_dim, int v_dtype, void* stream) {
+  if (n_tokens < 0 || n_heads < 0 || head_dim <= 0)
+    return set_error(PKC_ERR_INVALID_ARG, "merge_state: negative size");
+  if (v_dtype != PKC_F32 && v_dtype != PKC_F16 && v_dtype != PKC_BF16)
+    return set_error(PKC_ERR_INVALID_ARG, "merge_state: bad dtype %d", v_dtype);
+  const int esz = v_dtype == PKC_F32 ? 4 : 2;
+  if ((head_dim * esz) % 16 != 0)
+    return set_error(PKC_ERR_UNSUPPORTED, "merge_state: head_dim * element size must be a multiple of 16 bytes");
+  const int cpr = head_dim * esz / 16;
+  if (cpr > 32 ? cpr % 32 != 0 : 32 % cpr != 0)
+    return set_error(PKC_ERR_UNSUPPORTED, "merge_state: head_dim*esize/16 must divide 32 or be a multiple of 32");
+  if (n_tokens * n_heads == 0) return PKC_OK;
+  if (!v_a || !s_a || !v_b || !s_b || !v_out || !s_out)
+    return set_error(PKC_ERR_INVALID_ARG, "merge_state: NULL pointer");
+  if (!aligned16(v_a) || !aligned16(v_b) || !aligned16(v_out))
+    return set_error(PKC_ERR_INVALID_ARG, "merge_state: v pointers must be 16-byte aligned");
+  const int e = launch_merge_state(v_a, s_a, v_b, s_b, v_out, s_out, n_tokens * n_heads, head_dim, v_dtype, stream);
+  return e ? cuda_error(e, "merge_state launch") : PKC_OK;
+}
+
+int pkc_merge_states(const void* v, const float* s, void* v_out, float* s_out, int64_t n_tokens, int n_states,
+                     int n_heads, int head_dim, int v_dtype, void* stream) {
+  if (n_tokens < 0 || n_heads < 0 || head_dim <= 0 || n_states < 1)
+    return set_error(PKC_ERR_INVALID_ARG, "merge_states: bad size (n_states >= 1 required)");
+  if (v_dtype != PKC_F32 && v_dtype != PKC_F16 && v_dtype != PKC_BF16)
+    return set_error(PKC_ERR_INVALID_ARG, "merge_states: bad dtype %d", v_dtype);
+  const int esz = v_dtype == PKC_F32 ? 4 : 2;
+  if ((head_dim * esz) % 16 != 0)
+    return set_error(PKC_ERR_UNSUPPORTED, "merge_states: head_dim * element size must be a multiple of 16 bytes");
+  const int cpr = head_dim * esz / 16;
+  if (cpr > 32 ? cpr % 32 != 0 : 32 % cpr != 0)
+    return set_error(PKC_ERR_UNSUPPORTED, "merge_states: head_dim*esize/16 must divide 32 or be a multiple of 32");
+  if (n_tokens * n_heads == 0) return PKC_OK;
+  if (!v || !s || !v_out || !s_out) return set_error(PKC_ERR_INVALID_ARG, "merge_states: NULL pointer");
+  if (!aligned16(v) || !aligned16(v_out))
+    return set_error(PKC_ERR_INVALID_ARG, "merge_states: v pointers must be 16-byte aligned");
+  const int e = launch_merge_states(v, s, v_out, s_out, n_tokens, n_states, n_heads, head_dim, v_dtype, stream);
+  return e ? cuda_error(e, "merge_states launch") : PKC_OK;
+}
+
+int pkc_workspace_size(int batch, int num_qo_heads, int head_dim, int num_ctas, int prefix_splits, size_t* bytes) {
+  if (!bytes || batch < 0 || num_qo_heads <= 0 || head_dim <= 0 || num_ctas < 0 || prefix_splits < 0)
+    return set_error(PKC_ERR_INVALID_ARG, "workspace_size: bad argument");
+  const WsLayout L = ws_layout(batch, num_qo_heads, head_dim, num_ctas);
+  *bytes = L.fixed_end + (size_t)prefix_splits * L.prefix_split;
+  return PKC_OK;
+}
+
+int pkc_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (int rc = check_ws(workspace, workspace_bytes, PKC_STATUS_BYTES)) return rc;
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, PKC_STATUS_BYTES, (cudaStream_t)stream);
+  return e ? cuda_error(e, "workspace_init") : PKC_OK;
+}
+
+int pkc_device_status(void* workspace, void* stream, int32_t* status) {
+  if (!workspace || !status) return set_error(PKC_ERR_INVALID_ARG, "device_status: NULL pointer");
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (!e) e = cudaStreamSynchronize(st);
+  if (!e) e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), st);
+  if (e) return cuda_error(e, "device_status");
+  *status = v;
+  return PKC_OK;
+}
+
+int pkc_plan_upload(const int32_t* plan_host, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan_host) return set_error(PKC_ERR_INVALID_ARG, "plan_upload: plan is NULL");
+  if (plan_host[PKC_PLAN_MAGIC] != PKC_PLAN_MAGIC_VALUE) return set_error(PKC_ERR_PLAN, "plan_upload: bad magic");
+  const size_t words = (size_t)plan_host[PKC_PLAN_TOTAL_WORDS];
+  if (int rc = check_ws(workspace, workspace_bytes, PKC_STATUS_BYTES + 4 * words)) return rc;
+  const cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t*>(workspace) + PKC_STATUS_BYTES, plan_host, 4 * words,
+                                        cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  return e ? cuda_error(e, "plan_upload") : PKC_OK;
+}
+
+int pkc_paged_decode_state(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                           int block_table_stride, const int32_t* cache_seqlens, int batch, int num_qo_heads,
+                           int num_kv_heads, int head_dim, int page_size, int64_t num_pages, float sm_scale,
+                           const int32_t* plan_host, void* workspace, size_t workspace_bytes, void* o, float* lse,
+                           int dtype, void* stream) {
+  if (int rc = check_attn_dims(batch, num_qo_heads, num_kv_heads, head_dim, dtype)) return rc;
+  if (int rc = check_plan(plan_host, batch)) return rc;
+  if (page_size < 1 || block_table_stride < 1 || num_pages < 0)
+    return set_error(PKC_ERR_INVALID_ARG, "page_size and block_table_stride must be >= 1, num_pages >= 0");
+  const int num_ctas = plan_host ? plan_host[PKC_PLAN_NUM_CTAS] : 0;
+  const WsLayout L = ws_layout(batch, num_qo_heads, head_dim, num_ctas);
+  if (int rc = check_ws(workspace, workspace_bytes, L.fixed_end)) return rc;
+  if (batch == 0) return PKC_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !cache_seqlens || !o || !lse)
+    return set_error(PKC_ERR_INVALID_ARG, "paged_decode_state: NULL pointer");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+    return set_error(PKC_ERR_INVALID_ARG, "paged_decode_state: q, caches and o must be 16-byte aligned");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  DecodeParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.q = q; dp.k_cache = k_cache; dp.v_cache = v_cache;
+  dp.block_table = block_table; dp.cache_seqlens = cache_seqlens;
+  dp.bt_stride = block_table_stride; dp.num_pages = num_pages;
+  dp.batch = batch; dp.hq = num_qo_heads; dp.hkv = num_kv_heads; dp.page_size = page_size;
+  dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  dp.plan = plan_host ? reinterpret_cast<const int32_t*>(ws + L.plan) : nullptr;
+  dp.o_direct = o; dp.lse_direct = lse; dp.direct_f32 = 0;
+  dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  dp.status = status;
+  int e = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, stream);
+  if (e) return cuda_error(e, "paged decode launch");
+  if (plan_host) {
+    ContractParams cp;
+    std::memset(&cp, 0, sizeof(cp));
+    cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractPlanUnits; cp.plan = dp.plan;
+    cp.part_o = dp.part_o; cp.part_lse = dp.part_lse;
+    cp.o = o; cp.lse = lse; cp.out_dtype = dtype; cp.status = status;
+    e = launch_contract(cp, batch, stream);
+    if (e) return cuda_error(e, "contraction launch");
+  }
+  return PKC_OK;
+}
+
+int pkc_prefix_attention_state(const void* q, const void* k_prefix, const void* v_prefix,
+                               const int32_t* prefix_kv_indptr_host, const int32_t* prefix_req_indptr_host,
+                               int n_prefix, int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                               float sm_scale, void* workspace, size_t workspace_bytes, float* o, float* lse,
+                               int dtype, void* stream) {
+  if (int rc = check_attn_dims(batch, num_qo_heads, num_kv_heads, head_dim, dtype)) return rc;
+  const WsLayout L = ws_layout(batch, num_qo_heads, head_dim, 0);
+  if (int rc = check_ws(workspace, workspace_bytes, L.fixed_end)) return rc;
+  if (batch == 0) return PKC_OK;
+  if (!q || !k_prefix || !v_prefix || !o || !lse) return set_error(PKC_ERR_INVALID_ARG, "prefix_attention_state: NULL pointer");
+  if (!aligned16(q) || !aligned16(k_prefix) || !aligned16(v_prefix) || !aligned16(o))
+    return set_error(PKC_ERR_INVALID_ARG, "prefix_attention_state: tensors must be 16-byte aligned");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  PrefixSetup S;
+  if (int rc = setup_prefix(S, prefix_kv_indptr_host, prefix_req_indptr_host, n_prefix, batch, num_qo_heads,
+                            num_kv_heads, sm_scale, ws, workspace_bytes, L, status))
+    return rc;
+  int e = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, S.n_tiles, dtype, stream);
+  if (e == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
+  if (e) return cuda_error(e, "prefix launch");
+  ContractParams cp;
+  std::memset(&cp, 0, sizeof(cp));
+  cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractAllRequests;
+  fill_contract_prefix(cp, S);
+  cp.o = o; cp.lse = lse; cp.out_dtype = PKC_F32; cp.status = status;
+  e = launch_contract(cp, batch, stream);
+  return e ? cuda_error(e, "contraction launch") : PKC_OK;
+}
+
+int pkc_cascade_decode(const void* q, const void* k_prefix, const void* v_prefix,
+                       const int32_t* prefix_kv_indptr_host, const int32_t* prefix_req_indptr_host, int n_prefix,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table, int block_table_stride,
+                       const int32_t* cache_seqlens, int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                       int page_size, int64_t num_pages, float sm_scale, const int32_t* plan_host, void* workspace,
+                       size_t workspace_bytes, void* o, float* lse, int dtype, void* stream) {
+  if (int rc = check_attn_dims(batch, num_qo_heads, num_kv_heads, head_dim, dtype)) return rc;
+  if (int rc = check_plan(plan_host, batch)) return rc;
+  if (page_size < 1 || block_table_stride < 1 || num_pages < 0)
+    return set_error(PKC_ERR_INVALID_ARG, "page_size and block_table_stride must be >= 1, num_pages >= 0");
+  const int num_ctas = plan_host ? plan_host[PKC_PLAN_NUM_CTAS] : 0;
+  const WsLayout L = ws_layout(batch, num_qo_heads, head_dim, num_ctas);
+  if (int rc = check_ws(workspace, workspace_bytes, L.fixed_end)) return rc;
+  if (batch == 0) return PKC_OK;
+  if (!q || !k_prefix || !v_prefix || !k_cache || !v_cache || !block_table || !cache_seqlens || !o || !lse)
+    return set_error(PKC_ERR_INVALID_ARG, "cascade_decode: NULL pointer");
+  if (!aligned16(q) || !aligned16(k_prefix) || !aligned16(v_prefix) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(o))
+    return set_error(PKC_ERR_INVALID_ARG, "cascade_decode: tensors must be 16-byte aligned");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  PrefixSetup S;
+  if (int rc = setup_prefix(S, prefix_kv_indptr_host, prefix_req_indptr_host, n_prefix, batch, num_qo_heads,
+                            num_kv_heads, sm_scale, ws, workspace_bytes, L, status))
+    return rc;
+  cudaEvent_t ev[4];
+  for (int i = 0; i < 4; ++i) ev[i] = g_stage_events[i];
+  g_stage_events[0] = g_stage_events[1] = g_stage_events[2] = g_stage_events[3] = nullptr;
+  auto mark = [&](int i) {
+    if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
+  };
+  mark(0);
+  // 1. shared prefix: multi-query states on the tensor cores
+  int e = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, S.n_tiles, dtype, stream);
+  if (e == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
+  if (e) return cuda_error(e, "prefix launch");
+  mark(1);
+  // 2. unique suffixes: paged decode states (unsplit -> suffix states)
+  DecodeParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.q = q; dp.k_cache = k_cache; dp.v_cache = v_cache;
+  dp.block_table = block_table; dp.cache_seqlens = cache_seqlens;
+  dp.bt_stride = block_table_stride; dp.num_pages = num_pages;
+  dp.batch = batch; dp.hq = num_qo_heads; dp.hkv = num_kv_heads; dp.page_size = page_size;
+  dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  dp.plan = plan_host ? reinterpret_cast<const int32_t*>(ws + L.plan) : nullptr;
+  dp.o_direct = ws + L.suffix_o; dp.lse_direct = reinterpret_cast<float*>(ws + L.suffix_lse); dp.direct_f32 = 1;
+  dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  dp.status = status;
+  e = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, stream);
+  if (e) return cuda_error(e, "paged decode launch");
+  mark(2);
+  // 3. contraction + merge: prefix splits (+) suffix chunks -> final O, LSE
+  ContractParams cp;
+  std::memset(&cp, 0, sizeof(cp));
+  cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractAllRequests; cp.plan = dp.plan;
+  cp.suffix_o = reinterpret_cast<const float*>(dp.o_direct); cp.suffix_lse = dp.lse_direct;
+  cp.part_o = dp.part_o; cp.part_lse = dp.part_lse;
+  fill_contract_prefix(cp, S);
+  cp.o = o; cp.lse = lse; cp.out_dtype = dtype; cp.status = status;
+  e = launch_contract(cp, batch, stream);
+  if (e) return cuda_error(e, "contraction launch");
+  mark(3);
+  return PKC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,199 @@
+// Merge operator kernels: binary and n-ary (+) over attention states
+// ("Attention States and Recursive Attention", binary and n-ary merge
+// equations).  Pure streaming work: each (token, head) row is read once and
+// written once with 16-byte vector accesses; a row's LSE values are read by
+// every lane that handles the row, then written by one lane.
+#include <cuda_runtime.h>
+
+#include "pkc_device.cuh"
+#include "pkc_internal.h"
+
+namespace pkc {
+namespace {
+
+template <typename T> struct Vec;  // 16 bytes of T <-> 4 or 8 floats
+template <> struct Vec<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void load(const void* p, float* f) {
+    uint4 u = ldg_stream(p);
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  }
+  static __device__ __forceinline__ void store(void* p, const float* f) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  }
+};
+template <typename H> struct Vec16 {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void load(const void* p, float* f) {
+    uint4 u = ldg_stream(p);
+    float2 a = Elem<H>::to_f2(u.x), b = Elem<H>::to_f2(u.y);
+    float2 c = Elem<H>::to_f2(u.z), d = Elem<H>::to_f2(u.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+  static __device__ __forceinline__ void store(void* p, const float* f) {
+    uint4 u;
+    u.x = Elem<H>::from_f2(f[0], f[1]); u.y = Elem<H>::from_f2(f[2], f[3]);
+    u.z = Elem<H>::from_f2(f[4], f[5]); u.w = Elem<H>::from_f2(f[6], f[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+  }
+};
+template <> struct Vec<__half> : Vec16<__half> {};
+template <> struct Vec<__nv_bfloat16> : Vec16<__nv_bfloat16> {};
+
+// Rows are (token, head) pairs.  A warp covers `32 / cpr` rows at a time
+// when a row has cpr <= 32 16-byte chunks, else one row in 32-chunk steps.
+template <typename T>
+__global__ void __launch_bounds__(256) merge2_kernel(const T* __restrict__ va, const float* sa,
+                                                     const T* __restrict__ vb, const float* sb,
+                                                     T* vo, float* so, int64_t rows, int cpr) {
+  using V = Vec<T>;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (gridDim.x * (int64_t)blockDim.x) >> 5;
+  const int rpw = cpr >= 32 ? 1 : 32 / cpr;          // rows per warp step
+  const int sub_row = cpr >= 32 ? 0 : lane / cpr;
+  const int chunk0 = cpr >= 32 ? lane : lane % cpr;
+  const int cstep = cpr >= 32 ? 32 : cpr;
+  for (int64_t r0 = warp * rpw; r0 < rows; r0 += nwarps * rpw) {
+    const int64_t row = r0 + sub_row;
+    const bool active = row < rows;
+    float a = active ? sa[row] : 0.f, b = active ? sb[row] : 0.f;
+    const float m = fmaxf(a, b);
+    float wa = 0.f, wb = 0.f, s = neg_inf();
+    if (m != neg_inf()) {
+      wa = ex2((a - m) * kLog2e);
+      wb = ex2((b - m) * kLog2e);
+      const float den = wa + wb;
+      s = m + lg2(den) * kLn2;
+      const float inv = 1.f / den;
+      wa *= inv;
+      wb *= inv;
+    }
+    if (active) {
+      for (int c = chunk0; c < cpr; c += cstep) {
+        const int64_t off = (row * cpr + c) * V::N;
+        float x[V::N], y[V::N];
+        V::load(va + off, x);
+        V::load(vb + off, y);
+#pragma unroll
+        for (int i = 0; i < V::N; ++i) x[i] = x[i] * wa + y[i] * wb;
+        V::store(vo + off, x);
+      }
+    }
+    __syncwarp();
+    if (active && chunk0 == 0) so[row] = s;
+  }
+}
+
+// n-ary: v [T, n, H, D], s [T, n, H] -> [T, H, D], [T, H].
+template <typename T>
+__global__ void __launch_bounds__(256) mergen_kernel(const T* __restrict__ v, const float* s,
+                                                     T* vo, float* so, int64_t n_tokens,
+                                                     int n_states, int n_heads, int cpr) {
+  using V = Vec<T>;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (gridDim.x * (int64_t)blockDim.x) >> 5;
+  const int64_t rows = n_tokens * n_heads;
+  const int rpw = cpr >= 32 ? 1 : 32 / cpr;
+  const int sub_row = cpr >= 32 ? 0 : lane / cpr;
+  const int chunk0 = cpr >= 32 ? lane : lane % cpr;
+  const int cstep = cpr >= 32 ? 32 : cpr;
+  for (int64_t r0 = warp * rpw; r0 < rows; r0 += nwarps * rpw) {
+    const int64_t row = r0 + sub_row;
+    const bool active = row < rows;
+    const int64_t t = active ? row / n_heads : 0;
+    const int h = active ? (int)(row % n_heads) : 0;
+    const float* srow = s + t * n_states * n_heads + h;
+    float m = neg_inf();
+    if (active)
+      for (int i = 0; i < n_states; ++i) m = fmaxf(m, srow[(int64_t)i * n_heads]);
+    float den = 0.f;
+    if (active && m != neg_inf())
+      for (int i = 0; i < n_states; ++i) den += ex2((srow[(int64_t)i * n_heads] - m) * kLog2e);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    if (active) {
+      for (int c = chunk0; c < cpr; c += cstep) {
+        float acc[V::N];
+#pragma unroll
+        for (int k = 0; k < V::N; ++k) acc[k] = 0.f;
+        if (m != neg_inf()) {
+          int i = 0;
+          for (; i + 4 <= n_states; i += 4) {
+            float x[4][V::N], w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int64_t off = (((t * n_states + i + u) * n_heads + h) * cpr + c) * V::N;
+              V::load(v + off, x[u]);
+              w[u] = ex2((srow[(int64_t)(i + u) * n_heads] - m) * kLog2e) * inv;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int k = 0; k < V::N; ++k) acc[k] += w[u] * x[u][k];
+          }
+          for (; i < n_states; ++i) {
+            float x[V::N];
+            const int64_t off = (((t * n_states + i) * n_heads + h) * cpr + c) * V::N;
+            V::load(v + off, x);
+            const float w = ex2((srow[(int64_t)i * n_heads] - m) * kLog2e) * inv;
+#pragma unroll
+            for (int k = 0; k < V::N; ++k) acc[k] += w * x[k];
+          }
+        }
+        V::store(vo + (row * cpr + c) * V::N, acc);
+      }
+    }
+    __syncwarp();
+    if (active && chunk0 == 0) so[row] = (m == neg_inf()) ? neg_inf() : m + lg2(den) * kLn2;
+  }
+}
+
+int grid_for(int64_t warps_needed) {
+  const int64_t per_block = 8;  // 256 threads
+  int64_t blocks = (warps_needed + per_block - 1) / per_block;
+  const int64_t cap = (int64_t)num_sms() * 8;  // 8 x 256-thread blocks per SM resident
+  if (blocks > cap) blocks = cap;
+  return (int)(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+int launch_merge_state(const void* va, const float* sa, const void* vb, const float* sb, void* vo,
+                       float* so, int64_t rows, int head_dim, int dtype, void* stream) {
+  const int esz = dtype == PKC_F32 ? 4 : 2;
+  const int cpr = head_dim * esz / 16;
+  const int rpw = cpr >= 32 ? 1 : 32 / cpr;
+  const int grid = grid_for((rows + rpw - 1) / rpw);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (dtype == PKC_F32)
+    merge2_kernel<float><<<grid, 256, 0, st>>>((const float*)va, sa, (const float*)vb, sb, (float*)vo, so, rows, cpr);
+  else if (dtype == PKC_F16)
+    merge2_kernel<__half><<<grid, 256, 0, st>>>((const __half*)va, sa, (const __half*)vb, sb, (__half*)vo, so, rows, cpr);
+  else
+    merge2_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)va, sa, (const __nv_bfloat16*)vb, sb,
+                                                       (__nv_bfloat16*)vo, so, rows, cpr);
+  return (int)cudaGetLastError();
+}
+
+int launch_merge_states(const void* v, const float* s, void* vo, float* so, int64_t n_tokens,
+                        int n_states, int n_heads, int head_dim, int dtype, void* stream) {
+  const int esz = dtype == PKC_F32 ? 4 : 2;
+  const int cpr = head_dim * esz / 16;
+  const int rpw = cpr >= 32 ? 1 : 32 / cpr;
+  const int64_t rows = n_tokens * n_heads;
+  const int grid = grid_for((rows + rpw - 1) / rpw);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (dtype == PKC_F32)
+    mergen_kernel<float><<<grid, 256, 0, st>>>((const float*)v, s, (float*)vo, so, n_tokens, n_states, n_heads, cpr);
+  else if (dtype == PKC_F16)
+    mergen_kernel<__half><<<grid, 256, 0, st>>>((const __half*)v, s, (__half*)vo, so, n_tokens, n_states, n_heads, cpr);
+  else
+    mergen_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)v, s, (__nv_bfloat16*)vo, so, n_tokens,
+                                                       n_states, n_heads, cpr);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace pkc

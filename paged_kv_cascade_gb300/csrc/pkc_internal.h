@@ -1,0 +1,120 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include "pkc.h"
+
+#define PKC_VERSION 100  // 0.1.0
+#define PKC_HEAD_DIM 128
+#define PKC_MAX_PREFIX 256
+#define PKC_MAX_PREFIX_SPLITS 64
+#define PKC_STATUS_BYTES 256
+
+namespace pkc {
+
+// Record an error message for pkc_last_error(); returns `code`.
+int set_error(int code, const char* fmt, ...);
+int cuda_error(int cuda_code, const char* what);
+
+// Word offsets of the plan arrays (see pkc.h, "Load-balanced plan").
+struct PlanLayout {
+  int64_t cta_indptr, cta_work, work_unit, work_kv_begin, work_kv_end,
+      work_partial, unit_req, unit_qtile, unit_kv_len, unit_n_chunks,
+      unit_partial_begin, unit_list, cta_cost, total;
+};
+PlanLayout plan_layout(int64_t n_units, int num_ctas);
+
+// Byte offsets of the workspace regions (see pkc.h, pkc_workspace_size).
+struct WsLayout {
+  size_t plan;             // plan region
+  size_t suffix_o, suffix_lse;
+  size_t part_o, part_lse;
+  size_t prefix;           // first prefix split
+  size_t prefix_split;     // bytes per prefix split ([B, Hq, D] + [B, Hq])
+  size_t fixed_end;        // bytes before the prefix splits
+};
+WsLayout ws_layout(int batch, int hq, int d, int num_ctas);
+
+// ---------------------------------------------------------------------------
+// Kernel parameter blocks (plain data, passed by value to the kernels)
+// ---------------------------------------------------------------------------
+
+struct DecodeParams {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* cache_seqlens;
+  int64_t bt_stride;
+  int64_t num_pages;
+  int batch, hq, hkv, page_size;
+  float scale_log2;       // sm_scale * log2(e)
+  const int32_t* plan;    // device copy of the plan, or nullptr
+  void* o_direct;         // unsplit outputs: [B, Hq, D] (dtype or f32)
+  float* lse_direct;      // [B, Hq]
+  int direct_f32;         // 1: o_direct is float32 (suffix states)
+  float* part_o;          // partial slots [slot, Hq, D]
+  float* part_lse;        // [slot, Hq]
+  int32_t* status;
+};
+
+enum ContractMode {
+  kContractPlanUnits = 0,  // rows = the plan's split + empty units
+  kContractAllRequests = 1 // rows = every request
+};
+
+struct ContractParams {
+  int batch, hq;
+  int mode;
+  const int32_t* plan;      // device plan or nullptr
+  const float* suffix_o;    // direct suffix states or nullptr (no suffix)
+  const float* suffix_lse;
+  const float* part_o;
+  const float* part_lse;
+  const float* prefix_o;    // [split, B, Hq, D] or nullptr (no prefix)
+  const float* prefix_lse;  // [split, B, Hq]
+  int64_t prefix_stride_o, prefix_stride_lse;
+  int prefix_splits;
+  int n_prefix;
+  int32_t req_indptr[PKC_MAX_PREFIX + 1];
+  void* o;
+  float* lse;
+  int out_dtype;
+  int32_t* status;
+};
+
+struct PrefixParams {
+  int batch, hq, hkv, g;
+  float scale_log2;
+  int n_prefix;
+  int splits;                               // KV splits per group
+  int32_t kv_indptr[PKC_MAX_PREFIX + 1];
+  int32_t req_indptr[PKC_MAX_PREFIX + 1];
+  int32_t tile_indptr[PKC_MAX_PREFIX + 1];  // cumulative 128-row tiles
+  int32_t chunk[PKC_MAX_PREFIX];            // tokens per split (x128)
+  float* out_o;                             // [split, B, Hq, D]
+  float* out_lse;                           // [split, B, Hq]
+  int64_t split_stride_o, split_stride_lse;
+  int32_t* status;
+};
+
+// Launchers (defined in the .cu files); return a cudaError_t value.
+int launch_merge_state(const void* va, const float* sa, const void* vb,
+                       const float* sb, void* vo, float* so, int64_t rows,
+                       int head_dim, int dtype, void* stream);
+int launch_merge_states(const void* v, const float* s, void* vo, float* so,
+                        int64_t n_tokens, int n_states, int n_heads,
+                        int head_dim, int dtype, void* stream);
+int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype,
+                        void* stream);
+int launch_contract(const ContractParams& p, int n_rows, void* stream);
+// q/k/v tensor maps are built inside; returns cudaError_t or -1 when the
+// driver entry point for tensor maps is unavailable.
+int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix,
+                  const void* v_prefix, int64_t prefix_tokens, int n_tiles,
+                  int dtype, void* stream);
+
+int num_sms();
+
+}  // namespace pkc

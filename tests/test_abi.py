@@ -1,0 +1,141 @@
+"""C ABI checks that need no GPU: the library loads, exports every symbol
+that include/pkc.h declares, rejects bad arguments before touching the
+device, and its host-side plan equals the oracle's plan bit for bit."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cascade_gb300 as pkc
+import workloads
+from paged_kv_cascade_gb300 import build as pkc_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    pkc_build.build()
+    return pkc.lib()
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "pkc.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkc_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in pkc.h but not exported"
+        assert n in pkc.SIGNATURES, f"{n} has no Python binding"
+    assert set(pkc.SIGNATURES) == set(names)
+
+
+def test_version_and_error_string(L):
+    assert L.pkc_version() >= 100
+    assert isinstance(L.pkc_last_error(), bytes)
+
+
+def test_bad_arguments_are_rejected_without_a_device(L):
+    fake = ctypes.c_void_p(0x1000)
+    ws = ctypes.c_void_p(0x100000)
+    # head_dim 64 is valid but unsupported
+    rc = L.pkc_paged_decode_state(fake, fake, fake, fake, 4, fake, 2, 8, 8, 64, 16, 10, 1.0,
+                                  None, ws, 1 << 20, fake, fake, 1, None)
+    assert rc == 2 and b"head_dim" in L.pkc_last_error()
+    # heads not a multiple
+    rc = L.pkc_paged_decode_state(fake, fake, fake, fake, 4, fake, 2, 6, 4, 128, 16, 10, 1.0,
+                                  None, ws, 1 << 20, fake, fake, 1, None)
+    assert rc == 1
+    # workspace too small
+    rc = L.pkc_paged_decode_state(fake, fake, fake, fake, 4, fake, 2, 8, 8, 128, 16, 10, 1.0,
+                                  None, ws, 16, fake, fake, 1, None)
+    assert rc == 3
+    # misaligned workspace
+    rc = L.pkc_paged_decode_state(fake, fake, fake, fake, 4, fake, 2, 8, 8, 128, 16, 10, 1.0,
+                                  None, ctypes.c_void_p(0x100010), 1 << 20, fake, fake, 1, None)
+    assert rc == 3
+    # bad dtype for attention
+    rc = L.pkc_cascade_decode(fake, fake, fake, None, None, 1, fake, fake, fake, 4, fake, 2, 8,
+                              8, 128, 16, 10, 1.0, None, ws, 1 << 20, fake, fake, 0, None)
+    assert rc == 1
+    # n_states 0
+    rc = L.pkc_merge_states(fake, fake, fake, fake, 4, 0, 2, 128, 0, None)
+    assert rc == 1
+    # a plan made for another batch size
+    buf = pkc.plan([5, 6, 7], 4)
+    rc = L.pkc_paged_decode_state(fake, fake, fake, fake, 4, fake, 2, 8, 8, 128, 16, 10, 1.0,
+                                  ctypes.c_void_p(buf.ctypes.data), ws, 1 << 24, fake, fake, 1,
+                                  None)
+    assert rc == 7 and b"plan" in L.pkc_last_error()
+
+
+def test_workspace_size_matches_documented_layout(L):
+    def al(x):
+        return (x + 255) // 256 * 256
+    B, H, D, C, S = 7, 32, 128, 148, 3
+    words = pkc.plan_words(B, C)
+    want = 256 + al(4 * words) + al(4 * B * H * D) + al(4 * B * H) + al(4 * 2 * C * H * D) \
+        + al(4 * 2 * C * H) + S * (al(4 * B * H * D) + al(4 * B * H))
+    assert pkc.workspace_size(B, H, C, S) == want
+    assert pkc.workspace_size(B, H, 0, 0) == 256 + al(4 * B * H * D) + al(4 * B * H)
+
+
+def _compare_plans(kv, C, T=1, qo=None, alpha=1.0, beta=1.0):
+    ref = oracle.plan_ref(qo if qo is not None else [1] * len(kv), kv, T, C, alpha, beta)
+    got = pkc.plan_dict(pkc.plan(kv, C, tile_q=T, qo_len=qo, alpha=alpha, beta=beta))
+    assert got["header"]["MAGIC"] == pkc.PLAN_MAGIC
+    assert got["kv_chunk"] == ref["kv_chunk"]
+    assert got["work"] == [tuple(w) for w in ref["work"]]
+    assert got["cta_work"] == ref["cta_work"]
+    assert got["partial"] == ref["partial"]
+    assert got["split_units"] == ref["split_units"]
+    assert got["empty_units"] == ref["empty_units"]
+    assert got["cta_cost"] == ref["cta_cost"]
+    assert got["n_partials"] == ref["n_partials"]
+    assert got["unit_req"] == [u[0] for u in ref["units"]]
+    assert got["unit_qtile"] == [u[1] for u in ref["units"]]
+    assert got["unit_n_chunks"] == [len(c) for c in ref["unit_chunks"]]
+    return got
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_plan_equals_oracle_random(L, seed):
+    rng = np.random.default_rng(1000 + seed)
+    n = int(rng.integers(1, 300))
+    kv = rng.integers(0, 20000, size=n).tolist()
+    if seed % 5 == 0:
+        kv[: n // 3] = [0] * (n // 3)
+    C = int(rng.integers(1, 300))
+    T = int(rng.choice([1, 1, 1, 4, 128]))
+    qo = None if T == 1 else rng.integers(1, 400, size=n).tolist()
+    _compare_plans(kv, C, T, qo, float(rng.choice([1.0, 0.25, 3.0])), float(rng.choice([1.0, 2.0])))
+
+
+def test_plan_equals_oracle_on_every_workload(L):
+    for name in ["tiny_cascade", "paged_decode", "cascade_long_prompt", "gqa_cascade_lb"]:
+        w = workloads.WORKLOADS[name]
+        lens = workloads.suffix_lengths(w["suffix"], w["batch"], np.random.default_rng(w["seed"]))
+        got = _compare_plans(lens.tolist(), w.get("num_ctas", 148), 1, None,
+                             w.get("alpha", 1.0), w.get("beta", 1.0))
+        if name == "gqa_cascade_lb":
+            assert got["kv_chunk"] == 2974 and len(got["split_units"]) == 37
+
+
+def test_plan_is_deterministic(L):
+    a = pkc.plan(list(range(100)), 17)
+    b = pkc.plan(list(range(100)), 17)
+    assert np.array_equal(a, b)
+
+
+def test_plan_rejects_bad_input(L):
+    with pytest.raises(pkc.PkcError):
+        pkc.plan([3, -1], 4)
+    with pytest.raises(pkc.PkcError):
+        pkc.plan([3, 1], 0)

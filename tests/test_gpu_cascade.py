@@ -1,0 +1,124 @@
+"""prefix_attention_state and cascade_decode on the GPU against the oracle.
+
+The cascade's result must equal plain attention over prefix u suffix (the
+oracle computes that definition directly, not the cascade)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cascade_gb300 as pkc
+import workloads
+from pkc_testing import compare, oracle_args, sample_rows, to_device, workspace_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefix(p):
+    d = to_device(p)
+    ws = workspace_for(pkc, p)
+    o, lse = pkc.prefix_attention_state(d["q"], d["k_prefix"], d["v_prefix"],
+                                        p["prefix_kv_indptr"], p["prefix_req_indptr"],
+                                        p["sm_scale"], ws)
+    torch.cuda.synchronize()
+    assert pkc.device_status(ws) == pkc.PKC_OK
+    return o, lse
+
+
+def _cascade(p, num_ctas=None, alpha=1.0, beta=1.0):
+    d = to_device(p)
+    plan_buf = None
+    if num_ctas:
+        plan_buf = pkc.plan(p["cache_seqlens"], num_ctas, alpha=alpha, beta=beta)
+    ws = workspace_for(pkc, p, num_ctas=num_ctas or 0)
+    if plan_buf is not None:
+        pkc.plan_upload(plan_buf, ws)
+    o, lse = pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
+                                p["prefix_req_indptr"], d["k_cache"], d["v_cache"],
+                                d["block_table"], d["cache_seqlens"], p["sm_scale"], ws,
+                                plan_buf=plan_buf)
+    torch.cuda.synchronize()
+    assert pkc.device_status(ws) == pkc.PKC_OK
+    return o, lse
+
+
+PREFIX_CASES = [
+    # (hq, hkv, dtype, prefix_lens, groups, batch)
+    (32, 32, "f16", [256], [4], 4),
+    (32, 32, "f16", [1], [3], 3),                 # one prefix token
+    (32, 8, "bf16", [300, 77], [40, 30], 70),     # ragged tails, 2 groups, 2 row tiles
+    (8, 1, "bf16", [1000], [20], 25),             # g = 8, requests outside the group
+    (16, 8, "f16", [129, 0, 512], [5, 2, 9], 16), # an empty prefix
+]
+
+
+@pytest.mark.parametrize("case", range(len(PREFIX_CASES)))
+def test_prefix_state_small(case):
+    hq, hkv, dtype, pl, groups, batch = PREFIX_CASES[case]
+    p = workloads.make_problem(batch=batch, hq=hq, hkv=hkv, d=128, dtype=dtype, prefix_lens=pl,
+                               prefix_groups=groups, suffix=("const", 0), page_size=16,
+                               seed=20 + case)
+    o, lse = _prefix(p)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p, suffix=False))
+    # the prefix state is float32 output: same tolerance as the final output
+    compare(o, lse, ref_o, ref_lse)
+
+
+def test_prefix_peaky():
+    p = workloads.make_problem(batch=9, hq=32, hkv=8, d=128, dtype="bf16", prefix_lens=[700],
+                               prefix_groups=[9], suffix=("const", 0), page_size=16, seed=5,
+                               q_scale=8.0)
+    o, lse = _prefix(p)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p, suffix=False))
+    compare(o, lse, ref_o, ref_lse)
+
+
+@pytest.mark.parametrize("num_ctas", [None, 148])
+def test_cascade_tiny_workload_full(num_ctas):
+    p = workloads.workload("tiny_cascade", poison=True)
+    o, lse = _cascade(p, num_ctas)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse)
+
+
+CASCADE_CASES = [
+    # (hq, hkv, dtype, prefix_lens, groups, suffix lens, page_size)
+    (32, 32, "f16", [256], [4], [32, 0, 1, 33], 16),
+    (32, 8, "bf16", [1000, 300], [6, 5], [0, 5, 900, 17, 16, 2, 3000, 1, 0, 64, 65], 16),
+    (16, 4, "f16", [130], [12], list(range(0, 120, 10)), 32),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASCADE_CASES)))
+@pytest.mark.parametrize("num_ctas", [None, 5, 148])
+def test_cascade_small(case, num_ctas):
+    hq, hkv, dtype, pl, groups, lens, ps = CASCADE_CASES[case]
+    p = workloads.make_problem(batch=len(lens), hq=hq, hkv=hkv, d=128, dtype=dtype,
+                               prefix_lens=pl, prefix_groups=groups, suffix=("list", lens),
+                               page_size=ps, seed=30 + case, poison=True, extra_pages=3)
+    o, lse = _cascade(p, num_ctas)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse)
+
+
+def test_cascade_long_prompt_workload_sampled():
+    p = workloads.workload("cascade_long_prompt")
+    o, lse = _cascade(p, 148)
+    B, Hq, _ = p["q"].shape
+    rows = sample_rows(B, Hq, 96, seed=4)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], rows=rows, **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse, rows=rows)
+
+
+def test_gqa_cascade_lb_workload_sampled():
+    w = workloads.WORKLOADS["gqa_cascade_lb"]
+    p = workloads.workload("gqa_cascade_lb")
+    o, lse = _cascade(p, w["num_ctas"], w["alpha"], w["beta"])
+    B, Hq, _ = p["q"].shape
+    rows = sample_rows(B, Hq, 160, seed=5)
+    # include every split request's rows for head 0 and the longest request
+    lens = p["cache_seqlens"]
+    extra = [(int(b), 0) for b in np.argsort(-lens)[:6]]
+    rows = np.unique(np.concatenate([rows, np.array(extra, np.int32)]), axis=0)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], rows=rows, **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse, rows=rows)

@@ -45,6 +45,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["pkc", "reference"], default="pkc")
     ap.add_argument("--workload", default="gqa_cascade_lb",
                     choices=["gqa_cascade_lb", "cascade_long_prompt", "tiny_cascade"])
+    ap.add_argument("--batch", type=int, default=None,
+                    help="keep only the first N requests (and their prefix groups); "
+                         "a smaller case of the same workload, for profiling")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -68,12 +71,26 @@ def load_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def workload_cfg(name):
+def workload_cfg(name, batch=None):
     cfg = dict(workloads.WORKLOADS[name])
     cfg.setdefault("num_ctas", 148)
     cfg.setdefault("alpha", 1.0)
     cfg.setdefault("beta", 1.0)
+    if batch is not None and batch < cfg["batch"]:
+        lens, groups, left = [], [], batch
+        for L, g in zip(cfg["prefix_lens"], cfg["prefix_groups"]):
+            if left <= 0:
+                break
+            lens.append(L)
+            groups.append(min(g, left))
+            left -= g
+        cfg.update(batch=batch, prefix_lens=lens, prefix_groups=groups)
     return cfg
+
+
+def make_workload(name, batch=None):
+    cfg = workload_cfg(name, batch)
+    return cfg, workloads.make_problem(**cfg)
 
 
 def kv_bytes_per_token(p):
@@ -191,8 +208,7 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    cfg = workload_cfg(args.workload)
-    p = workloads.workload(args.workload)
+    cfg, p = make_workload(args.workload, args.batch)
     eff = workloads.effective_bytes(p)
     per_step_s = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     times, fracs = [], []
@@ -243,8 +259,7 @@ def main():
         dist.barrier()
     import paged_kv_cascade_gb300 as pkc
 
-    cfg = workload_cfg(args.workload)
-    p = workloads.workload(args.workload)
+    cfg, p = make_workload(args.workload, args.batch)
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from pkc_testing import to_device
     d = to_device(p, f"cuda:{local}")

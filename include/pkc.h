@@ -245,6 +245,38 @@ int pkc_paged_decode_state(const void* q, const void* k_cache,
                            int dtype, void* stream);
 
 /*
+ * Paged decode that allocates nothing (the pages have no counterpart; this
+ * is a deployment convenience).  Same computation, arguments and outputs as
+ * pkc_paged_decode_state, for callers that cannot call cudaMalloc or own no
+ * spare device memory for a workspace -- e.g. code running inside another
+ * framework's pre-reserved memory pool, or under a fixed memory budget.
+ * The split-KV scratch (status word, uploaded plan, partial states) lives in
+ * an 8 MiB array declared in device memory by the library itself; every GPU
+ * that loads the library holds it until the process exits.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - The plan (plan_host, as in pkc_paged_decode_state, or NULL) is copied
+ *     into the array by this call; no pkc_plan_upload is needed.  It needs
+ *     256 + plan + 2 * num_ctas * num_qo_heads * 129 * 4 bytes (rounded to
+ *     256-byte blocks) <= 8 MiB, else PKC_ERR_WORKSPACE with the numbers.
+ *   - Every call shares the one array and leaves its contents behind; the
+ *     call clears the status word itself.  Calls whose kernels overlap on
+ *     the GPU (different streams, or different host threads) race on the
+ *     array: serialise them.
+ *   - device_status: NULL, or a device int32 that receives the call's status
+ *     word (PKC_OK or the PKC_ERR_* a kernel recorded) in stream order.
+ * Calls no cudaMalloc / cudaFree and no allocating library routine.
+ */
+int pkc_paged_decode_state_noalloc(
+    const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_table, int block_table_stride,
+    const int32_t* cache_seqlens, int batch, int num_qo_heads,
+    int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+    float sm_scale, const int32_t* plan_host, void* o, float* lse,
+    int32_t* device_status, int dtype, void* stream);
+
+/*
  * Multi-query prefix state (blog "Cascade Inference", step 1 of the
  * algorithm): every request's queries against the KV of the shared prefix
  * of its group, on the tensor cores (tcgen05, TMEM accumulators).

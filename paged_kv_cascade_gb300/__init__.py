@@ -51,6 +51,8 @@ SIGNATURES = {
                                     _P, _P, _SZ, _P, _P, _I, _P]),
     "pkc_prefix_attention_state": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ,
                                         _P, _P, _I, _P]),
+    "pkc_paged_decode_state_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I64,
+                                            _F, _P, _P, _P, _P, _I, _P]),
     "pkc_set_stage_events": (_I, [_c.POINTER(_P), _I]),
     "pkc_cascade_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                 _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
@@ -207,6 +209,23 @@ def paged_decode_state(q, k_cache, v_cache, block_table, cache_seqlens, sm_scale
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(cache_seqlens), B, Hq, Hkv, D, ps, P, float(sm_scale), _hptr(plan_buf),
         _ptr(workspace), workspace.numel(), _ptr(o), _ptr(lse), _dtype_code(q), _stream(stream)))
+    return o, lse
+
+
+def paged_decode_state_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, sm_scale,
+                               plan_buf=None, o=None, lse=None, device_status=None, stream=None):
+    """paged_decode_state without a caller workspace, for callers that
+    cannot allocate device memory: the library's own fixed 8 MiB device
+    array holds the scratch.  Calls that overlap on the GPU race on it."""
+    import torch
+    B, Hq, D = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().pkc_paged_decode_state_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(cache_seqlens), B, Hq, Hkv, D, ps, P, float(sm_scale), _hptr(plan_buf), _ptr(o),
+        _ptr(lse), _ptr(device_status), _dtype_code(q), _stream(stream)))
     return o, lse
 
 

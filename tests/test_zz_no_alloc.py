@@ -1,0 +1,88 @@
+"""The decode entry point that allocates nothing, against the workspace one.
+
+pkc_paged_decode_state_noalloc serves callers that cannot call cudaMalloc
+(code inside another framework's pre-reserved memory pool, or on a fixed
+memory budget): its split-KV scratch is a fixed array inside the library.
+Two calls in a row, on different problems and plans, must each match
+pkc_paged_decode_state on the same inputs -- the second call must not be
+affected by what the first left in the shared array.  The test goes
+through the C ABI directly.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cascade_gb300 as pkc
+import workloads
+from pkc_testing import O_TOL, LSE_TOL, half_ulp, to_device, workspace_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem(seed, lens, hq, hkv, dtype):
+    return workloads.make_problem(batch=len(lens), hq=hq, hkv=hkv, d=128, dtype=dtype,
+                                  prefix_lens=[], prefix_groups=[], suffix=("list", lens),
+                                  page_size=16, seed=seed, poison=True, extra_pages=2)
+
+
+def _with_workspace(p, d, plan_buf, num_ctas):
+    ws = workspace_for(pkc, p, num_ctas=num_ctas, prefix_splits=0)
+    pkc.plan_upload(plan_buf, ws)
+    o, lse = pkc.paged_decode_state(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                    d["cache_seqlens"], p["sm_scale"], ws, plan_buf=plan_buf)
+    torch.cuda.synchronize()
+    assert pkc.device_status(ws) == pkc.PKC_OK
+    return o, lse
+
+
+def _no_alloc_via_c_abi(p, d, plan_buf):
+    L = pkc.lib()
+    B, Hq, D = d["q"].shape
+    P, ps, Hkv, _ = d["k_cache"].shape
+    o = torch.empty_like(d["q"])
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    dtype = pkc.BF16 if d["q"].dtype == torch.bfloat16 else pkc.F16
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = L.pkc_paged_decode_state_noalloc(
+        d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
+        d["block_table"].data_ptr(), d["block_table"].shape[1], d["cache_seqlens"].data_ptr(),
+        B, Hq, Hkv, D, ps, P, float(p["sm_scale"]), ctypes.c_void_p(plan_buf.ctypes.data),
+        o.data_ptr(), lse.data_ptr(), status.data_ptr(), dtype, stream)
+    assert rc == pkc.PKC_OK, L.pkc_last_error()
+    torch.cuda.synchronize()
+    assert int(status.item()) == pkc.PKC_OK
+    return o, lse
+
+
+def _close(a_o, a_lse, b_o, b_lse):
+    ref = b_o.float().cpu().numpy().astype(np.float64)
+    got = a_o.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= O_TOL + half_ulp(ref, a_o.dtype))
+    la, lb = a_lse.cpu().numpy(), b_lse.cpu().numpy()
+    assert np.array_equal(np.isneginf(la), np.isneginf(lb))
+    fin = ~np.isneginf(lb)
+    assert np.all(np.abs(la[fin] - lb[fin]) <= LSE_TOL)
+
+
+def test_no_alloc_matches_workspace_entry_point_two_calls_in_a_row():
+    first = _problem(41, [900, 0, 33, 4000, 17, 250], 32, 8, "bf16")
+    second = _problem(42, [5, 1200, 64, 2], 16, 16, "f16")
+    for p, num_ctas in ((first, 148), (second, 37)):
+        d = to_device(p)
+        plan_buf = pkc.plan(p["cache_seqlens"], num_ctas)
+        want_o, want_lse = _with_workspace(p, d, plan_buf, num_ctas)
+        got_o, got_lse = _no_alloc_via_c_abi(p, d, plan_buf)
+        _close(got_o, got_lse, want_o, want_lse)
+
+
+def test_no_alloc_rejects_a_plan_beyond_its_scratch():
+    p = _problem(43, [10, 20], 64, 64, "f16")
+    d = to_device(p)
+    plan_buf = pkc.plan(p["cache_seqlens"], 600)  # 2*600*64 rows of partials > 8 MiB
+    with pytest.raises(pkc.PkcError) as e:
+        pkc.paged_decode_state_noalloc(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                       d["cache_seqlens"], p["sm_scale"], plan_buf=plan_buf)
+    assert e.value.code == 3 and "8388608" in str(e.value)

@@ -275,12 +275,17 @@ def main():
     lse = torch.empty((B, Hq), dtype=torch.float32, device=d["q"].device)
 
     host_plan_s = []
+    # A pinned plan buffer is rewritten only after the previous upload from
+    # it has run on the GPU (the host runs ahead of the device).
+    uploaded = [torch.cuda.Event(), torch.cuda.Event()]
 
     def step(i):
+        uploaded[i & 1].synchronize()
         t0 = time.perf_counter()
         buf = pkc.plan(lens, num_ctas, alpha=cfg["alpha"], beta=cfg["beta"], out=plan_np[i & 1])
         host_plan_s.append(time.perf_counter() - t0)
         pkc.plan_upload(buf, ws)
+        uploaded[i & 1].record()
         pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
                            p["prefix_req_indptr"], d["k_cache"], d["v_cache"], d["block_table"],
                            d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse)

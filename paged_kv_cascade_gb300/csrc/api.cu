@@ -25,6 +25,7 @@ int set_error(int code, const char* fmt, ...) {
 }
 
 int cuda_error(int e, const char* what) {
+  if (e == -1) return set_error(PKC_ERR_CUDA, "%s: TMA tensor map encoding failed", what);
   return set_error(PKC_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)e));
 }
 

@@ -6,21 +6,34 @@
 // queries of different requests, so the kernel is bound by HBM bandwidth
 // and runs on the CUDA cores (a query tile of one row is below the tensor
 // cores' minimum M; MLSys'25 notes, A3 "micro-kernels of different tile
-// sizes").  The query heads of one KV head are fused into one thread block
-// so every K/V row is loaded once for the whole group (MLSys'25 notes,
-// appendix A).  Long sequences are split into KV chunks by the host plan;
-// each chunk yields a partial state, merged afterwards by the contraction
-// kernel (MLSys'25 notes, A3: "the final output is the contraction of the
-// partial outputs"; appendix D: unsplit requests write the output
-// directly).
+// sizes").  The query heads of one KV head are fused so every K/V row is
+// read once for the whole group (MLSys'25 notes, appendix A).  Long
+// sequences are split into KV chunks by the host plan; each chunk yields a
+// partial state, merged afterwards by the contraction kernel (MLSys'25
+// notes, A3: "the final output is the contraction of the partial outputs";
+// appendix D: unsplit requests write the output directly).
 //
-// Thread layout: 4 warps per block; a half-warp (16 lanes x 8 dims) holds
-// one 128-dim K or V row, so a warp consumes two tokens per step.  Loads
-// are 16-byte vectors straight from HBM, U steps in flight per warp.  Each
-// half-warp keeps its own online-softmax state (running max m, running sum
-// l, accumulator); the halves and the warps are merged at the end with the
-// same (+) operator.
+// One thread block = one planned CTA x one group of HG KV heads (HG = 8 when
+// Hkv is a multiple of 8).
+//  * Warp 8 (producer) walks the block's work items page slice by page
+//    slice.  A slice is up to 16 consecutive slots of one page; the TMA
+//    engine copies its K and V rows for the HG heads ([slot][head][128],
+//    256 bytes per row) into a 3-stage shared-memory ring, one 4-D tile per
+//    slice and tensor.  Page ids come from a 32-entry window of the block
+//    table that the warp loads in one go.  Each stage carries a header (work
+//    item, first/last flags) and a mask of the rows that belong to the item.
+//  * Warps 0..7 (consumers) own one KV head each (several warps share a head
+//    when HG < 8).  A half-warp reads one 256-byte row from shared memory (16
+//    lanes x 16 bytes).  q.k uses two-wide fp32 FMAs; the 16-lane reduction
+//    of the G heads' partial dots is a transposed butterfly, after which
+//    each lane owns one head's score.  The online softmax (base 2) updates
+//    once per stage; P.V accumulates every head's 8 dims per lane.
+//  * At the end of a work item the half-warps (and warps sharing a head)
+//    merge their states with (+) and write the chunk's state.
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "pkc_device.cuh"
 #include "pkc_internal.h"
@@ -29,229 +42,475 @@ namespace pkc {
 namespace {
 
 constexpr int D = PKC_HEAD_DIM;
-constexpr int kWarps = 4;
+constexpr int kConsumerWarps = 8;
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStageRows = 128;            // (slot, head) rows per stage and tensor
+constexpr int kRowBytes = D * 2;           // 256 bytes per 16-bit row
+constexpr int kStageHalf = kStageRows * kRowBytes;  // 32 KB of K (and of V)
+constexpr int kMaxSliceRows = 16;          // slots per slice
 
-struct WorkItem {
-  int req, kv_begin, kv_end, slot;
+enum : int { kFirst = 1, kLast = 2, kDone = 4 };
+
+struct StageHdr {
+  int32_t flags, req, slot, n_rows, hg, pad0, pad1, pad2;
+  uint32_t mask[kStageRows / 32];  // valid rows (row-major: slot, head slot)
 };
 
-template <typename T, int G>
-__global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeParams p) {
-  constexpr int U = G >= 4 ? 4 : 8;  // steps (token pairs) in flight per warp
-  __shared__ float s_m[kWarps][G], s_l[kWarps][G];
-  __shared__ __align__(16) float s_acc[kWarps][G][D];
+template <int HG>
+struct DecodeCfg {
+  static constexpr int kWph = kConsumerWarps / HG;  // warps per KV head
+  static constexpr int kStages = HG == 8 ? 3 : 2;
+};
+
+// Shared memory, from a 1024-byte aligned base: the K/V stages, the stage
+// headers, the full/empty barriers, the abort flag, then (when several warps
+// share a KV head) the buffer where those warps merge their states.
+template <int HG>
+struct DecodeSmem {
+  static constexpr int kStages = DecodeCfg<HG>::kStages;
+  static constexpr int kHdr = kStages * 2 * kStageHalf;
+  static constexpr int kBars = kHdr + kStages * (int)sizeof(StageHdr);
+  static constexpr int kMergeBars = kBars + 2 * kStages * 8;  // 2 merge barriers
+  static constexpr int kAbort = kMergeBars + 2 * 8;
+  static constexpr int kMerge = (kAbort + 16 + 15) & ~15;
+};
+
+// Two merge buffers (alternating work items) of 8 warps x G heads x (D + 2).
+template <int G, int HG>
+constexpr int decode_smem_bytes() {
+  return DecodeSmem<HG>::kMerge + (DecodeCfg<HG>::kWph > 1 ? 2 * kConsumerWarps * G * (D + 2) * 4 : 0) + 1024;
+}
+
+// Transposed butterfly over the 16 lanes of a half-warp: in, v[i] is this
+// lane's partial dot of head i; out, v[0] is the full dot of head
+// (sub >> (4 - log2 G)).
+template <int G>
+__device__ __forceinline__ float reduce_heads(float (&v)[G], int sub) {
+  float a[G];
+#pragma unroll
+  for (int i = 0; i < G; ++i) a[i] = v[i];
+  int n = G;
+#pragma unroll
+  for (int m = 8; m >= 1; m >>= 1) {
+    if (n > 1) {
+      const bool up = (sub & m) != 0;
+#pragma unroll
+      for (int i = 0; i < G / 2; ++i) {
+        if (i < n / 2) {
+          const float keep = up ? a[i + n / 2] : a[i];
+          const float send = up ? a[i] : a[i + n / 2];
+          a[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      n >>= 1;
+    } else {
+      a[0] += __shfl_xor_sync(0xffffffffu, a[0], m);
+    }
+  }
+  return a[0];
+}
+
+template <int G>
+struct HeadShift {
+  static constexpr int v = G == 1 ? 4 : G == 2 ? 3 : G == 4 ? 2 : 1;
+};
+
+template <typename T, int G, int HG>
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const DecodeParams p) {
+  using Cfg = DecodeCfg<HG>;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int kWph = Cfg::kWph;
+  constexpr int kShift = HeadShift<G>::v;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_kv = smem_u32(smem);  // stage s: K at s*64KB, V at +32KB
+  using L = DecodeSmem<HG>;
+  StageHdr* hdrs = reinterpret_cast<StageHdr*>(smem + L::kHdr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint64_t* empty = full + kStages;
+  uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + L::kMergeBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  float* merge_buf = reinterpret_cast<float*>(smem + L::kMerge);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, sub = lane & 15;
-  const int kvh = blockIdx.y;
   const int cta = blockIdx.x;
-  const T* __restrict__ kc = static_cast<const T*>(p.k_cache);
-  const T* __restrict__ vc = static_cast<const T*>(p.v_cache);
-  const int ps = p.page_size;
-  const int ps_shift = (ps & (ps - 1)) == 0 ? __ffs(ps) - 1 : -1;
-
-  int w_begin = 0, w_end = 1;
+  // Head groups of this block: blockIdx.y, blockIdx.y + gridDim.y, ...
+  const int n_hg_mine = (p.hkv / HG - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
   const int32_t* pl = p.plan;
+  int w_begin = 0, w_end = 1;
   if (pl) {
     w_begin = pl[pl[PKC_PLAN_OFF_CTA_INDPTR] + cta];
     w_end = pl[pl[PKC_PLAN_OFF_CTA_INDPTR] + cta + 1];
   }
-  for (int wi = w_begin; wi < w_end; ++wi) {
-    WorkItem it;
-    if (pl) {
-      const int w = pl[pl[PKC_PLAN_OFF_CTA_WORK] + wi];
-      const int unit = pl[pl[PKC_PLAN_OFF_WORK_UNIT] + w];
-      it.req = pl[pl[PKC_PLAN_OFF_UNIT_REQ] + unit];
-      it.kv_begin = pl[pl[PKC_PLAN_OFF_WORK_KV_BEGIN] + w];
-      it.kv_end = pl[pl[PKC_PLAN_OFF_WORK_KV_END] + w];
-      it.slot = pl[pl[PKC_PLAN_OFF_WORK_PARTIAL] + w];
-      const int len = p.cache_seqlens[it.req];
-      if (pl[pl[PKC_PLAN_OFF_UNIT_KV_LEN] + unit] != len) {
-        if (threadIdx.x == 0) report(p.status, PKC_ERR_PLAN);
-        it.kv_end = min(it.kv_end, len);
-        it.kv_begin = min(it.kv_begin, it.kv_end);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kConsumerWarps);
+    }
+    mbar_init(smem_u32(&merge_bar[0]), kConsumerWarps);
+    mbar_init(smem_u32(&merge_bar[1]), kConsumerWarps);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------ producer ------------------------------
+    const int ps = p.page_size;
+    const int sl = ps < kMaxSliceRows ? ps : kMaxSliceRows;      // slots per slice
+    const int spp = (ps + sl - 1) / sl;                           // slices per page
+    const int slices_per_stage = kStageRows / (sl * HG);
+    const uint32_t slice_bytes = (uint32_t)(sl * HG * kRowBytes);
+    const uint64_t pol = l2_policy_evict_first();
+    if (lane == 0) { prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); }
+    int k = 0;  // stage counter
+    bool ok = true;
+    auto acquire = [&](int kk) -> int {
+      const int s = kk % kStages;
+      bool got = true;
+      if (lane == 0) got = mbar_wait(smem_u32(&empty[s]), ((kk / kStages) & 1) ^ 1, abort, p.status);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      return got ? s : -1;
+    };
+    for (int it = 0; ok && it < n_hg_mine * (w_end - w_begin); ++it) {
+      const int hg = (int)blockIdx.y + (int)gridDim.y * (it / (w_end - w_begin));
+      const int wi = w_begin + it % (w_end - w_begin);
+      int req, kb, ke, slot;
+      if (pl) {
+        const int w = pl[pl[PKC_PLAN_OFF_CTA_WORK] + wi];
+        const int unit = pl[pl[PKC_PLAN_OFF_WORK_UNIT] + w];
+        req = pl[pl[PKC_PLAN_OFF_UNIT_REQ] + unit];
+        kb = pl[pl[PKC_PLAN_OFF_WORK_KV_BEGIN] + w];
+        ke = pl[pl[PKC_PLAN_OFF_WORK_KV_END] + w];
+        slot = pl[pl[PKC_PLAN_OFF_WORK_PARTIAL] + w];
+        const int len = p.cache_seqlens[req];
+        if (pl[pl[PKC_PLAN_OFF_UNIT_KV_LEN] + unit] != len) {
+          if (lane == 0 && hg == 0) report(p.status, PKC_ERR_PLAN);
+          ke = min(ke, len);
+          kb = min(kb, ke);
+        }
+      } else {
+        req = cta;
+        kb = 0;
+        ke = max(p.cache_seqlens[cta], 0);
+        slot = -1;
       }
-    } else {
-      it.req = cta;
-      it.kv_begin = 0;
-      it.kv_end = max(p.cache_seqlens[cta], 0);
-      it.slot = -1;
-    }
-    if ((int64_t)it.kv_end > p.bt_stride * ps) {  // more tokens than table entries
-      if (threadIdx.x == 0) report(p.status, PKC_ERR_BLOCK_TABLE);
-      it.kv_end = (int)(p.bt_stride * ps);
-      it.kv_begin = min(it.kv_begin, it.kv_end);
-    }
-
-    // Query rows of the G heads of this KV head, pre-scaled to log2 units.
-    float q[G][8];
+      if ((int64_t)ke > p.bt_stride * ps) {  // more tokens than table entries
+        if (lane == 0 && hg == 0) report(p.status, PKC_ERR_BLOCK_TABLE);
+        ke = (int)(p.bt_stride * ps);
+        kb = min(kb, ke);
+      }
+      const int32_t* bt_row = p.block_table + (int64_t)req * p.bt_stride;
+      const int n_pages_used = (ke + ps - 1) / ps;
+      int win_base = -1 << 30;
+      int32_t win_pid = -1;
+      const int first = kb < ke ? (kb / ps) * spp + (kb % ps) / sl : 0;
+      const int last = kb < ke ? ((ke - 1) / ps) * spp + ((ke - 1) % ps) / sl : -1;
+      int sl0 = first;
+      bool first_stage = true;
+      do {
+        const int s = acquire(k);
+        if (s < 0) { ok = false; break; }
+        const int n_sl = min(slices_per_stage, last - sl0 + 1);  // may be <= 0 for empty items
+        StageHdr& h = hdrs[s];
+        const uint32_t kst = s_kv + s * 2 * kStageHalf;
+        // Row validity: row j = i*sl*HG + t*HG + hh belongs to slice i, slot t.
+        uint32_t maskw[kStageRows / 32];
 #pragma unroll
-    for (int gi = 0; gi < G; ++gi) {
-      const T* qp = static_cast<const T*>(p.q) + ((int64_t)it.req * p.hq + kvh * G + gi) * D + sub * 8;
-      uint4 u = *reinterpret_cast<const uint4*>(qp);
-      float2 a = Elem<T>::to_f2(u.x), b = Elem<T>::to_f2(u.y), c = Elem<T>::to_f2(u.z), d = Elem<T>::to_f2(u.w);
-      q[gi][0] = a.x * p.scale_log2; q[gi][1] = a.y * p.scale_log2;
-      q[gi][2] = b.x * p.scale_log2; q[gi][3] = b.y * p.scale_log2;
-      q[gi][4] = c.x * p.scale_log2; q[gi][5] = c.y * p.scale_log2;
-      q[gi][6] = d.x * p.scale_log2; q[gi][7] = d.y * p.scale_log2;
-    }
-
-    float m[G], l[G], acc[G][8];
-#pragma unroll
-    for (int gi = 0; gi < G; ++gi) {
-      m[gi] = neg_inf();
-      l[gi] = 0.f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) acc[gi][k] = 0.f;
-    }
-
-    // Contiguous token range of this warp (whole token pairs).
-    const int n = it.kv_end - it.kv_begin;
-    const int pairs = (n + 1) >> 1;
-    const int ppw = (pairs + kWarps - 1) / kWarps;
-    const int wb = it.kv_begin + 2 * warp * ppw;
-    const int we = min(it.kv_end, wb + 2 * ppw);
-    const int nsteps = we > wb ? (we - wb + 1) >> 1 : 0;
-    const int32_t* bt_row = p.block_table + (int64_t)it.req * p.bt_stride;
-
-    for (int s0 = 0; s0 < nsteps; s0 += U) {
-      uint4 kr[U], vr[U];
-      bool valid[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int t = wb + 2 * (s0 + u) + half;
-        bool ok = t < we;
-        kr[u] = make_uint4(0, 0, 0, 0);
-        vr[u] = make_uint4(0, 0, 0, 0);
-        if (ok) {
-          int pi, slot;
-          if (ps_shift >= 0) { pi = t >> ps_shift; slot = t & (ps - 1); }
-          else { pi = t / ps; slot = t - pi * ps; }
-          const int32_t page = bt_row[pi];
-          if (page < 0 || page >= p.num_pages) {
-            report(p.status, PKC_ERR_BLOCK_TABLE);
-            ok = false;
-          } else {
-            const int64_t off = (((int64_t)page * ps + slot) * p.hkv + kvh) * D + sub * 8;
-            kr[u] = ldg_stream(kc + off);
-            vr[u] = ldg_stream(vc + off);
+        for (int q = 0; q < kStageRows / 32; ++q) maskw[q] = 0;
+        for (int i = 0; i < n_sl; ++i) {
+          const int sli = sl0 + i;
+          const int page_idx = sli / spp;
+          const int slot0 = (sli % spp) * sl;
+          if (page_idx < win_base || page_idx >= win_base + 32) {
+            win_base = page_idx;
+            const int pi = win_base + lane;
+            win_pid = pi < n_pages_used ? bt_row[pi] : -1;
+          }
+          const int32_t pid = __shfl_sync(0xffffffffu, win_pid, page_idx - win_base);
+          if (pid < 0 || pid >= p.num_pages) {
+            if (lane == 0) report(p.status, PKC_ERR_BLOCK_TABLE);
+            continue;  // rows stay invalid, nothing is copied
+          }
+          if (lane == 0) {
+            mbar_expect_tx(smem_u32(&full[s]), 2 * slice_bytes);  // before the copies it covers
+            tma_load_4d(kst + i * slice_bytes, &tm_k, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
+            tma_load_4d(kst + kStageHalf + i * slice_bytes, &tm_v, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
+          }
+          const int tok0 = page_idx * ps + slot0;
+          // lanes mark the valid rows of this slice
+          for (int r = lane; r < sl * HG; r += 32) {
+            const int t = r / HG;
+            const int tok = tok0 + t;
+            if (slot0 + t < ps && tok >= kb && tok < ke) {
+              const int row = i * sl * HG + r;
+              maskw[row >> 5] |= 1u << (row & 31);
+            }
           }
         }
-        valid[u] = ok;
-      }
-      // Scores s = q . k (log2 units), reduced over the 16 lanes of a half.
-      float sc[U][G];
+        // combine the lanes' mask words
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float2 k0 = Elem<T>::to_f2(kr[u].x), k1 = Elem<T>::to_f2(kr[u].y);
-        float2 k2 = Elem<T>::to_f2(kr[u].z), k3 = Elem<T>::to_f2(kr[u].w);
+        for (int q = 0; q < kStageRows / 32; ++q) {
+          uint32_t v = maskw[q];
 #pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-          float d = q[gi][0] * k0.x;
-          d = fmaf(q[gi][1], k0.y, d); d = fmaf(q[gi][2], k1.x, d); d = fmaf(q[gi][3], k1.y, d);
-          d = fmaf(q[gi][4], k2.x, d); d = fmaf(q[gi][5], k2.y, d); d = fmaf(q[gi][6], k3.x, d);
-          d = fmaf(q[gi][7], k3.y, d);
-          sc[u][gi] = d;
+          for (int o = 16; o >= 1; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+          maskw[q] = v;
         }
-      }
+        sl0 += slices_per_stage;
+        const bool last_stage = sl0 > last;
+        if (lane == 0) {
+          h.flags = (first_stage ? kFirst : 0) | (last_stage ? kLast : 0);
+          h.req = req;
+          h.slot = slot;
+          h.hg = hg;
+          h.n_rows = n_sl > 0 ? n_sl * sl * HG : 0;
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-          float d = sc[u][gi];
-          d += __shfl_xor_sync(0xffffffffu, d, 8);
-          d += __shfl_xor_sync(0xffffffffu, d, 4);
-          d += __shfl_xor_sync(0xffffffffu, d, 2);
-          d += __shfl_xor_sync(0xffffffffu, d, 1);
-          sc[u][gi] = valid[u] ? d : neg_inf();
+          for (int q = 0; q < kStageRows / 32; ++q) h.mask[q] = maskw[q];
+          mbar_arrive(smem_u32(&full[s]));  // header written; the copies carry their own bytes
         }
-      // Online softmax update, once per U steps.
-      float pr[U][G];
-#pragma unroll
-      for (int gi = 0; gi < G; ++gi) {
-        float mx = m[gi];
-#pragma unroll
-        for (int u = 0; u < U; ++u) mx = fmaxf(mx, sc[u][gi]);
-        const float corr = mx == neg_inf() ? 1.f : ex2(m[gi] - mx);
-        m[gi] = mx;
-        l[gi] *= corr;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[gi][k] *= corr;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          pr[u][gi] = valid[u] ? ex2(sc[u][gi] - mx) : 0.f;
-          l[gi] += pr[u][gi];
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float2 v0 = Elem<T>::to_f2(vr[u].x), v1 = Elem<T>::to_f2(vr[u].y);
-        float2 v2 = Elem<T>::to_f2(vr[u].z), v3 = Elem<T>::to_f2(vr[u].w);
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-          const float pw = pr[u][gi];
-          acc[gi][0] = fmaf(pw, v0.x, acc[gi][0]); acc[gi][1] = fmaf(pw, v0.y, acc[gi][1]);
-          acc[gi][2] = fmaf(pw, v1.x, acc[gi][2]); acc[gi][3] = fmaf(pw, v1.y, acc[gi][3]);
-          acc[gi][4] = fmaf(pw, v2.x, acc[gi][4]); acc[gi][5] = fmaf(pw, v2.y, acc[gi][5]);
-          acc[gi][6] = fmaf(pw, v3.x, acc[gi][6]); acc[gi][7] = fmaf(pw, v3.y, acc[gi][7]);
-        }
+        __syncwarp();
+        first_stage = false;
+        ++k;
+      } while (sl0 <= last);
+    }
+    // Tell the consumers there is no more work.
+    if (ok) {
+      const int s = acquire(k);
+      if (s >= 0 && lane == 0) {
+        hdrs[s].flags = kDone;
+        mbar_arrive(smem_u32(&full[s]));
       }
     }
+    if (*abort && lane == 0) {
+      // Let the copies already issued land before the block exits.
+      volatile int no_abort = 0;
+      for (int kk = k > kStages ? k - kStages : 0; kk < k; ++kk)
+        mbar_wait(smem_u32(&full[kk % kStages]), (kk / kStages) & 1, &no_abort, p.status);
+    }
+    return;
+  }
 
-    // Merge the two halves of the warp ((+) with log2-domain maxima).
+  // ------------------------------ consumers ------------------------------
+  const int half = lane >> 4, sub = lane & 15;
+  const int hh = warp % HG;       // KV head within the group
+  const int cls = warp / HG;      // which pairs of rows of the stage
+  const int src_base = half << 4;
+  int kvh = hh;
+
+  uint64_t q2[G][4];
+  uint64_t acc[G][4];
+  float m_own = neg_inf(), l_own = 0.f;
+  int req = 0, out_slot = -1;
+  int items_done = 0;  // work items finished by this warp (merge buffer parity)
+
+  for (int k = 0;; ++k) {
+    const int s = k % kStages;
+    if (!mbar_wait(smem_u32(&full[s]), (k / kStages) & 1, abort, p.status)) break;
+    const StageHdr& h = hdrs[s];
+    const int flags = h.flags;
+    if (flags & kDone) break;
+    if (flags & kFirst) {
+      req = h.req;
+      kvh = h.hg * HG + hh;
+      out_slot = h.slot;
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        const T* qp = static_cast<const T*>(p.q) + ((int64_t)req * p.hq + kvh * G + gi) * D + sub * 8;
+        const uint4 u = *reinterpret_cast<const uint4*>(qp);
+        const uint64_t sc2 = pk2(p.scale_log2, p.scale_log2);
+        q2[gi][0] = fmul2(widen2<T>(u.x), sc2);
+        q2[gi][1] = fmul2(widen2<T>(u.y), sc2);
+        q2[gi][2] = fmul2(widen2<T>(u.z), sc2);
+        q2[gi][3] = fmul2(widen2<T>(u.w), sc2);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[gi][c] = 0ull;
+      }
+      m_own = neg_inf();
+      l_own = 0.f;
+    }
+    const int n_rows = h.n_rows;
+    uint32_t mask[kStageRows / 32];
+#pragma unroll
+    for (int q = 0; q < kStageRows / 32; ++q) mask[q] = h.mask[q];
+    const uint32_t kst = s_kv + s * 2 * kStageHalf;
+    const uint32_t vst = kst + kStageHalf;
+
+    // Rows of this head in the stage: j = 0 .. rows/HG-1 (slot order);
+    // warp class `cls` takes token pairs cls, cls + kWph, ...
+    float sc[8];
+    bool valid[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int tok_in_stage = 2 * (cls + kWph * u) + half;
+      const int row = tok_in_stage * HG + hh;
+      const bool v = row < n_rows && ((mask[row >> 5] >> (row & 31)) & 1u);
+      valid[u] = v;
+      uint4 kr = make_uint4(0, 0, 0, 0);
+      if (v) kr = lds128(kst + row * kRowBytes + sub * 16);
+      const uint64_t k0 = widen2<T>(kr.x), k1 = widen2<T>(kr.y), k2 = widen2<T>(kr.z), k3 = widen2<T>(kr.w);
+      float part[G];
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        uint64_t a = fmul2(q2[gi][0], k0);
+        a = ffma2(q2[gi][1], k1, a);
+        a = ffma2(q2[gi][2], k2, a);
+        a = ffma2(q2[gi][3], k3, a);
+        const float2 f = upk2(a);
+        part[gi] = f.x + f.y;
+      }
+      const float d = reduce_heads<G>(part, sub);
+      sc[u] = v ? d : neg_inf();
+    }
+    // Online softmax for this lane's head, once per stage.
+    float mx = m_own;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mx = fmaxf(mx, sc[u]);
+    const float corr = mx == neg_inf() ? 1.f : ex2(m_own - mx);
+    m_own = mx;
+    float pr[8];
+    float lsum = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      pr[u] = valid[u] ? ex2(sc[u] - mx) : 0.f;
+      lsum += pr[u];
+    }
+    l_own = l_own * corr + lsum;
 #pragma unroll
     for (int gi = 0; gi < G; ++gi) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m[gi], 16);
-      const float lo = __shfl_xor_sync(0xffffffffu, l[gi], 16);
-      const float mm = fmaxf(m[gi], mo);
-      const float a = mm == neg_inf() ? 0.f : ex2(m[gi] - mm);
-      const float b = mm == neg_inf() ? 0.f : ex2(mo - mm);
-      l[gi] = l[gi] * a + lo * b;
+      const float c = __shfl_sync(0xffffffffu, corr, src_base | (gi << kShift));
+      const uint64_t c2 = pk2(c, c);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float ao = __shfl_xor_sync(0xffffffffu, acc[gi][k], 16);
-        acc[gi][k] = acc[gi][k] * a + ao * b;
+      for (int cc = 0; cc < 4; ++cc) acc[gi][cc] = fmul2(acc[gi][cc], c2);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int tok_in_stage = 2 * (cls + kWph * u) + half;
+      const int row = tok_in_stage * HG + hh;
+      uint4 vr = make_uint4(0, 0, 0, 0);
+      if (valid[u]) vr = lds128(vst + row * kRowBytes + sub * 16);
+      const uint64_t v0 = widen2<T>(vr.x), v1 = widen2<T>(vr.y), v2 = widen2<T>(vr.z), v3 = widen2<T>(vr.w);
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        const float pg = __shfl_sync(0xffffffffu, pr[u], src_base | (gi << kShift));
+        const uint64_t p2 = pk2(pg, pg);
+        acc[gi][0] = ffma2(p2, v0, acc[gi][0]);
+        acc[gi][1] = ffma2(p2, v1, acc[gi][1]);
+        acc[gi][2] = ffma2(p2, v2, acc[gi][2]);
+        acc[gi][3] = ffma2(p2, v3, acc[gi][3]);
       }
-      m[gi] = mm;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    if (!(flags & kLast)) continue;
+
+    // ---- end of a work item: merge half-warps (and warps), write ----
+    float mh[G], lh[G];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+      const float m_a = __shfl_sync(0xffffffffu, m_own, src_base | (gi << kShift));
+      const float l_a = __shfl_sync(0xffffffffu, l_own, src_base | (gi << kShift));
+      const float m_b = __shfl_xor_sync(0xffffffffu, m_a, 16);
+      const float l_b = __shfl_xor_sync(0xffffffffu, l_a, 16);
+      const float mm = fmaxf(m_a, m_b);
+      const float wa = mm == neg_inf() ? 0.f : ex2(m_a - mm);
+      const float wb = mm == neg_inf() ? 0.f : ex2(m_b - mm);
+      mh[gi] = mm;
+      lh[gi] = l_a * wa + l_b * wb;
+      const uint64_t wa2 = pk2(wa, wa), wb2 = pk2(wb, wb);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, acc[gi][cc], 16);
+        acc[gi][cc] = ffma2(acc[gi][cc], wa2, fmul2(other, wb2));
+      }
+    }
+    if (kWph > 1) {
+      // Warps of the same head meet in shared memory.  The merge barrier is
+      // an mbarrier with a bounded wait, so a warp that gave up earlier
+      // cannot leave the others waiting; buffers alternate between items.
+      const int par = items_done & 1;
+      float* mbuf = merge_buf + par * kConsumerWarps * G * (D + 2);
+      float* mine = mbuf + warp * G * (D + 2);
+      if (half == 0) {
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const float2 f = upk2(acc[gi][cc]);
+            mine[gi * (D + 2) + sub * 8 + 2 * cc] = f.x;
+            mine[gi * (D + 2) + sub * 8 + 2 * cc + 1] = f.y;
+          }
+          if (sub == 0) { mine[gi * (D + 2) + D] = mh[gi]; mine[gi * (D + 2) + D + 1] = lh[gi]; }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&merge_bar[par]));
+      const bool met = mbar_wait(smem_u32(&merge_bar[par]), (items_done >> 1) & 1, abort, p.status);
+      ++items_done;
+      if (!met) break;
+      if (cls == 0) {
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+          float mm = neg_inf();
+          for (int c2 = 0; c2 < kWph; ++c2) mm = fmaxf(mm, mbuf[(hh + HG * c2) * G * (D + 2) + gi * (D + 2) + D]);
+          float ll = 0.f;
+          float o8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o8[e] = 0.f;
+          if (mm != neg_inf()) {
+            for (int c2 = 0; c2 < kWph; ++c2) {
+              const float* src = mbuf + (hh + HG * c2) * G * (D + 2) + gi * (D + 2);
+              const float w = ex2(src[D] - mm);
+              ll += src[D + 1] * w;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o8[e] += src[(sub & 15) * 8 + e] * w;
+            }
+          }
+          mh[gi] = mm;
+          lh[gi] = ll;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) acc[gi][cc] = pk2(o8[2 * cc], o8[2 * cc + 1]);
+        }
+      }
+      if (cls != 0) continue;
     }
     if (half == 0) {
 #pragma unroll
       for (int gi = 0; gi < G; ++gi) {
-        if (sub == 0) { s_m[warp][gi] = m[gi]; s_l[warp][gi] = l[gi]; }
-        *reinterpret_cast<float4*>(&s_acc[warp][gi][sub * 8]) = make_float4(acc[gi][0], acc[gi][1], acc[gi][2], acc[gi][3]);
-        *reinterpret_cast<float4*>(&s_acc[warp][gi][sub * 8 + 4]) = make_float4(acc[gi][4], acc[gi][5], acc[gi][6], acc[gi][7]);
-      }
-    }
-    __syncthreads();
-    // Merge the warps and write the state of this chunk.
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-      const int gi = idx / D, d = idx % D;
-      float mm = neg_inf();
+        const bool has = lh[gi] > 0.f;
+        const float inv = has ? 1.f / lh[gi] : 0.f;
+        float o[8];
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, s_m[w][gi]);
-      float den = 0.f, num = 0.f;
-      if (mm != neg_inf()) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float e = ex2(s_m[w][gi] - mm);
-          den += s_l[w][gi] * e;
-          num += s_acc[w][gi][d] * e;
+        for (int cc = 0; cc < 4; ++cc) {
+          const float2 f = upk2(acc[gi][cc]);
+          o[2 * cc] = f.x * inv;
+          o[2 * cc + 1] = f.y * inv;
+        }
+        const float lse = has ? (mh[gi] + lg2(lh[gi])) * kLn2 : neg_inf();
+        const int hq = kvh * G + gi;
+        if (out_slot >= 0) {
+          float* dst = p.part_o + ((int64_t)out_slot * p.hq + hq) * D + sub * 8;
+          *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
+          if (sub == 0) p.part_lse[(int64_t)out_slot * p.hq + hq] = lse;
+        } else {
+          const int64_t row = (int64_t)req * p.hq + hq;
+          if (p.direct_f32) {
+            float* dst = static_cast<float*>(p.o_direct) + row * D + sub * 8;
+            *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
+          } else {
+            uint4 w;
+            w.x = Elem<T>::from_f2(o[0], o[1]); w.y = Elem<T>::from_f2(o[2], o[3]);
+            w.z = Elem<T>::from_f2(o[4], o[5]); w.w = Elem<T>::from_f2(o[6], o[7]);
+            *reinterpret_cast<uint4*>(static_cast<T*>(p.o_direct) + row * D + sub * 8) = w;
+          }
+          if (sub == 0) p.lse_direct[row] = lse;
         }
       }
-      const float o = den > 0.f ? num / den : 0.f;
-      const float lse = den > 0.f ? (mm + lg2(den)) * kLn2 : neg_inf();
-      const int h = kvh * G + gi;
-      if (it.slot >= 0) {
-        p.part_o[((int64_t)it.slot * p.hq + h) * D + d] = o;
-        if (d == 0) p.part_lse[(int64_t)it.slot * p.hq + h] = lse;
-      } else {
-        const int64_t row = (int64_t)it.req * p.hq + h;
-        if (p.direct_f32) static_cast<float*>(p.o_direct)[row * D + d] = o;
-        else static_cast<T*>(p.o_direct)[row * D + d] = Elem<T>::from_f(o);
-        if (d == 0) p.lse_direct[row] = lse;
-      }
     }
-    __syncthreads();
   }
 }
 
@@ -287,28 +546,45 @@ __global__ void __launch_bounds__(256) contract_kernel(const ContractParams p) {
     suf_kind = 1; suf_n = 1;
   }
   const int n_src = n_pref + suf_n;
-  auto src_lse = [&](int i) -> float {
-    if (i < n_pref) return p.prefix_lse[i * p.prefix_stride_lse + (int64_t)req * p.hq + h];
-    if (suf_kind == 1) return p.suffix_lse[(int64_t)req * p.hq + h];
-    return p.part_lse[(int64_t)(suf_begin + i - n_pref) * p.hq + h];
+  auto src_lse = [&](int i) -> const float* {
+    if (i < n_pref) return p.prefix_lse + i * p.prefix_stride_lse + (int64_t)req * p.hq + h;
+    if (suf_kind == 1) return p.suffix_lse + (int64_t)req * p.hq + h;
+    return p.part_lse + (int64_t)(suf_begin + i - n_pref) * p.hq + h;
   };
   auto src_o = [&](int i) -> const float* {
     if (i < n_pref) return p.prefix_o + i * p.prefix_stride_o + ((int64_t)req * p.hq + h) * D;
     if (suf_kind == 1) return p.suffix_o + ((int64_t)req * p.hq + h) * D;
     return p.part_o + ((int64_t)(suf_begin + i - n_pref) * p.hq + h) * D;
   };
-  float m = neg_inf();
-  for (int i = 0; i < n_src; ++i) m = fmaxf(m, src_lse(i));
+  // Sources go in batches of 8 whose loads are all in flight together; the
+  // running (max, sum, acc) is rescaled between batches.
+  constexpr int kB = 8;
+  float m = neg_inf(), den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  if (m != neg_inf()) {
-    for (int i = 0; i < n_src; ++i) {
-      const float w = ex2((src_lse(i) - m) * kLog2e);
-      const float4 x = *reinterpret_cast<const float4*>(src_o(i) + lane * 4);
-      den += w;
-      acc.x = fmaf(w, x.x, acc.x); acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z); acc.w = fmaf(w, x.w, acc.w);
+  for (int i0 = 0; i0 < n_src; i0 += kB) {
+    float ls[kB];
+    float4 xs[kB];
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const bool in = i0 + k < n_src;
+      ls[k] = in ? *src_lse(i0 + k) : neg_inf();
+      xs[k] = in ? *reinterpret_cast<const float4*>(src_o(i0 + k) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    float mb = m;
+#pragma unroll
+    for (int k = 0; k < kB; ++k) mb = fmaxf(mb, ls[k]);
+    if (mb == neg_inf()) continue;
+    const float c = ex2((m - mb) * kLog2e);  // 0 when m is -inf
+    den *= c;
+    acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const float w = ex2((ls[k] - mb) * kLog2e);  // 0 for empty states
+      den += w;
+      acc.x = fmaf(w, xs[k].x, acc.x); acc.y = fmaf(w, xs[k].y, acc.y);
+      acc.z = fmaf(w, xs[k].z, acc.z); acc.w = fmaf(w, xs[k].w, acc.w);
+    }
+    m = mb;
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
@@ -325,26 +601,63 @@ __global__ void __launch_bounds__(256) contract_kernel(const ContractParams p) {
   if (lane == 0) p.lse[row] = den > 0.f ? m + lg2(den) * kLn2 : neg_inf();
 }
 
-template <typename T>
-int launch_decode_t(const DecodeParams& p, int grid_x, cudaStream_t st) {
-  const dim3 grid(grid_x, p.hkv);
+template <typename T, int G, int HG>
+int launch_decode_g(const DecodeParams& p, int grid_x, const CUtensorMap& mk, const CUtensorMap& mv,
+                    cudaStream_t st) {
+  constexpr int smem = decode_smem_bytes<G, HG>();
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(paged_decode_kernel<T, G, HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr != cudaSuccess) return (int)attr;
+  const dim3 grid(grid_x, p.hkv / HG);  // one block per (planned CTA, head group)
+  paged_decode_kernel<T, G, HG><<<grid, kDecodeThreads, smem, st>>>(mk, mv, p);
+  return (int)cudaGetLastError();
+}
+
+template <typename T, int HG>
+int launch_decode_hg(const DecodeParams& p, int grid_x, const CUtensorMap& mk, const CUtensorMap& mv,
+                     cudaStream_t st) {
   switch (p.hq / p.hkv) {
-    case 1: paged_decode_kernel<T, 1><<<grid, 128, 0, st>>>(p); break;
-    case 2: paged_decode_kernel<T, 2><<<grid, 128, 0, st>>>(p); break;
-    case 4: paged_decode_kernel<T, 4><<<grid, 128, 0, st>>>(p); break;
-    case 8: paged_decode_kernel<T, 8><<<grid, 128, 0, st>>>(p); break;
+    case 1: return launch_decode_g<T, 1, HG>(p, grid_x, mk, mv, st);
+    case 2: return launch_decode_g<T, 2, HG>(p, grid_x, mk, mv, st);
+    case 4: return launch_decode_g<T, 4, HG>(p, grid_x, mk, mv, st);
+    case 8: return launch_decode_g<T, 8, HG>(p, grid_x, mk, mv, st);
     default: return (int)cudaErrorInvalidValue;
   }
-  return (int)cudaGetLastError();
+}
+
+template <typename T>
+int launch_decode_t(const DecodeParams& p, int grid_x, int hg, const CUtensorMap& mk, const CUtensorMap& mv,
+                    cudaStream_t st) {
+  switch (hg) {
+    case 8: return launch_decode_hg<T, 8>(p, grid_x, mk, mv, st);
+    case 4: return launch_decode_hg<T, 4>(p, grid_x, mk, mv, st);
+    case 2: return launch_decode_hg<T, 2>(p, grid_x, mk, mv, st);
+    default: return launch_decode_hg<T, 1>(p, grid_x, mk, mv, st);
+  }
 }
 
 }  // namespace
 
 int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype, void* stream) {
   if (grid_x <= 0) return 0;
+  // KV heads per block: the largest of 8, 4, 2, 1 that divides Hkv.
+  const int hg = p.hkv % 8 == 0 ? 8 : p.hkv % 4 == 0 ? 4 : p.hkv % 2 == 0 ? 2 : 1;
+  const int sl = p.page_size < kMaxSliceRows ? p.page_size : kMaxSliceRows;
+  // 4-D view [num_pages][page_size][Hkv][128]; one tile = sl slots x hg heads of a page.
+  const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.hkv, (uint64_t)p.page_size,
+                            (uint64_t)(p.num_pages > 0 ? p.num_pages : 1)};
+  const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)D * 2 * p.hkv, (uint64_t)D * 2 * p.hkv * p.page_size};
+  const uint32_t box[4] = {(uint32_t)D, (uint32_t)hg, (uint32_t)sl, 1u};
+  alignas(64) CUtensorMap mk, mv;
+  if (!encode_tiled_map(&mk, p.k_cache, dtype, 4, dims, strides, box, false) ||
+      !encode_tiled_map(&mv, p.v_cache, dtype, 4, dims, strides, box, false))
+    return -1;
   cudaStream_t st = (cudaStream_t)stream;
-  return dtype == PKC_F16 ? launch_decode_t<__half>(p, grid_x, st)
-                          : launch_decode_t<__nv_bfloat16>(p, grid_x, st);
+  return dtype == PKC_F16 ? launch_decode_t<__half>(p, grid_x, hg, mk, mv, st)
+                          : launch_decode_t<__nv_bfloat16>(p, grid_x, hg, mk, mv, st);
 }
 
 int launch_contract(const ContractParams& p, int n_rows, void* stream) {

@@ -117,4 +117,10 @@ int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix,
 
 int num_sms();
 
+// Encode a TMA tiled tensor map (a 128-byte CUtensorMap at `map`) over a
+// 16-bit tensor; dims[0] is the contiguous dimension.  Returns false if the
+// driver entry point is unavailable or the encoding is rejected.
+bool encode_tiled_map(void* map, const void* base, int dtype, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
+
 }  // namespace pkc

@@ -22,7 +22,6 @@
 // P_j overwrites K_j's shared memory once S_j is complete.  All waits are
 // bounded (2 s) and set PKC_ERR_TIMEOUT when they run out.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -39,7 +38,7 @@ constexpr int kStages = 3;
 constexpr int kSubTile = 16384;  // 128 rows x 128 bytes (64 elements)
 constexpr int kQBytes = 2 * kSubTile;
 constexpr int kStageBytes = 4 * kSubTile;  // K (2 sub-tiles) + V (2 sub-tiles)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // TMA warp, MMA warp, 8 softmax warps
 constexpr uint32_t kTmemCols = 512;
 
 struct __align__(8) Barriers {
@@ -51,17 +50,26 @@ struct __align__(8) Barriers {
   int abort;
 };
 
-constexpr int kSmemBytes = kQBytes + kStages * kStageBytes + 256 + 1024;
+// Q, the K/V ring, barriers (256 B) and the row-exchange buffer (2 KB).  The
+// base must be 1024-byte aligned for the 128B-swizzled TMA tiles; with no
+// static shared memory it is, and the kernel checks it.
+constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
+constexpr int kXchOffset = kBarOffset + 256;
+constexpr int kSmemBytes = kXchOffset + 2 * 2 * 128 * 4;
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefix_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023) != 0) {  // uniform: no thread has started yet
+    if (threadIdx.x == 0) report(p.status, PKC_ERR_UNSUPPORTED);
+    return;
+  }
   const uint32_t s_q = smem_u32(smem);
   const uint32_t s_stage0 = s_q + kQBytes;
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + kQBytes + kStages * kStageBytes);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + kBarOffset);
+  static_assert(sizeof(Barriers) <= 256, "barrier block");
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -86,10 +94,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(bars->s_full[b]), 1);
-      mbar_init(bar(bars->s_free[b]), 128);
-      mbar_init(bar(bars->p_full[b]), 128);
+      mbar_init(bar(bars->s_free[b]), 256);
+      mbar_init(bar(bars->p_full[b]), 256);
       mbar_init(bar(bars->o_full[b]), 1);
-      mbar_init(bar(bars->o_free[b]), 128);
+      mbar_init(bar(bars->o_free[b]), 256);
     }
     mbar_init(bar(bars->drain), 1);
     bars->abort = 0;
@@ -186,64 +194,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(bars->drain), 0, &no_abort, p.status);
     }
   } else {
-    // ---------------- softmax / correction: one query row per thread ----------------
-    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    // ------- softmax / correction: two threads per query row, 64 columns each -------
+    const int quad = warp & 3;         // TMEM lanes 32*quad .. 32*quad+31
+    const int ch = (warp - 2) >> 2;    // column half: 0 -> 0..63, 1 -> 64..127
     const int row = quad * 32 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-    float o_acc[128];
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16) + ch * 64;
+    float* xch = reinterpret_cast<float*>(smem + kXchOffset);  // [2 parity][2 half][128]
+    float o_acc[64];
 #pragma unroll
-    for (int i = 0; i < 128; ++i) o_acc[i] = 0.f;
+    for (int i = 0; i < 64; ++i) o_acc[i] = 0.f;
     float m_run = neg_inf(), l_run = 0.f, corr_prev = 1.f;
     bool ok = true;
-    auto fold = [&](int jp) {
+    // Every softmax thread reaches every exchange; stopping is decided
+    // together (barrier AND of the threads' wait results), so no thread can
+    // be left waiting at a barrier that the others skipped.
+    auto fold = [&](int jp) -> bool {
       const int bp = jp & 1;
-      if (!mbar_wait(bar(bars->o_full[bp]), (jp >> 1) & 1, abort, p.status)) { ok = false; return; }
+      if (!mbar_wait(bar(bars->o_full[bp]), (jp >> 1) & 1, abort, p.status)) return false;
       tc_fence_after();
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(lane_addr + 256 + bp * 128, r0);  // both loads in flight,
+      tmem_ld_32x32b_x32(lane_addr + 256 + bp * 128 + 32, r1);  // one wait
+      tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(lane_addr + 256 + bp * 128 + c * 32, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o_acc[c * 32 + i] = fmaf(o_acc[c * 32 + i], corr_prev, __uint_as_float(r[i]));
+      for (int i = 0; i < 32; ++i) {
+        o_acc[i] = fmaf(o_acc[i], corr_prev, __uint_as_float(r0[i]));
+        o_acc[32 + i] = fmaf(o_acc[32 + i], corr_prev, __uint_as_float(r1[i]));
       }
       tc_fence_before();
       mbar_arrive(bar(bars->o_free[bp]));
+      return true;
     };
-    for (int j = 0; ok && j < n_tiles; ++j) {
+    for (int j = 0; j < n_tiles; ++j) {
       const int b = j & 1, s = j % kStages;
-      if (!mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status)) { ok = false; break; }
+      bool mine = ok && mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
       tc_fence_after();
-      const int valid = min(kKvTile, kv_hi - (kv_lo + j * kKvTile));
+      const int valid = min(kKvTile, kv_hi - (kv_lo + j * kKvTile)) - ch * 64;  // columns of my half
+      // This thread's 64 scores, loaded once for both passes.
+      uint32_t sr[2][32];
       float mx = neg_inf();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(lane_addr + b * 128 + c * 32, r);
+      if (mine) {
+        tmem_ld_32x32b_x32(lane_addr + b * 128, sr[0]);
+        tmem_ld_32x32b_x32(lane_addr + b * 128 + 32, sr[1]);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(r[i]));
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
       }
+      float* xj = xch + (j & 1) * 256;
+      xj[ch * 128 + row] = mx;
+      if (!bar_and_sync(mine, 256)) { ok = false; break; }
+      mx = fmaxf(mx, xj[(ch ^ 1) * 128 + row]);
       const float m_new = fmaxf(m_run, mx * p.scale_log2);
       const float corr = m_new == neg_inf() ? 1.f : ex2(m_run - m_new);
       l_run *= corr;
-      const uint32_t pbase = s_stage0 + s * kStageBytes;
+      const uint32_t pbase = s_stage0 + s * kStageBytes + ch * kSubTile;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(lane_addr + b * 128 + c * 32, r);
-        tmem_ld_wait();
+      for (int c = 0; c < 2; ++c) {
         float pv[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          pv[i] = c * 32 + i < valid ? ex2(fmaf(__uint_as_float(r[i]), p.scale_log2, -m_new)) : 0.f;
+          pv[i] = c * 32 + i < valid ? ex2(fmaf(__uint_as_float(sr[c][i]), p.scale_log2, -m_new)) : 0.f;
           l_run += pv[i];
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint32_t chunk = (uint32_t)((c & 1) * 4 + k);
-          const uint32_t addr = pbase + (c >> 1) * kSubTile + row * 128 + ((chunk ^ (row & 7)) << 4);
+          const uint32_t chunk = (uint32_t)(c * 4 + k);
+          const uint32_t addr = pbase + row * 128 + ((chunk ^ (row & 7)) << 4);
           const uint32_t w0 = Elem<T>::from_f2(pv[8 * k + 0], pv[8 * k + 1]);
           const uint32_t w1 = Elem<T>::from_f2(pv[8 * k + 2], pv[8 * k + 3]);
           const uint32_t w2 = Elem<T>::from_f2(pv[8 * k + 4], pv[8 * k + 5]);
@@ -257,24 +276,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(bars->p_full[b]));
       mbar_arrive(bar(bars->s_free[b]));
       m_run = m_new;
-      if (j >= 1) fold(j - 1);
+      if (j >= 1) ok = fold(j - 1);
       corr_prev = corr;
     }
-    if (ok && n_tiles > 0) fold(n_tiles - 1);
+    if (ok && n_tiles > 0) ok = fold(n_tiles - 1);
+    // Both halves used the same running maximum: their sums add.  The
+    // exchange uses the parity the last tile did not use.
+    float* xl = xch + (n_tiles & 1) * 256;
+    xl[ch * 128 + row] = l_run;
+    const bool all_ok = bar_and_sync(ok, 256);
+    const float l_tot = l_run + xl[(ch ^ 1) * 128 + row];
 
     // Epilogue: rows that belong to this group write their state.
     const int rb = b0 + row / G;
     if (rb < req_hi && rb < p.batch) {
       const int h = kvh * G + row % G;
       const int64_t r = (int64_t)rb * p.hq + h;
-      float* out = p.out_o + split * p.split_stride_o + r * PKC_HEAD_DIM;
-      const bool has = ok && l_run > 0.f;
-      const float inv = has ? 1.f / l_run : 0.f;
+      float* out = p.out_o + split * p.split_stride_o + r * PKC_HEAD_DIM + ch * 64;
+      const bool has = all_ok && l_tot > 0.f;
+      const float inv = has ? 1.f / l_tot : 0.f;
 #pragma unroll
-      for (int i = 0; i < 128; i += 4)
+      for (int i = 0; i < 64; i += 4)
         *reinterpret_cast<float4*>(out + i) =
             make_float4(o_acc[i] * inv, o_acc[i + 1] * inv, o_acc[i + 2] * inv, o_acc[i + 3] * inv);
-      p.out_lse[split * p.split_stride_lse + r] = has ? (m_run + lg2(l_run)) * kLn2 : neg_inf();
+      if (ch == 0) p.out_lse[split * p.split_stride_lse + r] = has ? (m_run + lg2(l_tot)) * kLn2 : neg_inf();
     }
   }
 
@@ -284,35 +309,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
 // 3-D tiled map over a row-major [d2][d1][d0] tensor of 16-bit elements
 // with a {64, box1, box2} box and 128-byte swizzle (rows of 128 bytes).
 bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d0, uint64_t d1, uint64_t d2,
               uint32_t box1, uint32_t box2) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-  const cuuint32_t box[3] = {64, box1, box2};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType t =
-      dtype == PKC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return enc(m, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const uint32_t box[3] = {64, box1, box2};
+  return encode_tiled_map(m, base, dtype, 3, dims, strides, box, true);
 }
 
 template <typename T>

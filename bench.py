@@ -62,6 +62,25 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max(value, dist, device):
+    """Largest `value` over all ranks (every rank gets it); the value itself
+    when running alone.  Used for the timed region: the job is as slow as its
+    slowest replica."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step, steps, world, elapsed_s):
+    """Whole-job effective throughput: every replica processes the same
+    per-GPU workload (weak scaling), so N replicas move N times the bytes in
+    the slowest replica's time."""
+    return world * bytes_per_step * steps / elapsed_s / 1e9
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -318,11 +337,7 @@ def main():
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
-    elapsed_ms = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=d["q"].device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = reduce_max(start.elapsed_time(end), dist, d["q"].device)
     status = pkc.device_status(ws)
     if status != 0:
         raise RuntimeError(f"device status after timing: {pkc.STATUS_NAMES.get(status, status)}")
@@ -334,7 +349,7 @@ def main():
     }
     eff = workloads.effective_bytes(p)
     ms_per_step = elapsed_ms / K
-    value = world * eff * K / (elapsed_ms / 1e3) / 1e9
+    value = whole_job_gbs(eff, K, world, elapsed_ms / 1e3)
 
     hbm_peak, tf_peak, peak_kind = load_peaks()
     kvb = kv_bytes_per_token(p)
@@ -390,14 +405,10 @@ def main():
         t0 = time.perf_counter()
         for i in range(args.e2e_steps):
             e2e_step(i)
-        t_e2e = time.perf_counter() - t0
-        if dist is not None:
-            t = torch.tensor([t_e2e], device=d["q"].device, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
+        t_e2e = reduce_max(time.perf_counter() - t0, dist, d["q"].device)
         h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4 + words * 4
         d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * 4
-        e2e = {"value": world * eff * args.e2e_steps / t_e2e / 1e9, "unit": "GB/s",
+        e2e = {"value": whole_job_gbs(eff, args.e2e_steps, world, t_e2e), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": 1e3 * t_e2e / args.e2e_steps, "steps": args.e2e_steps}
 

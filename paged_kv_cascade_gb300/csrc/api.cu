@@ -174,6 +174,15 @@ void fill_contract_prefix(ContractParams& c, const PrefixSetup& S) {
   std::memcpy(c.req_indptr, S.pp.req_indptr, sizeof(c.req_indptr));
 }
 
+// Copy the plan-array offsets the contraction kernel needs.
+void contract_plan_offsets(ContractParams& c, const int32_t* plan_host) {
+  if (!plan_host) return;
+  c.off_unit_list = plan_host[PKC_PLAN_OFF_UNIT_LIST];
+  c.off_unit_req = plan_host[PKC_PLAN_OFF_UNIT_REQ];
+  c.off_unit_n_chunks = plan_host[PKC_PLAN_OFF_UNIT_N_CHUNKS];
+  c.off_unit_partial_begin = plan_host[PKC_PLAN_OFF_UNIT_PARTIAL_BEGIN];
+}
+
 }  // namespace
 
 extern "C" {
@@ -302,6 +311,7 @@ int pkc_paged_decode_state(const void* q, const void* k_cache, const void* v_cac
     ContractParams cp;
     std::memset(&cp, 0, sizeof(cp));
     cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractPlanUnits; cp.plan = dp.plan;
+    contract_plan_offsets(cp, plan_host);
     cp.part_o = dp.part_o; cp.part_lse = dp.part_lse;
     cp.o = o; cp.lse = lse; cp.out_dtype = dtype; cp.status = status;
     e = launch_contract(cp, batch, stream);
@@ -397,6 +407,7 @@ int pkc_cascade_decode(const void* q, const void* k_prefix, const void* v_prefix
   ContractParams cp;
   std::memset(&cp, 0, sizeof(cp));
   cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractAllRequests; cp.plan = dp.plan;
+  contract_plan_offsets(cp, plan_host);
   cp.suffix_o = reinterpret_cast<const float*>(dp.o_direct); cp.suffix_lse = dp.lse_direct;
   cp.part_o = dp.part_o; cp.part_lse = dp.part_lse;
   fill_contract_prefix(cp, S);

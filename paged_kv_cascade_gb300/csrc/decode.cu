@@ -522,13 +522,15 @@ __global__ void __launch_bounds__(256) contract_kernel(const ContractParams p) {
   const int64_t row_idx = gw / p.hq;
   const int h = (int)(gw % p.hq);
   const int32_t* pl = p.plan;
-  int64_t n_rows = p.batch;
-  if (p.mode == kContractPlanUnits) n_rows = pl[PKC_PLAN_N_SPLIT] + pl[PKC_PLAN_N_EMPTY];
+  // The list length changes with the lengths every step: read it from the
+  // device plan (the array offsets depend only on batch and CTA count).
+  const int64_t n_rows =
+      p.mode == kContractPlanUnits ? (int64_t)pl[PKC_PLAN_N_SPLIT] + pl[PKC_PLAN_N_EMPTY] : p.batch;
   if (row_idx >= n_rows) return;
   int req = (int)row_idx, unit = (int)row_idx;
   if (p.mode == kContractPlanUnits) {
-    unit = pl[pl[PKC_PLAN_OFF_UNIT_LIST] + row_idx];
-    req = pl[pl[PKC_PLAN_OFF_UNIT_REQ] + unit];
+    unit = pl[p.off_unit_list + row_idx];
+    req = pl[p.off_unit_req + unit];
   }
   // Sources: prefix splits of the request's group, then the suffix.
   int group = -1;
@@ -539,8 +541,9 @@ __global__ void __launch_bounds__(256) contract_kernel(const ContractParams p) {
   int n_pref = group >= 0 ? p.prefix_splits : 0;
   int suf_kind = 0, suf_begin = 0, suf_n = 0;  // 1: direct state, 2: partial slots
   if (pl) {
-    const int nch = pl[pl[PKC_PLAN_OFF_UNIT_N_CHUNKS] + unit];
-    if (nch >= 2) { suf_kind = 2; suf_begin = pl[pl[PKC_PLAN_OFF_UNIT_PARTIAL_BEGIN] + unit]; suf_n = nch; }
+    const int nch = pl[p.off_unit_n_chunks + unit];       // both loads in flight together
+    const int pbeg = pl[p.off_unit_partial_begin + unit];
+    if (nch >= 2) { suf_kind = 2; suf_begin = pbeg; suf_n = nch; }
     else if (nch == 1 && p.suffix_o) { suf_kind = 1; suf_n = 1; }
   } else if (p.suffix_o) {
     suf_kind = 1; suf_n = 1;

@@ -68,6 +68,9 @@ struct ContractParams {
   int batch, hq;
   int mode;
   const int32_t* plan;      // device plan or nullptr
+  // Word offsets of the plan arrays, copied from the host plan (they depend
+  // only on batch and CTA count) so the kernel's first loads are the arrays.
+  int32_t off_unit_list, off_unit_req, off_unit_n_chunks, off_unit_partial_begin;
   const float* suffix_o;    // direct suffix states or nullptr (no suffix)
   const float* suffix_lse;
   const float* part_o;

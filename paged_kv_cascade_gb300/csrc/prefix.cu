@@ -237,11 +237,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(lane_addr + b * 128, sr[0]);
         tmem_ld_32x32b_x32(lane_addr + b * 128 + 32, sr[1]);
         tmem_ld_wait();
+        // 8 independent partial maxima, then a tree: no 64-long chain.
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = neg_inf();
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+            if (c * 32 + i < valid) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sr[c][i]));
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
       float* xj = xch + (j & 1) * 256;
       xj[ch * 128 + row] = mx;
@@ -251,26 +256,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float corr = m_new == neg_inf() ? 1.f : ex2(m_run - m_new);
       l_run *= corr;
       const uint32_t pbase = s_stage0 + s * kStageBytes + ch * kSubTile;
+      float l8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) l8[k] = 0.f;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        float pv[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          pv[i] = c * 32 + i < valid ? ex2(fmaf(__uint_as_float(sr[c][i]), p.scale_log2, -m_new)) : 0.f;
-          l_run += pv[i];
-        }
+        for (int k = 0; k < 4; ++k) {  // 8 probabilities -> one 16-byte chunk of P
+          float pv[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+          for (int e = 0; e < 8; ++e) {
+            const int i = 8 * k + e;
+            pv[e] = c * 32 + i < valid ? ex2(fmaf(__uint_as_float(sr[c][i]), p.scale_log2, -m_new)) : 0.f;
+            l8[e] += pv[e];
+          }
           const uint32_t chunk = (uint32_t)(c * 4 + k);
           const uint32_t addr = pbase + row * 128 + ((chunk ^ (row & 7)) << 4);
-          const uint32_t w0 = Elem<T>::from_f2(pv[8 * k + 0], pv[8 * k + 1]);
-          const uint32_t w1 = Elem<T>::from_f2(pv[8 * k + 2], pv[8 * k + 3]);
-          const uint32_t w2 = Elem<T>::from_f2(pv[8 * k + 4], pv[8 * k + 5]);
-          const uint32_t w3 = Elem<T>::from_f2(pv[8 * k + 6], pv[8 * k + 7]);
+          const uint32_t w0 = Elem<T>::from_f2(pv[0], pv[1]);
+          const uint32_t w1 = Elem<T>::from_f2(pv[2], pv[3]);
+          const uint32_t w2 = Elem<T>::from_f2(pv[4], pv[5]);
+          const uint32_t w3 = Elem<T>::from_f2(pv[6], pv[7]);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
                        : "memory");
         }
       }
+      l_run += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(bars->p_full[b]));

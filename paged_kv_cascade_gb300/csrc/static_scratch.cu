@@ -135,6 +135,10 @@ extern "C" int pkc_paged_decode_state_noalloc(
     ContractParams cp;
     std::memset(&cp, 0, sizeof(cp));
     cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractPlanUnits; cp.plan = dp.plan;
+    cp.off_unit_list = plan_host[PKC_PLAN_OFF_UNIT_LIST];
+    cp.off_unit_req = plan_host[PKC_PLAN_OFF_UNIT_REQ];
+    cp.off_unit_n_chunks = plan_host[PKC_PLAN_OFF_UNIT_N_CHUNKS];
+    cp.off_unit_partial_begin = plan_host[PKC_PLAN_OFF_UNIT_PARTIAL_BEGIN];
     cp.part_o = dp.part_o; cp.part_lse = dp.part_lse;
     cp.o = o; cp.lse = lse; cp.out_dtype = dtype; cp.status = dp.status;
     le = launch_contract(cp, batch, stream);

@@ -122,3 +122,32 @@ def test_gqa_cascade_lb_workload_sampled():
     rows = np.unique(np.concatenate([rows, np.array(extra, np.int32)]), axis=0)
     ref_o, ref_lse = oracle.attention_rows(p["q"], rows=rows, **oracle_args(p))
     compare(o, lse, ref_o, ref_lse, rows=rows)
+
+
+def test_workspace_reused_across_calls_and_problems():
+    # The split-request arrival counters live in the workspace and must be
+    # back at zero after every call: run three different problems through
+    # one workspace, each checked against the oracle.
+    probs = [
+        workloads.make_problem(batch=9, hq=16, hkv=4, d=128, dtype="bf16", prefix_lens=[300],
+                               prefix_groups=[9], suffix=("list", [700, 0, 5, 1300, 64, 65, 2, 900, 33]),
+                               page_size=16, seed=61, poison=True),
+        workloads.make_problem(batch=5, hq=32, hkv=8, d=128, dtype="bf16", prefix_lens=[128, 256],
+                               prefix_groups=[2, 3], suffix=("list", [4000, 3, 0, 2500, 17]),
+                               page_size=16, seed=62, poison=True),
+    ]
+    B, Hq = 9, 32
+    ws = torch.empty(pkc.workspace_size(B, Hq, 11, 64), dtype=torch.uint8, device="cuda")
+    pkc.workspace_init(ws)
+    for p in probs + [probs[0]]:
+        d = to_device(p)
+        plan_buf = pkc.plan(p["cache_seqlens"], 11)
+        pkc.plan_upload(plan_buf, ws)
+        o, lse = pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
+                                    p["prefix_req_indptr"], d["k_cache"], d["v_cache"],
+                                    d["block_table"], d["cache_seqlens"], p["sm_scale"], ws,
+                                    plan_buf=plan_buf)
+        torch.cuda.synchronize()
+        assert pkc.device_status(ws) == pkc.PKC_OK
+        ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
+        compare(o, lse, ref_o, ref_lse)

@@ -205,9 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 64; ++i) o_acc[i] = 0.f;
     float m_run = neg_inf(), l_run = 0.f, corr_prev = 1.f;
     bool ok = true;
-    // Every softmax thread reaches every exchange; stopping is decided
-    // together (barrier AND of the threads' wait results), so no thread can
-    // be left waiting at a barrier that the others skipped.
+    // Each of a row's two threads reads the whole row of S for the maximum,
+    // so the softmax warps never wait for each other inside the loop; they
+    // meet once, after it, to add their halves' sums.
     auto fold = [&](int jp) -> bool {
       const int bp = jp & 1;
       if (!mbar_wait(bar(bars->o_full[bp]), (jp >> 1) & 1, abort, p.status)) return false;
@@ -230,28 +230,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool mine = ok && mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
       tc_fence_after();
       const int valid = min(kKvTile, kv_hi - (kv_lo + j * kKvTile)) - ch * 64;  // columns of my half
-      // This thread's 64 scores, loaded once for both passes.
+      // This thread's 64 scores, loaded once for both passes, and the row
+      // maximum over all 128 columns: both threads of a row read the other
+      // half too and reach the same maximum without meeting at a barrier.
       uint32_t sr[2][32];
       float mx = neg_inf();
+      const int vrow = min(kKvTile, kv_hi - (kv_lo + j * kKvTile));  // valid columns of the row
       if (mine) {
         tmem_ld_32x32b_x32(lane_addr + b * 128, sr[0]);
         tmem_ld_32x32b_x32(lane_addr + b * 128 + 32, sr[1]);
         tmem_ld_wait();
-        // 8 independent partial maxima, then a tree: no 64-long chain.
         float m8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) m8[k] = neg_inf();
+        // max over n consecutive scores starting at row column col0
+        auto fold_max = [&](const uint32_t* v, int n, int col0) {
+          if (col0 + n <= vrow) {  // all valid: three-input max, no per-element test
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+            for (int k = 0; k < n / 2; ++k)
+              m8[k & 7] = max3(m8[k & 7], __uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < valid) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sr[c][i]));
-        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int i = 0; i < n; ++i)
+              if (col0 + i < vrow) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(v[i]));
+          }
+        };
+        fold_max(sr[0], 32, ch * 64);
+        fold_max(sr[1], 32, ch * 64 + 32);
+        const uint32_t other = tmem + ((uint32_t)(quad * 32) << 16) + (ch ^ 1) * 64 + b * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // the other half, 16 columns at a time
+          uint32_t ov[16];
+          tmem_ld_32x32b_x16(other + c * 16, ov);
+          tmem_ld_wait();
+          fold_max(ov, 16, (ch ^ 1) * 64 + c * 16);
+        }
+        mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       }
-      float* xj = xch + (j & 1) * 256;
-      xj[ch * 128 + row] = mx;
-      if (!bar_and_sync(mine, 256)) { ok = false; break; }
-      mx = fmaxf(mx, xj[(ch ^ 1) * 128 + row]);
+      // No barrier between the softmax warps inside the loop: a failed wait
+      // sets the block's abort flag, every later wait then returns at once,
+      // and all threads still meet at the one barrier after the loop.
+      if (!mine) { ok = false; break; }
       const float m_new = fmaxf(m_run, mx * p.scale_log2);
       const float corr = m_new == neg_inf() ? 1.f : ex2(m_run - m_new);
       l_run *= corr;

@@ -44,7 +44,11 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["pkc", "reference"], default="pkc")
     ap.add_argument("--workload", default="gqa_cascade_lb",
-                    choices=["gqa_cascade_lb", "cascade_long_prompt", "tiny_cascade"])
+                    choices=["gqa_cascade_lb", "cascade_long_prompt", "tiny_cascade",
+                             "paged_decode", "merge"],
+                    help="cascade workloads time the whole step; 'paged_decode' times the "
+                         "non-cascade decode and 'merge' the binary / 16-ary merge kernels "
+                         "(auxiliary lines)")
     ap.add_argument("--batch", type=int, default=None,
                     help="keep only the first N requests (and their prefix groups); "
                          "a smaller case of the same workload, for profiling")
@@ -259,10 +263,86 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def time_region(torch, fn, steps, warmup):
+    """Mean ms of fn() over `steps` launches, CUDA events on the current stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_aux(args):
+    """Auxiliary single-kernel lines: merge kernels, non-cascade decode."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cascade_gb300 as pkc
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from pkc_testing import dev, to_device
+    hbm_peak, _, peak_kind = load_peaks()
+    K, W = max(args.steps, 3), max(args.warmup, 3)
+    if args.workload == "merge":
+        w = workloads.workload("merge")
+        va, sa, vb, sb = dev(w["v_a"]), dev(w["s_a"]), dev(w["v_b"]), dev(w["s_b"])
+        vn, sn = dev(w["v_n"]), dev(w["s_n"])
+        vo, so = torch.empty_like(va), torch.empty_like(sa)
+        T, H, D = va.shape
+        n = vn.shape[1]
+        ms2 = time_region(torch, lambda: pkc.merge_state(va, sa, vb, sb, vo, so), K, W)
+        msn = time_region(torch, lambda: pkc.merge_states(vn, sn, vo, so), K, W)
+        b2 = 3 * T * H * (D + 1) * 4       # read 2 states, write 1
+        bn = (n + 1) * T * H * (D + 1) * 4  # read n states, write 1
+        line = {"metric": "merge_state effective HBM throughput", "unit": "GB/s",
+                "value": b2 / (ms2 / 1e3) / 1e9, "us": 1e3 * ms2, "bytes": b2,
+                "frac": b2 / (ms2 / 1e3) / 1e9 / hbm_peak,
+                "n_ary": {"n": n, "value": bn / (msn / 1e3) / 1e9, "us": 1e3 * msn, "bytes": bn,
+                          "frac": bn / (msn / 1e3) / 1e9 / hbm_peak},
+                "peak": hbm_peak, "peak_source": f"{peak_kind} hbm_gbs", "steps": K, "warmup": W,
+                "dtype": "f32", "data": "synthetic",
+                "config": {"workload": "merge", "tokens": T, "heads": H, "head_dim": D,
+                           "l2": "inputs larger than L2 (203 MB / 1.15 GB)"}}
+    else:  # paged_decode: non-cascade decode through the plan
+        cfg = workload_cfg("paged_decode")
+        p = workloads.make_problem(**cfg)
+        d = to_device(p)
+        B, Hq, D = p["q"].shape
+        C = cfg["num_ctas"]
+        ws = torch.empty(pkc.workspace_size(B, Hq, C, 0), dtype=torch.uint8, device="cuda")
+        pkc.workspace_init(ws)
+        buf = pkc.plan(p["cache_seqlens"], C)
+        pkc.plan_upload(buf, ws)
+        o = torch.empty_like(d["q"])
+        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        ms = time_region(torch, lambda: pkc.paged_decode_state(
+            d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"],
+            p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse), K, W)
+        if pkc.device_status(ws) != 0:
+            raise RuntimeError("device status not OK")
+        eff = workloads.effective_bytes(p)
+        line = {"metric": "paged decode (non-cascade) effective KV throughput", "unit": "GB/s",
+                "value": eff / (ms / 1e3) / 1e9, "us": 1e3 * ms, "bytes": eff,
+                "frac": eff / (ms / 1e3) / 1e9 / hbm_peak, "peak": hbm_peak,
+                "peak_source": f"{peak_kind} hbm_gbs", "steps": K, "warmup": W,
+                "dtype": cfg["dtype"], "data": "synthetic",
+                "config": {"workload": "paged_decode", "batch": B, "num_qo_heads": Hq,
+                           "kv_tokens": int(p["cache_seqlens"].sum()), "num_ctas": C,
+                           "launches": "decode + contraction"}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload in ("merge", "paged_decode"):
+        run_aux(args)
         return
     import torch
     rank, world, local = dist_env()
@@ -336,7 +416,6 @@ def main():
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    clocks = sampler.stop()
     elapsed_ms = reduce_max(start.elapsed_time(end), dist, d["q"].device)
     status = pkc.device_status(ws)
     if status != 0:
@@ -348,8 +427,7 @@ def main():
         "contraction": statistics.mean(e[2].elapsed_time(e[3]) for e in ev),
     }
     eff = workloads.effective_bytes(p)
-    ms_per_step = elapsed_ms / K
-    value = whole_job_gbs(eff, K, world, elapsed_ms / 1e3)
+    direct_ms_per_step = elapsed_ms / K
 
     hbm_peak, tf_peak, peak_kind = load_peaks()
     kvb = kv_bytes_per_token(p)
@@ -369,6 +447,72 @@ def main():
     rows_per_prefix = np.diff(p["prefix_req_indptr"]) * (Hq // p["num_kv_heads"])
     prefix_flops = float(4 * D * np.sum(rows_per_prefix * np.diff(p["prefix_kv_indptr"])) *
                          p["num_kv_heads"])
+
+    # ---- the same step with the device work replayed from a CUDA graph ----
+    # The plan still runs on the host and is uploaded every step (outside the
+    # graph); the captured cascade call reads it from the workspace.
+    graph = None
+    try:
+        gstream = torch.cuda.Stream()
+        gplan = [torch.empty(words, dtype=torch.int32).pin_memory() for _ in range(2)]
+        gplan_np = [t.numpy() for t in gplan]
+        gdone = [torch.cuda.Event(), torch.cuda.Event()]
+        gbuf = pkc.plan(lens, num_ctas, alpha=cfg["alpha"], beta=cfg["beta"], out=gplan_np[0])
+
+        def g_run():
+            pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
+                               p["prefix_req_indptr"], d["k_cache"], d["v_cache"],
+                               d["block_table"], d["cache_seqlens"], p["sm_scale"], ws,
+                               plan_buf=gbuf, o=o, lse=lse, stream=gstream)
+
+        with torch.cuda.stream(gstream):
+            pkc.plan_upload(gbuf, ws, stream=gstream)
+            g_run()
+            gstream.synchronize()
+            cg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(cg, stream=gstream):
+                g_run()
+
+            def g_step(i):
+                gdone[i & 1].synchronize()
+                b = pkc.plan(lens, num_ctas, alpha=cfg["alpha"], beta=cfg["beta"],
+                             out=gplan_np[i & 1])
+                pkc.plan_upload(b, ws, stream=gstream)
+                gdone[i & 1].record(gstream)
+                cg.replay()
+
+            for i in range(max(3, args.warmup)):
+                g_step(i)
+            gstream.synchronize()
+            if dist is not None:
+                dist.barrier()
+            ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ga.record(gstream)
+            for i in range(K):
+                g_step(i)
+            gb.record(gstream)
+            gstream.synchronize()
+            if dist is not None:
+                dist.barrier()
+        g_ms = reduce_max(ga.elapsed_time(gb), dist, d["q"].device)
+        graph = {"value": whole_job_gbs(eff, K, world, g_ms / 1e3), "unit": "GB/s",
+                 "us_per_step": 1e3 * g_ms / K,
+                 "note": "host plan + upload each step, device work replayed from one CUDA graph"}
+        if pkc.device_status(ws) != 0:
+            raise RuntimeError("device status after graph replay")
+    except RuntimeError:
+        raise
+    except Exception as exc:  # graph capture unavailable: report why
+        graph = {"unavailable": str(exc)[:200]}
+    clocks = sampler.stop()
+    # Headline: the graph-replayed step (how the pages run it: plan per step
+    # on the CPU, the captured run replayed); the directly launched,
+    # event-instrumented run gives the per-stage times.
+    if graph and "us_per_step" in graph:
+        mode, ms_per_step = "cuda_graph", graph["us_per_step"] / 1e3
+    else:
+        mode, ms_per_step = "direct", direct_ms_per_step
+    value = whole_job_gbs(eff, 1, world, ms_per_step / 1e3)
 
     # ---- e2e through host buffers ----
     e2e = None
@@ -433,7 +577,8 @@ def main():
                        "suffix_tokens": suffix_tokens, "num_ctas": num_ctas,
                        "effective_bytes_per_step": eff,
                        "l2": "inputs larger than L2 (one step reads %.2f GB)" % (eff / 1e9),
-                       "parallelism": f"replicas x{world}"},
+                       "launch": mode, "parallelism": f"replicas x{world}"},
+            "direct_us_per_step": 1e3 * direct_ms_per_step,
             "hbm_fraction": value / world / hbm_peak,
             "stages_us": {k: 1e3 * v for k, v in stage_ms.items()},
             "host_plan_us": 1e6 * statistics.mean(host_plan_s) if host_plan_s else None,
@@ -447,6 +592,7 @@ def main():
                               "peak_tflops": tf_peak, "peak_source": f"{peak_kind} bf16_tflops"},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "graph": graph,
             "gpu_launches": 3 * K,
             "clocks": clocks,
         }

@@ -12,15 +12,18 @@
 //
 // Per 128-token KV tile j (FlashAttention-style online softmax, blog
 // section "Recursive Attention"):
-//   S_j = Q K_j^T            tcgen05.mma, M=N=128, K=128, fp32 in TMEM
-//   P_j = exp2(S_j*c - m_j)  softmax warps: TMEM -> registers -> smem (16b)
-//   O_j = P_j V_j            tcgen05.mma, P K-major, V MN-major, into TMEM
-//   O  <- O * exp2(m_{j-1} - m_j) + O_j   in registers of the row's thread
+//   S_j = Q K_j^T              tcgen05.mma, M=N=128, K=128, fp32 in TMEM
+//   P_j = exp2(S_j*c - m_ref)  softmax warps: TMEM -> registers -> smem (16b)
+//   O  += P_j V_j              tcgen05.mma, P K-major, V MN-major, O in TMEM
+// m_ref is a per-row reference maximum.  It changes only when a tile's row
+// maximum exceeds it by more than 2^8 (P stays <= 256); then the row's O
+// columns are rescaled in TMEM before the next P.V.  With a stable maximum
+// nothing touches O until the end.
 // Roles: warp 0 issues TMA loads (Q once, K/V into a 3-stage ring), warp 1
-// allocates TMEM and issues MMAs, warps 2..5 own one query row per thread.
-// TMEM: S double buffer (2 x 128 columns) + O double buffer (2 x 128).
-// P_j overwrites K_j's shared memory once S_j is complete.  All waits are
-// bounded (2 s) and set PKC_ERR_TIMEOUT when they run out.
+// allocates TMEM and issues MMAs, warps 2..9 own query rows, two threads
+// per row (64 columns each).  TMEM: S double buffer (2 x 128 columns) + O
+// (128).  P_j overwrites K_j's shared memory once S_j is complete.  All
+// waits are bounded (2 s) and set PKC_ERR_TIMEOUT when they run out.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,18 +47,18 @@ constexpr uint32_t kTmemCols = 512;
 struct __align__(8) Barriers {
   uint64_t q_full;
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2];
+  uint64_t s_full[2], s_free[2], p_full[2], o_full;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
-// Q, the K/V ring, barriers (256 B) and the row-exchange buffer (2 KB).  The
+// Q, the K/V ring, barriers (256 B) and the row-exchange buffer (1 KB).  The
 // base must be 1024-byte aligned for the 128B-swizzled TMA tiles; with no
 // static shared memory it is, and the kernel checks it.
 constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
 constexpr int kXchOffset = kBarOffset + 256;
-constexpr int kSmemBytes = kXchOffset + 2 * 2 * 128 * 4;
+constexpr int kSmemBytes = kXchOffset + 2 * 128 * 4;
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -96,9 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(bars->s_full[b]), 1);
       mbar_init(bar(bars->s_free[b]), 256);
       mbar_init(bar(bars->p_full[b]), 256);
-      mbar_init(bar(bars->o_full[b]), 1);
-      mbar_init(bar(bars->o_free[b]), 256);
     }
+    mbar_init(bar(bars->o_full), 1);
     mbar_init(bar(bars->drain), 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -172,19 +174,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (j >= 1) {
           const int jp = j - 1, sp = jp % kStages, bp = jp & 1;
-          ok = mbar_wait(bar(bars->p_full[bp]), (jp >> 1) & 1, abort, p.status) &&
-               mbar_wait(bar(bars->o_free[bp]), ((jp >> 1) & 1) ^ 1, abort, p.status);
+          ok = mbar_wait(bar(bars->p_full[bp]), (jp >> 1) & 1, abort, p.status);
           if (!ok) break;
           tc_fence_after();
           const uint32_t pb = s_stage0 + sp * kStageBytes;  // P overwrote K
           const uint32_t vb = pb + 2 * kSubTile;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < 8; ++kk) {  // O accumulates over the tiles
             const uint32_t a_off = (kk >> 2) * kSubTile + (kk & 3) * 32;
-            tc_mma_f16(tmem + 256 + bp * 128, smem_desc_sw128(pb + a_off, 16, 1024),
-                       smem_desc_sw128(vb + kk * 2048, kSubTile, 1024), idesc_pv, kk > 0);
+            tc_mma_f16(tmem + 256, smem_desc_sw128(pb + a_off, 16, 1024),
+                       smem_desc_sw128(vb + kk * 2048, kSubTile, 1024), idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(bar(bars->o_full[bp]));
+          tc_commit(bar(bars->o_full));
           tc_commit(bar(bars->kv_empty[sp]));
         }
       }
@@ -194,86 +195,85 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(bars->drain), 0, &no_abort, p.status);
     }
   } else {
-    // ------- softmax / correction: two threads per query row, 64 columns each -------
+    // ------- softmax: two threads per query row, 64 columns each -------
     const int quad = warp & 3;         // TMEM lanes 32*quad .. 32*quad+31
     const int ch = (warp - 2) >> 2;    // column half: 0 -> 0..63, 1 -> 64..127
     const int row = quad * 32 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16) + ch * 64;
-    float* xch = reinterpret_cast<float*>(smem + kXchOffset);  // [2 parity][2 half][128]
-    float o_acc[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) o_acc[i] = 0.f;
-    float m_run = neg_inf(), l_run = 0.f, corr_prev = 1.f;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t mine_cols = lane_base + ch * 64;         // this thread's columns
+    const uint32_t other_cols = lane_base + (ch ^ 1) * 64;  // the row partner's
+    float* xch = reinterpret_cast<float*>(smem + kXchOffset);  // [2 half][128]
+    constexpr float kRescaleLog2 = 8.f;  // move m_ref only when the max grows by > 2^8
+    float m_ref = neg_inf(), l_run = 0.f;
     bool ok = true;
     // Each of a row's two threads reads the whole row of S for the maximum,
-    // so the softmax warps never wait for each other inside the loop; they
-    // meet once, after it, to add their halves' sums.
-    auto fold = [&](int jp) -> bool {
-      const int bp = jp & 1;
-      if (!mbar_wait(bar(bars->o_full[bp]), (jp >> 1) & 1, abort, p.status)) return false;
-      tc_fence_after();
-      uint32_t r0[32], r1[32];
-      tmem_ld_32x32b_x32(lane_addr + 256 + bp * 128, r0);  // both loads in flight,
-      tmem_ld_32x32b_x32(lane_addr + 256 + bp * 128 + 32, r1);  // one wait
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        o_acc[i] = fmaf(o_acc[i], corr_prev, __uint_as_float(r0[i]));
-        o_acc[32 + i] = fmaf(o_acc[32 + i], corr_prev, __uint_as_float(r1[i]));
-      }
-      tc_fence_before();
-      mbar_arrive(bar(bars->o_free[bp]));
-      return true;
-    };
+    // so both reach the same m_ref and the softmax warps never wait for each
+    // other inside the loop.  Decisions that guard warp-collective TMEM
+    // accesses are made warp-uniform (__all_sync / __any_sync); warp w and
+    // warp w+4 hold the same rows and reach the same decisions.
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j & 1, s = j % kStages;
-      bool mine = ok && mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
+      const bool got = mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
+      if (!__all_sync(0xffffffffu, ok && got)) { ok = false; break; }
       tc_fence_after();
-      const int valid = min(kKvTile, kv_hi - (kv_lo + j * kKvTile)) - ch * 64;  // columns of my half
-      // This thread's 64 scores, loaded once for both passes, and the row
-      // maximum over all 128 columns: both threads of a row read the other
-      // half too and reach the same maximum without meeting at a barrier.
-      uint32_t sr[2][32];
-      float mx = neg_inf();
       const int vrow = min(kKvTile, kv_hi - (kv_lo + j * kKvTile));  // valid columns of the row
-      if (mine) {
-        tmem_ld_32x32b_x32(lane_addr + b * 128, sr[0]);
-        tmem_ld_32x32b_x32(lane_addr + b * 128 + 32, sr[1]);
+      const int valid = vrow - ch * 64;                                  // of my half
+      uint32_t sr[2][32];
+      float mx;
+      {
+        uint32_t ov[32];  // the partner's half, 32 columns at a time
+        tmem_ld_32x32b_x32(mine_cols + b * 128, sr[0]);
+        tmem_ld_32x32b_x32(mine_cols + b * 128 + 32, sr[1]);
+        tmem_ld_32x32b_x32(other_cols + b * 128, ov);
         tmem_ld_wait();
         float m8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) m8[k] = neg_inf();
-        // max over n consecutive scores starting at row column col0
-        auto fold_max = [&](const uint32_t* v, int n, int col0) {
-          if (col0 + n <= vrow) {  // all valid: three-input max, no per-element test
+        // max over 32 consecutive scores starting at row column col0
+        auto fold_max = [&](const uint32_t (&v)[32], int col0) {
+          if (col0 + 32 <= vrow) {  // all valid: three-input max, no per-element test
 #pragma unroll
-            for (int k = 0; k < n / 2; ++k)
+            for (int k = 0; k < 16; ++k)
               m8[k & 7] = max3(m8[k & 7], __uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
           } else {
 #pragma unroll
-            for (int i = 0; i < n; ++i)
+            for (int i = 0; i < 32; ++i)
               if (col0 + i < vrow) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(v[i]));
           }
         };
-        fold_max(sr[0], 32, ch * 64);
-        fold_max(sr[1], 32, ch * 64 + 32);
-        const uint32_t other = tmem + ((uint32_t)(quad * 32) << 16) + (ch ^ 1) * 64 + b * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {  // the other half, 16 columns at a time
-          uint32_t ov[16];
-          tmem_ld_32x32b_x16(other + c * 16, ov);
-          tmem_ld_wait();
-          fold_max(ov, 16, (ch ^ 1) * 64 + c * 16);
-        }
+        fold_max(sr[0], ch * 64);
+        fold_max(sr[1], ch * 64 + 32);
+        fold_max(ov, (ch ^ 1) * 64);
+        tmem_ld_32x32b_x32(other_cols + b * 128 + 32, ov);
+        tmem_ld_wait();
+        fold_max(ov, (ch ^ 1) * 64 + 32);
         mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       }
-      // No barrier between the softmax warps inside the loop: a failed wait
-      // sets the block's abort flag, every later wait then returns at once,
-      // and all threads still meet at the one barrier after the loop.
-      if (!mine) { ok = false; break; }
-      const float m_new = fmaxf(m_run, mx * p.scale_log2);
-      const float corr = m_new == neg_inf() ? 1.f : ex2(m_run - m_new);
-      l_run *= corr;
+      const float m_tile = mx * p.scale_log2;
+      if (__any_sync(0xffffffffu, m_tile > m_ref + kRescaleLog2)) {
+        const float m_new = fmaxf(m_ref, m_tile);
+        const float r = ex2(m_ref - m_new);  // 0 while m_ref is -inf, 1 if unchanged
+        l_run *= r;
+        if (j > 0) {
+          // O holds P.V of tiles < j: wait for the last of them (the S_j
+          // commit already covered tile j-2), rescale my columns in TMEM.
+          const bool done = mbar_wait(bar(bars->o_full), (j - 1) & 1, abort, p.status);
+          if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t o[2][32];
+          tmem_ld_32x32b_x32(mine_cols + 256, o[0]);
+          tmem_ld_32x32b_x32(mine_cols + 256 + 32, o[1]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[c][i] = __float_as_uint(__uint_as_float(o[c][i]) * r);
+          tmem_st_32x32b_x32(mine_cols + 256, o[0]);
+          tmem_st_32x32b_x32(mine_cols + 256 + 32, o[1]);
+          tmem_st_wait();
+        }
+        m_ref = m_new;
+      }
       const uint32_t pbase = s_stage0 + s * kStageBytes + ch * kSubTile;
       float l8[8];
 #pragma unroll
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int i = 8 * k + e;
-            pv[e] = c * 32 + i < valid ? ex2(fmaf(__uint_as_float(sr[c][i]), p.scale_log2, -m_new)) : 0.f;
+            pv[e] = c * 32 + i < valid ? ex2(fmaf(__uint_as_float(sr[c][i]), p.scale_log2, -m_ref)) : 0.f;
             l8[e] += pv[e];
           }
           const uint32_t chunk = (uint32_t)(c * 4 + k);
@@ -304,17 +304,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(bars->p_full[b]));
       mbar_arrive(bar(bars->s_free[b]));
-      m_run = m_new;
-      if (j >= 1) ok = fold(j - 1);
-      corr_prev = corr;
     }
-    if (ok && n_tiles > 0) ok = fold(n_tiles - 1);
-    // Both halves used the same running maximum: their sums add.  The
-    // exchange uses the parity the last tile did not use.
-    float* xl = xch + (n_tiles & 1) * 256;
-    xl[ch * 128 + row] = l_run;
+    // O is final once every MMA has completed (the MMA warp's drain barrier).
+    if (n_tiles > 0) {
+      const bool done = ok && mbar_wait(bar(bars->drain), 0, abort, p.status);
+      ok = __all_sync(0xffffffffu, done);
+    }
+    // Both halves used the same reference maximum: their sums add.
+    xch[ch * 128 + row] = l_run;
     const bool all_ok = bar_and_sync(ok, 256);
-    const float l_tot = l_run + xl[(ch ^ 1) * 128 + row];
+    const float l_tot = l_run + xch[(ch ^ 1) * 128 + row];
+    uint32_t o[2][32];
+    if (all_ok && n_tiles > 0) {
+      tc_fence_after();
+      tmem_ld_32x32b_x32(mine_cols + 256, o[0]);
+      tmem_ld_32x32b_x32(mine_cols + 256 + 32, o[1]);
+      tmem_ld_wait();
+    }
 
     // Epilogue: rows that belong to this group write their state.
     const int rb = b0 + row / G;
@@ -322,13 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = kvh * G + row % G;
       const int64_t r = (int64_t)rb * p.hq + h;
       float* out = p.out_o + split * p.split_stride_o + r * PKC_HEAD_DIM + ch * 64;
-      const bool has = all_ok && l_tot > 0.f;
+      const bool has = all_ok && n_tiles > 0 && l_tot > 0.f;
       const float inv = has ? 1.f / l_tot : 0.f;
 #pragma unroll
-      for (int i = 0; i < 64; i += 4)
-        *reinterpret_cast<float4*>(out + i) =
-            make_float4(o_acc[i] * inv, o_acc[i + 1] * inv, o_acc[i + 2] * inv, o_acc[i + 3] * inv);
-      if (ch == 0) p.out_lse[split * p.split_stride_lse + r] = has ? (m_run + lg2(l_tot)) * kLn2 : neg_inf();
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(out + c * 32 + i) =
+              has ? make_float4(__uint_as_float(o[c][i]) * inv, __uint_as_float(o[c][i + 1]) * inv,
+                                __uint_as_float(o[c][i + 2]) * inv, __uint_as_float(o[c][i + 3]) * inv)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ch == 0) p.out_lse[split * p.split_stride_lse + r] = has ? (m_ref + lg2(l_tot)) * kLn2 : neg_inf();
     }
   }
 

@@ -41,7 +41,7 @@ _LIB_PATH = os.path.join(_BUILD, "libpkc_oracle.so")
 _lib = None
 _lock = threading.Lock()
 
-F32, F16, BF16 = 0, 1, 2
+F32, F16, BF16, E4M3 = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -66,6 +66,8 @@ def _load():
             lib.pkc_oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
             lib.pkc_oracle_bf16_to_f64.restype = ctypes.c_double
             lib.pkc_oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.pkc_oracle_e4m3_to_f64.restype = ctypes.c_double
+            lib.pkc_oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
             lib.pkc_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -78,13 +80,16 @@ def _ptr(a):
 
 
 def _dtype_code(a) -> int:
-    """Element type of a host array: float32, float16, or bf16 bits (uint16)."""
+    """Element type of a host array: float32, float16, bf16 bits (uint16),
+    or e4m3 codes (uint8)."""
     if a.dtype == np.float32:
         return F32
     if a.dtype == np.float16:
         return F16
     if a.dtype == np.uint16:
         return BF16
+    if a.dtype == np.uint8:
+        return E4M3
     raise TypeError(f"unsupported element type {a.dtype}")
 
 
@@ -93,10 +98,13 @@ def max_threads() -> int:
 
 
 def decode_scalar(bits: int, dtype: int) -> float:
-    """float64 value of one fp16 / bf16 bit pattern (oracle's own decoder)."""
+    """float64 value of one fp16 / bf16 / e4m3 bit pattern (oracle's own
+    decoder)."""
     lib = _load()
     if dtype == F16:
         return lib.pkc_oracle_f16_to_f64(bits)
+    if dtype == E4M3:
+        return lib.pkc_oracle_e4m3_to_f64(bits)
     return lib.pkc_oracle_bf16_to_f64(bits)
 
 
@@ -182,7 +190,7 @@ def attention_rows(q, *, rows=None, sm_scale, num_kv_heads,
                    k_prefix=None, v_prefix=None, prefix_kv_indptr=None,
                    prefix_req_indptr=None, k_cache=None, v_cache=None,
                    block_table=None, cache_seqlens=None, page_size=None,
-                   n_threads=0):
+                   k_scale=1.0, v_scale=1.0, n_threads=0):
     """Attention state of each (request, query head) row over its full key set.
 
     The key set of request b is the shared prefix of b's group (requests
@@ -192,7 +200,10 @@ def attention_rows(q, *, rows=None, sm_scale, num_kv_heads,
     from k/v_cache [P, page_size, Hkv, D].  Computed in float64 from the
     definition (see pkc_oracle.c).
 
-    q: [B, Hq, D] float16 / bf16-bits uint16 / float32 host array.
+    q: [B, Hq, D] float16 / bf16-bits uint16 / float32 host array.  The
+    prefixes have q's element type; the paged cache has it too, or holds
+    e4m3 codes (uint8), the cached key and value then being k_scale and
+    v_scale times the decoded codes (an fp8 cache with per-tensor scales).
     rows: int array [n, 2] of (request, head); default all B*Hq rows.
     Returns (o [n, D] float64, lse [n] float64).
     """
@@ -217,6 +228,7 @@ def attention_rows(q, *, rows=None, sm_scale, num_kv_heads,
         assert _dtype_code(k_prefix) == dt and _dtype_code(v_prefix) == dt
     num_pages = 0
     bt_stride = 0
+    kv_dt = dt
     if k_cache is not None:
         k_cache = np.ascontiguousarray(k_cache)
         v_cache = np.ascontiguousarray(v_cache)
@@ -225,7 +237,10 @@ def attention_rows(q, *, rows=None, sm_scale, num_kv_heads,
         num_pages = k_cache.shape[0]
         bt_stride = block_table.shape[1]
         assert k_cache.shape[1] == page_size
-        assert _dtype_code(k_cache) == dt and _dtype_code(v_cache) == dt
+        kv_dt = _dtype_code(k_cache)
+        assert _dtype_code(v_cache) == kv_dt and kv_dt in (dt, E4M3)
+        if kv_dt != E4M3:
+            assert k_scale == 1.0 and v_scale == 1.0, "scales apply to an e4m3 cache only"
     rc = lib.pkc_oracle_attention_rows(
         _ptr(q), ctypes.c_int(B), ctypes.c_int(Hq), ctypes.c_int(num_kv_heads),
         ctypes.c_int(D), ctypes.c_int(dt), ctypes.c_double(sm_scale),
@@ -234,6 +249,7 @@ def attention_rows(q, *, rows=None, sm_scale, num_kv_heads,
         _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
         ctypes.c_int64(bt_stride), _ptr(cache_seqlens),
         ctypes.c_int(page_size or 0), ctypes.c_int64(num_pages),
+        ctypes.c_int(kv_dt), ctypes.c_double(k_scale), ctypes.c_double(v_scale),
         _ptr(rows), ctypes.c_int64(n), ctypes.c_int(n_threads),
         _ptr(o), _ptr(lse))
     if rc == 1:

@@ -39,7 +39,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_E4M3 = 3 };
 enum { ORC_OK = 0, ORC_BAD_PAGE = 1, ORC_BAD_ARG = 2, ORC_NOMEM = 3 };
 
 /* IEEE 754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
@@ -73,9 +73,31 @@ double pkc_oracle_bf16_to_f64(uint16_t h) {
   return sign ? -mag : mag;
 }
 
+/* 8-bit float E4M3 in the OCP "FP8 Formats for Deep Learning" form (the
+ * "e4m3fn" of the libraries): 1 sign, 4 exponent bits with bias 7, 3
+ * fraction bits.  Exponent field 0 is subnormal, f * 2^-9; there are no
+ * infinities: S.1111.111 is NaN and S.1111.ffff (f < 7) is an ordinary
+ * number, the largest 1.75 * 2^8 = 448.  The pages name "fp8" KV with fp16
+ * queries and outputs (MLSys'25 notes, appendix F) without fixing the
+ * variant; E4M3 is the one used for KV caches. */
+double pkc_oracle_e4m3_to_f64(uint8_t c) {
+  int sign = (c >> 7) & 1;
+  int e = (c >> 3) & 0xf;
+  int f = c & 7;
+  double mag;
+  if (e == 15 && f == 7)
+    mag = NAN;
+  else if (e == 0)
+    mag = ldexp((double)f, -9); /* f/8 * 2^(1-7) */
+  else
+    mag = ldexp((double)(f + 8), e - 10); /* (1 + f/8) * 2^(e-7) */
+  return sign ? -mag : mag;
+}
+
 static double elem(const void* x, int64_t i, int dtype) {
   if (dtype == ORC_F32) return (double)((const float*)x)[i];
   if (dtype == ORC_F16) return pkc_oracle_f16_to_f64(((const uint16_t*)x)[i]);
+  if (dtype == ORC_E4M3) return pkc_oracle_e4m3_to_f64(((const uint8_t*)x)[i]);
   return pkc_oracle_bf16_to_f64(((const uint16_t*)x)[i]);
 }
 
@@ -126,6 +148,11 @@ typedef struct {
   const int32_t* cache_seqlens;
   int page_size;
   int64_t num_pages;
+  /* element type of the paged cache, and its per-tensor scales: a cached
+   * key is k_scale * k_cache[...], a cached value v_scale * v_cache[...]
+   * (1 and 1 for 16-bit caches) */
+  int kv_dtype;
+  double k_scale, v_scale;
 } orc_problem;
 
 /* Address (in elements) of the key/value vector of token t of row b. */
@@ -178,9 +205,12 @@ static int one_row(const orc_problem* p, int b, int h, double* o, double* lse,
     int64_t off;
     int rc = resolve_token(p, b, kvh, t, prefix_lo, n_pref, &kb, &vb, &off);
     if (rc) return rc;
+    const int cached = t >= n_pref;
+    const int kd = cached ? p->kv_dtype : p->dtype;
+    const double ks = cached ? p->k_scale : 1.0;
     double dot = 0.0;
     for (int x = 0; x < p->d; ++x)
-      dot += elem(p->q, qoff + x, p->dtype) * elem(kb, off + x, p->dtype);
+      dot += elem(p->q, qoff + x, p->dtype) * (ks * elem(kb, off + x, kd));
     s[t] = p->sm_scale * dot;
   }
   /* s(I) = m + log sum exp(s_i - m) */
@@ -194,15 +224,19 @@ static int one_row(const orc_problem* p, int b, int h, double* o, double* lse,
     const void *kb, *vb;
     int64_t off;
     resolve_token(p, b, kvh, t, prefix_lo, n_pref, &kb, &vb, &off);
+    const int cached = t >= n_pref;
+    const int vd = cached ? p->kv_dtype : p->dtype;
+    const double vs = cached ? p->v_scale : 1.0;
     double w = exp(s[t] - m) / sum;
-    for (int x = 0; x < p->d; ++x) o[x] += w * elem(vb, off + x, p->dtype);
+    for (int x = 0; x < p->d; ++x) o[x] += w * (vs * elem(vb, off + x, vd));
   }
   return ORC_OK;
 }
 
 /*
  * Attention states for a list of rows.  rows[2*r] = request, rows[2*r+1] =
- * query head.  o_out [n_rows, d], lse_out [n_rows], float64.  Rows run in
+ * query head.  q and the prefixes are of dtype; the paged cache of kv_dtype
+ * with scales k_scale, v_scale (see orc_problem).  o_out [n_rows, d], lse_out [n_rows], float64.  Rows run in
  * parallel over n_threads OpenMP threads (0 = the runtime's default); each
  * row is computed by one thread in the order above.
  */
@@ -213,13 +247,14 @@ int pkc_oracle_attention_rows(
     int n_prefix, const void* k_cache, const void* v_cache,
     const int32_t* block_table, int64_t bt_stride,
     const int32_t* cache_seqlens, int page_size, int64_t num_pages,
+    int kv_dtype, double k_scale, double v_scale,
     const int32_t* rows, int64_t n_rows, int n_threads, double* o_out,
     double* lse_out) {
   if (hkv <= 0 || hq % hkv != 0 || d <= 0) return ORC_BAD_ARG;
   orc_problem p = {q, batch, hq, hkv, d, dtype, sm_scale, k_prefix, v_prefix,
                    prefix_kv_indptr, prefix_req_indptr, n_prefix, k_cache,
                    v_cache, block_table, bt_stride, cache_seqlens, page_size,
-                   num_pages};
+                   num_pages, kv_dtype, k_scale, v_scale};
   int64_t max_n = 0;
   for (int b = 0; b < batch; ++b) {
     int64_t n = 0;

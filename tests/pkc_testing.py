@@ -51,7 +51,8 @@ def oracle_args(p, prefix=True, suffix=True):
                  prefix_req_indptr=p["prefix_req_indptr"])
     if suffix:
         a.update(k_cache=p["k_cache"], v_cache=p["v_cache"], block_table=p["block_table"],
-                 cache_seqlens=p["cache_seqlens"], page_size=p["page_size"])
+                 cache_seqlens=p["cache_seqlens"], page_size=p["page_size"],
+                 k_scale=p.get("k_scale", 1.0), v_scale=p.get("v_scale", 1.0))
     return a
 
 

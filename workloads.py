@@ -8,7 +8,8 @@ and lays them out.  Both sides read the same bytes.
 Element encodings on the host:
   fp16 -> numpy float16;  bf16 -> numpy uint16 holding the bf16 bit pattern
   (float32 rounded to nearest-even, the same rounding torch uses);  fp32 ->
-  numpy float32.
+  numpy float32;  e4m3 -> numpy uint8 codes, float32 rounded by torch's own
+  cast to float8_e4m3fn (used for fp8 KV caches only).
 
 Workload shapes follow the pages' evaluation setup (LLaMA2-7B-like 32 heads
 x 128 dims, page size 16, shared prompts up to 32768 tokens, batches up to
@@ -40,6 +41,13 @@ WORKLOADS = {
     "cascade_long_prompt": dict(batch=128, hq=32, hkv=32, d=128, dtype="f16",
                                 prefix_lens=[32768], prefix_groups=[128],
                                 suffix=("const", 256), page_size=16, seed=4),
+    # FP8 KV paged decode at the GQA suffix shape: 32/8 heads, fp16 q and O,
+    # e4m3 cache with per-tensor scales, batch 256, lognormal lengths
+    "paged_decode_fp8": dict(batch=256, hq=32, hkv=8, d=128, dtype="f16",
+                             kv_dtype="e4m3", k_scale=0.5, v_scale=1.25,
+                             prefix_lens=[], prefix_groups=[],
+                             suffix=("lognormal", 7.0, 1.0, 16, 16384),
+                             page_size=16, seed=6, num_ctas=148),
     # GQA 32/8, bf16, batch 256; 4 prefixes x 8192 tokens, 64 requests each;
     # suffix ~ lognormal(7, 1) clipped to [16, 16384]; plan over 148 CTAs
     "gqa_cascade_lb": dict(batch=256, hq=32, hkv=8, d=128, dtype="bf16",
@@ -62,6 +70,13 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def f32_to_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """Round float32 to e4m3 codes with the library cast (torch)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
 def _encode(x32: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "f16":
         return x32.astype(np.float16)
@@ -69,12 +84,17 @@ def _encode(x32: np.ndarray, dtype: str) -> np.ndarray:
         return f32_to_bf16_bits(x32)
     if dtype == "f32":
         return x32.astype(np.float32)
+    if dtype == "e4m3":
+        return f32_to_e4m3_codes(x32)
     raise ValueError(dtype)
+
+
+_NP_DTYPE = {"f16": np.float16, "bf16": np.uint16, "f32": np.float32, "e4m3": np.uint8}
 
 
 def _nan_value(dtype: str):
     return {"f16": np.float16(np.nan), "bf16": np.uint16(0x7FC0),
-            "f32": np.float32(np.nan)}[dtype]
+            "f32": np.float32(np.nan), "e4m3": np.uint8(0x7F)}[dtype]
 
 
 def normal(shape, seed: int, tag: int, dtype: str, scale: float = 1.0,
@@ -86,7 +106,7 @@ def normal(shape, seed: int, tag: int, dtype: str, scale: float = 1.0,
     number of threads used to draw them.
     """
     n = int(np.prod(shape))
-    np_dtype = {"f16": np.float16, "bf16": np.uint16, "f32": np.float32}[dtype]
+    np_dtype = _NP_DTYPE[dtype]
     out = np.empty(n, np_dtype)
 
     def fill(j):
@@ -125,7 +145,8 @@ def suffix_lengths(spec, batch: int, rng: np.random.Generator) -> np.ndarray:
 
 def make_problem(*, batch, hq, hkv, d, dtype, prefix_lens, prefix_groups,
                  suffix, page_size, seed, max_blocks=None, extra_pages=0,
-                 poison=False, q_scale=1.0, threads=8, **_ignored):
+                 poison=False, q_scale=1.0, threads=8, kv_dtype=None, k_scale=1.0,
+                 v_scale=1.0, **_ignored):
     """A full decode problem: queries, shared prefixes and a paged cache.
 
     Layouts: q [B, Hq, D]; k/v_prefix [sum(prefix_lens), Hkv, D] with
@@ -138,7 +159,17 @@ def make_problem(*, batch, hq, hkv, d, dtype, prefix_lens, prefix_groups,
     order from a seeded permutation of the P pages (P = the pages needed
     plus `extra_pages` never referenced).  With `poison`, every cache slot
     no request may read (tails of last pages, unreferenced pages) is NaN.
+
+    kv_dtype (default: dtype) is the paged cache's encoding; "e4m3" stores
+    N(0,1) draws as e4m3 codes, and the problem then carries per-tensor
+    k_scale / v_scale (the cached key is k_scale times the decoded code).
+    The prefixes always have q's dtype.
     """
+    kv_dtype = kv_dtype or dtype
+    if kv_dtype != dtype and (kv_dtype != "e4m3" or dtype != "f16"):
+        raise ValueError("an e4m3 cache goes with fp16 queries")
+    if kv_dtype != "e4m3" and (k_scale != 1.0 or v_scale != 1.0):
+        raise ValueError("k_scale / v_scale apply to an e4m3 cache only")
     rng = np.random.default_rng(seed)
     lens = suffix_lengths(suffix, batch, rng)
     n_pages_req = (lens + page_size - 1) // page_size
@@ -160,15 +191,15 @@ def make_problem(*, batch, hq, hkv, d, dtype, prefix_lens, prefix_groups,
         v_prefix = normal((Lp, hkv, d), seed, 3, dtype, 1.0, threads)
     else:
         k_prefix = v_prefix = None
-    k_cache = normal((num_pages, page_size, hkv, d), seed, 4, dtype, 1.0, threads)
-    v_cache = normal((num_pages, page_size, hkv, d), seed, 5, dtype, 1.0, threads)
+    k_cache = normal((num_pages, page_size, hkv, d), seed, 4, kv_dtype, 1.0, threads)
+    v_cache = normal((num_pages, page_size, hkv, d), seed, 5, kv_dtype, 1.0, threads)
     if poison:
         used = np.zeros((num_pages, page_size), bool)
         for b in range(batch):
             n = int(lens[b])
             for j in range(int(n_pages_req[b])):
                 used[bt[b, j], :min(page_size, n - j * page_size)] = True
-        nanv = _nan_value(dtype)
+        nanv = _nan_value(kv_dtype)
         k_cache[~used] = nanv
         v_cache[~used] = nanv
     kv_indptr = np.zeros(len(prefix_lens) + 1, np.int32)
@@ -179,7 +210,8 @@ def make_problem(*, batch, hq, hkv, d, dtype, prefix_lens, prefix_groups,
                 prefix_kv_indptr=kv_indptr, prefix_req_indptr=req_indptr,
                 k_cache=k_cache, v_cache=v_cache, block_table=bt,
                 cache_seqlens=lens, page_size=page_size, num_kv_heads=hkv,
-                sm_scale=1.0 / math.sqrt(d), dtype=dtype)
+                sm_scale=1.0 / math.sqrt(d), dtype=dtype, kv_dtype=kv_dtype,
+                k_scale=float(k_scale), v_scale=float(v_scale))
 
 
 def make_merge(*, tokens, heads, d, n_states, seed, v_dtype="f32", threads=8,
@@ -214,7 +246,8 @@ def effective_bytes(problem) -> int:
     B, Hq, D = q.shape
     Hkv = problem["num_kv_heads"]
     esz = q.dtype.itemsize
+    kv_esz = problem["k_cache"].dtype.itemsize
     lp = int(problem["prefix_kv_indptr"][-1])
     s = int(problem["cache_seqlens"].sum())
-    kv = (lp + s) * 2 * Hkv * D * esz
+    kv = lp * 2 * Hkv * D * esz + s * 2 * Hkv * D * kv_esz
     return kv + 2 * B * Hq * D * esz + B * Hq * 4

@@ -45,10 +45,13 @@ def parse_args():
     ap.add_argument("--impl", choices=["pkc", "reference"], default="pkc")
     ap.add_argument("--workload", default="gqa_cascade_lb",
                     choices=["gqa_cascade_lb", "cascade_long_prompt", "tiny_cascade",
-                             "paged_decode", "merge"],
-                    help="cascade workloads time the whole step; 'paged_decode' times the "
-                         "non-cascade decode and 'merge' the binary / 16-ary merge kernels "
-                         "(auxiliary lines)")
+                             "paged_decode", "paged_decode_gqa", "paged_decode_fp8", "merge"],
+                    help="cascade workloads time the whole step; 'paged_decode*' time the "
+                         "non-cascade decode (fp16 MHA, fp16 GQA, fp8-KV GQA) and 'merge' the "
+                         "binary / 16-ary merge kernels (auxiliary lines)")
+    ap.add_argument("--decode-kernel", choices=["auto", "simt", "mma"], default="auto",
+                    help="paged-decode kernel for a 16-bit cache (auto: tensor cores for "
+                         "grouped heads)")
     ap.add_argument("--batch", type=int, default=None,
                     help="keep only the first N requests (and their prefix groups); "
                          "a smaller case of the same workload, for profiling")
@@ -308,10 +311,12 @@ def run_aux(args):
                 "dtype": "f32", "data": "synthetic",
                 "config": {"workload": "merge", "tokens": T, "heads": H, "head_dim": D,
                            "l2": "inputs larger than L2 (203 MB / 1.15 GB)"}}
-    else:  # paged_decode: non-cascade decode through the plan
-        cfg = workload_cfg("paged_decode")
+    else:  # paged_decode*: non-cascade decode through the plan
+        cfg = workload_cfg(args.workload)
         p = workloads.make_problem(**cfg)
         d = to_device(p)
+        fp8 = p["kv_dtype"] == "e4m3"
+        pkc.set_decode_kernel(args.decode_kernel)
         B, Hq, D = p["q"].shape
         C = cfg["num_ctas"]
         ws = torch.empty(pkc.workspace_size(B, Hq, C, 0), dtype=torch.uint8, device="cuda")
@@ -320,9 +325,16 @@ def run_aux(args):
         pkc.plan_upload(buf, ws)
         o = torch.empty_like(d["q"])
         lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
-        ms = time_region(torch, lambda: pkc.paged_decode_state(
-            d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"],
-            p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse), K, W)
+        if fp8:
+            call = lambda: pkc.paged_decode_state_fp8(
+                d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"],
+                p["sm_scale"], ws, k_scale=p["k_scale"], v_scale=p["v_scale"], plan_buf=buf,
+                o=o, lse=lse)
+        else:
+            call = lambda: pkc.paged_decode_state(
+                d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"],
+                p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse)
+        ms = time_region(torch, call, K, W)
         if pkc.device_status(ws) != 0:
             raise RuntimeError("device status not OK")
         eff = workloads.effective_bytes(p)
@@ -331,8 +343,10 @@ def run_aux(args):
                 "frac": eff / (ms / 1e3) / 1e9 / hbm_peak, "peak": hbm_peak,
                 "peak_source": f"{peak_kind} hbm_gbs", "steps": K, "warmup": W,
                 "dtype": cfg["dtype"], "data": "synthetic",
-                "config": {"workload": "paged_decode", "batch": B, "num_qo_heads": Hq,
+                "config": {"workload": args.workload, "batch": B, "num_qo_heads": Hq,
+                           "num_kv_heads": p["num_kv_heads"], "kv_dtype": p["kv_dtype"],
                            "kv_tokens": int(p["cache_seqlens"].sum()), "num_ctas": C,
+                           "decode_kernel": "mma" if fp8 else args.decode_kernel,
                            "launches": "decode + contraction"}}
     print(json.dumps(line), flush=True)
 
@@ -448,7 +462,7 @@ def main():
     if args.impl == "reference":
         run_reference(args)
         return
-    if args.workload in ("merge", "paged_decode"):
+    if args.workload == "merge" or args.workload.startswith("paged_decode"):
         run_aux(args)
         return
     import torch
@@ -464,6 +478,7 @@ def main():
     if dist is not None:
         dist.barrier()
     import paged_kv_cascade_gb300 as pkc
+    pkc.set_decode_kernel(args.decode_kernel)
 
     cfg, p = make_workload(args.workload, args.batch)
     sys.path.insert(0, os.path.join(ROOT, "tests"))
@@ -647,7 +662,8 @@ def main():
                        "suffix_tokens": suffix_tokens, "num_ctas": num_ctas,
                        "effective_bytes_per_step": eff,
                        "l2": "inputs larger than L2 (one step reads %.2f GB)" % (eff / 1e9),
-                       "launch": mode, "parallelism": f"replicas x{world}"},
+                       "launch": mode, "decode_kernel": args.decode_kernel,
+                       "parallelism": f"replicas x{world}"},
             "direct_us_per_step": 1e3 * direct_ms_per_step,
             "hbm_fraction": value / world / hbm_peak,
             "stages_us": {k: 1e3 * v for k, v in stage_ms.items()},

@@ -55,8 +55,10 @@ typedef enum {
   PKC_ERR_PLAN = 7         /* plan buffer invalid or inconsistent */
 } pkc_status;
 
-/* Element types. */
-typedef enum { PKC_F32 = 0, PKC_F16 = 1, PKC_BF16 = 2 } pkc_dtype;
+/* Element types.  PKC_E4M3 (8-bit float: 1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits; no infinities, S.1111.111 is NaN; largest
+ * finite 448) is accepted only for a KV cache (pkc_paged_decode_state_fp8). */
+typedef enum { PKC_F32 = 0, PKC_F16 = 1, PKC_BF16 = 2, PKC_E4M3 = 3 } pkc_dtype;
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int pkc_version(void);
@@ -277,6 +279,36 @@ int pkc_paged_decode_state_noalloc(
     int32_t* device_status, int dtype, void* stream);
 
 /*
+ * Paged decode state over an FP8 KV cache (MLSys'25 notes, appendix F,
+ * "FP8-FP16 mixed-precision attention": queries and outputs stay fp16, the
+ * KV cache is stored in fp8).  Same computation, plan and workspace as
+ * pkc_paged_decode_state, with:
+ *   q [batch, num_qo_heads, 128] fp16;  o [batch, num_qo_heads, 128] fp16
+ *   k_cache, v_cache [num_pages, page_size, num_kv_heads, 128] of one-byte
+ *            e4m3 codes (PKC_E4M3)
+ *   k_scale, v_scale > 0, finite: the cached values are k_scale * e4m3(code)
+ *            and v_scale * e4m3(code) (one scale per tensor; 1 for codes
+ *            stored unscaled)
+ * so the scores are sm_scale * k_scale * (q . e4m3(k)) and O is v_scale
+ * times the softmax-weighted sum of e4m3(v).  The codes are widened to
+ * fp16 exactly; products accumulate in fp32.  page_size must be a power of
+ * two with min(page_size, 16) * H >= 8, H = the largest of 8, 4, 2, 1 that
+ * divides num_kv_heads (else PKC_ERR_UNSUPPORTED).  Slots outside a
+ * request's sequence are never used, whatever bytes they hold.
+ */
+int pkc_paged_decode_state_fp8(const void* q, const void* k_cache,
+                               const void* v_cache,
+                               const int32_t* block_table,
+                               int block_table_stride,
+                               const int32_t* cache_seqlens, int batch,
+                               int num_qo_heads, int num_kv_heads,
+                               int head_dim, int page_size, int64_t num_pages,
+                               float sm_scale, float k_scale, float v_scale,
+                               const int32_t* plan_host, void* workspace,
+                               size_t workspace_bytes, void* o, float* lse,
+                               void* stream);
+
+/*
  * Multi-query prefix state (blog "Cascade Inference", step 1 of the
  * algorithm): every request's queries against the KV of the shared prefix
  * of its group, on the tensor cores (tcgen05, TMEM accumulators).
@@ -330,6 +362,19 @@ int pkc_cascade_decode(
  * caller; NULL clears the hook.
  */
 int pkc_set_stage_events(void* const* events, int n_events);
+
+/*
+ * Kernel used by the paged decode over a 16-bit cache (process-wide):
+ *   0 = automatic (default): tensor-core kernel for grouped heads
+ *       (num_qo_heads / num_kv_heads >= 2), CUDA-core kernel otherwise
+ *   1 = always the CUDA-core kernel
+ *   2 = the tensor-core kernel wherever it applies (page size a power of
+ *       two, min(page_size, 16) * heads per block >= 8), else CUDA cores
+ * Both compute the same states; the switch exists for measurement and
+ * tests.  An FP8 cache always uses the tensor-core kernel.  Returns
+ * PKC_ERR_INVALID_ARG for any other value.
+ */
+int pkc_set_decode_kernel(int which);
 
 #ifdef __cplusplus
 }

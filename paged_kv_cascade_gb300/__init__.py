@@ -53,7 +53,10 @@ SIGNATURES = {
                                         _P, _P, _I, _P]),
     "pkc_paged_decode_state_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I64,
                                             _F, _P, _P, _P, _P, _I, _P]),
+    "pkc_paged_decode_state_fp8": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I64, _F,
+                                        _F, _F, _P, _P, _SZ, _P, _P, _P]),
     "pkc_set_stage_events": (_I, [_c.POINTER(_P), _I]),
+    "pkc_set_decode_kernel": (_I, [_I]),
     "pkc_cascade_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                 _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
 }
@@ -210,6 +213,34 @@ def paged_decode_state(q, k_cache, v_cache, block_table, cache_seqlens, sm_scale
         _ptr(cache_seqlens), B, Hq, Hkv, D, ps, P, float(sm_scale), _hptr(plan_buf),
         _ptr(workspace), workspace.numel(), _ptr(o), _ptr(lse), _dtype_code(q), _stream(stream)))
     return o, lse
+
+
+def paged_decode_state_fp8(q, k_cache, v_cache, block_table, cache_seqlens, sm_scale, workspace,
+                           k_scale=1.0, v_scale=1.0, plan_buf=None, o=None, lse=None, stream=None):
+    """States of fp16 q [B, Hq, 128] over an e4m3 paged cache (uint8 codes
+    [P, page_size, Hkv, 128]); the cached values are k_scale * e4m3(k) and
+    v_scale * e4m3(v)."""
+    import torch
+    B, Hq, D = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    if q.dtype != torch.float16 or k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("paged_decode_state_fp8: q must be float16 and the caches uint8 e4m3 codes")
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().pkc_paged_decode_state_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(cache_seqlens), B, Hq, Hkv, D, ps, P, float(sm_scale), float(k_scale), float(v_scale),
+        _hptr(plan_buf), _ptr(workspace), workspace.numel(), _ptr(o), _ptr(lse), _stream(stream)))
+    return o, lse
+
+
+DECODE_KERNELS = {"auto": 0, "simt": 1, "mma": 2}
+
+
+def set_decode_kernel(which):
+    """Kernel for 16-bit paged decode: "auto", "simt" (CUDA cores) or "mma"
+    (tensor cores); process-wide."""
+    _check(lib().pkc_set_decode_kernel(DECODE_KERNELS[which]))
 
 
 def paged_decode_state_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, sm_scale,

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -274,15 +275,28 @@ int pkc_plan_upload(const int32_t* plan_host, void* workspace, size_t workspace_
   return e ? cuda_error(e, "plan_upload") : PKC_OK;
 }
 
-int pkc_paged_decode_state(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
-                           int block_table_stride, const int32_t* cache_seqlens, int batch, int num_qo_heads,
-                           int num_kv_heads, int head_dim, int page_size, int64_t num_pages, float sm_scale,
-                           const int32_t* plan_host, void* workspace, size_t workspace_bytes, void* o, float* lse,
-                           int dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+// Paged decode (+ contraction of split chunks) for both cache kinds.
+int paged_decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                      int block_table_stride, const int32_t* cache_seqlens, int batch, int num_qo_heads,
+                      int num_kv_heads, int head_dim, int page_size, int64_t num_pages, float sm_scale,
+                      float k_scale, float v_scale, const int32_t* plan_host, void* workspace,
+                      size_t workspace_bytes, void* o, float* lse, int dtype, int kv_dtype, void* stream) {
   if (int rc = check_attn_dims(batch, num_qo_heads, num_kv_heads, head_dim, dtype)) return rc;
   if (int rc = check_plan(plan_host, batch)) return rc;
   if (page_size < 1 || block_table_stride < 1 || num_pages < 0)
     return set_error(PKC_ERR_INVALID_ARG, "page_size and block_table_stride must be >= 1, num_pages >= 0");
+  if (kv_dtype == PKC_E4M3) {
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+      return set_error(PKC_ERR_INVALID_ARG, "paged_decode_state_fp8: k_scale and v_scale must be finite and > 0");
+    if (mma_decode_heads_per_block(num_kv_heads, page_size) == 0)
+      return set_error(PKC_ERR_UNSUPPORTED,
+                       "paged_decode_state_fp8: page_size %d with %d KV heads is not supported (page_size must "
+                       "be a power of two and min(page_size, 16) x heads per block >= 8)",
+                       page_size, num_kv_heads);
+  }
   const int num_ctas = plan_host ? plan_host[PKC_PLAN_NUM_CTAS] : 0;
   const WsLayout L = ws_layout(batch, num_qo_heads, head_dim, num_ctas);
   if (int rc = check_ws(workspace, workspace_bytes, L.fixed_end)) return rc;
@@ -299,13 +313,15 @@ int pkc_paged_decode_state(const void* q, const void* k_cache, const void* v_cac
   dp.block_table = block_table; dp.cache_seqlens = cache_seqlens;
   dp.bt_stride = block_table_stride; dp.num_pages = num_pages;
   dp.batch = batch; dp.hq = num_qo_heads; dp.hkv = num_kv_heads; dp.page_size = page_size;
-  dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  dp.scale_log2 = sm_scale * k_scale * 1.4426950408889634f;
+  dp.v_scale = v_scale;
   dp.plan = plan_host ? reinterpret_cast<const int32_t*>(ws + L.plan) : nullptr;
   dp.o_direct = o; dp.lse_direct = lse; dp.direct_f32 = 0;
   dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
   dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   dp.status = status;
-  int e = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, stream);
+  int e = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, kv_dtype, stream);
+  if (e == -1) return set_error(PKC_ERR_CUDA, "paged decode: could not build TMA tensor maps");
   if (e) return cuda_error(e, "paged decode launch");
   if (plan_host) {
     ContractParams cp;
@@ -317,6 +333,36 @@ int pkc_paged_decode_state(const void* q, const void* k_cache, const void* v_cac
     e = launch_contract(cp, batch, stream);
     if (e) return cuda_error(e, "contraction launch");
   }
+  return PKC_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int pkc_paged_decode_state(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                           int block_table_stride, const int32_t* cache_seqlens, int batch, int num_qo_heads,
+                           int num_kv_heads, int head_dim, int page_size, int64_t num_pages, float sm_scale,
+                           const int32_t* plan_host, void* workspace, size_t workspace_bytes, void* o, float* lse,
+                           int dtype, void* stream) {
+  return paged_decode_impl(q, k_cache, v_cache, block_table, block_table_stride, cache_seqlens, batch,
+                           num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale, 1.f, 1.f,
+                           plan_host, workspace, workspace_bytes, o, lse, dtype, dtype, stream);
+}
+
+int pkc_paged_decode_state_fp8(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int block_table_stride, const int32_t* cache_seqlens,
+                               int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                               int64_t num_pages, float sm_scale, float k_scale, float v_scale,
+                               const int32_t* plan_host, void* workspace, size_t workspace_bytes, void* o,
+                               float* lse, void* stream) {
+  return paged_decode_impl(q, k_cache, v_cache, block_table, block_table_stride, cache_seqlens, batch,
+                           num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale, k_scale, v_scale,
+                           plan_host, workspace, workspace_bytes, o, lse, PKC_F16, PKC_E4M3, stream);
+}
+
+int pkc_set_decode_kernel(int which) {
+  if (set_decode_kernel(which) != 0)
+    return set_error(PKC_ERR_INVALID_ARG, "set_decode_kernel: which must be 0, 1 or 2 (got %d)", which);
   return PKC_OK;
 }
 
@@ -395,12 +441,13 @@ int pkc_cascade_decode(const void* q, const void* k_prefix, const void* v_prefix
   dp.bt_stride = block_table_stride; dp.num_pages = num_pages;
   dp.batch = batch; dp.hq = num_qo_heads; dp.hkv = num_kv_heads; dp.page_size = page_size;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  dp.v_scale = 1.f;
   dp.plan = plan_host ? reinterpret_cast<const int32_t*>(ws + L.plan) : nullptr;
   dp.o_direct = ws + L.suffix_o; dp.lse_direct = reinterpret_cast<float*>(ws + L.suffix_lse); dp.direct_f32 = 1;
   dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
   dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   dp.status = status;
-  e = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, stream);
+  e = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, dtype, stream);
   if (e) return cuda_error(e, "paged decode launch");
   mark(2);
   // 3. contraction + merge: prefix splits (+) suffix chunks -> final O, LSE

@@ -33,6 +33,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pkc_device.cuh"
@@ -644,7 +645,7 @@ int launch_decode_t(const DecodeParams& p, int grid_x, int hg, const CUtensorMap
 
 }  // namespace
 
-int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype, void* stream) {
+int launch_paged_decode_simt(const DecodeParams& p, int grid_x, int dtype, void* stream) {
   if (grid_x <= 0) return 0;
   // KV heads per block: the largest of 8, 4, 2, 1 that divides Hkv.
   const int hg = p.hkv % 8 == 0 ? 8 : p.hkv % 4 == 0 ? 4 : p.hkv % 2 == 0 ? 2 : 1;
@@ -661,6 +662,32 @@ int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype, void* stre
   cudaStream_t st = (cudaStream_t)stream;
   return dtype == PKC_F16 ? launch_decode_t<__half>(p, grid_x, hg, mk, mv, st)
                           : launch_decode_t<__nv_bfloat16>(p, grid_x, hg, mk, mv, st);
+}
+
+// Kernel choice for a 16-bit cache: 0 = automatic, 1 = CUDA-core kernel,
+// 2 = tensor-core kernel (pkc_set_decode_kernel).
+static std::atomic<int> g_decode_kernel{0};
+
+int set_decode_kernel(int which) {
+  if (which < 0 || which > 2) return -1;
+  g_decode_kernel.store(which);
+  return 0;
+}
+
+// An fp8 cache always takes the tensor-core kernel.  A 16-bit cache takes it
+// for grouped heads (G >= 2), where the CUDA-core kernel runs out of issue
+// slots before HBM bandwidth, and the CUDA-core kernel for G = 1, unless
+// the choice is forced.
+int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype, int kv_dtype, void* stream) {
+  const bool mma_ok = mma_decode_heads_per_block(p.hkv, p.page_size) > 0;
+  if (kv_dtype == PKC_E4M3) {
+    if (dtype != PKC_F16 || !mma_ok) return (int)cudaErrorInvalidValue;
+    return launch_paged_decode_mma(p, grid_x, kKvE4M3, stream);
+  }
+  const int forced = g_decode_kernel.load();
+  const bool use_mma = mma_ok && (forced == 2 || (forced == 0 && p.hq / p.hkv >= 2));
+  if (use_mma) return launch_paged_decode_mma(p, grid_x, dtype == PKC_BF16 ? kKvBF16 : kKvF16, stream);
+  return launch_paged_decode_simt(p, grid_x, dtype, stream);
 }
 
 int launch_contract(const ContractParams& p, int n_rows, void* stream) {

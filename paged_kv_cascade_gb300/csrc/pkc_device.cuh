@@ -115,6 +115,64 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return r;
 }
 
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core fragments (m16n8k16, fp32 accumulation)
+// ---------------------------------------------------------------------------
+
+// Four 8x8 16-bit matrices from shared memory; lane l gives the address of
+// row (l & 7) of matrix (l >> 3).  Plain: lane (g, t) = (l >> 2, l & 3) gets
+// row g, elements 2t, 2t+1; .trans: elements [2t][g], [2t+1][g].
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+// Transpose of an 8x8 16-bit matrix held one row pair per lane.
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+  return d;
+}
+// d += a * b for one m16n8k16 tile (A row-major 16x16, B column-major 16x8).
+template <typename T> __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                               uint32_t b1);
+template <> __device__ __forceinline__ void mma16816<__half>(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                             uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <> __device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], const uint32_t (&a)[4],
+                                                                    uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Two e4m3 codes (low byte first) -> two fp16 values, exactly (every e4m3
+// value is an fp16 value).  lo: the low 16 bits of x; hi: the high 16.
+__device__ __forceinline__ uint32_t e4m3x2_lo(uint32_t x) {
+  uint32_t d;
+  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %1;\ncvt.rn.f16x2.e4m3x2 %0, l;\n}" : "=r"(d) : "r"(x));
+  return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi(uint32_t x) {
+  uint32_t d;
+  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %1;\ncvt.rn.f16x2.e4m3x2 %0, h;\n}" : "=r"(d) : "r"(x));
+  return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -57,7 +57,11 @@ struct DecodeParams {
   float* part_o;          // partial slots [slot, Hq, D]
   float* part_lse;        // [slot, Hq]
   int32_t* status;
+  float v_scale;          // V = v_scale * stored V (1 for 16-bit caches)
 };
+
+// Element kinds of a paged KV cache.
+enum KvKind { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2 };
 
 enum ContractMode {
   kContractPlanUnits = 0,  // rows = the plan's split + empty units
@@ -109,8 +113,19 @@ int launch_merge_state(const void* va, const float* sa, const void* vb,
 int launch_merge_states(const void* v, const float* s, void* vo, float* so,
                         int64_t n_tokens, int n_states, int n_heads,
                         int head_dim, int dtype, void* stream);
-int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype,
+// Paged decode: q of dtype (PKC_F16 / PKC_BF16) against a cache of
+// kv_dtype (the same, or PKC_E4M3 with an fp16 q); picks the tensor-core
+// kernel or the CUDA-core kernel.
+int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype, int kv_dtype,
                         void* stream);
+int set_decode_kernel(int which);  // 0 auto, 1 CUDA cores, 2 tensor cores
+int launch_paged_decode_simt(const DecodeParams& p, int grid_x, int dtype,
+                             void* stream);
+int launch_paged_decode_mma(const DecodeParams& p, int grid_x, int kv_kind,
+                            void* stream);
+// KV heads per block of the tensor-core kernel, or 0 if it cannot take
+// this head count and page size.
+int mma_decode_heads_per_block(int hkv, int page_size);
 int launch_contract(const ContractParams& p, int n_rows, void* stream);
 // q/k/v tensor maps are built inside; returns cudaError_t or -1 when the
 // driver entry point for tensor maps is unavailable.
@@ -121,7 +136,8 @@ int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix,
 int num_sms();
 
 // Encode a TMA tiled tensor map (a 128-byte CUtensorMap at `map`) over a
-// 16-bit tensor; dims[0] is the contiguous dimension.  Returns false if the
+// 16-bit (PKC_F16, PKC_BF16) or byte (PKC_E4M3) tensor; dims[0] is the
+// contiguous dimension.  Returns false if the
 // driver entry point is unavailable or the encoding is rejected.
 bool encode_tiled_map(void* map, const void* base, int dtype, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);

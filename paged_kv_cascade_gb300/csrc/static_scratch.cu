@@ -124,12 +124,13 @@ extern "C" int pkc_paged_decode_state_noalloc(
   dp.bt_stride = block_table_stride; dp.num_pages = num_pages;
   dp.batch = batch; dp.hq = num_qo_heads; dp.hkv = num_kv_heads; dp.page_size = page_size;
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
+  dp.v_scale = 1.f;
   dp.plan = plan_host ? reinterpret_cast<const int32_t*>(s + off_plan) : nullptr;
   dp.o_direct = o; dp.lse_direct = lse; dp.direct_f32 = 0;
   dp.part_o = reinterpret_cast<float*>(s + off_po);
   dp.part_lse = reinterpret_cast<float*>(s + off_pl);
   dp.status = reinterpret_cast<int32_t*>(s);
-  int le = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, stream);
+  int le = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, dtype, stream);
   if (le) return cuda_error(le, "paged_decode_state_noalloc: decode launch");
   if (plan_host) {
     ContractParams cp;

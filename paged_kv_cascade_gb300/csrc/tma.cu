@@ -37,8 +37,9 @@ bool encode_tiled_map(void* map, const void* base, int dtype, int rank, const ui
     e[i] = 1;
     if (i + 1 < rank) s[i] = strides_bytes[i];
   }
-  const CUtensorMapDataType t =
-      dtype == PKC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType t = dtype == PKC_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                : dtype == PKC_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   return enc(static_cast<CUtensorMap*>(map), t, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, e,
              CU_TENSOR_MAP_INTERLEAVE_NONE,
              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,

@@ -76,6 +76,32 @@ def test_bad_arguments_are_rejected_without_a_device(L):
     assert rc == 7 and b"plan" in L.pkc_last_error()
 
 
+def test_fp8_decode_and_kernel_switch_reject_bad_arguments(L):
+    fake = ctypes.c_void_p(0x1000)
+    ws = ctypes.c_void_p(0x100000)
+    args = [fake, fake, fake, fake, 4, fake, 2, 8, 8, 128, 16, 10, 1.0]
+    # scales must be finite and positive
+    for ks, vs in [(0.0, 1.0), (1.0, -2.0), (float("nan"), 1.0), (1.0, float("inf"))]:
+        rc = L.pkc_paged_decode_state_fp8(*args, ks, vs, None, ws, 1 << 20, fake, fake, None)
+        assert rc == 1 and b"scale" in L.pkc_last_error()
+    # page size 12 (not a power of two) is valid but unsupported for fp8
+    rc = L.pkc_paged_decode_state_fp8(fake, fake, fake, fake, 4, fake, 2, 8, 8, 128, 12, 10,
+                                      1.0, 1.0, 1.0, None, ws, 1 << 20, fake, fake, None)
+    assert rc == 2 and b"page_size" in L.pkc_last_error()
+    # one KV head with 4-slot pages: a slice is less than one swizzle atom
+    rc = L.pkc_paged_decode_state_fp8(fake, fake, fake, fake, 4, fake, 2, 2, 1, 128, 4, 10,
+                                      1.0, 1.0, 1.0, None, ws, 1 << 20, fake, fake, None)
+    assert rc == 2
+    # head_dim 64 is unsupported here too
+    rc = L.pkc_paged_decode_state_fp8(fake, fake, fake, fake, 4, fake, 2, 8, 8, 64, 16, 10,
+                                      1.0, 1.0, 1.0, None, ws, 1 << 20, fake, fake, None)
+    assert rc == 2
+    for bad in (-1, 3, 7):
+        assert L.pkc_set_decode_kernel(bad) == 1
+    for ok in (1, 2, 0):  # leaves the automatic choice set
+        assert L.pkc_set_decode_kernel(ok) == 0
+
+
 def test_workspace_size_matches_documented_layout(L):
     def al(x):
         return (x + 255) // 256 * 256

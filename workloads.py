@@ -48,6 +48,11 @@ WORKLOADS = {
                              prefix_lens=[], prefix_groups=[],
                              suffix=("lognormal", 7.0, 1.0, 16, 16384),
                              page_size=16, seed=6, num_ctas=148),
+    # the same shape with an fp16 cache (the 16-bit counterpart)
+    "paged_decode_gqa": dict(batch=256, hq=32, hkv=8, d=128, dtype="f16",
+                             prefix_lens=[], prefix_groups=[],
+                             suffix=("lognormal", 7.0, 1.0, 16, 16384),
+                             page_size=16, seed=6, num_ctas=148),
     # GQA 32/8, bf16, batch 256; 4 prefixes x 8192 tokens, 64 requests each;
     # suffix ~ lognormal(7, 1) clipped to [16, 16384]; plan over 148 CTAs
     "gqa_cascade_lb": dict(batch=256, hq=32, hkv=8, d=128, dtype="bf16",

@@ -21,13 +21,17 @@
 // nothing touches O until the end.
 // Roles: warp 0 issues TMA loads (Q once, K/V into a 3-stage ring), warp 1
 // allocates TMEM and issues MMAs, warps 2..9 own query rows, two threads
-// per row (64 columns each).  TMEM: S double buffer (2 x 128 columns) + O
+// per row (64 columns each).  The row maximum is each thread's half maximum
+// swapped with its partner through shared memory at a barrier of just the
+// two warps; the exponent argument S c - m and the row sums use packed
+// two-wide fp32 FMAs.  TMEM: S double buffer (2 x 128 columns) + O
 // (128).  P_j overwrites K_j's shared memory once S_j is complete.  All
 // waits are bounded (2 s) and set PKC_ERR_TIMEOUT when they run out.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "pkc_device.cuh"
 #include "pkc_internal.h"
@@ -51,6 +55,7 @@ struct __align__(8) Barriers {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int xok[2][2][4];  // [tile parity][column half][lane quadrant]: the warp had S
 };
 
 // Q, the K/V ring, barriers (256 B) and the row-exchange buffer (1 KB).  The
@@ -58,7 +63,7 @@ struct __align__(8) Barriers {
 // static shared memory it is, and the kernel checks it.
 constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
 constexpr int kXchOffset = kBarOffset + 256;
-constexpr int kSmemBytes = kXchOffset + 2 * 128 * 4;
+constexpr int kSmemBytes = kXchOffset + 4 * 128 * 4;
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -201,35 +206,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t mine_cols = lane_base + ch * 64;         // this thread's columns
-    const uint32_t other_cols = lane_base + (ch ^ 1) * 64;  // the row partner's
     float* xch = reinterpret_cast<float*>(smem + kXchOffset);  // [2 half][128]
+    float* xmx = xch;  // in the loop: [tile parity][half][128] row half-maxima
     constexpr float kRescaleLog2 = 8.f;  // move m_ref only when the max grows by > 2^8
     float m_ref = neg_inf(), l_run = 0.f;
     bool ok = true;
-    // Each of a row's two threads reads the whole row of S for the maximum,
-    // so both reach the same m_ref and the softmax warps never wait for each
-    // other inside the loop.  Decisions that guard warp-collective TMEM
-    // accesses are made warp-uniform (__all_sync / __any_sync); warp w and
-    // warp w+4 hold the same rows and reach the same decisions.
+    // Both threads of a row reach the same row maximum (their two half
+    // maxima, swapped), hence the same m_ref.  Decisions that guard
+    // warp-collective TMEM accesses are made warp-uniform (__all_sync /
+    // __any_sync); warp w and warp w+4 hold the same rows and reach the
+    // same decisions.
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j & 1, s = j % kStages;
-      const bool got = mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
-      if (!__all_sync(0xffffffffu, ok && got)) { ok = false; break; }
-      tc_fence_after();
+      const bool got = ok && mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
+      const bool have = __all_sync(0xffffffffu, got);
       const int vrow = min(kKvTile, kv_hi - (kv_lo + j * kKvTile));  // valid columns of the row
       const int valid = vrow - ch * 64;                                  // of my half
       uint32_t sr[2][32];
-      float mx;
-      {
-        uint32_t ov[32];  // the partner's half, 32 columns at a time
+      float mx = neg_inf();
+      if (have) {
+        tc_fence_after();
         tmem_ld_32x32b_x32(mine_cols + b * 128, sr[0]);
         tmem_ld_32x32b_x32(mine_cols + b * 128 + 32, sr[1]);
-        tmem_ld_32x32b_x32(other_cols + b * 128, ov);
         tmem_ld_wait();
+        reg_fence32(sr[0]);
+        reg_fence32(sr[1]);
         float m8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) m8[k] = neg_inf();
-        // max over 32 consecutive scores starting at row column col0
         auto fold_max = [&](const uint32_t (&v)[32], int col0) {
           if (col0 + 32 <= vrow) {  // all valid: three-input max, no per-element test
 #pragma unroll
@@ -243,12 +247,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         fold_max(sr[0], ch * 64);
         fold_max(sr[1], ch * 64 + 32);
-        fold_max(ov, (ch ^ 1) * 64);
-        tmem_ld_32x32b_x32(other_cols + b * 128 + 32, ov);
-        tmem_ld_wait();
-        fold_max(ov, (ch ^ 1) * 64 + 32);
         mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       }
+      // The row's two threads swap their half maxima through shared memory
+      // (slots alternate with the tile parity, so a fast warp cannot
+      // overwrite a value its partner has not read).  The named barrier
+      // joins just the two warps of this lane quadrant; both reach it on
+      // every tile, whether or not S arrived, and leave together.
+      xmx[(b * 2 + ch) * 128 + row] = mx;
+      if (lane == 0) bars->xok[b][ch][quad] = have ? 1 : 0;
+      asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
+      const bool both = have && bars->xok[b][ch ^ 1][quad] != 0;
+      if (!both) { ok = false; break; }
+      mx = fmaxf(mx, xmx[(b * 2 + (ch ^ 1)) * 128 + row]);
       const float m_tile = mx * p.scale_log2;
       if (__any_sync(0xffffffffu, m_tile > m_ref + kRescaleLog2)) {
         const float m_new = fmaxf(m_ref, m_tile);
@@ -257,13 +268,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j > 0) {
           // O holds P.V of tiles < j: wait for the last of them (the S_j
           // commit already covered tile j-2), rescale my columns in TMEM.
+          // On a timeout the warp skips the rest of the tile; its partner
+          // learns of it at the next pair barrier and both leave there.
           const bool done = mbar_wait(bar(bars->o_full), (j - 1) & 1, abort, p.status);
-          if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, done)) { ok = false; continue; }
           tc_fence_after();
           uint32_t o[2][32];
           tmem_ld_32x32b_x32(mine_cols + 256, o[0]);
           tmem_ld_32x32b_x32(mine_cols + 256 + 32, o[1]);
           tmem_ld_wait();
+          reg_fence32(o[0]);
+          reg_fence32(o[1]);
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -275,31 +290,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_new;
       }
       const uint32_t pbase = s_stage0 + s * kStageBytes + ch * kSubTile;
-      float l8[8];
+      // P = exp2(S c - m_ref), two scores per packed fp32 FMA; the row sum
+      // accumulates in packed pairs.  Full tiles take a path with no
+      // per-element validity test.
+      const uint64_t c2 = pk2(p.scale_log2, p.scale_log2), nm2 = pk2(-m_ref, -m_ref), one2 = pk2(1.f, 1.f);
+      uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};
+      auto p_chunks = [&](auto full_tag) {
+        constexpr bool kFull = decltype(full_tag)::value;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) l8[k] = 0.f;
+        for (int c = 0; c < 2; ++c) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+          for (int k = 0; k < 4; ++k) {  // 8 probabilities -> one 16-byte chunk of P
+            uint32_t w[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // 8 probabilities -> one 16-byte chunk of P
-          float pv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int i = 8 * k + e;
-            pv[e] = c * 32 + i < valid ? ex2(fmaf(__uint_as_float(sr[c][i]), p.scale_log2, -m_ref)) : 0.f;
-            l8[e] += pv[e];
+            for (int e = 0; e < 8; e += 2) {
+              const int i = 8 * k + e;
+              const float2 x = upk2(ffma2(pk2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), c2, nm2));
+              float p0 = ex2(x.x), p1 = ex2(x.y);
+              if (!kFull) {
+                p0 = c * 32 + i < valid ? p0 : 0.f;
+                p1 = c * 32 + i + 1 < valid ? p1 : 0.f;
+              }
+              l2[e >> 1] = ffma2(pk2(p0, p1), one2, l2[e >> 1]);
+              w[e >> 1] = Elem<T>::from_f2(p0, p1);
+            }
+            const uint32_t chunk = (uint32_t)(c * 4 + k);
+            const uint32_t addr = pbase + row * 128 + ((chunk ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                         "r"(w[3])
+                         : "memory");
           }
-          const uint32_t chunk = (uint32_t)(c * 4 + k);
-          const uint32_t addr = pbase + row * 128 + ((chunk ^ (row & 7)) << 4);
-          const uint32_t w0 = Elem<T>::from_f2(pv[0], pv[1]);
-          const uint32_t w1 = Elem<T>::from_f2(pv[2], pv[3]);
-          const uint32_t w2 = Elem<T>::from_f2(pv[4], pv[5]);
-          const uint32_t w3 = Elem<T>::from_f2(pv[6], pv[7]);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
-                       : "memory");
         }
-      }
-      l_run += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      };
+      if (valid >= 64) p_chunks(std::true_type{});
+      else p_chunks(std::false_type{});
+      const float2 la = upk2(l2[0]), lb = upk2(l2[1]), lc = upk2(l2[2]), ld = upk2(l2[3]);
+      l_run += ((la.x + la.y) + (lb.x + lb.y)) + ((lc.x + lc.y) + (ld.x + ld.y));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(bars->p_full[b]));
@@ -310,7 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool done = ok && mbar_wait(bar(bars->drain), 0, abort, p.status);
       ok = __all_sync(0xffffffffu, done);
     }
-    // Both halves used the same reference maximum: their sums add.
+    // Both halves used the same reference maximum: their sums add.  (xch
+    // doubles as the loop's max-exchange buffer: the two warps of a lane
+    // quadrant pass one more pair barrier before it is rewritten.)
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
     xch[ch * 128 + row] = l_run;
     const bool all_ok = bar_and_sync(ok, 256);
     const float l_tot = l_run + xch[(ch ^ 1) * 128 + row];
@@ -320,6 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_32x32b_x32(mine_cols + 256, o[0]);
       tmem_ld_32x32b_x32(mine_cols + 256 + 32, o[1]);
       tmem_ld_wait();
+      reg_fence32(o[0]);
+      reg_fence32(o[1]);
     }
 
     // Epilogue: rows that belong to this group write their state.

@@ -199,8 +199,13 @@ int pkc_plan_upload(const int32_t* plan_host, void* workspace,
  * 2 * #CTA * T_q * H * (D+1) with T_q = 1); and prefix_splits copies of
  * [batch, Hq, D+1] float32 for prefix partial states.
  *   num_ctas: CTAs of the plan the calls will use (0 if none).
- *   prefix_splits: most KV splits of the shared prefix (0 if no prefix;
- *                  the calls use as many as fit, up to the SM count).
+ *   prefix_splits: partial-state slots for the shared prefix (0 if no
+ *                  prefix).  The prefix stage spreads the KV tiles of all
+ *                  (128-row query tile, KV head) pairs evenly over one
+ *                  thread block per SM; a pair cut between blocks needs one
+ *                  slot per piece (at most 1 + ceil(pair tiles / tiles per
+ *                  block)).  With fewer slots the calls use fewer blocks;
+ *                  4 covers the workloads of the pages, 64 any problem.
  */
 int pkc_workspace_size(int batch, int num_qo_heads, int head_dim,
                        int num_ctas, int prefix_splits, size_t* bytes);

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cmath>
@@ -108,8 +109,9 @@ struct PrefixSetup {
   int64_t tokens = 0;
 };
 
-// Validate the prefix description and choose the KV split count: as many
-// splits as fill the SMs with one wave of row tiles, within the workspace.
+// Validate the prefix description and lay out its work: the flat KV tiles
+// of all (row tile, KV head) pairs split evenly over one block per SM, as
+// long as the pieces of any pair fit the workspace's partial slots.
 int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_indptr, int n_prefix, int batch,
                  int hq, int hkv, float sm_scale, uint8_t* ws, size_t ws_bytes, const WsLayout& L,
                  int32_t* status) {
@@ -131,32 +133,49 @@ int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_in
   p.g = hq / hkv;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.n_prefix = n_prefix;
+  // Flat KV tiles over the (row tile, KV head) pairs of every group.
   int tiles = 0;
-  int max_len = 0;
+  int64_t T = 0;
   for (int j = 0; j <= n_prefix; ++j) {
     p.kv_indptr[j] = kv_indptr[j];
     p.req_indptr[j] = req_indptr[j];
     p.tile_indptr[j] = tiles;
+    if (T > INT32_MAX) return set_error(PKC_ERR_UNSUPPORTED, "prefix: too many KV tiles (%lld)", (long long)T);
+    p.kvt_indptr[j] = (int32_t)T;
     if (j < n_prefix) {
       const int rows = (req_indptr[j + 1] - req_indptr[j]) * p.g;
-      tiles += (rows + 127) / 128;
-      max_len = std::max(max_len, kv_indptr[j + 1] - kv_indptr[j]);
+      const int rt = (rows + 127) / 128;
+      const int kvt = (kv_indptr[j + 1] - kv_indptr[j] + 127) / 128;
+      tiles += rt;
+      T += (int64_t)rt * hkv * kvt;
     }
   }
   S.n_tiles = tiles;
   S.tokens = kv_indptr[n_prefix];
   const size_t avail = ws_bytes > L.fixed_end ? (ws_bytes - L.fixed_end) / L.prefix_split : 0;
   if (avail < 1) return set_error(PKC_ERR_WORKSPACE, "workspace has no room for prefix partial states");
-  const int per_split = std::max(1, tiles * hkv);
-  int splits = std::max(1, num_sms() / per_split);
-  const int max_useful = std::max(1, (max_len + 127) / 128);
-  splits = std::min({splits, max_useful, (int)std::min<size_t>(avail, PKC_MAX_PREFIX_SPLITS)});
-  p.splits = splits;
-  for (int j = 0; j < n_prefix; ++j) {
-    const int len = kv_indptr[j + 1] - kv_indptr[j];
-    const int c = (len + splits - 1) / splits;
-    p.chunk[j] = std::max(128, (c + 127) / 128 * 128);
+  const int max_slots = (int)std::min<size_t>(avail, PKC_MAX_PREFIX_SPLITS);
+  // One block per SM (fewer if there are fewer tiles); the most pieces any
+  // pair is cut into must fit the workspace's partial slots.
+  int C = (int)std::min<int64_t>(num_sms(), T);
+  int slots = 0;
+  while (C > 0) {
+    slots = 1;
+    for (int j = 0; j < n_prefix; ++j) {
+      const int kvt = (kv_indptr[j + 1] - kv_indptr[j] + 127) / 128;
+      if (kvt == 0) continue;
+      const int n_pairs = (p.tile_indptr[j + 1] - p.tile_indptr[j]) * hkv;
+      for (int q = 0; q < n_pairs; ++q) {
+        const int64_t a = p.kvt_indptr[j] + (int64_t)q * kvt;
+        slots = std::max(slots, prefix_block_of(a + kvt - 1, T, C) - prefix_block_of(a, T, C) + 1);
+      }
+    }
+    if (slots <= max_slots) break;
+    --C;
   }
+  p.n_blocks = C;
+  p.total_tiles = T;
+  p.splits = std::max(1, slots);
   p.out_o = reinterpret_cast<float*>(ws + L.prefix);
   p.out_lse = reinterpret_cast<float*>(ws + L.prefix + al256(4 * (size_t)batch * hq * PKC_HEAD_DIM));
   p.split_stride_o = (int64_t)(L.prefix_split / 4);
@@ -172,7 +191,13 @@ void fill_contract_prefix(ContractParams& c, const PrefixSetup& S) {
   c.prefix_stride_lse = S.pp.split_stride_lse;
   c.prefix_splits = S.pp.splits;
   c.n_prefix = S.pp.n_prefix;
+  c.hkv = S.pp.hkv;
+  c.g = S.pp.g;
+  c.prefix_blocks = S.pp.n_blocks;
+  c.prefix_tiles = S.pp.total_tiles;
   std::memcpy(c.req_indptr, S.pp.req_indptr, sizeof(c.req_indptr));
+  std::memcpy(c.prefix_kv_indptr, S.pp.kv_indptr, sizeof(c.prefix_kv_indptr));
+  std::memcpy(c.prefix_kvt_indptr, S.pp.kvt_indptr, sizeof(c.prefix_kvt_indptr));
 }
 
 // Copy the plan-array offsets the contraction kernel needs.
@@ -384,7 +409,7 @@ int pkc_prefix_attention_state(const void* q, const void* k_prefix, const void* 
   if (int rc = setup_prefix(S, prefix_kv_indptr_host, prefix_req_indptr_host, n_prefix, batch, num_qo_heads,
                             num_kv_heads, sm_scale, ws, workspace_bytes, L, status))
     return rc;
-  int e = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, S.n_tiles, dtype, stream);
+  int e = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, stream);
   if (e == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
   if (e) return cuda_error(e, "prefix launch");
   ContractParams cp;
@@ -429,7 +454,7 @@ int pkc_cascade_decode(const void* q, const void* k_prefix, const void* v_prefix
   };
   mark(0);
   // 1. shared prefix: multi-query states on the tensor cores
-  int e = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, S.n_tiles, dtype, stream);
+  int e = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, stream);
   if (e == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
   if (e) return cuda_error(e, "prefix launch");
   mark(1);

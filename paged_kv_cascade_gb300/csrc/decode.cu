@@ -533,13 +533,26 @@ __global__ void __launch_bounds__(256) contract_kernel(const ContractParams p) {
     unit = pl[p.off_unit_list + row_idx];
     req = pl[p.off_unit_req + unit];
   }
-  // Sources: prefix splits of the request's group, then the suffix.
+  // Sources: the prefix pieces of the row's (row tile, KV head) pair, then
+  // the suffix.  A pair covering flat KV tiles [a, a + kvt) was computed in
+  // pieces by the prefix blocks block_of(a) .. block_of(a + kvt - 1), piece
+  // i in partial slot i.
   int group = -1;
   if (p.prefix_o) {
     for (int j = 0; j < p.n_prefix; ++j)
       if (p.req_indptr[j] <= req && req < p.req_indptr[j + 1]) { group = j; break; }
   }
-  int n_pref = group >= 0 ? p.prefix_splits : 0;
+  int n_pref = 0;
+  if (group >= 0) {
+    const int kvt = (p.prefix_kv_indptr[group + 1] - p.prefix_kv_indptr[group] + 127) / 128;
+    if (kvt > 0 && p.prefix_tiles > 0) {
+      const int rr = (req - p.req_indptr[group]) * p.g + h % p.g;  // row within the group's rows
+      const int pair = (rr / 128) * p.hkv + h / p.g;
+      const int64_t a = p.prefix_kvt_indptr[group] + (int64_t)pair * kvt;
+      n_pref = prefix_block_of(a + kvt - 1, p.prefix_tiles, p.prefix_blocks) -
+               prefix_block_of(a, p.prefix_tiles, p.prefix_blocks) + 1;
+    }
+  }
   int suf_kind = 0, suf_begin = 0, suf_n = 0;  // 1: direct state, 2: partial slots
   if (pl) {
     const int nch = pl[p.off_unit_n_chunks + unit];       // both loads in flight together

@@ -68,6 +68,22 @@ enum ContractMode {
   kContractAllRequests = 1 // rows = every request
 };
 
+// Prefix work split: the prefix stage's KV tiles are laid out flat, pair
+// after pair, where a pair is (128-row query tile, KV head) of one prefix
+// group (group j's pairs are q = row_tile * Hkv + kv_head, each covering
+// ceil(L_j / 128) KV tiles).  With T tiles over C thread blocks, block i
+// takes tiles [floor(i T / C), floor((i+1) T / C)); a pair that spans
+// several blocks is computed in pieces whose partial states are merged by
+// the contraction.  The piece of block i in a pair starting at tile A is
+// partial slot i - block_of(A).
+#if defined(__CUDACC__)
+#define PKC_HD __host__ __device__
+#else
+#define PKC_HD
+#endif
+PKC_HD inline int64_t prefix_block_begin(int i, int64_t T, int C) { return (int64_t)i * T / C; }
+PKC_HD inline int prefix_block_of(int64_t x, int64_t T, int C) { return (int)(((x + 1) * C - 1) / T); }
+
 struct ContractParams {
   int batch, hq;
   int mode;
@@ -84,7 +100,12 @@ struct ContractParams {
   int64_t prefix_stride_o, prefix_stride_lse;
   int prefix_splits;
   int n_prefix;
+  int hkv, g;                                      // KV heads, query heads per KV head
+  int prefix_blocks;                               // C of the prefix work split
+  int64_t prefix_tiles;                            // T of the prefix work split
   int32_t req_indptr[PKC_MAX_PREFIX + 1];
+  int32_t prefix_kv_indptr[PKC_MAX_PREFIX + 1];    // prefix tokens per group
+  int32_t prefix_kvt_indptr[PKC_MAX_PREFIX + 1];   // first flat KV tile of each group
   void* o;
   float* lse;
   int out_dtype;
@@ -95,11 +116,13 @@ struct PrefixParams {
   int batch, hq, hkv, g;
   float scale_log2;
   int n_prefix;
-  int splits;                               // KV splits per group
+  int splits;                               // partial slots per row (most pieces of one pair)
+  int n_blocks;                             // C: thread blocks of the work split
+  int64_t total_tiles;                      // T: flat KV tiles over all pairs
   int32_t kv_indptr[PKC_MAX_PREFIX + 1];
   int32_t req_indptr[PKC_MAX_PREFIX + 1];
   int32_t tile_indptr[PKC_MAX_PREFIX + 1];  // cumulative 128-row tiles
-  int32_t chunk[PKC_MAX_PREFIX];            // tokens per split (x128)
+  int32_t kvt_indptr[PKC_MAX_PREFIX + 1];   // first flat KV tile of each group
   float* out_o;                             // [split, B, Hq, D]
   float* out_lse;                           // [split, B, Hq]
   int64_t split_stride_o, split_stride_lse;
@@ -130,8 +153,8 @@ int launch_contract(const ContractParams& p, int n_rows, void* stream);
 // q/k/v tensor maps are built inside; returns cudaError_t or -1 when the
 // driver entry point for tensor maps is unavailable.
 int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix,
-                  const void* v_prefix, int64_t prefix_tokens, int n_tiles,
-                  int dtype, void* stream);
+                  const void* v_prefix, int64_t prefix_tokens, int dtype,
+                  void* stream);
 
 int num_sms();
 

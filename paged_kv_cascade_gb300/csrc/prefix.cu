@@ -6,9 +6,14 @@
 // computes all the group's queries against it on the tensor cores.  The
 // query rows of a tile are (request, query head) pairs of one KV head, GQA
 // heads fused with the request dimension (MLSys'25 notes, appendix A), 128
-// rows per tile.  The prefix KV is split into `splits` chunks per group so
-// the grid fills the SMs; each (row tile, chunk) writes a partial state
-// that the contraction kernel merges with (+).
+// rows per tile.
+//
+// Work split: the KV tiles of all (row tile, KV head) pairs are laid end to
+// end and cut evenly over one block per SM (see prefix_block_begin).  A
+// block walks its range piece by piece; a piece is the part of one pair
+// inside the range and yields a partial state in the pair's partial slot,
+// merged by the contraction kernel with (+) (MLSys'25 notes, A3: the final
+// output is the contraction of the partial outputs).
 //
 // Per 128-token KV tile j (FlashAttention-style online softmax, blog
 // section "Recursive Attention"):
@@ -18,13 +23,13 @@
 // m_ref is a per-row reference maximum.  It changes only when a tile's row
 // maximum exceeds it by more than 2^8 (P stays <= 256); then the row's O
 // columns are rescaled in TMEM before the next P.V.  With a stable maximum
-// nothing touches O until the end.
-// Roles: warp 0 issues TMA loads (Q once, K/V into a 3-stage ring), warp 1
-// allocates TMEM and issues MMAs, warps 2..9 own query rows, two threads
-// per row (64 columns each).  The row maximum is each thread's half maximum
-// swapped with its partner through shared memory at a barrier of just the
-// two warps; the exponent argument S c - m and the row sums use packed
-// two-wide fp32 FMAs.  TMEM: S double buffer (2 x 128 columns) + O
+// nothing touches O until the end of the piece.
+// Roles: warp 0 issues TMA loads (each piece's Q tile, K/V into a 3-stage
+// ring), warp 1 allocates TMEM and issues MMAs, warps 2..9 own query rows,
+// two threads per row (64 columns each).  The row maximum is each thread's
+// half maximum swapped with its partner through shared memory at a barrier
+// of just the two warps; the exponent argument S c - m and the row sums use
+// packed two-wide fp32 FMAs.  TMEM: S double buffer (2 x 128 columns) + O
 // (128).  P_j overwrites K_j's shared memory once S_j is complete.  All
 // waits are bounded (2 s) and set PKC_ERR_TIMEOUT when they run out.
 #include <cuda.h>
@@ -49,16 +54,46 @@ constexpr int kThreads = 320;  // TMA warp, MMA warp, 8 softmax warps
 constexpr uint32_t kTmemCols = 512;
 
 struct __align__(8) Barriers {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;  // a piece's Q tile landed / no longer read
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], o_full;
+  uint64_t o_done, o_free;   // a piece's O is final / has been read out
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int xok[2][2][4];  // [tile parity][column half][lane quadrant]: the warp had S
 };
 
-// Q, the K/V ring, barriers (256 B) and the row-exchange buffer (1 KB).  The
+// A piece of a block's range: KV tiles of one (row tile, KV head) pair.
+struct Piece {
+  int grp, mt, kvh, slot;  // prefix group, row tile within it, KV head, partial slot
+  int kv_lo, kv_hi;        // its prefix tokens
+  int n;                   // its KV tiles
+  int next;                // the flat tile after it
+};
+
+// The piece that starts at flat tile x of a block whose range ends at s1.
+__device__ __forceinline__ Piece piece_at(const PrefixParams& p, int x, int s1) {
+  int j = 0;
+  while (j + 1 < p.n_prefix && p.kvt_indptr[j + 1] <= x) ++j;
+  const int kvt = (p.kv_indptr[j + 1] - p.kv_indptr[j] + kKvTile - 1) / kKvTile;
+  const int off = x - p.kvt_indptr[j];
+  const int q = off / kvt, kt0 = off % kvt;
+  const int pair0 = p.kvt_indptr[j] + q * kvt;
+  const int end = min(s1, pair0 + kvt);
+  Piece g;
+  g.grp = j;
+  g.mt = q / p.hkv;
+  g.kvh = q % p.hkv;
+  g.slot = (int)blockIdx.x - prefix_block_of(pair0, p.total_tiles, p.n_blocks);
+  g.n = end - x;
+  g.kv_lo = p.kv_indptr[j] + kt0 * kKvTile;
+  g.kv_hi = min(p.kv_indptr[j + 1], g.kv_lo + g.n * kKvTile);
+  g.next = end;
+  return g;
+}
+
+// Q, the K/V ring, barriers (256 B) and the row-exchange buffer (2 KB).  The
 // base must be 1024-byte aligned for the 128B-swizzled TMA tiles; with no
 // static shared memory it is, and the kernel checks it.
 constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
@@ -82,20 +117,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.g;
-  const int kvh = blockIdx.y;
-  const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
-  int grp = 0;
-  while (grp + 1 < p.n_prefix && p.tile_indptr[grp + 1] <= tile) ++grp;
-  const int mt = tile - p.tile_indptr[grp];
-  const int req_hi = p.req_indptr[grp + 1];
-  const int b0 = p.req_indptr[grp] + mt * (kRows / G);
-  const int kv_lo = p.kv_indptr[grp] + split * p.chunk[grp];
-  const int kv_hi = min(p.kv_indptr[grp + 1], kv_lo + p.chunk[grp]);
-  const int n_tiles = kv_hi > kv_lo ? (kv_hi - kv_lo + kKvTile - 1) / kKvTile : 0;
+  // This block's flat KV tiles [s0, s1); every role walks the same pieces.
+  // (T fits in 32 bits: the host checks it.)
+  const int s0 = (int)prefix_block_begin((int)blockIdx.x, p.total_tiles, p.n_blocks);
+  const int s1 = (int)prefix_block_begin((int)blockIdx.x + 1, p.total_tiles, p.n_blocks);
 
   auto bar = [&](uint64_t& b) { return smem_u32(&b); };
   if (threadIdx.x == 0) {
     mbar_init(bar(bars->q_full), 1);
+    mbar_init(bar(bars->q_empty), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(bars->kv_full[s]), 1);
       mbar_init(bar(bars->kv_empty[s]), 1);
@@ -106,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(bars->p_full[b]), 256);
     }
     mbar_init(bar(bars->o_full), 1);
+    mbar_init(bar(bars->o_done), 1);
+    mbar_init(bar(bars->o_free), 256);
     mbar_init(bar(bars->drain), 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -126,73 +158,96 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
-      mbar_arrive_expect_tx(bar(bars->q_full), kQBytes);
-      tma_load_3d(s_q, &tm_q, bar(bars->q_full), 0, kvh * G, b0, pol_q);
-      tma_load_3d(s_q + kSubTile, &tm_q, bar(bars->q_full), 64, kvh * G, b0, pol_q);
-      int issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kStages;
-        if (!mbar_wait(bar(bars->kv_empty[s]), ((j / kStages) & 1) ^ 1, abort, p.status)) break;
-        const uint32_t st = s_stage0 + s * kStageBytes;
-        const int t0 = kv_lo + j * kKvTile;
-        mbar_arrive_expect_tx(bar(bars->kv_full[s]), kStageBytes);
-        tma_load_3d(st, &tm_k, bar(bars->kv_full[s]), 0, kvh, t0, pol);
-        tma_load_3d(st + kSubTile, &tm_k, bar(bars->kv_full[s]), 64, kvh, t0, pol);
-        tma_load_3d(st + 2 * kSubTile, &tm_v, bar(bars->kv_full[s]), 0, kvh, t0, pol);
-        tma_load_3d(st + 3 * kSubTile, &tm_v, bar(bars->kv_full[s]), 64, kvh, t0, pol);
-        issued = j + 1;
+      int g = 0, q_issued = 0;  // KV tiles and Q tiles issued
+      bool ok = true;
+      for (int x = s0; ok && x < s1;) {
+        const Piece pc = piece_at(p, x, s1);
+        x = pc.next;
+        // The previous piece's QK products must be done with the Q buffer.
+        if (q_issued > 0 && !mbar_wait(bar(bars->q_empty), (q_issued - 1) & 1, abort, p.status)) break;
+        const int b0 = p.req_indptr[pc.grp] + pc.mt * (kRows / G);
+        mbar_arrive_expect_tx(bar(bars->q_full), kQBytes);
+        tma_load_3d(s_q, &tm_q, bar(bars->q_full), 0, pc.kvh * G, b0, pol_q);
+        tma_load_3d(s_q + kSubTile, &tm_q, bar(bars->q_full), 64, pc.kvh * G, b0, pol_q);
+        ++q_issued;
+        for (int u = 0; u < pc.n; ++u) {
+          const int s = g % kStages;
+          if (!mbar_wait(bar(bars->kv_empty[s]), ((g / kStages) & 1) ^ 1, abort, p.status)) { ok = false; break; }
+          const uint32_t st = s_stage0 + s * kStageBytes;
+          const int t0 = pc.kv_lo + u * kKvTile;
+          mbar_arrive_expect_tx(bar(bars->kv_full[s]), kStageBytes);
+          tma_load_3d(st, &tm_k, bar(bars->kv_full[s]), 0, pc.kvh, t0, pol);
+          tma_load_3d(st + kSubTile, &tm_k, bar(bars->kv_full[s]), 64, pc.kvh, t0, pol);
+          tma_load_3d(st + 2 * kSubTile, &tm_v, bar(bars->kv_full[s]), 0, pc.kvh, t0, pol);
+          tma_load_3d(st + 3 * kSubTile, &tm_v, bar(bars->kv_full[s]), 64, pc.kvh, t0, pol);
+          ++g;
+        }
       }
       if (*abort) {
         // Let the copies already issued land before the block exits.
         volatile int no_abort = 0;
-        mbar_wait(bar(bars->q_full), 0, &no_abort, p.status);
-        for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+        if (q_issued > 0) mbar_wait(bar(bars->q_full), (q_issued - 1) & 1, &no_abort, p.status);
+        for (int j = g > kStages ? g - kStages : 0; j < g; ++j)
           mbar_wait(bar(bars->kv_full[j % kStages]), (j / kStages) & 1, &no_abort, p.status);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0) {
       constexpr uint32_t kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value ? 1 : 0;
       constexpr uint32_t idesc_qk = idesc_f16(128, 128, kBf16, 0, 0);
       constexpr uint32_t idesc_pv = idesc_f16(128, 128, kBf16, 0, 1);
-      bool ok = mbar_wait(bar(bars->q_full), 0, abort, p.status);
-      tc_fence_after();
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          const int s = j % kStages, b = j & 1;
-          ok = mbar_wait(bar(bars->kv_full[s]), (j / kStages) & 1, abort, p.status) &&
-               mbar_wait(bar(bars->s_free[b]), ((j >> 1) & 1) ^ 1, abort, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t kb = s_stage0 + s * kStageBytes;
+      bool ok = true;
+      int g = 0, k = 0;  // first KV tile of the piece, piece index
+      for (int x = s0; ok && x < s1; ++k) {
+        const Piece pc = piece_at(p, x, s1);
+        x = pc.next;
+        ok = mbar_wait(bar(bars->q_full), k & 1, abort, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        for (int u = 0; ok && u <= pc.n; ++u) {
+          if (u < pc.n) {
+            const int j = g + u, s = j % kStages, b = j & 1;
+            ok = mbar_wait(bar(bars->kv_full[s]), (j / kStages) & 1, abort, p.status) &&
+                 mbar_wait(bar(bars->s_free[b]), ((j >> 1) & 1) ^ 1, abort, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t kb = s_stage0 + s * kStageBytes;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kSubTile + (kk & 3) * 32;
-            tc_mma_f16(tmem + b * 128, smem_desc_sw128(s_q + off, 16, 1024),
-                       smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * kSubTile + (kk & 3) * 32;
+              tc_mma_f16(tmem + b * 128, smem_desc_sw128(s_q + off, 16, 1024),
+                         smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+            }
+            tc_commit(bar(bars->s_full[b]));
+            if (u == pc.n - 1) tc_commit(bar(bars->q_empty));  // the piece's last read of Q
           }
-          tc_commit(bar(bars->s_full[b]));
-        }
-        if (j >= 1) {
-          const int jp = j - 1, sp = jp % kStages, bp = jp & 1;
-          ok = mbar_wait(bar(bars->p_full[bp]), (jp >> 1) & 1, abort, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t pb = s_stage0 + sp * kStageBytes;  // P overwrote K
-          const uint32_t vb = pb + 2 * kSubTile;
+          if (u >= 1) {
+            const int jp = g + u - 1, sp = jp % kStages, bp = jp & 1;
+            ok = mbar_wait(bar(bars->p_full[bp]), (jp >> 1) & 1, abort, p.status);
+            // The first P.V of a piece overwrites O: the previous piece's O
+            // must have been read out.
+            if (ok && u == 1 && k > 0) ok = mbar_wait(bar(bars->o_free), (k - 1) & 1, abort, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t pb = s_stage0 + sp * kStageBytes;  // P overwrote K
+            const uint32_t vb = pb + 2 * kSubTile;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // O accumulates over the tiles
-            const uint32_t a_off = (kk >> 2) * kSubTile + (kk & 3) * 32;
-            tc_mma_f16(tmem + 256, smem_desc_sw128(pb + a_off, 16, 1024),
-                       smem_desc_sw128(vb + kk * 2048, kSubTile, 1024), idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {  // O accumulates over the piece's tiles
+              const uint32_t a_off = (kk >> 2) * kSubTile + (kk & 3) * 32;
+              tc_mma_f16(tmem + 256, smem_desc_sw128(pb + a_off, 16, 1024),
+                         smem_desc_sw128(vb + kk * 2048, kSubTile, 1024), idesc_pv, (u > 1 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(bar(bars->o_full));
+            tc_commit(bar(bars->kv_empty[sp]));
           }
-          tc_commit(bar(bars->o_full));
-          tc_commit(bar(bars->kv_empty[sp]));
         }
+        if (!ok) break;
+        tc_commit(bar(bars->o_done));
+        g += pc.n;
       }
       // Drain: every MMA issued above completes before TMEM is released.
       tc_commit(bar(bars->drain));
@@ -209,18 +264,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xch = reinterpret_cast<float*>(smem + kXchOffset);  // [2 half][128]
     float* xmx = xch;  // in the loop: [tile parity][half][128] row half-maxima
     constexpr float kRescaleLog2 = 8.f;  // move m_ref only when the max grows by > 2^8
-    float m_ref = neg_inf(), l_run = 0.f;
     bool ok = true;
     // Both threads of a row reach the same row maximum (their two half
     // maxima, swapped), hence the same m_ref.  Decisions that guard
     // warp-collective TMEM accesses are made warp-uniform (__all_sync /
     // __any_sync); warp w and warp w+4 hold the same rows and reach the
     // same decisions.
-    for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1, s = j % kStages;
+    int g = 0, k = 0;  // first KV tile of the piece, piece index
+    for (int x = s0; x < s1; ++k) {
+    const int x_piece = x;
+    int n_kv, kv_lo, kv_hi;  // the loop needs only these; the rest is recomputed for the epilogue
+    {
+      const Piece pc = piece_at(p, x, s1);
+      x = pc.next;
+      n_kv = pc.n;
+      kv_lo = pc.kv_lo;
+      kv_hi = pc.kv_hi;
+    }
+    float m_ref = neg_inf(), l_run = 0.f;
+    for (int u = 0; u < n_kv; ++u) {
+      const int j = g + u, b = j & 1, s = j % kStages;
       const bool got = ok && mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
       const bool have = __all_sync(0xffffffffu, got);
-      const int vrow = min(kKvTile, kv_hi - (kv_lo + j * kKvTile));  // valid columns of the row
+      const int vrow = min(kKvTile, kv_hi - (kv_lo + u * kKvTile));  // valid columns of the row
       const int valid = vrow - ch * 64;                                  // of my half
       uint32_t sr[2][32];
       float mx = neg_inf();
@@ -265,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = fmaxf(m_ref, m_tile);
         const float r = ex2(m_ref - m_new);  // 0 while m_ref is -inf, 1 if unchanged
         l_run *= r;
-        if (j > 0) {
+        if (u > 0) {
           // O holds P.V of tiles < j: wait for the last of them (the S_j
           // commit already covered tile j-2), rescale my columns in TMEM.
           // On a timeout the warp skips the rest of the tile; its partner
@@ -273,19 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool done = mbar_wait(bar(bars->o_full), (j - 1) & 1, abort, p.status);
           if (!__all_sync(0xffffffffu, done)) { ok = false; continue; }
           tc_fence_after();
-          uint32_t o[2][32];
-          tmem_ld_32x32b_x32(mine_cols + 256, o[0]);
-          tmem_ld_32x32b_x32(mine_cols + 256 + 32, o[1]);
-          tmem_ld_wait();
-          reg_fence32(o[0]);
-          reg_fence32(o[1]);
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {  // 32 columns at a time: S stays in registers
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(mine_cols + 256 + c * 32, o);
+            tmem_ld_wait();
+            reg_fence32(o);
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[c][i] = __float_as_uint(__uint_as_float(o[c][i]) * r);
-          tmem_st_32x32b_x32(mine_cols + 256, o[0]);
-          tmem_st_32x32b_x32(mine_cols + 256 + 32, o[1]);
-          tmem_st_wait();
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * r);
+            tmem_st_32x32b_x32(mine_cols + 256 + c * 32, o);
+            tmem_st_wait();
+          }
         }
         m_ref = m_new;
       }
@@ -331,45 +395,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(bars->p_full[b]));
       mbar_arrive(bar(bars->s_free[b]));
     }
-    // O is final once every MMA has completed (the MMA warp's drain barrier).
-    if (n_tiles > 0) {
-      const bool done = ok && mbar_wait(bar(bars->drain), 0, abort, p.status);
-      ok = __all_sync(0xffffffffu, done);
-    }
+    g += n_kv;
+    // O of the piece is final once its last P.V has completed.
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(bars->o_done), k & 1, abort, p.status));
     // Both halves used the same reference maximum: their sums add.  (xch
     // doubles as the loop's max-exchange buffer: the two warps of a lane
-    // quadrant pass one more pair barrier before it is rewritten.)
+    // quadrant pass a pair barrier before and after using it here.)
     asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
     xch[ch * 128 + row] = l_run;
     const bool all_ok = bar_and_sync(ok, 256);
     const float l_tot = l_run + xch[(ch ^ 1) * 128 + row];
-    uint32_t o[2][32];
-    if (all_ok && n_tiles > 0) {
-      tc_fence_after();
-      tmem_ld_32x32b_x32(mine_cols + 256, o[0]);
-      tmem_ld_32x32b_x32(mine_cols + 256 + 32, o[1]);
-      tmem_ld_wait();
-      reg_fence32(o[0]);
-      reg_fence32(o[1]);
-    }
-
-    // Epilogue: rows that belong to this group write their state.
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
+    // Epilogue: rows that belong to the piece's group write its state, 32
+    // columns at a time.
+    const Piece pc = piece_at(p, x_piece, s1);
+    const int b0 = p.req_indptr[pc.grp] + pc.mt * (kRows / G);
     const int rb = b0 + row / G;
-    if (rb < req_hi && rb < p.batch) {
-      const int h = kvh * G + row % G;
-      const int64_t r = (int64_t)rb * p.hq + h;
-      float* out = p.out_o + split * p.split_stride_o + r * PKC_HEAD_DIM + ch * 64;
-      const bool has = all_ok && n_tiles > 0 && l_tot > 0.f;
-      const float inv = has ? 1.f / l_tot : 0.f;
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
+    const bool mine_row = rb < p.req_indptr[pc.grp + 1] && rb < p.batch;
+    const int64_t r = (int64_t)rb * p.hq + pc.kvh * G + row % G;
+    float* out = p.out_o + pc.slot * p.split_stride_o + r * PKC_HEAD_DIM + ch * 64;
+    const bool has = all_ok && l_tot > 0.f;
+    const float inv = has ? 1.f / l_tot : 0.f;
+    if (all_ok) tc_fence_after();
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      uint32_t o[32];
+      if (all_ok) {  // warp-uniform
+        tmem_ld_32x32b_x32(mine_cols + 256 + c * 32, o);
+        tmem_ld_wait();
+        reg_fence32(o);
+      }
+      if (mine_row) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
           *reinterpret_cast<float4*>(out + c * 32 + i) =
-              has ? make_float4(__uint_as_float(o[c][i]) * inv, __uint_as_float(o[c][i + 1]) * inv,
-                                __uint_as_float(o[c][i + 2]) * inv, __uint_as_float(o[c][i + 3]) * inv)
+              has ? make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                                __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv)
                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ch == 0) p.out_lse[split * p.split_stride_lse + r] = has ? (m_ref + lg2(l_tot)) * kLn2 : neg_inf();
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(bar(bars->o_free));  // the next piece's first P.V may overwrite O
+    if (mine_row && ch == 0)
+      p.out_lse[pc.slot * p.split_stride_lse + r] = has ? (m_ref + lg2(l_tot)) * kLn2 : neg_inf();
+    if (!all_ok) break;  // uniform over the softmax warps
     }
   }
 
@@ -391,7 +460,7 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d0, uint64_t
 
 template <typename T>
 int launch_t(const PrefixParams& p, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-             int n_tiles, cudaStream_t st) {
+             cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -399,7 +468,7 @@ int launch_t(const PrefixParams& p, const CUtensorMap& q, const CUtensorMap& k, 
                                     kSmemBytes);
   });
   if (attr_err != cudaSuccess) return (int)attr_err;
-  const dim3 grid(n_tiles * p.splits, p.hkv);
+  const dim3 grid(p.n_blocks, 1);  // one block per SM, each over an even share of the KV tiles
   prefix_state_kernel<T><<<grid, kThreads, kSmemBytes, st>>>(q, k, v, p);
   return (int)cudaGetLastError();
 }
@@ -407,16 +476,16 @@ int launch_t(const PrefixParams& p, const CUtensorMap& q, const CUtensorMap& k, 
 }  // namespace
 
 int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix, const void* v_prefix,
-                  int64_t prefix_tokens, int n_tiles, int dtype, void* stream) {
-  if (n_tiles <= 0) return 0;
+                  int64_t prefix_tokens, int dtype, void* stream) {
+  if (p.n_blocks <= 0 || p.total_tiles <= 0) return 0;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, dtype, PKC_HEAD_DIM, p.hq, p.batch, p.g, kRows / p.g) ||
       !make_map(&mk, k_prefix, dtype, PKC_HEAD_DIM, p.hkv, prefix_tokens, 1, kKvTile) ||
       !make_map(&mv, v_prefix, dtype, PKC_HEAD_DIM, p.hkv, prefix_tokens, 1, kKvTile))
     return -1;
   cudaStream_t st = (cudaStream_t)stream;
-  return dtype == PKC_BF16 ? launch_t<__nv_bfloat16>(p, mq, mk, mv, n_tiles, st)
-                           : launch_t<__half>(p, mq, mk, mv, n_tiles, st);
+  return dtype == PKC_BF16 ? launch_t<__nv_bfloat16>(p, mq, mk, mv, st)
+                           : launch_t<__half>(p, mq, mk, mv, st);
 }
 
 }  // namespace pkc

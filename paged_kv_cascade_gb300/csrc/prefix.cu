@@ -30,8 +30,10 @@
 // half maximum swapped with its partner through shared memory at a barrier
 // of just the two warps; the exponent argument S c - m and the row sums use
 // packed two-wide fp32 FMAs.  TMEM: S double buffer (2 x 128 columns) + O
-// (128).  P_j overwrites K_j's shared memory once S_j is complete.  All
-// waits are bounded (2 s) and set PKC_ERR_TIMEOUT when they run out.
+// double buffer (2 x 128): a piece's O is read out while the next piece
+// accumulates into the other.  P_j overwrites K_j's shared memory once S_j
+// is complete.  All waits are bounded (2 s) and set PKC_ERR_TIMEOUT when
+// they run out.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -57,7 +59,8 @@ struct __align__(8) Barriers {
   uint64_t q_full, q_empty;  // a piece's Q tile landed / no longer read
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], o_full;
-  uint64_t o_done, o_free;   // a piece's O is final / has been read out
+  uint64_t o_done;           // a piece's O is final
+  uint64_t o_free[2];        // O buffer b has been read out
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -137,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(bars->o_full), 1);
     mbar_init(bar(bars->o_done), 1);
-    mbar_init(bar(bars->o_free), 256);
+    mbar_init(bar(bars->o_free[0]), 256);
+    mbar_init(bar(bars->o_free[1]), 256);
     mbar_init(bar(bars->drain), 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -166,16 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int x = s0; ok && x < s1;) {
         const Piece pc = piece_at(p, x, s1);
         x = pc.next;
-        // The previous piece's QK products must be done with the Q buffer.
-        if (q_issued > 0 && !mbar_wait(bar(bars->q_empty), (q_issued - 1) & 1, abort, p.status)) break;
-        const int b0 = p.req_indptr[pc.grp] + pc.mt * (kRows / G);
-        mbar_arrive_expect_tx(bar(bars->q_full), kQBytes);
-        tma_load_3d(s_q, &tm_q, bar(bars->q_full), 0, pc.kvh * G, b0, pol_q);
-        tma_load_3d(s_q + kSubTile, &tm_q, bar(bars->q_full), 64, pc.kvh * G, b0, pol_q);
-        ++q_issued;
-        for (int u = 0; u < pc.n; ++u) {
+        auto load_kv = [&](int u) -> bool {
           const int s = g % kStages;
-          if (!mbar_wait(bar(bars->kv_empty[s]), ((g / kStages) & 1) ^ 1, abort, p.status)) { ok = false; break; }
+          if (!mbar_wait(bar(bars->kv_empty[s]), ((g / kStages) & 1) ^ 1, abort, p.status)) return false;
           const uint32_t st = s_stage0 + s * kStageBytes;
           const int t0 = pc.kv_lo + u * kKvTile;
           mbar_arrive_expect_tx(bar(bars->kv_full[s]), kStageBytes);
@@ -184,7 +181,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(st + 2 * kSubTile, &tm_v, bar(bars->kv_full[s]), 0, pc.kvh, t0, pol);
           tma_load_3d(st + 3 * kSubTile, &tm_v, bar(bars->kv_full[s]), 64, pc.kvh, t0, pol);
           ++g;
-        }
+          return true;
+        };
+        // After the first piece, the ring fills with this piece's KV tiles
+        // while the previous piece's products still read the Q buffer.
+        const int pre = q_issued > 0 ? min(pc.n, kStages) : 0;
+        for (int u = 0; ok && u < pre; ++u) ok = load_kv(u);
+        if (!ok) break;
+        if (q_issued > 0 && !mbar_wait(bar(bars->q_empty), (q_issued - 1) & 1, abort, p.status)) break;
+        const int b0 = p.req_indptr[pc.grp] + pc.mt * (kRows / G);
+        mbar_arrive_expect_tx(bar(bars->q_full), kQBytes);
+        tma_load_3d(s_q, &tm_q, bar(bars->q_full), 0, pc.kvh * G, b0, pol_q);
+        tma_load_3d(s_q + kSubTile, &tm_q, bar(bars->q_full), 64, pc.kvh * G, b0, pol_q);
+        ++q_issued;
+        for (int u = pre; ok && u < pc.n; ++u) ok = load_kv(u);
       }
       if (*abort) {
         // Let the copies already issued land before the block exits.
@@ -230,7 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(bar(bars->p_full[bp]), (jp >> 1) & 1, abort, p.status);
             // The first P.V of a piece overwrites O: the previous piece's O
             // must have been read out.
-            if (ok && u == 1 && k > 0) ok = mbar_wait(bar(bars->o_free), (k - 1) & 1, abort, p.status);
+            // (O is double-buffered: piece k uses buffer k & 1, last read
+            // out by the epilogue of piece k - 2.)
+            if (ok && u == 1 && k > 1) ok = mbar_wait(bar(bars->o_free[k & 1]), ((k >> 1) - 1) & 1, abort, p.status);
             if (!ok) break;
             tc_fence_after();
             const uint32_t pb = s_stage0 + sp * kStageBytes;  // P overwrote K
@@ -238,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {  // O accumulates over the piece's tiles
               const uint32_t a_off = (kk >> 2) * kSubTile + (kk & 3) * 32;
-              tc_mma_f16(tmem + 256, smem_desc_sw128(pb + a_off, 16, 1024),
+              tc_mma_f16(tmem + 256 + (k & 1) * 128, smem_desc_sw128(pb + a_off, 16, 1024),
                          smem_desc_sw128(vb + kk * 2048, kSubTile, 1024), idesc_pv, (u > 1 || kk > 0) ? 1u : 0u);
             }
             tc_commit(bar(bars->o_full));
@@ -282,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       kv_hi = pc.kv_hi;
     }
     float m_ref = neg_inf(), l_run = 0.f;
+    const uint32_t o_cols = mine_cols + 256 + (k & 1) * 128;  // this piece's O buffer, my columns
     for (int u = 0; u < n_kv; ++u) {
       const int j = g + u, b = j & 1, s = j % kStages;
       const bool got = ok && mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
@@ -342,12 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {  // 32 columns at a time: S stays in registers
             uint32_t o[32];
-            tmem_ld_32x32b_x32(mine_cols + 256 + c * 32, o);
+            tmem_ld_32x32b_x32(o_cols + c * 32, o);
             tmem_ld_wait();
             reg_fence32(o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * r);
-            tmem_st_32x32b_x32(mine_cols + 256 + c * 32, o);
+            tmem_st_32x32b_x32(o_cols + c * 32, o);
             tmem_st_wait();
           }
         }
@@ -421,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < 2; ++c) {
       uint32_t o[32];
       if (all_ok) {  // warp-uniform
-        tmem_ld_32x32b_x32(mine_cols + 256 + c * 32, o);
+        tmem_ld_32x32b_x32(o_cols + c * 32, o);
         tmem_ld_wait();
         reg_fence32(o);
       }
@@ -435,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     tc_fence_before();
-    mbar_arrive(bar(bars->o_free));  // the next piece's first P.V may overwrite O
+    mbar_arrive(bar(bars->o_free[k & 1]));  // piece k + 2 may overwrite this O buffer
     if (mine_row && ch == 0)
       p.out_lse[pc.slot * p.split_stride_lse + r] = has ? (m_ref + lg2(l_tot)) * kLn2 : neg_inf();
     if (!all_ok) break;  // uniform over the softmax warps

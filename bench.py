@@ -128,7 +128,8 @@ def kernel_traffic(kernel, workload):
     source hash matches the current kernel source and it was recorded on
     this workload; else None."""
     import hashlib
-    src_file = {"paged_decode": "decode.cu", "prefix_state": "prefix.cu"}.get(kernel)
+    src_file = {"paged_decode_kernel": "decode.cu", "paged_decode_mma_kernel": "decode_mma.cu",
+                "prefix_state_kernel": "prefix.cu"}.get(kernel)
     summ = os.path.join(ROOT, "profiles", f"{kernel}_traffic.md")
     if not src_file or not os.path.exists(summ):
         return None
@@ -564,7 +565,12 @@ def main():
         alg_bytes = suffix_tokens * kvb
         unit_desc = f"{kvb} B per suffix token x {suffix_tokens} tokens"
     achieved = alg_bytes / (stage_ms[dominant] / 1e3) / 1e9
-    tr = kernel_traffic(dominant, args.workload if args.batch is None else None)
+    # the decode kernel the library picks (pkc_set_decode_kernel semantics)
+    G = Hq // p["num_kv_heads"]
+    mma = args.decode_kernel == "mma" or (args.decode_kernel == "auto" and G >= 2)
+    kernel_name = {"prefix_state": "prefix_state_kernel"}.get(
+        dominant, "paged_decode_mma_kernel" if mma else "paged_decode_kernel")
+    tr = kernel_traffic(kernel_name, args.workload if args.batch is None else None)
     # prefix stage on the tensor cores: FLOPs 4*D per (row, prefix token)
     rows_per_prefix = np.diff(p["prefix_req_indptr"]) * (Hq // p["num_kv_heads"])
     prefix_flops = float(4 * D * np.sum(rows_per_prefix * np.diff(p["prefix_kv_indptr"])) *
@@ -668,7 +674,7 @@ def main():
             "hbm_fraction": value / world / hbm_peak,
             "stages_us": {k: 1e3 * v for k, v in stage_ms.items()},
             "host_plan_us": 1e6 * statistics.mean(host_plan_s) if host_plan_s else None,
-            "roofline": {"kernel": dominant, "bound": "hbm", "achieved": achieved,
+            "roofline": {"kernel": kernel_name, "stage": dominant, "bound": "hbm", "achieved": achieved,
                          "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                          "peak_source": f"{peak_kind} hbm_gbs",
                          "algorithmic_bytes_per_launch": alg_bytes, "per_unit": unit_desc,

@@ -25,11 +25,12 @@
 // columns are rescaled in TMEM before the next P.V.  With a stable maximum
 // nothing touches O until the end of the piece.
 // Roles: warp 0 issues TMA loads (each piece's Q tile, K/V into a 3-stage
-// ring), warp 1 allocates TMEM and issues MMAs, warps 2..9 own query rows,
-// two threads per row (64 columns each).  The row maximum is each thread's
-// half maximum swapped with its partner through shared memory at a barrier
-// of just the two warps; the exponent argument S c - m and the row sums use
-// packed two-wide fp32 FMAs.  TMEM: S double buffer (2 x 128 columns) + O
+// ring), warp 1 allocates TMEM and issues MMAs, warps 2..9 own 16 query rows
+// each.  They read S with the 16x256b TMEM shape, four threads per row and
+// two rows per thread, so row maxima and sums are two shuffles and no
+// softmax warp waits for another; P goes back to shared memory with
+// stmatrix.  The exponent argument S c - m and the row sums use packed
+// two-wide fp32 FMAs.  TMEM: S double buffer (2 x 128 columns) + O
 // double buffer (2 x 128): a piece's O is read out while the next piece
 // accumulates into the other.  P_j overwrites K_j's shared memory once S_j
 // is complete.  All waits are bounded (2 s) and set PKC_ERR_TIMEOUT when
@@ -64,7 +65,6 @@ struct __align__(8) Barriers {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int xok[2][2][4];  // [tile parity][column half][lane quadrant]: the warp had S
 };
 
 // A piece of a block's range: KV tiles of one (row tile, KV head) pair.
@@ -96,12 +96,11 @@ __device__ __forceinline__ Piece piece_at(const PrefixParams& p, int x, int s1) 
   return g;
 }
 
-// Q, the K/V ring, barriers (256 B) and the row-exchange buffer (2 KB).  The
-// base must be 1024-byte aligned for the 128B-swizzled TMA tiles; with no
-// static shared memory it is, and the kernel checks it.
+// Q, the K/V ring and the barriers (256 B).  The base must be 1024-byte
+// aligned for the 128B-swizzled TMA tiles; with no static shared memory it
+// is, and the kernel checks it.
 constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
-constexpr int kXchOffset = kBarOffset + 256;
-constexpr int kSmemBytes = kXchOffset + 4 * 128 * 4;
+constexpr int kSmemBytes = kBarOffset + 256;
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -267,191 +266,211 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(bars->drain), 0, &no_abort, p.status);
     }
   } else {
-    // ------- softmax: two threads per query row, 64 columns each -------
-    const int quad = warp & 3;         // TMEM lanes 32*quad .. 32*quad+31
-    const int ch = (warp - 2) >> 2;    // column half: 0 -> 0..63, 1 -> 64..127
-    const int row = quad * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-    const uint32_t mine_cols = lane_base + ch * 64;         // this thread's columns
-    float* xch = reinterpret_cast<float*>(smem + kXchOffset);  // [2 half][128]
-    float* xmx = xch;  // in the loop: [tile parity][half][128] row half-maxima
+    // ------- softmax: 16 rows per warp, four threads per row -------
+    // The 16x256b TMEM shape gives each thread two rows (the warp's rows l
+    // and l + 8) and 32 columns of each (pairs 8j + 2c, +1 with c = lane % 4),
+    // so a row's maximum and sum take two shuffles among its four threads and
+    // no softmax warp ever waits for another.
+    const int quad = warp & 3;                // TMEM lane quadrant
+    const int hq16 = (warp - 2) >> 2;         // which 16 lanes of the quadrant
+    const int rbase = quad * 32 + hq16 * 16;  // the warp's first row
+    const int g4 = lane >> 2, c4 = lane & 3;
+    const uint32_t lane_base = tmem + ((uint32_t)rbase << 16);
     constexpr float kRescaleLog2 = 8.f;  // move m_ref only when the max grows by > 2^8
+    const uint64_t c2 = pk2(p.scale_log2, p.scale_log2), one2 = pk2(1.f, 1.f);
     bool ok = true;
-    // Both threads of a row reach the same row maximum (their two half
-    // maxima, swapped), hence the same m_ref.  Decisions that guard
-    // warp-collective TMEM accesses are made warp-uniform (__all_sync /
-    // __any_sync); warp w and warp w+4 hold the same rows and reach the
-    // same decisions.
     int g = 0, k = 0;  // first KV tile of the piece, piece index
-    for (int x = s0; x < s1; ++k) {
-    const int x_piece = x;
-    int n_kv, kv_lo, kv_hi;  // the loop needs only these; the rest is recomputed for the epilogue
-    {
-      const Piece pc = piece_at(p, x, s1);
-      x = pc.next;
-      n_kv = pc.n;
-      kv_lo = pc.kv_lo;
-      kv_hi = pc.kv_hi;
-    }
-    float m_ref = neg_inf(), l_run = 0.f;
-    const uint32_t o_cols = mine_cols + 256 + (k & 1) * 128;  // this piece's O buffer, my columns
-    for (int u = 0; u < n_kv; ++u) {
-      const int j = g + u, b = j & 1, s = j % kStages;
-      const bool got = ok && mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
-      const bool have = __all_sync(0xffffffffu, got);
-      const int vrow = min(kKvTile, kv_hi - (kv_lo + u * kKvTile));  // valid columns of the row
-      const int valid = vrow - ch * 64;                                  // of my half
-      uint32_t sr[2][32];
-      float mx = neg_inf();
-      if (have) {
+    for (int x = s0; ok && x < s1; ++k) {
+      const int x_piece = x;
+      int n_kv, kv_lo, kv_hi;
+      {
+        const Piece pc = piece_at(p, x, s1);
+        x = pc.next;
+        n_kv = pc.n;
+        kv_lo = pc.kv_lo;
+        kv_hi = pc.kv_hi;
+      }
+      float mt_ref = neg_inf(), mb_ref = neg_inf();  // rows l (top) and l + 8 (bottom)
+      uint64_t lt2 = 0ull, lb2 = 0ull;                 // packed row sums
+      const uint32_t o_base = lane_base + 256 + (k & 1) * 128;  // this piece's O buffer
+      for (int u = 0; u < n_kv; ++u) {
+        const int j = g + u, b = j & 1, s = j % kStages;
+        const bool got = ok && mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc_fence_after();
-        tmem_ld_32x32b_x32(mine_cols + b * 128, sr[0]);
-        tmem_ld_32x32b_x32(mine_cols + b * 128 + 32, sr[1]);
+        const int vrow = min(kKvTile, kv_hi - (kv_lo + u * kKvTile));  // valid columns
+        uint32_t sr[2][32];  // [64-column half][4 j + e]
+        tmem_ld_16x256b_x8(lane_base + b * 128, sr[0]);
+        tmem_ld_16x256b_x8(lane_base + b * 128 + 64, sr[1]);
         tmem_ld_wait();
         reg_fence32(sr[0]);
         reg_fence32(sr[1]);
-        float m8[8];
+        float mt = neg_inf(), mb = neg_inf();
+        if (vrow == kKvTile) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = neg_inf();
-        auto fold_max = [&](const uint32_t (&v)[32], int col0) {
-          if (col0 + 32 <= vrow) {  // all valid: three-input max, no per-element test
+          for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-              m8[k & 7] = max3(m8[k & 7], __uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
-          } else {
+            for (int jj = 0; jj < 8; ++jj) {
+              mt = max3(mt, __uint_as_float(sr[h][4 * jj]), __uint_as_float(sr[h][4 * jj + 1]));
+              mb = max3(mb, __uint_as_float(sr[h][4 * jj + 2]), __uint_as_float(sr[h][4 * jj + 3]));
+            }
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col0 + i < vrow) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(v[i]));
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int col = 64 * h + 8 * jj + 2 * c4 + (e & 1);
+                const float v = __uint_as_float(sr[h][4 * jj + e]);
+                if (col < vrow) {
+                  if (e < 2) mt = fmaxf(mt, v);
+                  else mb = fmaxf(mb, v);
+                }
+              }
+        }
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        const float tt = mt * p.scale_log2, tb = mb * p.scale_log2;
+        if (__any_sync(0xffffffffu, tt > mt_ref + kRescaleLog2 || tb > mb_ref + kRescaleLog2)) {
+          const float nt = fmaxf(mt_ref, tt), nb = fmaxf(mb_ref, tb);
+          const float rt = ex2(mt_ref - nt), rb = ex2(mb_ref - nb);  // 0 while the reference is -inf
+          {
+            const float2 a = upk2(lt2), c = upk2(lb2);
+            lt2 = pk2(a.x * rt, a.y * rt);
+            lb2 = pk2(c.x * rb, c.y * rb);
           }
-        };
-        fold_max(sr[0], ch * 64);
-        fold_max(sr[1], ch * 64 + 32);
-        mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-      }
-      // The row's two threads swap their half maxima through shared memory
-      // (slots alternate with the tile parity, so a fast warp cannot
-      // overwrite a value its partner has not read).  The named barrier
-      // joins just the two warps of this lane quadrant; both reach it on
-      // every tile, whether or not S arrived, and leave together.
-      xmx[(b * 2 + ch) * 128 + row] = mx;
-      if (lane == 0) bars->xok[b][ch][quad] = have ? 1 : 0;
-      asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
-      const bool both = have && bars->xok[b][ch ^ 1][quad] != 0;
-      if (!both) { ok = false; break; }
-      mx = fmaxf(mx, xmx[(b * 2 + (ch ^ 1)) * 128 + row]);
-      const float m_tile = mx * p.scale_log2;
-      if (__any_sync(0xffffffffu, m_tile > m_ref + kRescaleLog2)) {
-        const float m_new = fmaxf(m_ref, m_tile);
-        const float r = ex2(m_ref - m_new);  // 0 while m_ref is -inf, 1 if unchanged
-        l_run *= r;
-        if (u > 0) {
-          // O holds P.V of tiles < j: wait for the last of them (the S_j
-          // commit already covered tile j-2), rescale my columns in TMEM.
-          // On a timeout the warp skips the rest of the tile; its partner
-          // learns of it at the next pair barrier and both leave there.
-          const bool done = mbar_wait(bar(bars->o_full), (j - 1) & 1, abort, p.status);
-          if (!__all_sync(0xffffffffu, done)) { ok = false; continue; }
-          tc_fence_after();
+          if (u > 0) {
+            // O holds P.V of the piece's tiles < u: wait for the last of them
+            // (the S_j commit already covered tile j-2), rescale my rows.
+            const bool done = mbar_wait(bar(bars->o_full), (j - 1) & 1, abort, p.status);
+            if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 2; ++c) {  // 32 columns at a time: S stays in registers
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(o_cols + c * 32, o);
-            tmem_ld_wait();
-            reg_fence32(o);
+            for (int c = 0; c < 2; ++c) {
+              uint32_t o[32];
+              tmem_ld_16x256b_x8(o_base + c * 64, o);
+              tmem_ld_wait();
+              reg_fence32(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * r);
-            tmem_st_32x32b_x32(o_cols + c * 32, o);
+              for (int jj = 0; jj < 8; ++jj) {
+                o[4 * jj] = __float_as_uint(__uint_as_float(o[4 * jj]) * rt);
+                o[4 * jj + 1] = __float_as_uint(__uint_as_float(o[4 * jj + 1]) * rt);
+                o[4 * jj + 2] = __float_as_uint(__uint_as_float(o[4 * jj + 2]) * rb);
+                o[4 * jj + 3] = __float_as_uint(__uint_as_float(o[4 * jj + 3]) * rb);
+              }
+              tmem_st_16x256b_x8(o_base + c * 64, o);
+            }
             tmem_st_wait();
           }
+          mt_ref = nt;
+          mb_ref = nb;
         }
-        m_ref = m_new;
-      }
-      const uint32_t pbase = s_stage0 + s * kStageBytes + ch * kSubTile;
-      // P = exp2(S c - m_ref), two scores per packed fp32 FMA; the row sum
-      // accumulates in packed pairs.  Full tiles take a path with no
-      // per-element validity test.
-      const uint64_t c2 = pk2(p.scale_log2, p.scale_log2), nm2 = pk2(-m_ref, -m_ref), one2 = pk2(1.f, 1.f);
-      uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};
-      auto p_chunks = [&](auto full_tag) {
-        constexpr bool kFull = decltype(full_tag)::value;
+        // P_j = exp2(S_j c - m_ref) as 16-bit pairs, stored over K_j with
+        // stmatrix: matrices (top, octet jj), (bottom, jj), (top, jj+1),
+        // (bottom, jj+1); lane l addresses row l % 8 of matrix l / 8.
+        const uint32_t pst = s_stage0 + s * kStageBytes;
+        const uint64_t nt2 = pk2(-mt_ref, -mt_ref), nb2 = pk2(-mb_ref, -mb_ref);
+        const int mrow = rbase + (lane & 7) + 8 * ((lane >> 3) & 1);  // row this lane addresses
+        const uint32_t mrow_addr = pst + mrow * 128;
+        const uint32_t mkey = (uint32_t)(mrow & 7), moct = (uint32_t)(lane >> 4);
+        auto p_half = [&](auto full_tag, const uint32_t (&v)[32], int h) {
+          constexpr bool kFull = decltype(full_tag)::value;
+          uint32_t pw[16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {  // 8 probabilities -> one 16-byte chunk of P
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const int i = 8 * k + e;
-              const float2 x = upk2(ffma2(pk2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), c2, nm2));
-              float p0 = ex2(x.x), p1 = ex2(x.y);
-              if (!kFull) {
-                p0 = c * 32 + i < valid ? p0 : 0.f;
-                p1 = c * 32 + i + 1 < valid ? p1 : 0.f;
-              }
-              l2[e >> 1] = ffma2(pk2(p0, p1), one2, l2[e >> 1]);
-              w[e >> 1] = Elem<T>::from_f2(p0, p1);
+          for (int jj = 0; jj < 8; ++jj) {
+            const int col = 64 * h + 8 * jj + 2 * c4;
+            const float2 xt = upk2(ffma2(pk2(__uint_as_float(v[4 * jj]), __uint_as_float(v[4 * jj + 1])), c2, nt2));
+            const float2 xb =
+                upk2(ffma2(pk2(__uint_as_float(v[4 * jj + 2]), __uint_as_float(v[4 * jj + 3])), c2, nb2));
+            float p0 = ex2(xt.x), p1 = ex2(xt.y), p2 = ex2(xb.x), p3 = ex2(xb.y);
+            if (!kFull) {
+              p0 = col < vrow ? p0 : 0.f;
+              p1 = col + 1 < vrow ? p1 : 0.f;
+              p2 = col < vrow ? p2 : 0.f;
+              p3 = col + 1 < vrow ? p3 : 0.f;
             }
-            const uint32_t chunk = (uint32_t)(c * 4 + k);
-            const uint32_t addr = pbase + row * 128 + ((chunk ^ (row & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                         "r"(w[3])
-                         : "memory");
+            lt2 = ffma2(pk2(p0, p1), one2, lt2);
+            lb2 = ffma2(pk2(p2, p3), one2, lb2);
+            pw[2 * jj] = Elem<T>::from_f2(p0, p1);
+            pw[2 * jj + 1] = Elem<T>::from_f2(p2, p3);
           }
-        }
-      };
-      if (valid >= 64) p_chunks(std::true_type{});
-      else p_chunks(std::false_type{});
-      const float2 la = upk2(l2[0]), lb = upk2(l2[1]), lc = upk2(l2[2]), ld = upk2(l2[3]);
-      l_run += ((la.x + la.y) + (lb.x + lb.y)) + ((lc.x + lc.y) + (ld.x + ld.y));
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(bars->p_full[b]));
-      mbar_arrive(bar(bars->s_free[b]));
-    }
-    g += n_kv;
-    // O of the piece is final once its last P.V has completed.
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(bars->o_done), k & 1, abort, p.status));
-    // Both halves used the same reference maximum: their sums add.  (xch
-    // doubles as the loop's max-exchange buffer: the two warps of a lane
-    // quadrant pass a pair barrier before and after using it here.)
-    asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
-    xch[ch * 128 + row] = l_run;
-    const bool all_ok = bar_and_sync(ok, 256);
-    const float l_tot = l_run + xch[(ch ^ 1) * 128 + row];
-    asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
-    // Epilogue: rows that belong to the piece's group write its state, 32
-    // columns at a time.
-    const Piece pc = piece_at(p, x_piece, s1);
-    const int b0 = p.req_indptr[pc.grp] + pc.mt * (kRows / G);
-    const int rb = b0 + row / G;
-    const bool mine_row = rb < p.req_indptr[pc.grp + 1] && rb < p.batch;
-    const int64_t r = (int64_t)rb * p.hq + pc.kvh * G + row % G;
-    float* out = p.out_o + pc.slot * p.split_stride_o + r * PKC_HEAD_DIM + ch * 64;
-    const bool has = all_ok && l_tot > 0.f;
-    const float inv = has ? 1.f / l_tot : 0.f;
-    if (all_ok) tc_fence_after();
-#pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      uint32_t o[32];
-      if (all_ok) {  // warp-uniform
-        tmem_ld_32x32b_x32(o_cols + c * 32, o);
-        tmem_ld_wait();
-        reg_fence32(o);
-      }
-      if (mine_row) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(out + c * 32 + i) =
-              has ? make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                                __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int jj = 0; jj < 8; jj += 2) {
+            const uint32_t chunk = (uint32_t)jj + moct;
+            stsm_x4(mrow_addr + h * kSubTile + ((chunk ^ mkey) << 4), pw[2 * jj], pw[2 * jj + 1], pw[2 * jj + 2],
+                    pw[2 * jj + 3]);
+          }
+        };
+        if (vrow == kKvTile) {
+          p_half(std::true_type{}, sr[0], 0);
+          p_half(std::true_type{}, sr[1], 1);
+        } else {
+          p_half(std::false_type{}, sr[0], 0);
+          p_half(std::false_type{}, sr[1], 1);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(bars->p_full[b]));
+        mbar_arrive(bar(bars->s_free[b]));
       }
-    }
-    tc_fence_before();
-    mbar_arrive(bar(bars->o_free[k & 1]));  // piece k + 2 may overwrite this O buffer
-    if (mine_row && ch == 0)
-      p.out_lse[pc.slot * p.split_stride_lse + r] = has ? (m_ref + lg2(l_tot)) * kLn2 : neg_inf();
-    if (!all_ok) break;  // uniform over the softmax warps
+      g += n_kv;
+      // O of the piece is final once its last P.V has completed.
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(bars->o_done), k & 1, abort, p.status));
+      float lt, lb;
+      {
+        const float2 a = upk2(lt2), c = upk2(lb2);
+        lt = a.x + a.y;
+        lb = c.x + c.y;
+      }
+      lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+      lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+      lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+
+      // Epilogue: rows that belong to the piece's group write its state.
+      const Piece pc = piece_at(p, x_piece, s1);
+      const int b0 = p.req_indptr[pc.grp] + pc.mt * (kRows / G);
+      const int req_hi = min(p.req_indptr[pc.grp + 1], p.batch);
+      const int rt_row = rbase + g4, rb_row = rt_row + 8;
+      const int bt = b0 + rt_row / G, bb = b0 + rb_row / G;
+      const bool mine_t = bt < req_hi, mine_b = bb < req_hi;
+      const int64_t r_t = (int64_t)bt * p.hq + pc.kvh * G + rt_row % G;
+      const int64_t r_b = (int64_t)bb * p.hq + pc.kvh * G + rb_row % G;
+      float* out_t = p.out_o + pc.slot * p.split_stride_o + r_t * PKC_HEAD_DIM;
+      float* out_b = p.out_o + pc.slot * p.split_stride_o + r_b * PKC_HEAD_DIM;
+      const bool has_t = ok && lt > 0.f, has_b = ok && lb > 0.f;
+      const float inv_t = has_t ? 1.f / lt : 0.f, inv_b = has_b ? 1.f / lb : 0.f;
+      if (ok) tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        if (ok) {  // warp-uniform
+          tmem_ld_16x256b_x8(o_base + c * 64, o);
+          tmem_ld_wait();
+          reg_fence32(o);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int col = 64 * c + 8 * jj + 2 * c4;
+          if (mine_t)
+            *reinterpret_cast<float2*>(out_t + col) =
+                has_t ? make_float2(__uint_as_float(o[4 * jj]) * inv_t, __uint_as_float(o[4 * jj + 1]) * inv_t)
+                      : make_float2(0.f, 0.f);
+          if (mine_b)
+            *reinterpret_cast<float2*>(out_b + col) =
+                has_b ? make_float2(__uint_as_float(o[4 * jj + 2]) * inv_b, __uint_as_float(o[4 * jj + 3]) * inv_b)
+                      : make_float2(0.f, 0.f);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(bars->o_free[k & 1]));  // piece k + 2 may overwrite this O buffer
+      if (c4 == 0) {
+        if (mine_t) p.out_lse[pc.slot * p.split_stride_lse + r_t] = has_t ? (mt_ref + lg2(lt)) * kLn2 : neg_inf();
+        if (mine_b) p.out_lse[pc.slot * p.split_stride_lse + r_b] = has_b ? (mb_ref + lg2(lb)) * kLn2 : neg_inf();
+      }
     }
   }
 

@@ -188,7 +188,7 @@ def merge_n(v, s):
 
 def attention_rows(q, *, rows=None, sm_scale, num_kv_heads,
                    k_prefix=None, v_prefix=None, prefix_kv_indptr=None,
-                   prefix_req_indptr=None, k_cache=None, v_cache=None,
+                   prefix_req_indptr=None, prefix_req_ranges=None, k_cache=None, v_cache=None,
                    block_table=None, cache_seqlens=None, page_size=None,
                    k_scale=1.0, v_scale=1.0, n_threads=0):
     """Attention state of each (request, query head) row over its full key set.
@@ -197,6 +197,10 @@ def attention_rows(q, *, rows=None, sm_scale, num_kv_heads,
     prefix_req_indptr[j] <= b < prefix_req_indptr[j+1] share prefix j, tokens
     prefix_kv_indptr[j]..prefix_kv_indptr[j+1]-1 of k/v_prefix [L, Hkv, D])
     followed by its cache_seqlens[b] cached tokens, read through block_table
+    from k/v_cache [P, page_size, Hkv, D].  A multi-level cascade gives
+    prefix_req_ranges = [(begin_j, end_j)] instead: the ranges may overlap and
+    a request attends to the prefixes of every group that holds it, in group
+    order, then to its cache
     from k/v_cache [P, page_size, Hkv, D].  Computed in float64 from the
     definition (see pkc_oracle.c).
 
@@ -219,12 +223,20 @@ def attention_rows(q, *, rows=None, sm_scale, num_kv_heads,
     o = np.empty((n, D), np.float64)
     lse = np.empty((n,), np.float64)
     n_prefix = 0
+    req_begin = req_end = None
     if k_prefix is not None:
         k_prefix = np.ascontiguousarray(k_prefix)
         v_prefix = np.ascontiguousarray(v_prefix)
         prefix_kv_indptr = np.ascontiguousarray(prefix_kv_indptr, np.int32)
-        prefix_req_indptr = np.ascontiguousarray(prefix_req_indptr, np.int32)
         n_prefix = len(prefix_kv_indptr) - 1
+        if prefix_req_ranges is not None:
+            rr = np.asarray(prefix_req_ranges, np.int32).reshape(-1, 2)
+        else:
+            ind = np.asarray(prefix_req_indptr, np.int32)
+            rr = np.stack([ind[:-1], ind[1:]], axis=1)
+        assert rr.shape[0] == n_prefix
+        req_begin = np.ascontiguousarray(rr[:, 0])
+        req_end = np.ascontiguousarray(rr[:, 1])
         assert _dtype_code(k_prefix) == dt and _dtype_code(v_prefix) == dt
     num_pages = 0
     bt_stride = 0
@@ -245,7 +257,7 @@ def attention_rows(q, *, rows=None, sm_scale, num_kv_heads,
         _ptr(q), ctypes.c_int(B), ctypes.c_int(Hq), ctypes.c_int(num_kv_heads),
         ctypes.c_int(D), ctypes.c_int(dt), ctypes.c_double(sm_scale),
         _ptr(k_prefix), _ptr(v_prefix), _ptr(prefix_kv_indptr),
-        _ptr(prefix_req_indptr), ctypes.c_int(n_prefix),
+        _ptr(req_begin), _ptr(req_end), ctypes.c_int(n_prefix),
         _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
         ctypes.c_int64(bt_stride), _ptr(cache_seqlens),
         ctypes.c_int(page_size or 0), ctypes.c_int64(num_pages),

@@ -22,7 +22,8 @@
  * say is done "in practice" for stability; it cancels exactly.
  *
  * The key set I of a (request b, query head h) row is the shared prefix of
- * b's group (if any) followed by b's own cached tokens, found through the
+ * every group b belongs to (one group in the two-level cascade, several in
+ * a multi-level one) followed by b's own cached tokens, found through the
  * block table (Hugging Face "Paged attention", decoding path, indexing
  * mechanism): token t of request b lives in physical page
  * block_table[b][t / page_size], slot t % page_size, for
@@ -41,6 +42,7 @@
 
 enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_E4M3 = 3 };
 enum { ORC_OK = 0, ORC_BAD_PAGE = 1, ORC_BAD_ARG = 2, ORC_NOMEM = 3 };
+enum { ORC_MAX_GROUPS = 256 };
 
 /* IEEE 754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
 double pkc_oracle_f16_to_f64(uint16_t h) {
@@ -132,12 +134,15 @@ typedef struct {
   int batch, hq, hkv, d, dtype;
   double sm_scale;
   /* shared prefixes: k/v_prefix [sum Lp, hkv, d]; requests
-   * req_indptr[j] <= b < req_indptr[j+1] share prefix j, whose tokens are
-   * kv_indptr[j] .. kv_indptr[j+1]-1.  n_prefix == 0 means no prefix. */
+   * req_begin[j] <= b < req_end[j] share prefix j, whose tokens are
+   * kv_indptr[j] .. kv_indptr[j+1]-1.  Ranges may overlap: a request in
+   * several groups (a multi-level cascade) attends to all their prefixes,
+   * in group order.  n_prefix == 0 means no prefix. */
   const void* k_prefix;
   const void* v_prefix;
   const int32_t* prefix_kv_indptr;
-  const int32_t* prefix_req_indptr;
+  const int32_t* prefix_req_begin;
+  const int32_t* prefix_req_end;
   int n_prefix;
   /* paged suffix: k/v_cache [num_pages, page_size, hkv, d]; NULL cache
    * means no suffix. */
@@ -155,17 +160,27 @@ typedef struct {
   double k_scale, v_scale;
 } orc_problem;
 
+/* The prefix segments of row b's key list: (first prefix token, length)
+ * of each group containing b, in group order. */
+typedef struct {
+  int n;
+  int64_t total;
+  int64_t lo[ORC_MAX_GROUPS], len[ORC_MAX_GROUPS];
+} orc_segments;
+
 /* Address (in elements) of the key/value vector of token t of row b. */
 static int resolve_token(const orc_problem* p, int b, int kvh, int64_t t,
-                         int64_t prefix_lo, int64_t n_pref,
-                         const void** kbase, const void** vbase,
-                         int64_t* off) {
-  if (t < n_pref) {
+                         const orc_segments* sg, const void** kbase,
+                         const void** vbase, int64_t* off) {
+  if (t < sg->total) {
+    int i = 0;
+    while (t >= sg->len[i]) t -= sg->len[i++];
     *kbase = p->k_prefix;
     *vbase = p->v_prefix;
-    *off = ((prefix_lo + t) * p->hkv + kvh) * (int64_t)p->d;
+    *off = ((sg->lo[i] + t) * p->hkv + kvh) * (int64_t)p->d;
     return ORC_OK;
   }
+  const int64_t n_pref = sg->total;
   int64_t ts = t - n_pref;
   int32_t page = p->block_table[(int64_t)b * p->bt_stride + ts / p->page_size];
   if (page < 0 || page >= p->num_pages) return ORC_BAD_PAGE;
@@ -181,18 +196,20 @@ static int one_row(const orc_problem* p, int b, int h, double* o, double* lse,
                    double* s /* scratch, >= row length */) {
   int g = p->hq / p->hkv;
   int kvh = h / g;
-  int64_t prefix_lo = 0, n_pref = 0, n_suf = 0;
-  if (p->n_prefix > 0) {
-    int j = -1;
-    for (int jj = 0; jj < p->n_prefix; ++jj)
-      if (p->prefix_req_indptr[jj] <= b && b < p->prefix_req_indptr[jj + 1]) j = jj;
-    if (j >= 0) {
-      prefix_lo = p->prefix_kv_indptr[j];
-      n_pref = p->prefix_kv_indptr[j + 1] - prefix_lo;
+  int64_t n_suf = 0;
+  orc_segments sg;
+  sg.n = 0;
+  sg.total = 0;
+  for (int j = 0; j < p->n_prefix; ++j) {
+    if (p->prefix_req_begin[j] <= b && b < p->prefix_req_end[j]) {
+      sg.lo[sg.n] = p->prefix_kv_indptr[j];
+      sg.len[sg.n] = p->prefix_kv_indptr[j + 1] - p->prefix_kv_indptr[j];
+      sg.total += sg.len[sg.n];
+      ++sg.n;
     }
   }
   if (p->k_cache) n_suf = p->cache_seqlens[b];
-  int64_t n = n_pref + n_suf;
+  int64_t n = sg.total + n_suf;
   for (int x = 0; x < p->d; ++x) o[x] = 0.0;
   if (n == 0) {
     *lse = -INFINITY; /* empty key set: identity state */
@@ -203,9 +220,9 @@ static int one_row(const orc_problem* p, int b, int h, double* o, double* lse,
   for (int64_t t = 0; t < n; ++t) {
     const void *kb, *vb;
     int64_t off;
-    int rc = resolve_token(p, b, kvh, t, prefix_lo, n_pref, &kb, &vb, &off);
+    int rc = resolve_token(p, b, kvh, t, &sg, &kb, &vb, &off);
     if (rc) return rc;
-    const int cached = t >= n_pref;
+    const int cached = t >= sg.total;
     const int kd = cached ? p->kv_dtype : p->dtype;
     const double ks = cached ? p->k_scale : 1.0;
     double dot = 0.0;
@@ -223,8 +240,8 @@ static int one_row(const orc_problem* p, int b, int h, double* o, double* lse,
   for (int64_t t = 0; t < n; ++t) {
     const void *kb, *vb;
     int64_t off;
-    resolve_token(p, b, kvh, t, prefix_lo, n_pref, &kb, &vb, &off);
-    const int cached = t >= n_pref;
+    resolve_token(p, b, kvh, t, &sg, &kb, &vb, &off);
+    const int cached = t >= sg.total;
     const int vd = cached ? p->kv_dtype : p->dtype;
     const double vs = cached ? p->v_scale : 1.0;
     double w = exp(s[t] - m) / sum;
@@ -243,23 +260,24 @@ static int one_row(const orc_problem* p, int b, int h, double* o, double* lse,
 int pkc_oracle_attention_rows(
     const void* q, int batch, int hq, int hkv, int d, int dtype,
     double sm_scale, const void* k_prefix, const void* v_prefix,
-    const int32_t* prefix_kv_indptr, const int32_t* prefix_req_indptr,
-    int n_prefix, const void* k_cache, const void* v_cache,
+    const int32_t* prefix_kv_indptr, const int32_t* prefix_req_begin,
+    const int32_t* prefix_req_end, int n_prefix, const void* k_cache,
+    const void* v_cache,
     const int32_t* block_table, int64_t bt_stride,
     const int32_t* cache_seqlens, int page_size, int64_t num_pages,
     int kv_dtype, double k_scale, double v_scale,
     const int32_t* rows, int64_t n_rows, int n_threads, double* o_out,
     double* lse_out) {
-  if (hkv <= 0 || hq % hkv != 0 || d <= 0) return ORC_BAD_ARG;
+  if (hkv <= 0 || hq % hkv != 0 || d <= 0 || n_prefix < 0 || n_prefix > ORC_MAX_GROUPS) return ORC_BAD_ARG;
   orc_problem p = {q, batch, hq, hkv, d, dtype, sm_scale, k_prefix, v_prefix,
-                   prefix_kv_indptr, prefix_req_indptr, n_prefix, k_cache,
+                   prefix_kv_indptr, prefix_req_begin, prefix_req_end, n_prefix, k_cache,
                    v_cache, block_table, bt_stride, cache_seqlens, page_size,
                    num_pages, kv_dtype, k_scale, v_scale};
   int64_t max_n = 0;
   for (int b = 0; b < batch; ++b) {
     int64_t n = 0;
     for (int j = 0; j < n_prefix; ++j)
-      if (prefix_req_indptr[j] <= b && b < prefix_req_indptr[j + 1])
+      if (prefix_req_begin[j] <= b && b < prefix_req_end[j])
         n += prefix_kv_indptr[j + 1] - prefix_kv_indptr[j];
     if (k_cache) n += cache_seqlens[b];
     if (n > max_n) max_n = n;

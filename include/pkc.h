@@ -314,6 +314,33 @@ int pkc_paged_decode_state_fp8(const void* q, const void* k_cache,
                                void* stream);
 
 /*
+ * In-place append of one new token per request to the paged cache
+ * (Hugging Face "Paged attention", decoding path: the next token of request
+ * b is written to page block_table[b][len / page_size], slot
+ * len % page_size, len = cache_seqlens[b]; then the length grows by one).
+ *   k_new, v_new [batch, num_kv_heads, 128] of dtype: the new token's K, V
+ *   k_cache, v_cache [num_pages, page_size, num_kv_heads, 128] of dtype,
+ *            written in place
+ *   block_table [batch, block_table_stride] int32: the caller allocates
+ *            the next page before the token that starts it
+ *   cache_seqlens [batch] int32, incremented in place (device memory)
+ *   append_mask: NULL (every request appends) or [batch] uint8 in device
+ *            memory: only requests with a nonzero entry append
+ *   dtype: PKC_F16, PKC_BF16 or PKC_E4M3 (an fp8 cache: k_new / v_new are
+ *            e4m3 codes too)
+ * A request whose next page id is negative or >= num_pages is skipped (its
+ * cache and length untouched) and PKC_ERR_BLOCK_TABLE is recorded in the
+ * workspace status word.  Every pointer except the mask must be 16-byte
+ * aligned.
+ */
+int pkc_append_kv(const void* k_new, const void* v_new, void* k_cache,
+                  void* v_cache, const int32_t* block_table,
+                  int block_table_stride, int32_t* cache_seqlens,
+                  const uint8_t* append_mask, int batch, int num_kv_heads,
+                  int head_dim, int page_size, int64_t num_pages, int dtype,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Multi-query prefix state (blog "Cascade Inference", step 1 of the
  * algorithm): every request's queries against the KV of the shared prefix
  * of its group, on the tensor cores (tcgen05, TMEM accumulators).

@@ -21,7 +21,7 @@ PKC_OK = 0
 STATUS_NAMES = {0: "PKC_OK", 1: "PKC_ERR_INVALID_ARG", 2: "PKC_ERR_UNSUPPORTED",
                 3: "PKC_ERR_WORKSPACE", 4: "PKC_ERR_BLOCK_TABLE", 5: "PKC_ERR_CUDA",
                 6: "PKC_ERR_TIMEOUT", 7: "PKC_ERR_PLAN"}
-F32, F16, BF16 = 0, 1, 2
+F32, F16, BF16, E4M3 = 0, 1, 2, 3
 
 # Header indices of the plan buffer (include/pkc.h).
 PLAN_FIELDS = ["MAGIC", "TOTAL_WORDS", "NUM_CTAS", "TILE_Q", "N_REQ", "KV_CHUNK",
@@ -57,6 +57,7 @@ SIGNATURES = {
                                         _F, _F, _P, _P, _SZ, _P, _P, _P]),
     "pkc_set_stage_events": (_I, [_c.POINTER(_P), _I]),
     "pkc_set_decode_kernel": (_I, [_I]),
+    "pkc_append_kv": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I64, _I, _P, _SZ, _P]),
     "pkc_cascade_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                 _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
 }
@@ -232,6 +233,24 @@ def paged_decode_state_fp8(q, k_cache, v_cache, block_table, cache_seqlens, sm_s
         _ptr(cache_seqlens), B, Hq, Hkv, D, ps, P, float(sm_scale), float(k_scale), float(v_scale),
         _hptr(plan_buf), _ptr(workspace), workspace.numel(), _ptr(o), _ptr(lse), _stream(stream)))
     return o, lse
+
+
+def append_kv(k_new, v_new, k_cache, v_cache, block_table, cache_seqlens, workspace,
+              append_mask=None, stream=None):
+    """Write one new token per request (k_new / v_new [B, Hkv, 128]) into the
+    paged cache at each request's next slot and grow cache_seqlens by one, in
+    place; an fp8 cache takes uint8 e4m3 codes."""
+    import torch
+    B, Hkv, D = k_new.shape
+    P, ps, _, _ = k_cache.shape
+    if k_cache.dtype == torch.uint8:
+        code = E4M3
+    else:
+        code = _dtype_code(k_cache)
+    _check(lib().pkc_append_kv(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], _ptr(cache_seqlens), _ptr(append_mask), B, Hkv, D, ps, P, code,
+        _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 DECODE_KERNELS = {"auto": 0, "simt": 1, "mma": 2}

@@ -385,6 +385,34 @@ int pkc_paged_decode_state_fp8(const void* q, const void* k_cache, const void* v
                            plan_host, workspace, workspace_bytes, o, lse, PKC_F16, PKC_E4M3, stream);
 }
 
+int pkc_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache, const int32_t* block_table,
+                  int block_table_stride, int32_t* cache_seqlens, const uint8_t* append_mask, int batch,
+                  int num_kv_heads, int head_dim, int page_size, int64_t num_pages, int dtype, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  if (batch < 0 || num_kv_heads <= 0 || page_size < 1 || block_table_stride < 1 || num_pages < 0)
+    return set_error(PKC_ERR_INVALID_ARG, "append_kv: bad size");
+  if (head_dim != PKC_HEAD_DIM)
+    return set_error(PKC_ERR_UNSUPPORTED, "append_kv: head_dim must be %d (got %d)", PKC_HEAD_DIM, head_dim);
+  if (dtype != PKC_F16 && dtype != PKC_BF16 && dtype != PKC_E4M3)
+    return set_error(PKC_ERR_INVALID_ARG, "append_kv: dtype must be PKC_F16, PKC_BF16 or PKC_E4M3 (got %d)", dtype);
+  if (int rc = check_ws(workspace, workspace_bytes, PKC_STATUS_BYTES)) return rc;
+  if (batch == 0) return PKC_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !cache_seqlens)
+    return set_error(PKC_ERR_INVALID_ARG, "append_kv: NULL pointer");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return set_error(PKC_ERR_INVALID_ARG, "append_kv: K/V pointers must be 16-byte aligned");
+  AppendParams ap;
+  std::memset(&ap, 0, sizeof(ap));
+  ap.k_new = k_new; ap.v_new = v_new; ap.k_cache = k_cache; ap.v_cache = v_cache;
+  ap.block_table = block_table; ap.cache_seqlens = cache_seqlens; ap.mask = append_mask;
+  ap.bt_stride = block_table_stride; ap.num_pages = num_pages;
+  ap.hkv = num_kv_heads; ap.page_size = page_size;
+  ap.row_bytes = PKC_HEAD_DIM * (dtype == PKC_E4M3 ? 1 : 2);
+  ap.status = static_cast<int32_t*>(workspace);
+  const int e = launch_append_kv(ap, batch, stream);
+  return e ? cuda_error(e, "append_kv launch") : PKC_OK;
+}
+
 int pkc_set_decode_kernel(int which) {
   if (set_decode_kernel(which) != 0)
     return set_error(PKC_ERR_INVALID_ARG, "set_decode_kernel: which must be 0, 1 or 2 (got %d)", which);

@@ -129,6 +129,19 @@ struct PrefixParams {
   int32_t* status;
 };
 
+struct AppendParams {
+  const void* k_new;       // [batch, Hkv, 128] of the cache's element type
+  const void* v_new;
+  void* k_cache;           // [num_pages, page_size, Hkv, 128]
+  void* v_cache;
+  const int32_t* block_table;
+  int32_t* cache_seqlens;  // incremented in place
+  const uint8_t* mask;     // [batch] or nullptr (all append)
+  int64_t bt_stride, num_pages;
+  int hkv, page_size, row_bytes;  // row_bytes: one head's 128 elements
+  int32_t* status;
+};
+
 // Launchers (defined in the .cu files); return a cudaError_t value.
 int launch_merge_state(const void* va, const float* sa, const void* vb,
                        const float* sb, void* vo, float* so, int64_t rows,
@@ -150,6 +163,7 @@ int launch_paged_decode_mma(const DecodeParams& p, int grid_x, int kv_kind,
 // this head count and page size.
 int mma_decode_heads_per_block(int hkv, int page_size);
 int launch_contract(const ContractParams& p, int n_rows, void* stream);
+int launch_append_kv(const AppendParams& p, int batch, void* stream);
 // q/k/v tensor maps are built inside; returns cudaError_t or -1 when the
 // driver entry point for tensor maps is unavailable.
 int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix,

@@ -102,6 +102,20 @@ def test_fp8_decode_and_kernel_switch_reject_bad_arguments(L):
         assert L.pkc_set_decode_kernel(ok) == 0
 
 
+def test_append_kv_rejects_bad_arguments(L):
+    fake = ctypes.c_void_p(0x1000)
+    ws = ctypes.c_void_p(0x100000)
+    args = (fake, fake, fake, fake, fake, 4, fake, None, 2, 8)
+    assert L.pkc_append_kv(*args, 64, 16, 10, 1, ws, 1 << 20, None) == 2   # head_dim
+    assert L.pkc_append_kv(*args, 128, 16, 10, 0, ws, 1 << 20, None) == 1  # fp32 cache
+    assert L.pkc_append_kv(*args, 128, 0, 10, 1, ws, 1 << 20, None) == 1   # page_size
+    assert L.pkc_append_kv(*args, 128, 16, 10, 1, ws, 16, None) == 3       # workspace
+    mis = ctypes.c_void_p(0x1008)
+    assert L.pkc_append_kv(mis, fake, fake, fake, fake, 4, fake, None, 2, 8, 128, 16, 10, 1,
+                           ws, 1 << 20, None) == 1                         # alignment
+    assert L.pkc_append_kv(*args[:8], 0, 8, 128, 16, 10, 1, ws, 1 << 20, None) == 0  # empty
+
+
 def test_workspace_size_matches_documented_layout(L):
     def al(x):
         return (x + 255) // 256 * 256

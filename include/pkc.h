@@ -381,6 +381,33 @@ int pkc_cascade_decode(
     float sm_scale, const int32_t* plan_host, void* workspace,
     size_t workspace_bytes, void* o, float* lse, int dtype, void* stream);
 
+/*
+ * Multi-level cascade decode: the cascade above with prefix groups given as
+ * request ranges that may overlap.  Group j holds requests
+ * prefix_req_begin[j] <= b < prefix_req_end[j] and prefix tokens
+ * prefix_kv_indptr[j] .. prefix_kv_indptr[j+1]-1 of k/v_prefix; a request
+ * attends to the prefixes of every group holding it (e.g. level 0: one
+ * system prompt for all requests; level 1: a prompt per request group),
+ * then to its own cached tokens.  The state of the union is the (+) of the
+ * parts' states (tutorial "Attention States and Recursive Attention"), so
+ * each group is computed once for all its requests, as in the two-level
+ * cascade (blog "Cascade Inference").  Other arguments as in
+ * pkc_cascade_decode.  Groups that share a request use disjoint partial
+ * slots: the workspace's prefix_splits must cover, for every request, the
+ * slots of all its groups (else fewer prefix blocks are used, and
+ * PKC_ERR_WORKSPACE when even one block per group does not fit).
+ * 1 <= n_prefix <= 256; 0 <= begin <= end <= batch.
+ */
+int pkc_cascade_decode_multilevel(
+    const void* q, const void* k_prefix, const void* v_prefix,
+    const int32_t* prefix_kv_indptr_host, const int32_t* prefix_req_begin_host,
+    const int32_t* prefix_req_end_host, int n_prefix, const void* k_cache,
+    const void* v_cache, const int32_t* block_table, int block_table_stride,
+    const int32_t* cache_seqlens, int batch, int num_qo_heads,
+    int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+    float sm_scale, const int32_t* plan_host, void* workspace,
+    size_t workspace_bytes, void* o, float* lse, int dtype, void* stream);
+
 /* ------------------------------------------------------------------------
  * Stage timing
  * ---------------------------------------------------------------------- */

@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "pkc.h"
 #include "pkc_internal.h"
@@ -112,19 +113,20 @@ struct PrefixSetup {
 // Validate the prefix description and lay out its work: the flat KV tiles
 // of all (row tile, KV head) pairs split evenly over one block per SM, as
 // long as the pieces of any pair fit the workspace's partial slots.
-int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_indptr, int n_prefix, int batch,
-                 int hq, int hkv, float sm_scale, uint8_t* ws, size_t ws_bytes, const WsLayout& L,
-                 int32_t* status) {
+int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_begin, const int32_t* req_end,
+                 int n_prefix, int batch, int hq, int hkv, float sm_scale, uint8_t* ws, size_t ws_bytes,
+                 const WsLayout& L, int32_t* status) {
   if (n_prefix < 1 || n_prefix > PKC_MAX_PREFIX)
     return set_error(PKC_ERR_INVALID_ARG, "n_prefix must be in [1, %d] (got %d)", PKC_MAX_PREFIX, n_prefix);
-  if (!kv_indptr || !req_indptr) return set_error(PKC_ERR_INVALID_ARG, "prefix indptr arrays are NULL");
-  if (kv_indptr[0] < 0 || req_indptr[0] < 0)
-    return set_error(PKC_ERR_INVALID_ARG, "prefix indptr arrays must start >= 0");
-  for (int j = 0; j < n_prefix; ++j)
-    if (kv_indptr[j + 1] < kv_indptr[j] || req_indptr[j + 1] < req_indptr[j])
-      return set_error(PKC_ERR_INVALID_ARG, "prefix indptr arrays must be non-decreasing (at %d)", j);
-  if (req_indptr[n_prefix] > batch)
-    return set_error(PKC_ERR_INVALID_ARG, "prefix_req_indptr ends at %d > batch %d", req_indptr[n_prefix], batch);
+  if (!kv_indptr || !req_begin || !req_end) return set_error(PKC_ERR_INVALID_ARG, "prefix arrays are NULL");
+  if (kv_indptr[0] < 0) return set_error(PKC_ERR_INVALID_ARG, "prefix_kv_indptr must start >= 0");
+  for (int j = 0; j < n_prefix; ++j) {
+    if (kv_indptr[j + 1] < kv_indptr[j])
+      return set_error(PKC_ERR_INVALID_ARG, "prefix_kv_indptr must be non-decreasing (at %d)", j);
+    if (req_begin[j] < 0 || req_end[j] < req_begin[j] || req_end[j] > batch)
+      return set_error(PKC_ERR_INVALID_ARG, "prefix group %d: requests [%d, %d) outside [0, batch %d]", j,
+                       req_begin[j], req_end[j], batch);
+  }
   PrefixParams& p = S.pp;
   std::memset(&p, 0, sizeof(p));
   p.batch = batch;
@@ -138,12 +140,13 @@ int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_in
   int64_t T = 0;
   for (int j = 0; j <= n_prefix; ++j) {
     p.kv_indptr[j] = kv_indptr[j];
-    p.req_indptr[j] = req_indptr[j];
     p.tile_indptr[j] = tiles;
     if (T > INT32_MAX) return set_error(PKC_ERR_UNSUPPORTED, "prefix: too many KV tiles (%lld)", (long long)T);
     p.kvt_indptr[j] = (int32_t)T;
     if (j < n_prefix) {
-      const int rows = (req_indptr[j + 1] - req_indptr[j]) * p.g;
+      p.req_begin[j] = req_begin[j];
+      p.req_end[j] = req_end[j];
+      const int rows = (req_end[j] - req_begin[j]) * p.g;
       const int rt = (rows + 127) / 128;
       const int kvt = (kv_indptr[j + 1] - kv_indptr[j] + 127) / 128;
       tiles += rt;
@@ -155,24 +158,40 @@ int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_in
   const size_t avail = ws_bytes > L.fixed_end ? (ws_bytes - L.fixed_end) / L.prefix_split : 0;
   if (avail < 1) return set_error(PKC_ERR_WORKSPACE, "workspace has no room for prefix partial states");
   const int max_slots = (int)std::min<size_t>(avail, PKC_MAX_PREFIX_SPLITS);
-  // One block per SM (fewer if there are fewer tiles); the most pieces any
-  // pair is cut into must fit the workspace's partial slots.
+  // One block per SM (fewer if there are fewer tiles).  Group j needs as
+  // many partial slots as the most pieces any of its pairs is cut into;
+  // groups sharing a request get disjoint slot ranges (first fit in group
+  // order), and every request's slots must fit the workspace.
   int C = (int)std::min<int64_t>(num_sms(), T);
+  if (T * C >= INT32_MAX) return set_error(PKC_ERR_UNSUPPORTED, "prefix: too many KV tiles (%lld)", (long long)T);
   int slots = 0;
+  std::vector<int> need(n_prefix), base(n_prefix);
   while (C > 0) {
-    slots = 1;
     for (int j = 0; j < n_prefix; ++j) {
+      need[j] = 0;
       const int kvt = (kv_indptr[j + 1] - kv_indptr[j] + 127) / 128;
       if (kvt == 0) continue;
       const int n_pairs = (p.tile_indptr[j + 1] - p.tile_indptr[j]) * hkv;
       for (int q = 0; q < n_pairs; ++q) {
         const int64_t a = p.kvt_indptr[j] + (int64_t)q * kvt;
-        slots = std::max(slots, prefix_block_of(a + kvt - 1, T, C) - prefix_block_of(a, T, C) + 1);
+        need[j] = std::max(need[j], prefix_block_of(a + kvt - 1, T, C) - prefix_block_of(a, T, C) + 1);
       }
+    }
+    slots = 1;
+    for (int j = 0; j < n_prefix; ++j) {
+      base[j] = 0;
+      for (int i = 0; i < j; ++i)  // after every earlier group that shares a request
+        if (need[i] > 0 && req_begin[i] < req_end[j] && req_begin[j] < req_end[i])
+          base[j] = std::max(base[j], base[i] + need[i]);
+      slots = std::max(slots, base[j] + need[j]);
     }
     if (slots <= max_slots) break;
     --C;
   }
+  if (T > 0 && C == 0)
+    return set_error(PKC_ERR_WORKSPACE, "workspace has too few prefix partial slots for %d overlapping groups",
+                     n_prefix);
+  for (int j = 0; j < n_prefix; ++j) p.slot_base[j] = base[j];
   p.n_blocks = C;
   p.total_tiles = T;
   p.splits = std::max(1, slots);
@@ -181,6 +200,22 @@ int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_in
   p.split_stride_o = (int64_t)(L.prefix_split / 4);
   p.split_stride_lse = (int64_t)(L.prefix_split / 4);
   p.status = status;
+  return PKC_OK;
+}
+
+// Request ranges [indptr[j], indptr[j+1]) of the contiguous groups of the
+// two-level calls (validated; setup_prefix checks the bounds).
+int indptr_ranges(const int32_t* req_indptr, int n_prefix, int32_t* begin, int32_t* end) {
+  if (!req_indptr) return set_error(PKC_ERR_INVALID_ARG, "prefix_req_indptr is NULL");
+  if (n_prefix < 1 || n_prefix > PKC_MAX_PREFIX)
+    return set_error(PKC_ERR_INVALID_ARG, "n_prefix must be in [1, %d] (got %d)", PKC_MAX_PREFIX, n_prefix);
+  if (req_indptr[0] < 0) return set_error(PKC_ERR_INVALID_ARG, "prefix_req_indptr must start >= 0");
+  for (int j = 0; j < n_prefix; ++j) {
+    if (req_indptr[j + 1] < req_indptr[j])
+      return set_error(PKC_ERR_INVALID_ARG, "prefix_req_indptr must be non-decreasing (at %d)", j);
+    begin[j] = req_indptr[j];
+    end[j] = req_indptr[j + 1];
+  }
   return PKC_OK;
 }
 
@@ -195,7 +230,9 @@ void fill_contract_prefix(ContractParams& c, const PrefixSetup& S) {
   c.g = S.pp.g;
   c.prefix_blocks = S.pp.n_blocks;
   c.prefix_tiles = S.pp.total_tiles;
-  std::memcpy(c.req_indptr, S.pp.req_indptr, sizeof(c.req_indptr));
+  std::memcpy(c.prefix_req_begin, S.pp.req_begin, sizeof(c.prefix_req_begin));
+  std::memcpy(c.prefix_req_end, S.pp.req_end, sizeof(c.prefix_req_end));
+  std::memcpy(c.prefix_slot_base, S.pp.slot_base, sizeof(c.prefix_slot_base));
   std::memcpy(c.prefix_kv_indptr, S.pp.kv_indptr, sizeof(c.prefix_kv_indptr));
   std::memcpy(c.prefix_kvt_indptr, S.pp.kvt_indptr, sizeof(c.prefix_kvt_indptr));
 }
@@ -433,9 +470,11 @@ int pkc_prefix_attention_state(const void* q, const void* k_prefix, const void* 
     return set_error(PKC_ERR_INVALID_ARG, "prefix_attention_state: tensors must be 16-byte aligned");
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
+  int32_t rb[PKC_MAX_PREFIX], re[PKC_MAX_PREFIX];
+  if (int rc = indptr_ranges(prefix_req_indptr_host, n_prefix, rb, re)) return rc;
   PrefixSetup S;
-  if (int rc = setup_prefix(S, prefix_kv_indptr_host, prefix_req_indptr_host, n_prefix, batch, num_qo_heads,
-                            num_kv_heads, sm_scale, ws, workspace_bytes, L, status))
+  if (int rc = setup_prefix(S, prefix_kv_indptr_host, rb, re, n_prefix, batch, num_qo_heads, num_kv_heads, sm_scale,
+                            ws, workspace_bytes, L, status))
     return rc;
   int e = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, stream);
   if (e == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
@@ -449,12 +488,17 @@ int pkc_prefix_attention_state(const void* q, const void* k_prefix, const void* 
   return e ? cuda_error(e, "contraction launch") : PKC_OK;
 }
 
-int pkc_cascade_decode(const void* q, const void* k_prefix, const void* v_prefix,
-                       const int32_t* prefix_kv_indptr_host, const int32_t* prefix_req_indptr_host, int n_prefix,
-                       const void* k_cache, const void* v_cache, const int32_t* block_table, int block_table_stride,
-                       const int32_t* cache_seqlens, int batch, int num_qo_heads, int num_kv_heads, int head_dim,
-                       int page_size, int64_t num_pages, float sm_scale, const int32_t* plan_host, void* workspace,
-                       size_t workspace_bytes, void* o, float* lse, int dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+// The cascade for prefix groups given as request ranges (overlapping ranges:
+// a multi-level cascade).
+int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, const int32_t* prefix_kv_indptr_host,
+                 const int32_t* req_begin, const int32_t* req_end, int n_prefix, const void* k_cache,
+                 const void* v_cache, const int32_t* block_table, int block_table_stride, const int32_t* cache_seqlens,
+                 int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+                 float sm_scale, const int32_t* plan_host, void* workspace, size_t workspace_bytes, void* o,
+                 float* lse, int dtype, void* stream) {
   if (int rc = check_attn_dims(batch, num_qo_heads, num_kv_heads, head_dim, dtype)) return rc;
   if (int rc = check_plan(plan_host, batch)) return rc;
   if (page_size < 1 || block_table_stride < 1 || num_pages < 0)
@@ -471,7 +515,7 @@ int pkc_cascade_decode(const void* q, const void* k_prefix, const void* v_prefix
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   PrefixSetup S;
-  if (int rc = setup_prefix(S, prefix_kv_indptr_host, prefix_req_indptr_host, n_prefix, batch, num_qo_heads,
+  if (int rc = setup_prefix(S, prefix_kv_indptr_host, req_begin, req_end, n_prefix, batch, num_qo_heads,
                             num_kv_heads, sm_scale, ws, workspace_bytes, L, status))
     return rc;
   cudaEvent_t ev[4];
@@ -516,6 +560,36 @@ int pkc_cascade_decode(const void* q, const void* k_prefix, const void* v_prefix
   if (e) return cuda_error(e, "contraction launch");
   mark(3);
   return PKC_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int pkc_cascade_decode(const void* q, const void* k_prefix, const void* v_prefix,
+                       const int32_t* prefix_kv_indptr_host, const int32_t* prefix_req_indptr_host, int n_prefix,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table, int block_table_stride,
+                       const int32_t* cache_seqlens, int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                       int page_size, int64_t num_pages, float sm_scale, const int32_t* plan_host, void* workspace,
+                       size_t workspace_bytes, void* o, float* lse, int dtype, void* stream) {
+  int32_t rb[PKC_MAX_PREFIX], re[PKC_MAX_PREFIX];
+  if (int rc = check_attn_dims(batch, num_qo_heads, num_kv_heads, head_dim, dtype)) return rc;
+  if (int rc = indptr_ranges(prefix_req_indptr_host, n_prefix, rb, re)) return rc;
+  return cascade_impl(q, k_prefix, v_prefix, prefix_kv_indptr_host, rb, re, n_prefix, k_cache, v_cache, block_table,
+                      block_table_stride, cache_seqlens, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                      num_pages, sm_scale, plan_host, workspace, workspace_bytes, o, lse, dtype, stream);
+}
+
+int pkc_cascade_decode_multilevel(
+    const void* q, const void* k_prefix, const void* v_prefix, const int32_t* prefix_kv_indptr_host,
+    const int32_t* prefix_req_begin_host, const int32_t* prefix_req_end_host, int n_prefix, const void* k_cache,
+    const void* v_cache, const int32_t* block_table, int block_table_stride, const int32_t* cache_seqlens, int batch,
+    int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages, float sm_scale,
+    const int32_t* plan_host, void* workspace, size_t workspace_bytes, void* o, float* lse, int dtype,
+    void* stream) {
+  return cascade_impl(q, k_prefix, v_prefix, prefix_kv_indptr_host, prefix_req_begin_host, prefix_req_end_host,
+                      n_prefix, k_cache, v_cache, block_table, block_table_stride, cache_seqlens, batch, num_qo_heads,
+                      num_kv_heads, head_dim, page_size, num_pages, sm_scale, plan_host, workspace, workspace_bytes, o,
+                      lse, dtype, stream);
 }
 
 }  // extern "C"

@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
 // One warp per (row, head): (+) over every state that belongs to the row,
 // lane i owning dims 4i..4i+3.
-__global__ void __launch_bounds__(256) contract_kernel(const ContractParams p) {
+__global__ void __launch_bounds__(256, 3) contract_kernel(const ContractParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t row_idx = gw / p.hq;
@@ -533,26 +533,26 @@ __global__ void __launch_bounds__(256) contract_kernel(const ContractParams p) {
     unit = pl[p.off_unit_list + row_idx];
     req = pl[p.off_unit_req + unit];
   }
-  // Sources: the prefix pieces of the row's (row tile, KV head) pair, then
-  // the suffix.  A pair covering flat KV tiles [a, a + kvt) was computed in
-  // pieces by the prefix blocks block_of(a) .. block_of(a + kvt - 1), piece
-  // i in partial slot i.
-  int group = -1;
-  if (p.prefix_o) {
-    for (int j = 0; j < p.n_prefix; ++j)
-      if (p.req_indptr[j] <= req && req < p.req_indptr[j + 1]) { group = j; break; }
-  }
-  int n_pref = 0;
-  if (group >= 0) {
-    const int kvt = (p.prefix_kv_indptr[group + 1] - p.prefix_kv_indptr[group] + 127) / 128;
-    if (kvt > 0 && p.prefix_tiles > 0) {
-      const int rr = (req - p.req_indptr[group]) * p.g + h % p.g;  // row within the group's rows
-      const int pair = (rr / 128) * p.hkv + h / p.g;
-      const int64_t a = p.prefix_kvt_indptr[group] + (int64_t)pair * kvt;
-      n_pref = prefix_block_of(a + kvt - 1, p.prefix_tiles, p.prefix_blocks) -
-               prefix_block_of(a, p.prefix_tiles, p.prefix_blocks) + 1;
-    }
-  }
+  // Running state of the merge: maximum m, denominator den, unnormalised
+  // acc.  Sources go in batches of 8 whose loads are all in flight
+  // together; the running state is rescaled between batches.
+  constexpr int kB = 8;
+  float m = neg_inf(), den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t row_off = (int64_t)req * p.hq + h;
+  // Sources: the prefix pieces of every group holding the request (one
+  // group in a two-level cascade, several in a multi-level one), then the
+  // suffix.  Group j's pair covering flat KV tiles [a, a + kvt) was computed
+  // in pieces by the prefix blocks block_of(a) .. block_of(a + kvt - 1),
+  // piece i in partial slot slot_base[j] + i.  One pass per group; the last
+  // pass also takes the suffix, so a two-level row is a single pass.
+  auto in_group = [&](int j) { return p.prefix_req_begin[j] <= req && req < p.prefix_req_end[j]; };
+  auto next_group = [&](int j) {  // first group after j holding the request, or -1
+    if (!p.prefix_o) return -1;
+    for (++j; j < p.n_prefix; ++j)
+      if (in_group(j)) return j;
+    return -1;
+  };
   int suf_kind = 0, suf_begin = 0, suf_n = 0;  // 1: direct state, 2: partial slots
   if (pl) {
     const int nch = pl[p.off_unit_n_chunks + unit];       // both loads in flight together
@@ -562,46 +562,60 @@ __global__ void __launch_bounds__(256) contract_kernel(const ContractParams p) {
   } else if (p.suffix_o) {
     suf_kind = 1; suf_n = 1;
   }
-  const int n_src = n_pref + suf_n;
-  auto src_lse = [&](int i) -> const float* {
-    if (i < n_pref) return p.prefix_lse + i * p.prefix_stride_lse + (int64_t)req * p.hq + h;
-    if (suf_kind == 1) return p.suffix_lse + (int64_t)req * p.hq + h;
-    return p.part_lse + (int64_t)(suf_begin + i - n_pref) * p.hq + h;
-  };
-  auto src_o = [&](int i) -> const float* {
-    if (i < n_pref) return p.prefix_o + i * p.prefix_stride_o + ((int64_t)req * p.hq + h) * D;
-    if (suf_kind == 1) return p.suffix_o + ((int64_t)req * p.hq + h) * D;
-    return p.part_o + ((int64_t)(suf_begin + i - n_pref) * p.hq + h) * D;
-  };
-  // Sources go in batches of 8 whose loads are all in flight together; the
-  // running (max, sum, acc) is rescaled between batches.
-  constexpr int kB = 8;
-  float m = neg_inf(), den = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i0 = 0; i0 < n_src; i0 += kB) {
-    float ls[kB];
-    float4 xs[kB];
-#pragma unroll
-    for (int k = 0; k < kB; ++k) {
-      const bool in = i0 + k < n_src;
-      ls[k] = in ? *src_lse(i0 + k) : neg_inf();
-      xs[k] = in ? *reinterpret_cast<const float4*>(src_o(i0 + k) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = next_group(-1);;) {
+    int n_pref = 0, base = 0;
+    if (j >= 0) {
+      const int kvt = (p.prefix_kv_indptr[j + 1] - p.prefix_kv_indptr[j] + 127) / 128;
+      if (kvt > 0 && p.prefix_tiles > 0) {
+        const int rr = (req - p.prefix_req_begin[j]) * p.g + h % p.g;  // row within the group's rows
+        const int pair = (rr / 128) * p.hkv + h / p.g;
+        // block_of(x) = ((x + 1) C - 1) / T, in 32 bits (the host keeps T C < 2^31)
+        const int a = p.prefix_kvt_indptr[j] + pair * kvt;
+        const int T = (int)p.prefix_tiles, C = p.prefix_blocks;
+        n_pref = ((a + kvt) * C - 1) / T - ((a + 1) * C - 1) / T + 1;
+        base = p.prefix_slot_base[j];
+      }
     }
-    float mb = m;
+    const int jn = j >= 0 ? next_group(j) : -1;
+    const int n_suf = jn < 0 ? suf_n : 0;  // the last pass takes the suffix
+    const int n_src = n_pref + n_suf;
+    auto src_lse = [&](int i) -> const float* {
+      if (i < n_pref) return p.prefix_lse + (int64_t)(base + i) * p.prefix_stride_lse + row_off;
+      if (suf_kind == 1) return p.suffix_lse + row_off;
+      return p.part_lse + (int64_t)(suf_begin + i - n_pref) * p.hq + h;
+    };
+    auto src_o = [&](int i) -> const float* {
+      if (i < n_pref) return p.prefix_o + (int64_t)(base + i) * p.prefix_stride_o + row_off * D;
+      if (suf_kind == 1) return p.suffix_o + row_off * D;
+      return p.part_o + ((int64_t)(suf_begin + i - n_pref) * p.hq + h) * D;
+    };
+    for (int i0 = 0; i0 < n_src; i0 += kB) {
+      float ls[kB];
+      float4 xs[kB];
 #pragma unroll
-    for (int k = 0; k < kB; ++k) mb = fmaxf(mb, ls[k]);
-    if (mb == neg_inf()) continue;
-    const float c = ex2((m - mb) * kLog2e);  // 0 when m is -inf
-    den *= c;
-    acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
+      for (int k = 0; k < kB; ++k) {
+        const bool in = i0 + k < n_src;
+        ls[k] = in ? *src_lse(i0 + k) : neg_inf();
+        xs[k] = in ? *reinterpret_cast<const float4*>(src_o(i0 + k) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float mb = m;
 #pragma unroll
-    for (int k = 0; k < kB; ++k) {
-      const float w = ex2((ls[k] - mb) * kLog2e);  // 0 for empty states
-      den += w;
-      acc.x = fmaf(w, xs[k].x, acc.x); acc.y = fmaf(w, xs[k].y, acc.y);
-      acc.z = fmaf(w, xs[k].z, acc.z); acc.w = fmaf(w, xs[k].w, acc.w);
+      for (int k = 0; k < kB; ++k) mb = fmaxf(mb, ls[k]);
+      if (mb == neg_inf()) continue;
+      const float c = ex2((m - mb) * kLog2e);  // 0 when m is -inf
+      den *= c;
+      acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
+#pragma unroll
+      for (int k = 0; k < kB; ++k) {
+        const float w = ex2((ls[k] - mb) * kLog2e);  // 0 for empty states
+        den += w;
+        acc.x = fmaf(w, xs[k].x, acc.x); acc.y = fmaf(w, xs[k].y, acc.y);
+        acc.z = fmaf(w, xs[k].z, acc.z); acc.w = fmaf(w, xs[k].w, acc.w);
+      }
+      m = mb;
     }
-    m = mb;
+    if (jn < 0) break;
+    j = jn;
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;

@@ -68,6 +68,10 @@ enum ContractMode {
   kContractAllRequests = 1 // rows = every request
 };
 
+// Prefix groups hold contiguous request ranges that may overlap (a
+// multi-level cascade: a request shares several prefixes).  Groups that
+// share a request write their pieces to disjoint partial-slot ranges.
+//
 // Prefix work split: the prefix stage's KV tiles are laid out flat, pair
 // after pair, where a pair is (128-row query tile, KV head) of one prefix
 // group (group j's pairs are q = row_tile * Hkv + kv_head, each covering
@@ -75,7 +79,7 @@ enum ContractMode {
 // takes tiles [floor(i T / C), floor((i+1) T / C)); a pair that spans
 // several blocks is computed in pieces whose partial states are merged by
 // the contraction.  The piece of block i in a pair starting at tile A is
-// partial slot i - block_of(A).
+// partial slot slot_base[group] + i - block_of(A).
 #if defined(__CUDACC__)
 #define PKC_HD __host__ __device__
 #else
@@ -103,7 +107,9 @@ struct ContractParams {
   int hkv, g;                                      // KV heads, query heads per KV head
   int prefix_blocks;                               // C of the prefix work split
   int64_t prefix_tiles;                            // T of the prefix work split
-  int32_t req_indptr[PKC_MAX_PREFIX + 1];
+  int32_t prefix_req_begin[PKC_MAX_PREFIX];       // group j holds requests [begin, end)
+  int32_t prefix_req_end[PKC_MAX_PREFIX];          //   (ranges may overlap: levels)
+  int32_t prefix_slot_base[PKC_MAX_PREFIX];        // first partial slot of group j
   int32_t prefix_kv_indptr[PKC_MAX_PREFIX + 1];    // prefix tokens per group
   int32_t prefix_kvt_indptr[PKC_MAX_PREFIX + 1];   // first flat KV tile of each group
   void* o;
@@ -120,7 +126,9 @@ struct PrefixParams {
   int n_blocks;                             // C: thread blocks of the work split
   int64_t total_tiles;                      // T: flat KV tiles over all pairs
   int32_t kv_indptr[PKC_MAX_PREFIX + 1];
-  int32_t req_indptr[PKC_MAX_PREFIX + 1];
+  int32_t req_begin[PKC_MAX_PREFIX];        // group j holds requests [begin, end)
+  int32_t req_end[PKC_MAX_PREFIX];
+  int32_t slot_base[PKC_MAX_PREFIX];        // first partial slot of group j's pieces
   int32_t tile_indptr[PKC_MAX_PREFIX + 1];  // cumulative 128-row tiles
   int32_t kvt_indptr[PKC_MAX_PREFIX + 1];   // first flat KV tile of each group
   float* out_o;                             // [split, B, Hq, D]

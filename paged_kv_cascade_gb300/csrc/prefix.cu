@@ -88,7 +88,7 @@ __device__ __forceinline__ Piece piece_at(const PrefixParams& p, int x, int s1) 
   g.grp = j;
   g.mt = q / p.hkv;
   g.kvh = q % p.hkv;
-  g.slot = (int)blockIdx.x - prefix_block_of(pair0, p.total_tiles, p.n_blocks);
+  g.slot = p.slot_base[j] + (int)blockIdx.x - prefix_block_of(pair0, p.total_tiles, p.n_blocks);
   g.n = end - x;
   g.kv_lo = p.kv_indptr[j] + kt0 * kKvTile;
   g.kv_hi = min(p.kv_indptr[j + 1], g.kv_lo + g.n * kKvTile);
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; ok && u < pre; ++u) ok = load_kv(u);
         if (!ok) break;
         if (q_issued > 0 && !mbar_wait(bar(bars->q_empty), (q_issued - 1) & 1, abort, p.status)) break;
-        const int b0 = p.req_indptr[pc.grp] + pc.mt * (kRows / G);
+        const int b0 = p.req_begin[pc.grp] + pc.mt * (kRows / G);
         mbar_arrive_expect_tx(bar(bars->q_full), kQBytes);
         tma_load_3d(s_q, &tm_q, bar(bars->q_full), 0, pc.kvh * G, b0, pol_q);
         tma_load_3d(s_q + kSubTile, &tm_q, bar(bars->q_full), 64, pc.kvh * G, b0, pol_q);
@@ -432,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // Epilogue: rows that belong to the piece's group write its state.
       const Piece pc = piece_at(p, x_piece, s1);
-      const int b0 = p.req_indptr[pc.grp] + pc.mt * (kRows / G);
-      const int req_hi = min(p.req_indptr[pc.grp + 1], p.batch);
+      const int b0 = p.req_begin[pc.grp] + pc.mt * (kRows / G);
+      const int req_hi = min(p.req_end[pc.grp], p.batch);
       const int rt_row = rbase + g4, rb_row = rt_row + 8;
       const int bt = b0 + rt_row / G, bb = b0 + rb_row / G;
       const bool mine_t = bt < req_hi, mine_b = bb < req_hi;

@@ -408,6 +408,33 @@ int pkc_cascade_decode_multilevel(
     float sm_scale, const int32_t* plan_host, void* workspace,
     size_t workspace_bytes, void* o, float* lse, int dtype, void* stream);
 
+/*
+ * Cascade decode with the shared prefixes kept in the page pool (MLSys'25
+ * notes, A3 "composable formats": the prefix is a block of the same paged
+ * KV, read in place, not copied out).  As pkc_cascade_decode_multilevel,
+ * except:
+ *   prefix_pages: device int32 page ids into k_cache / v_cache; group j's
+ *            prefix tokens are, in order, the slots of pages
+ *            prefix_pages[prefix_page_indptr[j] .. prefix_page_indptr[j+1]-1]
+ *            (the last page filled only up to the group's length)
+ *   prefix_page_indptr_host [n_prefix + 1]: cumulative page counts; group j
+ *            needs at least ceil(len_j / page_size) pages, len_j =
+ *            prefix_kv_indptr[j+1] - prefix_kv_indptr[j]
+ * page_size must divide 128 and be >= 8 (PKC_ERR_UNSUPPORTED otherwise).
+ * A page id < 0 or >= num_pages in a list is read as zeros and recorded as
+ * PKC_ERR_BLOCK_TABLE.  Slots past a group's length may hold anything.
+ */
+int pkc_cascade_decode_paged_prefix(
+    const void* q, const int32_t* prefix_pages,
+    const int32_t* prefix_page_indptr_host, const int32_t* prefix_kv_indptr_host,
+    const int32_t* prefix_req_begin_host, const int32_t* prefix_req_end_host,
+    int n_prefix, const void* k_cache, const void* v_cache,
+    const int32_t* block_table, int block_table_stride,
+    const int32_t* cache_seqlens, int batch, int num_qo_heads,
+    int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+    float sm_scale, const int32_t* plan_host, void* workspace,
+    size_t workspace_bytes, void* o, float* lse, int dtype, void* stream);
+
 /* ------------------------------------------------------------------------
  * Stage timing
  * ---------------------------------------------------------------------- */

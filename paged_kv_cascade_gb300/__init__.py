@@ -60,6 +60,8 @@ SIGNATURES = {
     "pkc_append_kv": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I64, _I, _P, _SZ, _P]),
     "pkc_cascade_decode_multilevel": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I,
                                            _I, _I, _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
+    "pkc_cascade_decode_paged_prefix": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I,
+                                             _I, _I, _I, _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
     "pkc_cascade_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                 _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
 }
@@ -330,6 +332,28 @@ def cascade_decode_multilevel(q, k_prefix, v_prefix, prefix_kv_indptr, prefix_re
     lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
     _check(lib().pkc_cascade_decode_multilevel(
         _ptr(q), _ptr(k_prefix), _ptr(v_prefix), _hptr(kv_ptr), _hptr(rb), _hptr(re), len(kv_ptr) - 1,
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens),
+        B, Hq, Hkv, D, ps, P, float(sm_scale), _hptr(plan_buf), _ptr(workspace),
+        workspace.numel(), _ptr(o), _ptr(lse), _dtype_code(q), _stream(stream)))
+    return o, lse
+
+
+def cascade_decode_paged_prefix(q, prefix_pages, prefix_page_indptr, prefix_kv_indptr,
+                                prefix_req_ranges, k_cache, v_cache, block_table, cache_seqlens,
+                                sm_scale, workspace, plan_buf=None, o=None, lse=None, stream=None):
+    """The multi-level cascade with each group's prefix read in place from the
+    page pool: prefix_pages (device int32) lists group j's pages at
+    prefix_page_indptr[j] .. prefix_page_indptr[j+1]-1."""
+    import torch
+    B, Hq, D = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    kv_ptr, pg_ptr = _host_i32(prefix_kv_indptr), _host_i32(prefix_page_indptr)
+    rr = _host_i32(prefix_req_ranges).reshape(-1, 2)
+    rb, re = np.ascontiguousarray(rr[:, 0]), np.ascontiguousarray(rr[:, 1])
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().pkc_cascade_decode_paged_prefix(
+        _ptr(q), _ptr(prefix_pages), _hptr(pg_ptr), _hptr(kv_ptr), _hptr(rb), _hptr(re), len(kv_ptr) - 1,
         _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens),
         B, Hq, Hkv, D, ps, P, float(sm_scale), _hptr(plan_buf), _ptr(workspace),
         workspace.numel(), _ptr(o), _ptr(lse), _dtype_code(q), _stream(stream)))

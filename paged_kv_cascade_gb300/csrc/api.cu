@@ -493,12 +493,19 @@ int pkc_prefix_attention_state(const void* q, const void* k_prefix, const void* 
 namespace {
 // The cascade for prefix groups given as request ranges (overlapping ranges:
 // a multi-level cascade).
+// prefix_pages (device) / page_indptr (host): a paged prefix read from the
+// cache's page pool (k_prefix, v_prefix unused); nullptr: contiguous prefixes.
 int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, const int32_t* prefix_kv_indptr_host,
                  const int32_t* req_begin, const int32_t* req_end, int n_prefix, const void* k_cache,
                  const void* v_cache, const int32_t* block_table, int block_table_stride, const int32_t* cache_seqlens,
                  int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
                  float sm_scale, const int32_t* plan_host, void* workspace, size_t workspace_bytes, void* o,
-                 float* lse, int dtype, void* stream) {
+                 float* lse, int dtype, void* stream, const int32_t* prefix_pages = nullptr,
+                 const int32_t* page_indptr = nullptr) {
+  if (prefix_pages) {
+    k_prefix = k_cache;
+    v_prefix = v_cache;
+  }
   if (int rc = check_attn_dims(batch, num_qo_heads, num_kv_heads, head_dim, dtype)) return rc;
   if (int rc = check_plan(plan_host, batch)) return rc;
   if (page_size < 1 || block_table_stride < 1 || num_pages < 0)
@@ -518,6 +525,23 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   if (int rc = setup_prefix(S, prefix_kv_indptr_host, req_begin, req_end, n_prefix, batch, num_qo_heads,
                             num_kv_heads, sm_scale, ws, workspace_bytes, L, status))
     return rc;
+  if (prefix_pages) {
+    if (!page_indptr) return set_error(PKC_ERR_INVALID_ARG, "paged prefix: prefix_page_indptr is NULL");
+    if (page_size < 8 || 128 % page_size != 0)
+      return set_error(PKC_ERR_UNSUPPORTED, "paged prefix: page_size must divide 128 and be >= 8 (got %d)",
+                       page_size);
+    if (page_indptr[0] < 0) return set_error(PKC_ERR_INVALID_ARG, "prefix_page_indptr must start >= 0");
+    for (int j = 0; j < n_prefix; ++j) {
+      const int len = prefix_kv_indptr_host[j + 1] - prefix_kv_indptr_host[j];
+      if (page_indptr[j + 1] - page_indptr[j] < (len + page_size - 1) / page_size)
+        return set_error(PKC_ERR_INVALID_ARG, "paged prefix: group %d has %d tokens but %d pages", j, len,
+                         page_indptr[j + 1] - page_indptr[j]);
+    }
+    S.pp.prefix_pages = prefix_pages;
+    for (int j = 0; j <= n_prefix; ++j) S.pp.page_indptr[j] = page_indptr[j];
+    S.pp.page_size = page_size;
+    S.pp.num_pages = num_pages;
+  }
   cudaEvent_t ev[4];
   for (int i = 0; i < 4; ++i) ev[i] = g_stage_events[i];
   g_stage_events[0] = g_stage_events[1] = g_stage_events[2] = g_stage_events[3] = nullptr;
@@ -577,6 +601,20 @@ int pkc_cascade_decode(const void* q, const void* k_prefix, const void* v_prefix
   return cascade_impl(q, k_prefix, v_prefix, prefix_kv_indptr_host, rb, re, n_prefix, k_cache, v_cache, block_table,
                       block_table_stride, cache_seqlens, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
                       num_pages, sm_scale, plan_host, workspace, workspace_bytes, o, lse, dtype, stream);
+}
+
+int pkc_cascade_decode_paged_prefix(
+    const void* q, const int32_t* prefix_pages, const int32_t* prefix_page_indptr_host,
+    const int32_t* prefix_kv_indptr_host, const int32_t* prefix_req_begin_host, const int32_t* prefix_req_end_host,
+    int n_prefix, const void* k_cache, const void* v_cache, const int32_t* block_table, int block_table_stride,
+    const int32_t* cache_seqlens, int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+    int64_t num_pages, float sm_scale, const int32_t* plan_host, void* workspace, size_t workspace_bytes, void* o,
+    float* lse, int dtype, void* stream) {
+  if (!prefix_pages) return set_error(PKC_ERR_INVALID_ARG, "paged prefix: prefix_pages is NULL");
+  return cascade_impl(q, k_cache, v_cache, prefix_kv_indptr_host, prefix_req_begin_host, prefix_req_end_host,
+                      n_prefix, k_cache, v_cache, block_table, block_table_stride, cache_seqlens, batch, num_qo_heads,
+                      num_kv_heads, head_dim, page_size, num_pages, sm_scale, plan_host, workspace, workspace_bytes, o,
+                      lse, dtype, stream, prefix_pages, prefix_page_indptr_host);
 }
 
 int pkc_cascade_decode_multilevel(

@@ -135,6 +135,14 @@ struct PrefixParams {
   float* out_lse;                           // [split, B, Hq]
   int64_t split_stride_o, split_stride_lse;
   int32_t* status;
+  // Paged prefix (the prefix KV stays in the page pool [num_pages,
+  // page_size, Hkv, 128]): group j's tokens are pages
+  // prefix_pages[page_indptr[j] ..] in order, the last one partly filled.
+  // page_size divides 128.  nullptr prefix_pages: contiguous prefixes.
+  const int32_t* prefix_pages;              // device
+  int32_t page_indptr[PKC_MAX_PREFIX + 1];
+  int page_size;
+  int64_t num_pages;
 };
 
 struct AppendParams {
@@ -174,6 +182,8 @@ int launch_contract(const ContractParams& p, int n_rows, void* stream);
 int launch_append_kv(const AppendParams& p, int batch, void* stream);
 // q/k/v tensor maps are built inside; returns cudaError_t or -1 when the
 // driver entry point for tensor maps is unavailable.
+// Contiguous prefixes: k/v_prefix [prefix_tokens, Hkv, 128].  Paged
+// prefixes (p.prefix_pages set): k/v_prefix are the page pools.
 int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix,
                   const void* v_prefix, int64_t prefix_tokens, int dtype,
                   void* stream);

@@ -175,10 +175,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = s_stage0 + s * kStageBytes;
           const int t0 = pc.kv_lo + u * kKvTile;
           mbar_arrive_expect_tx(bar(bars->kv_full[s]), kStageBytes);
-          tma_load_3d(st, &tm_k, bar(bars->kv_full[s]), 0, pc.kvh, t0, pol);
-          tma_load_3d(st + kSubTile, &tm_k, bar(bars->kv_full[s]), 64, pc.kvh, t0, pol);
-          tma_load_3d(st + 2 * kSubTile, &tm_v, bar(bars->kv_full[s]), 0, pc.kvh, t0, pol);
-          tma_load_3d(st + 3 * kSubTile, &tm_v, bar(bars->kv_full[s]), 64, pc.kvh, t0, pol);
+          if (!p.prefix_pages) {
+            tma_load_3d(st, &tm_k, bar(bars->kv_full[s]), 0, pc.kvh, t0, pol);
+            tma_load_3d(st + kSubTile, &tm_k, bar(bars->kv_full[s]), 64, pc.kvh, t0, pol);
+            tma_load_3d(st + 2 * kSubTile, &tm_v, bar(bars->kv_full[s]), 0, pc.kvh, t0, pol);
+            tma_load_3d(st + 3 * kSubTile, &tm_v, bar(bars->kv_full[s]), 64, pc.kvh, t0, pol);
+          } else {
+            // One box per page: {64 dims, 1 head, page_size slots}; pages past
+            // the group's list load from page num_pages, outside the pool,
+            // which the copy engine fills with zeros.
+            const int ps = p.page_size;
+            const int rel = t0 - p.kv_indptr[pc.grp];  // token offset within the group
+            const int pg0 = p.page_indptr[pc.grp], n_pg = p.page_indptr[pc.grp + 1] - pg0;
+            for (int r = 0; r < kKvTile; r += ps) {
+              const int pi = (rel + r) / ps;
+              int32_t page = pi < n_pg ? p.prefix_pages[pg0 + pi] : (int32_t)p.num_pages;
+              if (pi < n_pg && (page < 0 || page >= p.num_pages)) {
+                report(p.status, PKC_ERR_BLOCK_TABLE);
+                page = (int32_t)p.num_pages;  // read as zeros
+              }
+              const uint32_t row = (uint32_t)r * 128;
+              tma_load_4d(st + row, &tm_k, bar(bars->kv_full[s]), 0, pc.kvh, 0, page, pol);
+              tma_load_4d(st + kSubTile + row, &tm_k, bar(bars->kv_full[s]), 64, pc.kvh, 0, page, pol);
+              tma_load_4d(st + 2 * kSubTile + row, &tm_v, bar(bars->kv_full[s]), 0, pc.kvh, 0, page, pol);
+              tma_load_4d(st + 3 * kSubTile + row, &tm_v, bar(bars->kv_full[s]), 64, pc.kvh, 0, page, pol);
+            }
+          }
           ++g;
           return true;
         };
@@ -410,6 +432,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           p_half(std::false_type{}, sr[0], 0);
           p_half(std::false_type{}, sr[1], 1);
+          if (p.prefix_pages) {
+            // A paged prefix's last page may hold anything (even NaN) past the
+            // prefix: zero those V rows so that P = 0 meets V = 0 in P.V.
+            const uint32_t vst = s_stage0 + s * kStageBytes + 2 * kSubTile;
+            const int n_chunks = (kKvTile - vrow) * 16;  // 16-byte chunks in both 64-dim halves
+            for (int c = (int)threadIdx.x - 64; c < n_chunks; c += 256) {
+              const int r = vrow + (c >> 4), half = (c >> 3) & 1, ch16 = c & 7;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vst + half * kSubTile + r * 128 + ch16 * 16),
+                           "r"(0u)
+                           : "memory");
+            }
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -511,10 +545,23 @@ int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix, co
                   int64_t prefix_tokens, int dtype, void* stream) {
   if (p.n_blocks <= 0 || p.total_tiles <= 0) return 0;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, dtype, PKC_HEAD_DIM, p.hq, p.batch, p.g, kRows / p.g) ||
-      !make_map(&mk, k_prefix, dtype, PKC_HEAD_DIM, p.hkv, prefix_tokens, 1, kKvTile) ||
-      !make_map(&mv, v_prefix, dtype, PKC_HEAD_DIM, p.hkv, prefix_tokens, 1, kKvTile))
-    return -1;
+  if (!make_map(&mq, q, dtype, PKC_HEAD_DIM, p.hq, p.batch, p.g, kRows / p.g)) return -1;
+  if (!p.prefix_pages) {
+    if (!make_map(&mk, k_prefix, dtype, PKC_HEAD_DIM, p.hkv, prefix_tokens, 1, kKvTile) ||
+        !make_map(&mv, v_prefix, dtype, PKC_HEAD_DIM, p.hkv, prefix_tokens, 1, kKvTile))
+      return -1;
+  } else {
+    // 4-D view (dim, head, slot, page) of the pool [num_pages][page_size][Hkv][128];
+    // a box is one head's page_size slots of one page, 64 dims (128 bytes) wide.
+    const uint64_t dims[4] = {(uint64_t)PKC_HEAD_DIM, (uint64_t)p.hkv, (uint64_t)p.page_size,
+                              (uint64_t)(p.num_pages > 0 ? p.num_pages : 1)};
+    const uint64_t strides[3] = {(uint64_t)PKC_HEAD_DIM * 2, (uint64_t)PKC_HEAD_DIM * 2 * p.hkv,
+                                 (uint64_t)PKC_HEAD_DIM * 2 * p.hkv * p.page_size};
+    const uint32_t box[4] = {64u, 1u, (uint32_t)p.page_size, 1u};
+    if (!encode_tiled_map(&mk, k_prefix, dtype, 4, dims, strides, box, true) ||
+        !encode_tiled_map(&mv, v_prefix, dtype, 4, dims, strides, box, true))
+      return -1;
+  }
   cudaStream_t st = (cudaStream_t)stream;
   return dtype == PKC_BF16 ? launch_t<__nv_bfloat16>(p, mq, mk, mv, st)
                            : launch_t<__half>(p, mq, mk, mv, st);

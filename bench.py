@@ -45,7 +45,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["pkc", "reference"], default="pkc")
     ap.add_argument("--workload", default="gqa_cascade_lb",
                     choices=["gqa_cascade_lb", "cascade_long_prompt", "tiny_cascade",
-                             "paged_decode", "paged_decode_gqa", "paged_decode_fp8", "merge"],
+                             "paged_decode", "paged_decode_gqa", "paged_decode_fp8", "merge",
+                             "gqa_cascade_3level", "gqa_cascade_paged_prefix"],
                     help="cascade workloads time the whole step; 'paged_decode*' time the "
                          "non-cascade decode (fp16 MHA, fp16 GQA, fp8-KV GQA) and 'merge' the "
                          "binary / 16-ary merge kernels (auxiliary lines)")
@@ -352,6 +353,69 @@ def run_aux(args):
     print(json.dumps(line), flush=True)
 
 
+def run_cascade_variant(args):
+    """Auxiliary cascade lines: the three-level cascade, and the two-level
+    cascade with its prefixes read in place from the page pool (timed beside
+    the contiguous-prefix call on the same tokens)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cascade_gb300 as pkc
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from pkc_testing import dev, to_device
+    hbm_peak, _, peak_kind = load_peaks()
+    K, W = max(args.steps, 3), max(args.warmup, 3)
+    paged = args.workload == "gqa_cascade_paged_prefix"
+    cfg = workload_cfg("gqa_cascade_lb" if paged else args.workload)
+    p = workloads.make_problem(**cfg)
+    d = to_device(p)
+    B, Hq, D = p["q"].shape
+    C = cfg["num_ctas"]
+    ws = torch.empty(pkc.workspace_size(B, Hq, C, 64), dtype=torch.uint8, device="cuda")
+    pkc.workspace_init(ws)
+    buf = pkc.plan(p["cache_seqlens"], C)
+    pkc.plan_upload(buf, ws)
+    o = torch.empty_like(d["q"])
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    eff = workloads.effective_bytes(p)
+    extra = {}
+    if paged:
+        kc, vc, pages, page_indptr = workloads.pool_prefixes(p, 5, poison=False)
+        kc, vc, pages = dev(kc), dev(vc), dev(pages)
+        ind = p["prefix_req_indptr"]
+        ranges = [(int(ind[j]), int(ind[j + 1])) for j in range(len(ind) - 1)]
+        call = lambda: pkc.cascade_decode_paged_prefix(
+            d["q"], pages, page_indptr, p["prefix_kv_indptr"], ranges, kc, vc, d["block_table"],
+            d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse)
+        ms_contig = time_region(torch, lambda: pkc.cascade_decode(
+            d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"], p["prefix_req_indptr"],
+            d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"], p["sm_scale"], ws,
+            plan_buf=buf, o=o, lse=lse), K, W)
+        extra = {"contiguous_prefix_us": 1e3 * ms_contig,
+                 "contiguous_prefix_value": eff / (ms_contig / 1e3) / 1e9}
+        metric = "cascade decode effective KV throughput, prefix read from the page pool"
+    else:
+        ranges = cfg["prefix_ranges"]
+        call = lambda: pkc.cascade_decode_multilevel(
+            d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"], ranges, d["k_cache"],
+            d["v_cache"], d["block_table"], d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf,
+            o=o, lse=lse)
+        metric = "three-level cascade decode effective KV throughput"
+    ms = time_region(torch, call, K, W)
+    if pkc.device_status(ws) != 0:
+        raise RuntimeError("device status not OK")
+    line = {"metric": metric, "unit": "GB/s", "value": eff / (ms / 1e3) / 1e9, "us": 1e3 * ms,
+            "bytes": eff, "frac": eff / (ms / 1e3) / 1e9 / hbm_peak, "peak": hbm_peak,
+            "peak_source": f"{peak_kind} hbm_gbs", "steps": K, "warmup": W, "dtype": cfg["dtype"],
+            "data": "synthetic", "launch": "direct (prefix, decode, contraction)",
+            "config": {"workload": args.workload, "batch": B, "num_qo_heads": Hq,
+                       "num_kv_heads": p["num_kv_heads"], "prefix_lens": cfg["prefix_lens"],
+                       "prefix_ranges": ranges, "suffix_tokens": int(p["cache_seqlens"].sum()),
+                       "num_ctas": C}}
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
 def run_e2e(torch, pkc, p, d, cfg, eff, steps, num_ctas, world, dist):
     """Effective GB/s through the public API with host buffers.
 
@@ -462,6 +526,9 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload in ("gqa_cascade_3level", "gqa_cascade_paged_prefix"):
+        run_cascade_variant(args)
         return
     if args.workload == "merge" or args.workload.startswith("paged_decode"):
         run_aux(args)

@@ -20,28 +20,8 @@ def _pooled(prefix_lens, ranges, lens, ps, hq=32, hkv=8, dtype="bf16", seed=41):
     p = workloads.make_problem(batch=len(lens), hq=hq, hkv=hkv, d=128, dtype=dtype,
                                prefix_lens=prefix_lens, prefix_groups=[1] * len(prefix_lens),
                                suffix=("list", lens), page_size=ps, seed=seed, poison=True)
-    n_pg = [(L + ps - 1) // ps for L in prefix_lens]
-    P0 = p["k_cache"].shape[0]
-    total = sum(n_pg)
-    order = np.random.default_rng(seed).permutation(total).astype(np.int32) + P0
-    kc = np.concatenate([p["k_cache"], np.zeros((total,) + p["k_cache"].shape[1:], p["k_cache"].dtype)])
-    vc = np.concatenate([p["v_cache"], np.zeros((total,) + p["v_cache"].shape[1:], p["v_cache"].dtype)])
-    nan = workloads._nan_value(dtype)
-    pages, off = [], 0
-    for j, L in enumerate(prefix_lens):
-        lo = int(p["prefix_kv_indptr"][j])
-        for i in range(n_pg[j]):
-            page = int(order[off + i])
-            n = min(ps, L - i * ps)
-            kc[page] = nan
-            vc[page] = nan
-            kc[page, :n] = p["k_prefix"][lo + i * ps:lo + i * ps + n]
-            vc[page, :n] = p["v_prefix"][lo + i * ps:lo + i * ps + n]
-            pages.append(page)
-        off += n_pg[j]
-    page_indptr = np.concatenate([[0], np.cumsum(n_pg)]).astype(np.int32)
-    return p, dict(k_cache=kc, v_cache=vc, pages=np.asarray(pages, np.int32),
-                   page_indptr=page_indptr, ranges=ranges)
+    kc, vc, pages, page_indptr = workloads.pool_prefixes(p, seed)
+    return p, dict(k_cache=kc, v_cache=vc, pages=pages, page_indptr=page_indptr, ranges=ranges)
 
 
 def _run(p, pool, num_ctas):

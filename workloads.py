@@ -53,6 +53,14 @@ WORKLOADS = {
                              prefix_lens=[], prefix_groups=[],
                              suffix=("lognormal", 7.0, 1.0, 16, 16384),
                              page_size=16, seed=6, num_ctas=148),
+    # three-level cascade at the GQA shape: a 2048-token prompt for all 256
+    # requests (level 0), then 4 prompts x 8192 tokens for 64 requests each
+    # (level 1, request ranges in "prefix_ranges"), then the paged suffixes
+    "gqa_cascade_3level": dict(batch=256, hq=32, hkv=8, d=128, dtype="bf16",
+                               prefix_lens=[2048] + [8192] * 4, prefix_groups=[1] * 5,
+                               prefix_ranges=[(0, 256), (0, 64), (64, 128), (128, 192), (192, 256)],
+                               suffix=("lognormal", 7.0, 1.0, 16, 16384),
+                               page_size=16, seed=7, num_ctas=148, alpha=1.0, beta=1.0),
     # GQA 32/8, bf16, batch 256; 4 prefixes x 8192 tokens, 64 requests each;
     # suffix ~ lognormal(7, 1) clipped to [16, 16384]; plan over 148 CTAs
     "gqa_cascade_lb": dict(batch=256, hq=32, hkv=8, d=128, dtype="bf16",
@@ -217,6 +225,40 @@ def make_problem(*, batch, hq, hkv, d, dtype, prefix_lens, prefix_groups,
                 cache_seqlens=lens, page_size=page_size, num_kv_heads=hkv,
                 sm_scale=1.0 / math.sqrt(d), dtype=dtype, kv_dtype=kv_dtype,
                 k_scale=float(k_scale), v_scale=float(v_scale))
+
+
+def pool_prefixes(p, seed, poison=True):
+    """Lay a problem's shared prefixes into pages of its cache pool.
+
+    The suffix pages stay first; the prefix pages are appended in a seeded
+    order (group after group, page after page); with `poison` every slot past
+    a prefix's end in its last page is NaN.  Returns (k_pool, v_pool,
+    prefix_pages int32, prefix_page_indptr int32)."""
+    ps = p["page_size"]
+    ind = p["prefix_kv_indptr"]
+    lens = np.diff(ind).astype(np.int64)
+    n_pg = [(int(L) + ps - 1) // ps for L in lens]
+    P0 = p["k_cache"].shape[0]
+    total = sum(n_pg)
+    order = np.random.default_rng(seed).permutation(total).astype(np.int32) + P0
+    shape = (total,) + p["k_cache"].shape[1:]
+    kc = np.concatenate([p["k_cache"], np.zeros(shape, p["k_cache"].dtype)])
+    vc = np.concatenate([p["v_cache"], np.zeros(shape, p["v_cache"].dtype)])
+    nanv = _nan_value(p["kv_dtype"]) if poison else 0
+    pages, off = [], 0
+    for j, L in enumerate(lens):
+        lo = int(ind[j])
+        for i in range(n_pg[j]):
+            page = int(order[off + i])
+            n = min(ps, int(L) - i * ps)
+            kc[page] = nanv
+            vc[page] = nanv
+            kc[page, :n] = p["k_prefix"][lo + i * ps:lo + i * ps + n]
+            vc[page, :n] = p["v_prefix"][lo + i * ps:lo + i * ps + n]
+            pages.append(page)
+        off += n_pg[j]
+    page_indptr = np.concatenate([[0], np.cumsum(n_pg)]).astype(np.int32)
+    return kc, vc, np.asarray(pages, np.int32), page_indptr
 
 
 def make_merge(*, tokens, heads, d, n_states, seed, v_dtype="f32", threads=8,

@@ -161,69 +161,80 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      const uint64_t pol_q = l2_policy_evict_last();
-      int g = 0, q_issued = 0;  // KV tiles and Q tiles issued
-      bool ok = true;
-      for (int x = s0; ok && x < s1;) {
-        const Piece pc = piece_at(p, x, s1);
-        x = pc.next;
-        auto load_kv = [&](int u) -> bool {
-          const int s = g % kStages;
-          if (!mbar_wait(bar(bars->kv_empty[s]), ((g / kStages) & 1) ^ 1, abort, p.status)) return false;
-          const uint32_t st = s_stage0 + s * kStageBytes;
-          const int t0 = pc.kv_lo + u * kKvTile;
-          mbar_arrive_expect_tx(bar(bars->kv_full[s]), kStageBytes);
-          if (!p.prefix_pages) {
-            tma_load_3d(st, &tm_k, bar(bars->kv_full[s]), 0, pc.kvh, t0, pol);
-            tma_load_3d(st + kSubTile, &tm_k, bar(bars->kv_full[s]), 64, pc.kvh, t0, pol);
-            tma_load_3d(st + 2 * kSubTile, &tm_v, bar(bars->kv_full[s]), 0, pc.kvh, t0, pol);
-            tma_load_3d(st + 3 * kSubTile, &tm_v, bar(bars->kv_full[s]), 64, pc.kvh, t0, pol);
-          } else {
-            // One box per page: {64 dims, 1 head, page_size slots}; pages past
-            // the group's list load from page num_pages, outside the pool,
-            // which the copy engine fills with zeros.
-            const int ps = p.page_size;
-            const int rel = t0 - p.kv_indptr[pc.grp];  // token offset within the group
-            const int pg0 = p.page_indptr[pc.grp], n_pg = p.page_indptr[pc.grp + 1] - pg0;
-            for (int r = 0; r < kKvTile; r += ps) {
-              const int pi = (rel + r) / ps;
-              int32_t page = pi < n_pg ? p.prefix_pages[pg0 + pi] : (int32_t)p.num_pages;
-              if (pi < n_pg && (page < 0 || page >= p.num_pages)) {
-                report(p.status, PKC_ERR_BLOCK_TABLE);
-                page = (int32_t)p.num_pages;  // read as zeros
-              }
-              const uint32_t row = (uint32_t)r * 128;
-              tma_load_4d(st + row, &tm_k, bar(bars->kv_full[s]), 0, pc.kvh, 0, page, pol);
-              tma_load_4d(st + kSubTile + row, &tm_k, bar(bars->kv_full[s]), 64, pc.kvh, 0, page, pol);
-              tma_load_4d(st + 2 * kSubTile + row, &tm_v, bar(bars->kv_full[s]), 0, pc.kvh, 0, page, pol);
-              tma_load_4d(st + 3 * kSubTile + row, &tm_v, bar(bars->kv_full[s]), 64, pc.kvh, 0, page, pol);
-            }
+    // The whole warp runs the loop; lane 0 waits on the barriers and the
+    // warp learns the result.  A contiguous tile is four boxes from lane 0; a
+    // paged tile is four boxes per page, issued by the lanes in parallel.
+    const uint64_t pol = l2_policy_evict_first();
+    const uint64_t pol_q = l2_policy_evict_last();
+    int g = 0, q_issued = 0;  // KV tiles and Q tiles issued
+    bool ok = true;
+    auto wait0 = [&](uint64_t& b, uint32_t parity) -> bool {
+      bool got = true;
+      if (lane == 0) got = mbar_wait(bar(b), parity, abort, p.status);
+      return __shfl_sync(0xffffffffu, got, 0);
+    };
+    for (int x = s0; ok && x < s1;) {
+      const Piece pc = piece_at(p, x, s1);
+      x = pc.next;
+      auto load_kv = [&](int u) -> bool {
+        const int s = g % kStages;
+        if (!wait0(bars->kv_empty[s], ((g / kStages) & 1) ^ 1)) return false;
+        const uint32_t st = s_stage0 + s * kStageBytes;
+        const uint32_t fb = bar(bars->kv_full[s]);
+        const int t0 = pc.kv_lo + u * kKvTile;
+        if (lane == 0) mbar_arrive_expect_tx(fb, kStageBytes);
+        __syncwarp();
+        if (!p.prefix_pages) {
+          if (lane == 0) {
+            tma_load_3d(st, &tm_k, fb, 0, pc.kvh, t0, pol);
+            tma_load_3d(st + kSubTile, &tm_k, fb, 64, pc.kvh, t0, pol);
+            tma_load_3d(st + 2 * kSubTile, &tm_v, fb, 0, pc.kvh, t0, pol);
+            tma_load_3d(st + 3 * kSubTile, &tm_v, fb, 64, pc.kvh, t0, pol);
           }
-          ++g;
-          return true;
-        };
-        // After the first piece, the ring fills with this piece's KV tiles
-        // while the previous piece's products still read the Q buffer.
-        const int pre = q_issued > 0 ? min(pc.n, kStages) : 0;
-        for (int u = 0; ok && u < pre; ++u) ok = load_kv(u);
-        if (!ok) break;
-        if (q_issued > 0 && !mbar_wait(bar(bars->q_empty), (q_issued - 1) & 1, abort, p.status)) break;
-        const int b0 = p.req_begin[pc.grp] + pc.mt * (kRows / G);
+        } else {
+          // Box c: page c / 4 of the tile, {K, V} x {dims 0-63, 64-127} by
+          // c % 4, {64 dims, 1 head, page_size slots}.  Pages past the group's
+          // list load from page num_pages, outside the pool: zero fill.
+          const int ps = p.page_size;
+          const int rel = t0 - p.kv_indptr[pc.grp];  // token offset within the group
+          const int pg0 = p.page_indptr[pc.grp], n_pg = p.page_indptr[pc.grp + 1] - pg0;
+          for (int c = lane; c < 4 * (kKvTile / ps); c += 32) {
+            const int r = (c >> 2) * ps, kind = c & 3;
+            const int pi = (rel + r) / ps;
+            int32_t page = pi < n_pg ? p.prefix_pages[pg0 + pi] : (int32_t)p.num_pages;
+            if (pi < n_pg && (page < 0 || page >= p.num_pages)) {
+              report(p.status, PKC_ERR_BLOCK_TABLE);
+              page = (int32_t)p.num_pages;  // read as zeros
+            }
+            const uint32_t dst = st + (kind >> 1) * 2 * kSubTile + (kind & 1) * kSubTile + (uint32_t)r * 128;
+            tma_load_4d(dst, kind < 2 ? (const void*)&tm_k : (const void*)&tm_v, fb, (kind & 1) * 64, pc.kvh, 0,
+                        page, pol);
+          }
+        }
+        ++g;
+        return true;
+      };
+      // After the first piece, the ring fills with this piece's KV tiles
+      // while the previous piece's products still read the Q buffer.
+      const int pre = q_issued > 0 ? min(pc.n, kStages) : 0;
+      for (int u = 0; ok && u < pre; ++u) ok = load_kv(u);
+      if (!ok) break;
+      if (q_issued > 0 && !wait0(bars->q_empty, (q_issued - 1) & 1)) break;
+      const int b0 = p.req_begin[pc.grp] + pc.mt * (kRows / G);
+      if (lane == 0) {
         mbar_arrive_expect_tx(bar(bars->q_full), kQBytes);
         tma_load_3d(s_q, &tm_q, bar(bars->q_full), 0, pc.kvh * G, b0, pol_q);
         tma_load_3d(s_q + kSubTile, &tm_q, bar(bars->q_full), 64, pc.kvh * G, b0, pol_q);
-        ++q_issued;
-        for (int u = pre; ok && u < pc.n; ++u) ok = load_kv(u);
       }
-      if (*abort) {
-        // Let the copies already issued land before the block exits.
-        volatile int no_abort = 0;
-        if (q_issued > 0) mbar_wait(bar(bars->q_full), (q_issued - 1) & 1, &no_abort, p.status);
-        for (int j = g > kStages ? g - kStages : 0; j < g; ++j)
-          mbar_wait(bar(bars->kv_full[j % kStages]), (j / kStages) & 1, &no_abort, p.status);
-      }
+      ++q_issued;
+      for (int u = pre; ok && u < pc.n; ++u) ok = load_kv(u);
+    }
+    if (*abort && lane == 0) {
+      // Let the copies already issued land before the block exits.
+      volatile int no_abort = 0;
+      if (q_issued > 0) mbar_wait(bar(bars->q_full), (q_issued - 1) & 1, &no_abort, p.status);
+      for (int j = g > kStages ? g - kStages : 0; j < g; ++j)
+        mbar_wait(bar(bars->kv_full[j % kStages]), (j / kStages) & 1, &no_abort, p.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------

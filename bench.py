@@ -98,9 +98,24 @@ def load_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def host_plan(pkc, lens, num_ctas, cfg, out=None):
+    """The step's host plan, or None where the workload decodes without one
+    (one block per (request, KV-head group), scheduled by the hardware)."""
+    if not num_ctas:
+        return None
+    return pkc.plan(lens, num_ctas, alpha=cfg["alpha"], beta=cfg["beta"], out=out)
+
+
+def upload_plan(pkc, buf, ws, stream=None):
+    if buf is not None:
+        pkc.plan_upload(buf, ws, stream=stream)
+
+
 def workload_cfg(name, batch=None):
     cfg = dict(workloads.WORKLOADS[name])
     cfg.setdefault("num_ctas", 148)
+    if not cfg.get("plan", True):
+        cfg["num_ctas"] = 0
     cfg.setdefault("alpha", 1.0)
     cfg.setdefault("beta", 1.0)
     if batch is not None and batch < cfg["batch"]:
@@ -426,7 +441,7 @@ def run_e2e(torch, pkc, p, d, cfg, eff, steps, num_ctas, world, dist):
     a set is reused only after its previous result has been read.
     """
     B, Hq, D = p["q"].shape
-    words = pkc.plan_words(B, num_ctas)
+    words = pkc.plan_words(B, num_ctas) if num_ctas else 1
     q_h = torch.from_numpy(p["q"].view(np.int16) if p["q"].dtype == np.uint16 else p["q"]).pin_memory()
     bt_h = torch.from_numpy(p["block_table"]).pin_memory()
     sl_h = torch.from_numpy(p["cache_seqlens"]).pin_memory()
@@ -452,13 +467,12 @@ def run_e2e(torch, pkc, p, d, cfg, eff, steps, num_ctas, world, dist):
 
     def enqueue(st):
         # inputs go in on their own stream so they overlap the other set's run
-        buf = pkc.plan(sl_h.numpy(), num_ctas, alpha=cfg["alpha"], beta=cfg["beta"],
-                       out=st["plan"].numpy())
+        buf = host_plan(pkc, sl_h.numpy(), num_ctas, cfg, out=st["plan"].numpy())
         with torch.cuda.stream(copy_stream):
             qview(st["q"]).copy_(q_h, non_blocking=True)
             st["bt"].copy_(bt_h, non_blocking=True)
             st["sl"].copy_(sl_h, non_blocking=True)
-            pkc.plan_upload(buf, st["ws"], stream=copy_stream)
+            upload_plan(pkc, buf, st["ws"], stream=copy_stream)
             st["copied"].record(copy_stream)
         stream.wait_event(st["copied"])
         return buf
@@ -513,7 +527,7 @@ def run_e2e(torch, pkc, p, d, cfg, eff, steps, num_ctas, world, dist):
     for st in sets:
         if pkc.device_status(st["ws"]) != 0:
             raise RuntimeError("device status not OK after the e2e run")
-    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4 + words * 4
+    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4 + (words * 4 if num_ctas else 0)
     d2h = sets[0]["o_h"].numel() * sets[0]["o_h"].element_size() + sets[0]["lse_h"].numel() * 4
     return {"value": whole_job_gbs(eff, steps, world, t), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -557,7 +571,7 @@ def main():
     lens = p["cache_seqlens"]
     ws = torch.empty(pkc.workspace_size(B, Hq, num_ctas, 64), dtype=torch.uint8, device=d["q"].device)
     pkc.workspace_init(ws)
-    words = pkc.plan_words(B, num_ctas)
+    words = pkc.plan_words(B, num_ctas) if num_ctas else 1
     pinned = [torch.empty(words, dtype=torch.int32).pin_memory() for _ in range(2)]
     plan_np = [t.numpy() for t in pinned]
     o = torch.empty_like(d["q"])
@@ -571,9 +585,9 @@ def main():
     def step(i):
         uploaded[i & 1].synchronize()
         t0 = time.perf_counter()
-        buf = pkc.plan(lens, num_ctas, alpha=cfg["alpha"], beta=cfg["beta"], out=plan_np[i & 1])
+        buf = host_plan(pkc, lens, num_ctas, cfg, out=plan_np[i & 1])
         host_plan_s.append(time.perf_counter() - t0)
-        pkc.plan_upload(buf, ws)
+        upload_plan(pkc, buf, ws)
         uploaded[i & 1].record()
         pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
                            p["prefix_req_indptr"], d["k_cache"], d["v_cache"], d["block_table"],
@@ -652,7 +666,7 @@ def main():
         gplan = [torch.empty(words, dtype=torch.int32).pin_memory() for _ in range(2)]
         gplan_np = [t.numpy() for t in gplan]
         gdone = [torch.cuda.Event(), torch.cuda.Event()]
-        gbuf = pkc.plan(lens, num_ctas, alpha=cfg["alpha"], beta=cfg["beta"], out=gplan_np[0])
+        gbuf = host_plan(pkc, lens, num_ctas, cfg, out=gplan_np[0])
 
         def g_run():
             pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
@@ -661,7 +675,7 @@ def main():
                                plan_buf=gbuf, o=o, lse=lse, stream=gstream)
 
         with torch.cuda.stream(gstream):
-            pkc.plan_upload(gbuf, ws, stream=gstream)
+            upload_plan(pkc, gbuf, ws, stream=gstream)
             g_run()
             gstream.synchronize()
             cg = torch.cuda.CUDAGraph()
@@ -670,9 +684,8 @@ def main():
 
             def g_step(i):
                 gdone[i & 1].synchronize()
-                b = pkc.plan(lens, num_ctas, alpha=cfg["alpha"], beta=cfg["beta"],
-                             out=gplan_np[i & 1])
-                pkc.plan_upload(b, ws, stream=gstream)
+                b = host_plan(pkc, lens, num_ctas, cfg, out=gplan_np[i & 1])
+                upload_plan(pkc, b, ws, stream=gstream)
                 gdone[i & 1].record(gstream)
                 cg.replay()
 
@@ -732,7 +745,10 @@ def main():
             "config": {"workload": args.workload, "batch": B, "num_qo_heads": Hq,
                        "num_kv_heads": p["num_kv_heads"], "head_dim": D,
                        "page_size": cfg["page_size"], "prefix_lens": cfg["prefix_lens"],
-                       "suffix_tokens": suffix_tokens, "num_ctas": num_ctas,
+                       "suffix_tokens": suffix_tokens,
+                       "num_ctas": num_ctas or None,
+                       "plan": "host plan over num_ctas CTAs" if num_ctas else
+                               "none: one decode block per (request, KV-head group)",
                        "effective_bytes_per_step": eff,
                        "l2": "inputs larger than L2 (one step reads %.2f GB)" % (eff / 1e9),
                        "launch": mode, "decode_kernel": args.decode_kernel,

@@ -42,6 +42,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "decode_common.cuh"
 #include "pkc_device.cuh"
 #include "pkc_internal.h"
 
@@ -174,34 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       got = __shfl_sync(0xffffffffu, got, 0);
       return got ? s : -1;
     };
-    for (int it = 0; ok && it < n_hg_mine * (w_end - w_begin); ++it) {
-      const int hg = (int)blockIdx.y + (int)gridDim.y * (it / (w_end - w_begin));
-      const int wi = w_begin + it % (w_end - w_begin);
-      int req, kb, ke, slot;
-      if (pl) {
-        const int w = pl[pl[PKC_PLAN_OFF_CTA_WORK] + wi];
-        const int unit = pl[pl[PKC_PLAN_OFF_WORK_UNIT] + w];
-        req = pl[pl[PKC_PLAN_OFF_UNIT_REQ] + unit];
-        kb = pl[pl[PKC_PLAN_OFF_WORK_KV_BEGIN] + w];
-        ke = pl[pl[PKC_PLAN_OFF_WORK_KV_END] + w];
-        slot = pl[pl[PKC_PLAN_OFF_WORK_PARTIAL] + w];
-        const int len = p.cache_seqlens[req];
-        if (pl[pl[PKC_PLAN_OFF_UNIT_KV_LEN] + unit] != len) {
-          if (lane == 0 && hg == 0) report(p.status, PKC_ERR_PLAN);
-          ke = min(ke, len);
-          kb = min(kb, ke);
-        }
-      } else {
-        req = cta;
-        kb = 0;
-        ke = max(p.cache_seqlens[cta], 0);
-        slot = -1;
-      }
-      if ((int64_t)ke > p.bt_stride * ps) {  // more tokens than table entries
-        if (lane == 0 && hg == 0) report(p.status, PKC_ERR_BLOCK_TABLE);
-        ke = (int)(p.bt_stride * ps);
-        kb = min(kb, ke);
-      }
+    const int n_w = w_end - w_begin;
+    DecodeItemWindow items;
+    for (int it = 0; ok && it < n_hg_mine * n_w; ++it) {
+      const int hg = (int)blockIdx.y + (int)gridDim.y * (it / n_w);
+      const DecodeItem item = items.get(p, cta, w_begin, n_w, it % n_w, lane);
+      const int req = item.req, kb = item.kb, ke = item.ke, slot = item.slot;
       const int32_t* bt_row = p.block_table + (int64_t)req * p.bt_stride;
       const int n_pages_used = (ke + ps - 1) / ps;
       int win_base = -1 << 30;

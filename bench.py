@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--decode-kernel", choices=["auto", "simt", "mma"], default="auto",
                     help="paged-decode kernel for a 16-bit cache (auto: tensor cores for "
                          "grouped heads)")
+    ap.add_argument("--decode-schedule", choices=["dynamic", "static"], default="dynamic",
+                    help="planned decode: blocks take the plan's chunks from a shared "
+                         "longest-first queue (dynamic) or run their CTA's plan list (static)")
     ap.add_argument("--batch", type=int, default=None,
                     help="keep only the first N requests (and their prefix groups); "
                          "a smaller case of the same workload, for profiling")
@@ -334,6 +337,7 @@ def run_aux(args):
         d = to_device(p)
         fp8 = p["kv_dtype"] == "e4m3"
         pkc.set_decode_kernel(args.decode_kernel)
+        pkc.set_decode_schedule(args.decode_schedule)
         B, Hq, D = p["q"].shape
         C = cfg["num_ctas"]
         ws = torch.empty(pkc.workspace_size(B, Hq, C, 0), dtype=torch.uint8, device="cuda")
@@ -364,6 +368,7 @@ def run_aux(args):
                            "num_kv_heads": p["num_kv_heads"], "kv_dtype": p["kv_dtype"],
                            "kv_tokens": int(p["cache_seqlens"].sum()), "num_ctas": C,
                            "decode_kernel": "mma" if fp8 else args.decode_kernel,
+                           "decode_schedule": args.decode_schedule,
                            "launches": "decode + contraction"}}
     print(json.dumps(line), flush=True)
 
@@ -561,6 +566,7 @@ def main():
         dist.barrier()
     import paged_kv_cascade_gb300 as pkc
     pkc.set_decode_kernel(args.decode_kernel)
+    pkc.set_decode_schedule(args.decode_schedule)
 
     cfg, p = make_workload(args.workload, args.batch)
     sys.path.insert(0, os.path.join(ROOT, "tests"))
@@ -752,6 +758,7 @@ def main():
                        "effective_bytes_per_step": eff,
                        "l2": "inputs larger than L2 (one step reads %.2f GB)" % (eff / 1e9),
                        "launch": mode, "decode_kernel": args.decode_kernel,
+                       "decode_schedule": args.decode_schedule if num_ctas else None,
                        "parallelism": f"replicas x{world}"},
             "direct_us_per_step": 1e3 * direct_ms_per_step,
             "hbm_fraction": value / world / hbm_peak,

@@ -130,6 +130,11 @@ int pkc_merge_states(const void* v, const float* s, void* v_out, float* s_out,
  *                               [n_units] each (partial_begin -1 if unsplit)
  *   unit_list[n_split + n_empty] split units then empty units, unit order
  *   cta_cost[num_ctas]          final cost per CTA, as float64 (2 words each)
+ *   work_order[n_work]          the chunks w in the order of step 4
+ *   order_rec[n_work][4]        for work_order[i]: (unit, kv_begin, kv_end,
+ *                               partial), 16-byte aligned; the queue a
+ *                               dynamically scheduled decode takes chunks
+ *                               from (pkc_set_decode_schedule)
  * The plan depends on lengths only: it is the same for every head.
  */
 enum {
@@ -157,6 +162,8 @@ enum {
   PKC_PLAN_OFF_UNIT_PARTIAL_BEGIN,
   PKC_PLAN_OFF_UNIT_LIST,
   PKC_PLAN_OFF_CTA_COST,
+  PKC_PLAN_OFF_WORK_ORDER,
+  PKC_PLAN_OFF_ORDER_REC,
   PKC_PLAN_HEADER_WORDS = 32
 };
 #define PKC_PLAN_MAGIC_VALUE 0x504b4331 /* "PKC1" */
@@ -461,6 +468,21 @@ int pkc_set_stage_events(void* const* events, int n_events);
  * PKC_ERR_INVALID_ARG for any other value.
  */
 int pkc_set_decode_kernel(int which);
+
+/*
+ * Schedule of a planned paged decode (process-wide):
+ *   1 = dynamic (default): one block per planned CTA; the blocks take the
+ *       plan's chunks (x the KV-head groups) from a queue in the plan's
+ *       longest-first order (order_rec), so blocks that run ahead take the
+ *       short chunks at the end and all finish together.  The queue's
+ *       counters live in the workspace's status block; the last block resets
+ *       them, so a workspace must not be shared by two decodes in flight.
+ *   0 = static: block c runs CTA c's list of the plan (the pages' greedy
+ *       assignment), one block per (CTA, KV-head group).
+ * The states are the same either way; chunks and partial slots come from the
+ * plan.  Returns PKC_ERR_INVALID_ARG for any other value.
+ */
+int pkc_set_decode_schedule(int dynamic);
 
 #ifdef __cplusplus
 }

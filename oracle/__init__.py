@@ -403,4 +403,5 @@ def plan_ref(qo_len, kv_len, tile_q, num_ctas, alpha=1.0, beta=1.0):
         "split_units": [u for u in range(len(units)) if len(unit_chunks[u]) >= 2],
         "empty_units": [u for u in range(len(units)) if len(unit_chunks[u]) == 0],
         "n_partials": slot,
+        "order": order,
     }

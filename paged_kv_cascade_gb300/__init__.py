@@ -29,7 +29,7 @@ PLAN_FIELDS = ["MAGIC", "TOTAL_WORDS", "NUM_CTAS", "TILE_Q", "N_REQ", "KV_CHUNK"
                "OFF_CTA_INDPTR", "OFF_CTA_WORK", "OFF_WORK_UNIT", "OFF_WORK_KV_BEGIN",
                "OFF_WORK_KV_END", "OFF_WORK_PARTIAL", "OFF_UNIT_REQ", "OFF_UNIT_QTILE",
                "OFF_UNIT_KV_LEN", "OFF_UNIT_N_CHUNKS", "OFF_UNIT_PARTIAL_BEGIN",
-               "OFF_UNIT_LIST", "OFF_CTA_COST"]
+               "OFF_UNIT_LIST", "OFF_CTA_COST", "OFF_WORK_ORDER", "OFF_ORDER_REC"]
 PLAN = {name: i for i, name in enumerate(PLAN_FIELDS)}
 PLAN_MAGIC = 0x504B4331
 
@@ -57,6 +57,7 @@ SIGNATURES = {
                                         _F, _F, _P, _P, _SZ, _P, _P, _P]),
     "pkc_set_stage_events": (_I, [_c.POINTER(_P), _I]),
     "pkc_set_decode_kernel": (_I, [_I]),
+    "pkc_set_decode_schedule": (_I, [_I]),
     "pkc_append_kv": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I64, _I, _P, _SZ, _P]),
     "pkc_cascade_decode_multilevel": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I,
                                            _I, _I, _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
@@ -266,6 +267,16 @@ def set_decode_kernel(which):
     _check(lib().pkc_set_decode_kernel(DECODE_KERNELS[which]))
 
 
+DECODE_SCHEDULES = {"dynamic": 1, "static": 0}
+
+
+def set_decode_schedule(which):
+    """Schedule of a planned decode: "dynamic" (blocks take the plan's chunks
+    from a shared longest-first queue; default) or "static" (each block runs
+    its CTA's list of the plan); process-wide."""
+    _check(lib().pkc_set_decode_schedule(DECODE_SCHEDULES[which]))
+
+
 def paged_decode_state_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, sm_scale,
                                plan_buf=None, o=None, lse=None, device_status=None, stream=None):
     """paged_decode_state without a caller workspace, for callers that
@@ -396,4 +407,7 @@ def plan_dict(buf):
                            h["OFF_UNIT_LIST"] + h["N_SPLIT"] + h["N_EMPTY"]].tolist(),
         "cta_cost": buf[h["OFF_CTA_COST"]:h["OFF_CTA_COST"] + 2 * nc].view(np.float64).tolist(),
         "n_partials": h["N_PARTIALS"],
+        "order": arr("OFF_WORK_ORDER", nw),
+        "order_rec": [tuple(buf[h["OFF_ORDER_REC"] + 4 * i:h["OFF_ORDER_REC"] + 4 * i + 4].tolist())
+                      for i in range(nw)],
     }

@@ -456,6 +456,12 @@ int pkc_set_decode_kernel(int which) {
   return PKC_OK;
 }
 
+int pkc_set_decode_schedule(int dynamic) {
+  if (set_decode_schedule(dynamic) != 0)
+    return set_error(PKC_ERR_INVALID_ARG, "set_decode_schedule: dynamic must be 0 or 1 (got %d)", dynamic);
+  return PKC_OK;
+}
+
 int pkc_prefix_attention_state(const void* q, const void* k_prefix, const void* v_prefix,
                                const int32_t* prefix_kv_indptr_host, const int32_t* prefix_req_indptr_host,
                                int n_prefix, int batch, int num_qo_heads, int num_kv_heads, int head_dim,

@@ -177,12 +177,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       got = __shfl_sync(0xffffffffu, got, 0);
       return got ? s : -1;
     };
+    // Items: this CTA's plan list (or its request) for each of its head
+    // groups; or, scheduled dynamically, tickets from the shared queue, the
+    // next one taken once the current item's last stage is issued (a block
+    // holds no second ticket while it works through a long chunk).
+    const bool dyn = p.dynamic && pl;
     const int n_w = w_end - w_begin;
     DecodeItemWindow items;
-    for (int it = 0; ok && it < n_hg_mine * n_w; ++it) {
-      const int hg = (int)blockIdx.y + (int)gridDim.y * (it / n_w);
-      const DecodeItem item = items.get(p, cta, w_begin, n_w, it % n_w, lane);
+    DecodeQueue queue(p, HG, dyn);
+    DecodeItem item{0, 0, 0, -1}, item_n{0, 0, 0, -1};
+    int hg = (int)blockIdx.y, hg_n = 0, it = 0;
+    bool have = dyn ? queue.take(p, lane, item, hg) : n_hg_mine * n_w > 0;
+    if (!dyn && have) item = items.get(p, cta, w_begin, n_w, 0, lane);
+    while (ok && have) {
       const int req = item.req, kb = item.kb, ke = item.ke, slot = item.slot;
+      bool have_n = false;
       const int32_t* bt_row = p.block_table + (int64_t)req * p.bt_stride;
       const int n_pages_used = (ke + ps - 1) / ps;
       int win_base = -1 << 30;
@@ -252,9 +261,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           mbar_arrive(smem_u32(&full[s]));  // header written; the copies carry their own bytes
         }
         __syncwarp();
+        if (dyn && last_stage) have_n = queue.take(p, lane, item_n, hg_n);
         first_stage = false;
         ++k;
       } while (sl0 <= last);
+      if (dyn) {
+        have = have_n;
+        item = item_n;
+        hg = hg_n;
+      } else {
+        ++it;
+        have = it < n_hg_mine * n_w;
+        hg = (int)blockIdx.y + (int)gridDim.y * (it / max(n_w, 1));
+        if (have) item = items.get(p, cta, w_begin, n_w, it % n_w, lane);
+      }
     }
     // Tell the consumers there is no more work.
     if (ok) {
@@ -270,6 +290,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (int kk = k > kStages ? k - kStages : 0; kk < k; ++kk)
         mbar_wait(smem_u32(&full[kk % kStages]), (kk / kStages) & 1, &no_abort, p.status);
     }
+    if (dyn) queue.finish(lane);
     return;
   }
 
@@ -621,7 +642,9 @@ int launch_decode_g(const DecodeParams& p, int grid_x, const CUtensorMap& mk, co
     attr = cudaFuncSetAttribute(paged_decode_kernel<T, G, HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr != cudaSuccess) return (int)attr;
-  const dim3 grid(grid_x, p.hkv / HG);  // one block per (planned CTA, head group)
+  // one block per (planned CTA, head group); one per planned CTA when the
+  // blocks take their items from the shared queue
+  const dim3 grid(grid_x, p.dynamic ? 1 : p.hkv / HG);
   paged_decode_kernel<T, G, HG><<<grid, kDecodeThreads, smem, st>>>(mk, mv, p);
   return (int)cudaGetLastError();
 }
@@ -680,11 +703,27 @@ int set_decode_kernel(int which) {
   return 0;
 }
 
+// Planned decodes: 1 = blocks take the plan's chunks from a shared queue in
+// the plan's longest-first order (default), 0 = each block runs its CTA's
+// list of the plan (pkc_set_decode_schedule).
+static std::atomic<int> g_decode_dynamic{1};
+
+int set_decode_schedule(int dynamic) {
+  if (dynamic != 0 && dynamic != 1) return -1;
+  g_decode_dynamic.store(dynamic);
+  return 0;
+}
+
 // An fp8 cache always takes the tensor-core kernel.  A 16-bit cache takes it
 // for grouped heads (G >= 2), where the CUDA-core kernel runs out of issue
 // slots before HBM bandwidth, and the CUDA-core kernel for G = 1, unless
 // the choice is forced.
-int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype, int kv_dtype, void* stream) {
+int launch_paged_decode(const DecodeParams& p_in, int grid_x, int dtype, int kv_dtype, void* stream) {
+  DecodeParams p = p_in;
+  // The queue's counters: words 16 and 17 of the status block, which every
+  // workspace starts with (zeroed by pkc_workspace_init).
+  p.dynamic = p.plan != nullptr && g_decode_dynamic.load() != 0;
+  p.sched = p.status + 16;
   const bool mma_ok = mma_decode_heads_per_block(p.hkv, p.page_size) > 0;
   if (kv_dtype == PKC_E4M3) {
     if (dtype != PKC_F16 || !mma_ok) return (int)cudaErrorInvalidValue;

@@ -15,30 +15,18 @@ struct DecodeItem {
   int req, kb, ke, slot;  // request, KV range [kb, ke), partial slot or -1
 };
 
-// Item wi of this CTA (valid = wi < w_end).  A plan whose request length no
-// longer matches cache_seqlens is reported (PKC_ERR_PLAN) and its range is
-// clamped to the cache; a range past the block table is reported
-// (PKC_ERR_BLOCK_TABLE) and clamped to the table.
-__device__ __forceinline__ DecodeItem load_decode_item(const DecodeParams& p, int cta, int wi, bool valid) {
-  DecodeItem d{0, 0, 0, -1};
-  if (!valid) return d;
-  const int32_t* pl = p.plan;
-  if (pl) {
-    const int w = pl[pl[PKC_PLAN_OFF_CTA_WORK] + wi];
-    const int unit = pl[pl[PKC_PLAN_OFF_WORK_UNIT] + w];
-    d.req = pl[pl[PKC_PLAN_OFF_UNIT_REQ] + unit];
-    d.kb = pl[pl[PKC_PLAN_OFF_WORK_KV_BEGIN] + w];
-    d.ke = pl[pl[PKC_PLAN_OFF_WORK_KV_END] + w];
-    d.slot = pl[pl[PKC_PLAN_OFF_WORK_PARTIAL] + w];
+// Checks of a planned item against the cache: a plan whose request length
+// (plan_len) no longer matches cache_seqlens is reported (PKC_ERR_PLAN) and
+// the range is clamped to the cache; a range past the block table is
+// reported (PKC_ERR_BLOCK_TABLE) and clamped to the table.
+__device__ __forceinline__ DecodeItem checked_item(const DecodeParams& p, DecodeItem d, int plan_len, bool planned) {
+  if (planned) {
     const int len = p.cache_seqlens[d.req];
-    if (pl[pl[PKC_PLAN_OFF_UNIT_KV_LEN] + unit] != len) {
+    if (plan_len != len) {
       report(p.status, PKC_ERR_PLAN);
       d.ke = min(d.ke, len);
       d.kb = min(d.kb, d.ke);
     }
-  } else {
-    d.req = cta;
-    d.ke = max(p.cache_seqlens[cta], 0);
   }
   if ((int64_t)d.ke > p.bt_stride * p.page_size) {  // more tokens than table entries
     report(p.status, PKC_ERR_BLOCK_TABLE);
@@ -46,6 +34,26 @@ __device__ __forceinline__ DecodeItem load_decode_item(const DecodeParams& p, in
     d.kb = min(d.kb, d.ke);
   }
   return d;
+}
+
+// Item wi of this CTA's plan list (valid = wi < w_end), or request `cta`
+// without a plan.
+__device__ __forceinline__ DecodeItem load_decode_item(const DecodeParams& p, int cta, int wi, bool valid) {
+  DecodeItem d{0, 0, 0, -1};
+  if (!valid) return d;
+  const int32_t* pl = p.plan;
+  if (!pl) {
+    d.req = cta;
+    d.ke = max(p.cache_seqlens[cta], 0);
+    return checked_item(p, d, 0, false);
+  }
+  const int w = pl[pl[PKC_PLAN_OFF_CTA_WORK] + wi];
+  const int unit = pl[pl[PKC_PLAN_OFF_WORK_UNIT] + w];
+  d.req = pl[pl[PKC_PLAN_OFF_UNIT_REQ] + unit];
+  d.kb = pl[pl[PKC_PLAN_OFF_WORK_KV_BEGIN] + w];
+  d.ke = pl[pl[PKC_PLAN_OFF_WORK_KV_END] + w];
+  d.slot = pl[pl[PKC_PLAN_OFF_WORK_PARTIAL] + w];
+  return checked_item(p, d, pl[pl[PKC_PLAN_OFF_UNIT_KV_LEN] + unit], true);
 }
 
 // The warp's copy of item li of the CTA's list (0-based), reloading the
@@ -66,6 +74,55 @@ struct DecodeItemWindow {
     d.ke = __shfl_sync(0xffffffffu, mine.ke, src);
     d.slot = __shfl_sync(0xffffffffu, mine.slot, src);
     return d;
+  }
+};
+
+// The dynamic schedule: the blocks take tickets from a counter in the
+// workspace's status block.  Ticket t is chunk t / n_hg of the plan's
+// longest-first order (its 16-byte record) for head group t % n_hg, so the
+// blocks that run ahead take the short chunks at the end and the blocks
+// finish together.  Each block counts itself out once the queue is empty;
+// the last one resets both counters for the next launch (every block
+// reaches that point, on the error paths too).
+struct DecodeQueue {
+  int32_t* ctr;     // [0] next ticket, [1] blocks finished
+  const int4* rec;  // order_rec of the plan
+  const int32_t* plan_len;
+  int n_total, n_hg;
+  __device__ __forceinline__ DecodeQueue(const DecodeParams& p, int hg_per_block, bool active) {
+    ctr = nullptr;
+    rec = nullptr;
+    plan_len = nullptr;
+    n_total = 0;
+    n_hg = 1;
+    if (!active) return;
+    const int32_t* pl = p.plan;
+    ctr = p.sched;
+    rec = reinterpret_cast<const int4*>(pl + pl[PKC_PLAN_OFF_ORDER_REC]);
+    plan_len = pl + pl[PKC_PLAN_OFF_UNIT_KV_LEN];
+    n_hg = p.hkv / hg_per_block;
+    n_total = pl[PKC_PLAN_N_WORK] * n_hg;
+  }
+  // The next ticket's item (all lanes get it), or false once the queue is
+  // empty.  A decode plan's unit is its request.
+  __device__ __forceinline__ bool take(const DecodeParams& p, int lane, DecodeItem& d, int& hg) {
+    int t = 0;
+    if (lane == 0) t = atomicAdd(ctr, 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t < 0 || t >= n_total) return false;
+    const int4 r = rec[t / n_hg];
+    hg = t % n_hg;
+    d = checked_item(p, DecodeItem{r.x, r.y, r.z, r.w}, plan_len[r.x], true);
+    return true;
+  }
+  __device__ __forceinline__ void finish(int lane) {
+    if (lane != 0) return;
+    __threadfence();
+    const int n_blocks = (int)(gridDim.x * gridDim.y);
+    if (atomicAdd(ctr + 1, 1) == n_blocks - 1) {
+      atomicExch(ctr, 0);
+      atomicExch(ctr + 1, 0);
+    }
   }
 };
 

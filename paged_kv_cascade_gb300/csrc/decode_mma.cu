@@ -175,12 +175,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       got = __shfl_sync(0xffffffffu, got, 0);
       return got ? s : -1;
     };
+    // Items: this CTA's plan list (or its request) for each of its head
+    // groups; or, scheduled dynamically, tickets from the shared queue, the
+    // next one taken once the current item's last stage is issued (a block
+    // holds no second ticket while it works through a long chunk).
+    const bool dyn = p.dynamic && pl;
     const int n_w = w_end - w_begin;
     DecodeItemWindow items;
-    for (int it = 0; ok && it < n_hg_mine * n_w; ++it) {
-      const int hg = (int)blockIdx.y + (int)gridDim.y * (it / n_w);
-      const DecodeItem item = items.get(p, cta, w_begin, n_w, it % n_w, lane);
+    DecodeQueue queue(p, HG, dyn);
+    DecodeItem item{0, 0, 0, -1}, item_n{0, 0, 0, -1};
+    int hg = (int)blockIdx.y, hg_n = 0, it = 0;
+    bool have = dyn ? queue.take(p, lane, item, hg) : n_hg_mine * n_w > 0;
+    if (!dyn && have) item = items.get(p, cta, w_begin, n_w, 0, lane);
+    while (ok && have) {
       const int req = item.req, kb = item.kb, ke = item.ke, slot = item.slot;
+      bool have_n = false;
       const int32_t* bt_row = p.block_table + (int64_t)req * p.bt_stride;
       const int n_pages_used = (ke + ps - 1) / ps;
       int win_base = -1 << 30;
@@ -251,9 +260,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar);  // header written; the copies carry their own bytes
         }
         __syncwarp();
+        if (dyn && last_stage) have_n = queue.take(p, lane, item_n, hg_n);
         first_stage = false;
         ++k;
       } while (sl0 <= last);
+      if (dyn) {
+        have = have_n;
+        item = item_n;
+        hg = hg_n;
+      } else {
+        ++it;
+        have = it < n_hg_mine * n_w;
+        hg = (int)blockIdx.y + (int)gridDim.y * (it / max(n_w, 1));
+        if (have) item = items.get(p, cta, w_begin, n_w, it % n_w, lane);
+      }
     }
     if (ok) {  // no more work
       const int s = acquire(k);
@@ -268,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = k > kStages ? k - kStages : 0; kk < k; ++kk)
         mbar_wait(smem_u32(&full[kk % kStages]), (kk / kStages) & 1, &no_abort, p.status);
     }
+    if (dyn) queue.finish(lane);
     return;
   }
 
@@ -531,7 +552,7 @@ int launch_mma_g(const DecodeParams& p, int grid_x, const CUtensorMap& mk, const
                                 smem);
   });
   if (attr != cudaSuccess) return (int)attr;
-  const dim3 grid(grid_x, p.hkv / HG);
+  const dim3 grid(grid_x, p.dynamic ? 1 : p.hkv / HG);
   paged_decode_mma_kernel<KV, G, HG><<<grid, kThreads, smem, st>>>(mk, mv, p);
   return (int)cudaGetLastError();
 }

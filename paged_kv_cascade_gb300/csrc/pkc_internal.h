@@ -9,6 +9,8 @@
 #define PKC_HEAD_DIM 128
 #define PKC_MAX_PREFIX 256
 #define PKC_MAX_PREFIX_SPLITS 64
+// The status block at the start of every workspace: word 0 is the status
+// word (pkc_device_status), words 16-17 the dynamic decode queue's counters.
 #define PKC_STATUS_BYTES 256
 
 namespace pkc {
@@ -21,7 +23,7 @@ int cuda_error(int cuda_code, const char* what);
 struct PlanLayout {
   int64_t cta_indptr, cta_work, work_unit, work_kv_begin, work_kv_end,
       work_partial, unit_req, unit_qtile, unit_kv_len, unit_n_chunks,
-      unit_partial_begin, unit_list, cta_cost, total;
+      unit_partial_begin, unit_list, cta_cost, work_order, order_rec, total;
 };
 PlanLayout plan_layout(int64_t n_units, int num_ctas);
 
@@ -58,6 +60,8 @@ struct DecodeParams {
   float* part_lse;        // [slot, Hq]
   int32_t* status;
   float v_scale;          // V = v_scale * stored V (1 for 16-bit caches)
+  int dynamic;            // 1: blocks take the plan's chunks from a shared queue
+  int32_t* sched;         // the queue's two counters (in the status block)
 };
 
 // Element kinds of a paged KV cache.
@@ -171,6 +175,7 @@ int launch_merge_states(const void* v, const float* s, void* vo, float* so,
 int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype, int kv_dtype,
                         void* stream);
 int set_decode_kernel(int which);  // 0 auto, 1 CUDA cores, 2 tensor cores
+int set_decode_schedule(int dynamic);  // 1 shared queue (default), 0 the plan's CTA lists
 int launch_paged_decode_simt(const DecodeParams& p, int grid_x, int dtype,
                              void* stream);
 int launch_paged_decode_mma(const DecodeParams& p, int grid_x, int kv_kind,

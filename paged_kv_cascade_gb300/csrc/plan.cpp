@@ -34,6 +34,9 @@ PlanLayout plan_layout(int64_t n_units, int num_ctas) {
   L.unit_list = o;          o += n_units;
   o += (o & 1);  // float64 costs start on an 8-byte boundary
   L.cta_cost = o;           o += 2 * (int64_t)num_ctas;
+  L.work_order = o;         o += cap_work;
+  o = (o + 3) & ~int64_t(3);  // 16-byte records
+  L.order_rec = o;          o += 4 * cap_work;
   L.total = o;
   return L;
 }
@@ -161,6 +164,8 @@ extern "C" int pkc_plan(const int32_t* qo_len_host, const int32_t* kv_len_host,
   h[PKC_PLAN_OFF_UNIT_PARTIAL_BEGIN] = (int32_t)Lay.unit_partial_begin;
   h[PKC_PLAN_OFF_UNIT_LIST] = (int32_t)Lay.unit_list;
   h[PKC_PLAN_OFF_CTA_COST] = (int32_t)Lay.cta_cost;
+  h[PKC_PLAN_OFF_WORK_ORDER] = (int32_t)Lay.work_order;
+  h[PKC_PLAN_OFF_ORDER_REC] = (int32_t)Lay.order_rec;
 
   int32_t k = 0;
   for (int32_t c = 0; c < num_ctas; ++c) {
@@ -188,5 +193,16 @@ extern "C" int pkc_plan(const int32_t* qo_len_host, const int32_t* kv_len_host,
   h[PKC_PLAN_N_SPLIT] = n_split;
   h[PKC_PLAN_N_EMPTY] = n_empty;
   std::memcpy(h + Lay.cta_cost, cost.data(), sizeof(double) * (size_t)num_ctas);
+  // The chunks in the order of step 4, and one 16-byte record per chunk in
+  // that order, for a kernel that takes them from a shared queue.
+  for (int64_t i = 0; i < n_work; ++i) {
+    const int32_t w = order[i];
+    h[Lay.work_order + i] = w;
+    int32_t* r = h + Lay.order_rec + 4 * i;
+    r[0] = work[w].unit;
+    r[1] = work[w].b;
+    r[2] = work[w].e;
+    r[3] = partial[w];
+  }
   return PKC_OK;
 }

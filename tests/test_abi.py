@@ -100,6 +100,10 @@ def test_fp8_decode_and_kernel_switch_reject_bad_arguments(L):
         assert L.pkc_set_decode_kernel(bad) == 1
     for ok in (1, 2, 0):  # leaves the automatic choice set
         assert L.pkc_set_decode_kernel(ok) == 0
+    for bad in (-1, 2):
+        assert L.pkc_set_decode_schedule(bad) == 1
+    for ok in (0, 1):  # leaves the dynamic schedule set
+        assert L.pkc_set_decode_schedule(ok) == 0
 
 
 def test_append_kv_rejects_bad_arguments(L):
@@ -142,6 +146,10 @@ def _compare_plans(kv, C, T=1, qo=None, alpha=1.0, beta=1.0):
     assert got["unit_req"] == [u[0] for u in ref["units"]]
     assert got["unit_qtile"] == [u[1] for u in ref["units"]]
     assert got["unit_n_chunks"] == [len(c) for c in ref["unit_chunks"]]
+    # the step-4 order and its records (the dynamic decode's queue)
+    assert got["order"] == ref["order"]
+    assert got["order_rec"] == [(ref["work"][w][0], ref["work"][w][1], ref["work"][w][2], ref["partial"][w])
+                                for w in ref["order"]]
     return got
 
 

@@ -26,6 +26,7 @@ def test_hand_table_split_and_tie_break():
     assert p["cta_cost"] == [12.0, 10.0]
     assert p["partial"] == [0, 1, -1, -1]
     assert p["split_units"] == [0] and p["empty_units"] == []
+    assert p["order"] == [0, 3, 2, 1]
 
 
 def test_hand_table_empty_request_and_idle_cta():

@@ -142,6 +142,17 @@ def kv_bytes_per_token(p):
     return 2 * p["num_kv_heads"] * p["q"].shape[2] * p["q"].dtype.itemsize
 
 
+def kernel_source_sha(src_file):
+    """First 16 hex digits of sha256 over a kernel's source file and the
+    library's headers it includes (any change to them invalidates a record)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "paged_kv_cascade_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in [src_file] + sorted(f for f in os.listdir(csrc) if f.endswith((".h", ".cuh"))):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(kernel, workload):
     """Per-launch DRAM bytes from a committed ncu summary, if its recorded
     source hash matches the current kernel source and it was recorded on
@@ -152,8 +163,7 @@ def kernel_traffic(kernel, workload):
     summ = os.path.join(ROOT, "profiles", f"{kernel}_traffic.md")
     if not src_file or not os.path.exists(summ):
         return None
-    src = os.path.join(ROOT, "paged_kv_cascade_gb300", "csrc", src_file)
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha(src_file)
     rec = {}
     for line in open(summ):
         if line.startswith("traffic_record:"):

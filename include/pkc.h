@@ -377,6 +377,13 @@ int pkc_prefix_attention_state(
  * num_qo_heads] float32, equal to attention over prefix u suffix.
  * Arguments as in the two calls above; cache_seqlens counts suffix tokens
  * only; plan_host as in pkc_paged_decode_state.
+ * The prefix and suffix stages do not depend on each other: the prefix
+ * kernel runs on a library-owned side stream (one per host thread and
+ * device) forked from `stream` after the work already queued there, next to
+ * the suffix decode, and joined back before the contraction.  To the caller
+ * the call stays ordered on `stream`, under CUDA-graph capture too (the
+ * side stream is created on the first call made outside a capture; a
+ * captured first call runs the stages one after the other).
  */
 int pkc_cascade_decode(
     const void* q, const void* k_prefix, const void* v_prefix,
@@ -451,8 +458,10 @@ int pkc_cascade_decode_paged_prefix(
  * the NEXT pkc_cascade_decode call on this thread records events[0] on its
  * stream before its first kernel, then events[1], events[2], events[3]
  * after the prefix, suffix-decode and contraction kernels; the hook is then
- * cleared.  events: n_events >= 4 cudaEvent_t handles created by the
- * caller; NULL clears the hook.
+ * cleared.  A timed call runs its stages one after the other on `stream`
+ * (no side stream), so that each pair of events brackets one kernel.
+ * events: n_events >= 4 cudaEvent_t handles created by the caller; NULL
+ * clears the hook.
  */
 int pkc_set_stage_events(void* const* events, int n_events);
 

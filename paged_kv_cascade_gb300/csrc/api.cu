@@ -27,6 +27,37 @@ int set_error(int code, const char* fmt, ...) {
   return code;
 }
 
+// A side stream per (host thread, device) on which the cascade runs its
+// prefix stage next to the suffix decode, with the two events that fork it
+// from and join it to the caller's stream.  Created on first use outside a
+// stream capture; while one is being captured before that, the stages run
+// one after the other on the caller's stream.
+struct SideStream {
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static SideStream* side_stream(cudaStream_t caller) {
+  static thread_local SideStream per_dev[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream& s = per_dev[dev];
+  if (s.side) return &s;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
+  if (cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking) != cudaSuccess) {
+    s.side = nullptr;
+    return nullptr;
+  }
+  if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaStreamDestroy(s.side);
+    s.side = nullptr;
+    return nullptr;
+  }
+  return &s;
+}
+
 int cuda_error(int e, const char* what) {
   if (e == -1) return set_error(PKC_ERR_CUDA, "%s: TMA tensor map encoding failed", what);
   return set_error(PKC_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)e));
@@ -554,11 +585,29 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   auto mark = [&](int i) {
     if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
   };
+  // The prefix and suffix stages are independent: unless per-stage timing
+  // is asked for, the prefix runs on a side stream forked from the caller's
+  // stream, next to the decode, and the contraction waits for both.  The
+  // decode is launched first so that its blocks take the SMs first; the
+  // prefix blocks fill the SMs left free and those the decode releases.
+  const bool timed = ev[0] || ev[1] || ev[2] || ev[3];
+  SideStream* side = timed ? nullptr : side_stream((cudaStream_t)stream);
+  auto run_prefix = [&](void* st) -> int {
+    const int r = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, st);
+    if (r == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
+    if (r) return cuda_error(r, "prefix launch");
+    return PKC_OK;
+  };
   mark(0);
-  // 1. shared prefix: multi-query states on the tensor cores
-  int e = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, stream);
-  if (e == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
-  if (e) return cuda_error(e, "prefix launch");
+  int e = 0;
+  if (side) {
+    e = (int)cudaEventRecord(side->fork, (cudaStream_t)stream);
+    if (!e) e = (int)cudaStreamWaitEvent(side->side, side->fork, 0);
+    if (e) return cuda_error(e, "cascade: stream fork");
+  } else {
+    // 1. shared prefix: multi-query states on the tensor cores
+    if (int rc = run_prefix(stream)) return rc;
+  }
   mark(1);
   // 2. unique suffixes: paged decode states (unsplit -> suffix states)
   DecodeParams dp;
@@ -576,6 +625,17 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   dp.status = status;
   e = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, dtype, stream);
   if (e) return cuda_error(e, "paged decode launch");
+  if (side) {
+    // 1. shared prefix, on the side stream; the caller's stream waits for it
+    if (int rc = run_prefix(side->side)) {
+      cudaEventRecord(side->join, side->side);  // keep the fork joined
+      cudaStreamWaitEvent((cudaStream_t)stream, side->join, 0);
+      return rc;
+    }
+    e = (int)cudaEventRecord(side->join, side->side);
+    if (!e) e = (int)cudaStreamWaitEvent((cudaStream_t)stream, side->join, 0);
+    if (e) return cuda_error(e, "cascade: stream join");
+  }
   mark(2);
   // 3. contraction + merge: prefix splits (+) suffix chunks -> final O, LSE
   ContractParams cp;

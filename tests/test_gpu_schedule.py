@@ -102,3 +102,47 @@ def test_dynamic_cascade_gqa_workload_rows():
     assert torch.equal(res["static"][0], res["dynamic"][0])
     assert torch.equal(res["static"][1], res["dynamic"][1])
     assert not _status_block(ws)[16:18].any()
+
+
+def test_cascade_side_stream_and_timed_sequential_run_agree():
+    """The cascade forks its prefix stage onto a side stream next to the
+    decode; a call with stage events runs the stages in order on one stream.
+    Both give the same bits, also replayed from a CUDA graph."""
+    w = dict(workloads.WORKLOADS["gqa_cascade_lb"])
+    p = workloads.make_problem(**dict(w, batch=32, prefix_lens=[2048], prefix_groups=[32]))
+    d = to_device(p)
+    buf = pkc.plan(p["cache_seqlens"], 40)
+    ws = workspace_for(pkc, p, num_ctas=40)
+    pkc.plan_upload(buf, ws)
+    o = torch.empty_like(d["q"])
+    lse = torch.empty(p["q"].shape[:2], dtype=torch.float32, device="cuda")
+
+    def run():
+        pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
+                           p["prefix_req_indptr"], d["k_cache"], d["v_cache"], d["block_table"],
+                           d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in ev:  # torch creates the CUDA event on its first record
+        e.record()
+    pkc.set_stage_events(ev)
+    run()
+    torch.cuda.synchronize()
+    seq = (o.clone(), lse.clone())
+    assert all(ev[i].elapsed_time(ev[i + 1]) > 0 for i in range(3))
+    o.zero_()
+    run()  # forked
+    torch.cuda.synchronize()
+    assert torch.equal(o, seq[0]) and torch.equal(lse, seq[1])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            run()
+    o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, seq[0]) and torch.equal(lse, seq[1])
+    assert pkc.device_status(ws) == pkc.PKC_OK
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse)

@@ -461,7 +461,8 @@ def run_e2e(torch, pkc, p, d, cfg, eff, steps, num_ctas, world, dist):
     bt_h = torch.from_numpy(p["block_table"]).pin_memory()
     sl_h = torch.from_numpy(p["cache_seqlens"]).pin_memory()
     stream = torch.cuda.Stream()
-    copy_stream = torch.cuda.Stream()
+    copy_stream = torch.cuda.Stream()  # inputs in
+    out_stream = torch.cuda.Stream()   # results out
     sets = []
     for _ in range(2):
         st = {"q": torch.empty_like(d["q"]), "bt": torch.empty_like(d["block_table"]),
@@ -473,7 +474,8 @@ def run_e2e(torch, pkc, p, d, cfg, eff, steps, num_ctas, world, dist):
               "plan": torch.empty(words, dtype=torch.int32).pin_memory(),
               "o_h": torch.empty(d["q"].shape, dtype=d["q"].dtype).pin_memory(),
               "lse_h": torch.empty((B, Hq), dtype=torch.float32).pin_memory(),
-              "done": torch.cuda.Event(), "copied": torch.cuda.Event(), "pending": False}
+              "done": torch.cuda.Event(), "copied": torch.cuda.Event(), "ran": torch.cuda.Event(),
+              "pending": False}
         pkc.workspace_init(st["ws"])
         sets.append(st)
 
@@ -516,9 +518,14 @@ def run_e2e(torch, pkc, p, d, cfg, eff, steps, num_ctas, world, dist):
                 checksum += float(st["lse_h"][0, 0])
             enqueue(st)
             st["graph"].replay()
-            st["o_h"].copy_(st["o"], non_blocking=True)
-            st["lse_h"].copy_(st["lse"], non_blocking=True)
-            st["done"].record(stream)
+            # the result goes out on its own copy stream, overlapping the
+            # other set's step on the compute stream and its input copies
+            st["ran"].record(stream)
+            out_stream.wait_event(st["ran"])
+            with torch.cuda.stream(out_stream):
+                st["o_h"].copy_(st["o"], non_blocking=True)
+                st["lse_h"].copy_(st["lse"], non_blocking=True)
+                st["done"].record(out_stream)
             st["pending"] = True
 
         def drain():
@@ -548,7 +555,8 @@ def run_e2e(torch, pkc, p, d, cfg, eff, steps, num_ctas, world, dist):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": 1e3 * t / steps, "steps": steps,
             "note": "pinned host inputs in, O/LSE out and read every step; two buffer sets "
-                    "alternate so host work overlaps the previous step"}
+                    "alternate, inputs in and results out on two copy streams, so host work "
+                    "and copies overlap the other set's step"}
 
 
 def main():
@@ -675,35 +683,51 @@ def main():
 
     # ---- the same step with the device work replayed from a CUDA graph ----
     # The plan still runs on the host and is uploaded every step (outside the
-    # graph); the captured cascade call reads it from the workspace.
+    # graph); the captured cascade call reads it from its workspace.  Two
+    # workspaces and two graphs alternate, so that step i+1's plan upload (on
+    # a copy stream) overlaps step i's device work; a workspace's plan is
+    # overwritten only after the graph that read it has run.
     graph = None
     try:
-        gstream = torch.cuda.Stream()
+        gstream, cstream = torch.cuda.Stream(), torch.cuda.Stream()
         gplan = [torch.empty(words, dtype=torch.int32).pin_memory() for _ in range(2)]
         gplan_np = [t.numpy() for t in gplan]
-        gdone = [torch.cuda.Event(), torch.cuda.Event()]
-        gbuf = host_plan(pkc, lens, num_ctas, cfg, out=gplan_np[0])
-
-        def g_run():
-            pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
-                               p["prefix_req_indptr"], d["k_cache"], d["v_cache"],
-                               d["block_table"], d["cache_seqlens"], p["sm_scale"], ws,
-                               plan_buf=gbuf, o=o, lse=lse, stream=gstream)
-
+        gws = [ws, torch.empty_like(ws)]
+        pkc.workspace_init(gws[1])
+        gdone = [torch.cuda.Event(), torch.cuda.Event()]      # graph s has run
+        uploaded = [torch.cuda.Event(), torch.cuda.Event()]   # plan s is on the GPU
+        graphs = []
         with torch.cuda.stream(gstream):
-            upload_plan(pkc, gbuf, ws, stream=gstream)
-            g_run()
-            gstream.synchronize()
-            cg = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(cg, stream=gstream):
+            for sidx in range(2):
+                gbuf = host_plan(pkc, lens, num_ctas, cfg, out=gplan_np[sidx])
+
+                def g_run(sidx=sidx, gbuf=gbuf):
+                    pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
+                                       p["prefix_req_indptr"], d["k_cache"], d["v_cache"],
+                                       d["block_table"], d["cache_seqlens"], p["sm_scale"], gws[sidx],
+                                       plan_buf=gbuf, o=o, lse=lse, stream=gstream)
+
+                upload_plan(pkc, gbuf, gws[sidx], stream=gstream)
                 g_run()
+                gstream.synchronize()
+                cg = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(cg, stream=gstream):
+                    g_run()
+                graphs.append(cg)
+            for e in gdone + uploaded:
+                e.record(gstream)
+            gstream.synchronize()
 
             def g_step(i):
-                gdone[i & 1].synchronize()
-                b = host_plan(pkc, lens, num_ctas, cfg, out=gplan_np[i & 1])
-                upload_plan(pkc, b, ws, stream=gstream)
-                gdone[i & 1].record(gstream)
-                cg.replay()
+                sidx = i & 1
+                uploaded[sidx].synchronize()  # the pinned plan buffer is free again
+                b = host_plan(pkc, lens, num_ctas, cfg, out=gplan_np[sidx])
+                cstream.wait_event(gdone[sidx])  # the graph that read this plan has run
+                upload_plan(pkc, b, gws[sidx], stream=cstream)
+                uploaded[sidx].record(cstream)
+                gstream.wait_event(uploaded[sidx])
+                graphs[sidx].replay()
+                gdone[sidx].record(gstream)
 
             for i in range(max(3, args.warmup)):
                 g_step(i)
@@ -721,8 +745,9 @@ def main():
         g_ms = reduce_max(ga.elapsed_time(gb), dist, d["q"].device)
         graph = {"value": whole_job_gbs(eff, K, world, g_ms / 1e3), "unit": "GB/s",
                  "us_per_step": 1e3 * g_ms / K,
-                 "note": "host plan + upload each step, device work replayed from one CUDA graph"}
-        if pkc.device_status(ws) != 0:
+                 "note": "host plan + upload each step (on a copy stream, two workspaces "
+                         "alternating), device work replayed from a CUDA graph"}
+        if pkc.device_status(gws[0]) != 0 or pkc.device_status(gws[1]) != 0:
             raise RuntimeError("device status after graph replay")
     except RuntimeError:
         raise

@@ -126,6 +126,54 @@ def _hptr(a):
     return None if a is None else ctypes.c_void_p(a.ctypes.data)
 
 
+# ---------------------------------------------------------------------------
+# Argument checks.  The C ABI takes raw pointers and sizes, so a tensor of the
+# wrong dtype, shape or device would be read past its end; the binding
+# checks every tensor against the sizes it passes down.
+# ---------------------------------------------------------------------------
+
+def _expect(name, t, dtypes, shape, device=None):
+    """t must be a contiguous CUDA tensor of one of `dtypes` whose shape
+    matches `shape` (None entries match any size) on `device`."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {list(dtypes)}")
+    if len(t.shape) != len(shape) or any(w is not None and w != g for g, w in zip(t.shape, shape)):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)} (None = any)")
+    if not t.is_cuda or (device is not None and t.device != device):
+        raise ValueError(f"{name} must be on {device if device is not None else 'a CUDA device'}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_paged(q, k_cache, v_cache, block_table, cache_seqlens, workspace, o, lse, kv_dtypes):
+    """The common tensors of the paged-decode and cascade calls."""
+    import torch
+    _expect("q", q, (torch.float16, torch.bfloat16), (None, None, None))
+    B, Hq, D = q.shape
+    dev = q.device
+    _expect("k_cache", k_cache, kv_dtypes, (None, None, None, D), dev)
+    _expect("v_cache", v_cache, (k_cache.dtype,), tuple(k_cache.shape), dev)
+    _expect("block_table", block_table, (torch.int32,), (B, None), dev)
+    _expect("cache_seqlens", cache_seqlens, (torch.int32,), (B,), dev)
+    if workspace is not None:
+        _expect("workspace", workspace, (torch.uint8,), (None,), dev)
+    if o is not None:
+        _expect("o", o, (q.dtype,), (B, Hq, D), dev)
+    if lse is not None:
+        _expect("lse", lse, (torch.float32,), (B, Hq), dev)
+
+
+def _check_prefix(q, k_prefix, v_prefix, prefix_kv_indptr):
+    """Contiguous shared prefixes [L, Hkv, D] of q's dtype, L >= the last indptr."""
+    _expect("k_prefix", k_prefix, (q.dtype,), (None, None, q.shape[2]), q.device)
+    _expect("v_prefix", v_prefix, (q.dtype,), tuple(k_prefix.shape), q.device)
+    if len(prefix_kv_indptr) and int(prefix_kv_indptr[-1]) > k_prefix.shape[0]:
+        raise ValueError("prefix_kv_indptr ends past the prefix tensors")
+
+
 def version() -> int:
     return lib().pkc_version()
 
@@ -137,7 +185,13 @@ def version() -> int:
 def merge_state(v_a, s_a, v_b, s_b, v_out=None, s_out=None, stream=None):
     """(v_a, s_a) (+) (v_b, s_b); v [T, H, D], s [T, H] float32."""
     import torch
+    _expect("v_a", v_a, (torch.float32, torch.float16, torch.bfloat16), (None, None, None))
     T, H, D = v_a.shape
+    for name, t, dt, shp in (("s_a", s_a, torch.float32, (T, H)), ("v_b", v_b, v_a.dtype, (T, H, D)),
+                             ("s_b", s_b, torch.float32, (T, H)), ("v_out", v_out, v_a.dtype, (T, H, D)),
+                             ("s_out", s_out, torch.float32, (T, H))):
+        if t is not None:
+            _expect(name, t, (dt,), shp, v_a.device)
     v_out = torch.empty_like(v_a) if v_out is None else v_out
     s_out = torch.empty_like(s_a) if s_out is None else s_out
     _check(lib().pkc_merge_state(_ptr(v_a), _ptr(s_a), _ptr(v_b), _ptr(s_b), _ptr(v_out),
@@ -148,7 +202,13 @@ def merge_state(v_a, s_a, v_b, s_b, v_out=None, s_out=None, stream=None):
 def merge_states(v, s, v_out=None, s_out=None, stream=None):
     """n-ary (+) over axis 1: v [T, n, H, D], s [T, n, H] -> [T, H, D], [T, H]."""
     import torch
+    _expect("v", v, (torch.float32, torch.float16, torch.bfloat16), (None, None, None, None))
     T, n, H, D = v.shape
+    _expect("s", s, (torch.float32,), (T, n, H), v.device)
+    if v_out is not None:
+        _expect("v_out", v_out, (v.dtype,), (T, H, D), v.device)
+    if s_out is not None:
+        _expect("s_out", s_out, (torch.float32,), (T, H), v.device)
     v_out = torch.empty((T, H, D), dtype=v.dtype, device=v.device) if v_out is None else v_out
     s_out = torch.empty((T, H), dtype=torch.float32, device=v.device) if s_out is None else s_out
     _check(lib().pkc_merge_states(_ptr(v), _ptr(s), _ptr(v_out), _ptr(s_out), T, n, H, D,
@@ -210,6 +270,7 @@ def paged_decode_state(q, k_cache, v_cache, block_table, cache_seqlens, sm_scale
                        plan_buf=None, o=None, lse=None, stream=None):
     """States of q [B, Hq, 128] over each request's paged cache."""
     import torch
+    _check_paged(q, k_cache, v_cache, block_table, cache_seqlens, workspace, o, lse, (q.dtype,))
     B, Hq, D = q.shape
     P, ps, Hkv, _ = k_cache.shape
     o = torch.empty_like(q) if o is None else o
@@ -231,6 +292,7 @@ def paged_decode_state_fp8(q, k_cache, v_cache, block_table, cache_seqlens, sm_s
     P, ps, Hkv, _ = k_cache.shape
     if q.dtype != torch.float16 or k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
         raise TypeError("paged_decode_state_fp8: q must be float16 and the caches uint8 e4m3 codes")
+    _check_paged(q, k_cache, v_cache, block_table, cache_seqlens, workspace, o, lse, (torch.uint8,))
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
     _check(lib().pkc_paged_decode_state_fp8(
@@ -246,8 +308,18 @@ def append_kv(k_new, v_new, k_cache, v_cache, block_table, cache_seqlens, worksp
     paged cache at each request's next slot and grow cache_seqlens by one, in
     place; an fp8 cache takes uint8 e4m3 codes."""
     import torch
-    B, Hkv, D = k_new.shape
-    P, ps, _, _ = k_cache.shape
+    _expect("k_cache", k_cache, (torch.float16, torch.bfloat16, torch.uint8), (None, None, None, None))
+    P, ps, Hkv, D = k_cache.shape
+    dev = k_cache.device
+    _expect("v_cache", v_cache, (k_cache.dtype,), tuple(k_cache.shape), dev)
+    _expect("k_new", k_new, (k_cache.dtype,), (None, Hkv, D), dev)
+    B = k_new.shape[0]
+    _expect("v_new", v_new, (k_cache.dtype,), (B, Hkv, D), dev)
+    _expect("block_table", block_table, (torch.int32,), (B, None), dev)
+    _expect("cache_seqlens", cache_seqlens, (torch.int32,), (B,), dev)
+    _expect("workspace", workspace, (torch.uint8,), (None,), dev)
+    if append_mask is not None:
+        _expect("append_mask", append_mask, (torch.uint8,), (B,), dev)
     if k_cache.dtype == torch.uint8:
         code = E4M3
     else:
@@ -283,6 +355,7 @@ def paged_decode_state_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, 
     cannot allocate device memory: the library's own fixed 8 MiB device
     array holds the scratch.  Calls that overlap on the GPU race on it."""
     import torch
+    _check_paged(q, k_cache, v_cache, block_table, cache_seqlens, None, o, lse, (q.dtype,))
     B, Hq, D = q.shape
     P, ps, Hkv, _ = k_cache.shape
     o = torch.empty_like(q) if o is None else o
@@ -298,6 +371,13 @@ def prefix_attention_state(q, k_prefix, v_prefix, prefix_kv_indptr, prefix_req_i
                            workspace, o=None, lse=None, stream=None):
     """States of q [B, Hq, 128] over each request's shared prefix (fp32 O)."""
     import torch
+    _expect("q", q, (torch.float16, torch.bfloat16), (None, None, None))
+    _check_prefix(q, k_prefix, v_prefix, _host_i32(prefix_kv_indptr))
+    _expect("workspace", workspace, (torch.uint8,), (None,), q.device)
+    if o is not None:
+        _expect("o", o, (torch.float32,), tuple(q.shape), q.device)
+    if lse is not None:
+        _expect("lse", lse, (torch.float32,), tuple(q.shape[:2]), q.device)
     B, Hq, D = q.shape
     Hkv = k_prefix.shape[1]
     kv_ptr, req_ptr = _host_i32(prefix_kv_indptr), _host_i32(prefix_req_indptr)
@@ -315,6 +395,8 @@ def cascade_decode(q, k_prefix, v_prefix, prefix_kv_indptr, prefix_req_indptr, k
                    lse=None, stream=None):
     """Final O [B, Hq, 128] and LSE [B, Hq] over shared prefix + paged suffix."""
     import torch
+    _check_paged(q, k_cache, v_cache, block_table, cache_seqlens, workspace, o, lse, (q.dtype,))
+    _check_prefix(q, k_prefix, v_prefix, _host_i32(prefix_kv_indptr))
     B, Hq, D = q.shape
     P, ps, Hkv, _ = k_cache.shape
     kv_ptr, req_ptr = _host_i32(prefix_kv_indptr), _host_i32(prefix_req_indptr)
@@ -334,6 +416,8 @@ def cascade_decode_multilevel(q, k_prefix, v_prefix, prefix_kv_indptr, prefix_re
     """The cascade with prefix groups as request ranges [(begin, end)] that may
     overlap: each request attends to every group's prefix that holds it."""
     import torch
+    _check_paged(q, k_cache, v_cache, block_table, cache_seqlens, workspace, o, lse, (q.dtype,))
+    _check_prefix(q, k_prefix, v_prefix, _host_i32(prefix_kv_indptr))
     B, Hq, D = q.shape
     P, ps, Hkv, _ = k_cache.shape
     kv_ptr = _host_i32(prefix_kv_indptr)
@@ -356,6 +440,10 @@ def cascade_decode_paged_prefix(q, prefix_pages, prefix_page_indptr, prefix_kv_i
     page pool: prefix_pages (device int32) lists group j's pages at
     prefix_page_indptr[j] .. prefix_page_indptr[j+1]-1."""
     import torch
+    _check_paged(q, k_cache, v_cache, block_table, cache_seqlens, workspace, o, lse, (q.dtype,))
+    _expect("prefix_pages", prefix_pages, (torch.int32,), (None,), q.device)
+    if len(prefix_page_indptr) and int(_host_i32(prefix_page_indptr)[-1]) > prefix_pages.shape[0]:
+        raise ValueError("prefix_page_indptr ends past prefix_pages")
     B, Hq, D = q.shape
     P, ps, Hkv, _ = k_cache.shape
     kv_ptr, pg_ptr = _host_i32(prefix_kv_indptr), _host_i32(prefix_page_indptr)

@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
 // One warp per (row, head): (+) over every state that belongs to the row,
 // lane i owning dims 4i..4i+3.
-__global__ void __launch_bounds__(256, 3) contract_kernel(const ContractParams p) {
+__global__ void __launch_bounds__(256, 4) contract_kernel(const ContractParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t row_idx = gw / p.hq;
@@ -534,9 +534,11 @@ __global__ void __launch_bounds__(256, 3) contract_kernel(const ContractParams p
     req = pl[p.off_unit_req + unit];
   }
   // Running state of the merge: maximum m, denominator den, unnormalised
-  // acc.  Sources go in batches of 8 whose loads are all in flight
-  // together; the running state is rescaled between batches.
-  constexpr int kB = 8;
+  // acc.  Sources go in batches of 4 whose loads are all in flight
+  // together; the running state is rescaled between batches.  (Batches of 4
+  // keep the kernel at 56 registers, 4 blocks per SM: more rows in flight
+  // than batches of 8 at 3 blocks per SM.)
+  constexpr int kB = 4;
   float m = neg_inf(), den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int64_t row_off = (int64_t)req * p.hq + h;

@@ -187,3 +187,20 @@ def test_plan_rejects_bad_input(L):
         pkc.plan([3, -1], 4)
     with pytest.raises(pkc.PkcError):
         pkc.plan([3, 1], 0)
+
+
+def test_binding_refuses_host_tensors_before_any_call():
+    """The binding passes raw pointers down: host tensors (or tensors of the
+    wrong shape or dtype) are refused in Python, before the library is called."""
+    import torch
+    q = torch.zeros(2, 8, 128, dtype=torch.float16)
+    kc = torch.zeros(4, 16, 2, 128, dtype=torch.float16)
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    sl = torch.zeros(2, dtype=torch.int32)
+    ws = torch.zeros(1024, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA"):
+        pkc.paged_decode_state(q, kc, kc, bt, sl, 0.1, ws)
+    with pytest.raises(TypeError, match="dtype"):
+        pkc.merge_state(torch.zeros(2, 2, 128, dtype=torch.int32), None, None, None)
+    with pytest.raises(ValueError, match="shape"):
+        pkc.merge_states(torch.zeros(2, 128), None)

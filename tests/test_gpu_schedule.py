@@ -146,3 +146,24 @@ def test_cascade_side_stream_and_timed_sequential_run_agree():
     assert pkc.device_status(ws) == pkc.PKC_OK
     ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
     compare(o, lse, ref_o, ref_lse)
+
+
+def test_binding_refuses_mismatched_cache_dtype_and_shapes():
+    """A 1-byte e4m3 cache handed to the 16-bit decode would be read as twice
+    its size: the binding refuses it, and mismatched shapes, in Python."""
+    q = torch.zeros(2, 8, 128, dtype=torch.float16, device="cuda")
+    kc8 = torch.zeros(4, 16, 2, 128, dtype=torch.uint8, device="cuda")
+    kc = torch.zeros(4, 16, 2, 128, dtype=torch.float16, device="cuda")
+    bt = torch.zeros(2, 4, dtype=torch.int32, device="cuda")
+    sl = torch.zeros(2, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(TypeError):
+        pkc.paged_decode_state(q, kc8, kc8, bt, sl, 0.1, ws)
+    with pytest.raises(TypeError):
+        pkc.paged_decode_state_fp8(q, kc, kc, bt, sl, 0.1, ws)
+    with pytest.raises(ValueError):
+        pkc.paged_decode_state(q, kc, kc[:2], bt, sl, 0.1, ws)
+    with pytest.raises(ValueError):
+        pkc.paged_decode_state(q, kc, kc, bt[:1], sl, 0.1, ws)
+    with pytest.raises(TypeError):
+        pkc.paged_decode_state(q, kc, kc, bt.long(), sl, 0.1, ws)

@@ -466,6 +466,19 @@ int pkc_cascade_decode_paged_prefix(
 int pkc_set_stage_events(void* const* events, int n_events);
 
 /*
+ * Diagnostics: the failure path of the kernels' bounded waits, without a
+ * fault.  Launches one block on `stream` whose thread waits on an mbarrier
+ * that nothing arrives at, through the bounded wait all kernels use.  After
+ * the limit (2 s of %globaltimer) the wait records PKC_ERR_TIMEOUT in the
+ * workspace status word and returns; the kernel then ends normally and the
+ * context stays usable.  *gave_up_host receives 1 if the wait gave up as
+ * designed (0 otherwise); the call synchronises `stream`.  The workspace
+ * needs PKC status bytes only (pkc_workspace_size(0, 1, ...)).
+ */
+int pkc_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int32_t* gave_up_host,
+                              void* stream);
+
+/*
  * Kernel used by the paged decode over a 16-bit cache (process-wide):
  *   0 = automatic (default): tensor-core kernel for grouped heads
  *       (num_qo_heads / num_kv_heads >= 2), CUDA-core kernel otherwise

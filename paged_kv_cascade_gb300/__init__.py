@@ -58,6 +58,7 @@ SIGNATURES = {
     "pkc_set_stage_events": (_I, [_c.POINTER(_P), _I]),
     "pkc_set_decode_kernel": (_I, [_I]),
     "pkc_set_decode_schedule": (_I, [_I]),
+    "pkc_selftest_wait_timeout": (_I, [_P, _SZ, _c.POINTER(_c.c_int32), _P]),
     "pkc_append_kv": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I64, _I, _P, _SZ, _P]),
     "pkc_cascade_decode_multilevel": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I,
                                            _I, _I, _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
@@ -457,6 +458,18 @@ def cascade_decode_paged_prefix(q, prefix_pages, prefix_page_indptr, prefix_kv_i
         B, Hq, Hkv, D, ps, P, float(sm_scale), _hptr(plan_buf), _ptr(workspace),
         workspace.numel(), _ptr(o), _ptr(lse), _dtype_code(q), _stream(stream)))
     return o, lse
+
+
+def selftest_wait_timeout(workspace, stream=None) -> bool:
+    """Run the bounded-wait failure path on the GPU (about 2 s): True if the
+    wait gave up and returned as designed; the status word then holds
+    PKC_ERR_TIMEOUT (read it with device_status)."""
+    import torch
+    _expect("workspace", workspace, (torch.uint8,), (None,))
+    out = ctypes.c_int32(0)
+    _check(lib().pkc_selftest_wait_timeout(_ptr(workspace), workspace.numel(), ctypes.byref(out),
+                                           _stream(stream)))
+    return out.value == 1
 
 
 def set_stage_events(events):

@@ -493,6 +493,21 @@ int pkc_set_decode_schedule(int dynamic) {
   return PKC_OK;
 }
 
+int pkc_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int32_t* gave_up_host, void* stream) {
+  if (!gave_up_host) return set_error(PKC_ERR_INVALID_ARG, "selftest_wait_timeout: NULL result pointer");
+  if (int rc = check_ws(workspace, workspace_bytes, PKC_STATUS_BYTES)) return rc;
+  int32_t* status = static_cast<int32_t*>(workspace);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(status + 32, 0, sizeof(int32_t), st);
+  if (!e) e = (cudaError_t)launch_wait_timeout(status, stream);
+  int32_t v = 0;
+  if (!e) e = cudaMemcpyAsync(&v, status + 32, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (!e) e = cudaStreamSynchronize(st);
+  if (e) return cuda_error(e, "selftest_wait_timeout");
+  *gave_up_host = v;
+  return PKC_OK;
+}
+
 int pkc_prefix_attention_state(const void* q, const void* k_prefix, const void* v_prefix,
                                const int32_t* prefix_kv_indptr_host, const int32_t* prefix_req_indptr_host,
                                int n_prefix, int batch, int num_qo_heads, int num_kv_heads, int head_dim,

@@ -236,25 +236,26 @@ def gpu_smi_id(torch, local):
         return vis.split(",")[local] if vis else local
 
 
-def cpu_oracle_sample(p, target_s, rows_total_cap=None):
-    """Time the oracle on a bounded sample of (request, head) rows."""
+def cpu_oracle_sample(p, target_s, rows_total_cap=None, n_threads=0):
+    """Time the oracle on a bounded sample of (request, head) rows (all host
+    cores, or n_threads)."""
     import oracle
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from pkc_testing import oracle_args
     B, Hq, _ = p["q"].shape
     args = oracle_args(p)
-    threads = oracle.max_threads()
+    threads = n_threads or oracle.max_threads()
     rng = np.random.default_rng(123)
     order = rng.permutation(B * Hq)
     n = min(32, B * Hq)
     rows = np.stack([order[:n] // Hq, order[:n] % Hq], 1).astype(np.int32)
     t0 = time.perf_counter()
-    oracle.attention_rows(p["q"], rows=rows, **args)
+    oracle.attention_rows(p["q"], rows=rows, n_threads=n_threads, **args)
     t_cal = time.perf_counter() - t0
     n2 = int(min(B * Hq, max(n, n * target_s / max(t_cal, 1e-6))))
     rows = np.stack([order[:n2] // Hq, order[:n2] % Hq], 1).astype(np.int32)
     t0 = time.perf_counter()
-    oracle.attention_rows(p["q"], rows=rows, **args)
+    oracle.attention_rows(p["q"], rows=rows, n_threads=n_threads, **args)
     t = time.perf_counter() - t0
     return n2, B * Hq, t, threads
 
@@ -742,11 +743,31 @@ def main():
             gstream.synchronize()
             if dist is not None:
                 dist.barrier()
+            # Single replays with and without an L2 flush (a 256 MB write)
+            # before each, timed alone: the median step with a cold L2 and
+            # with whatever the previous step left in it.
+            flush = torch.empty((256 << 20) // 4, dtype=torch.int32, device=d["q"].device)
+            n_iso = min(K, 50)
+            iso = {}
+            for flushed in (True, False):
+                evs = []
+                for i in range(n_iso):
+                    if flushed:
+                        flush.fill_(i)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(gstream)
+                    graphs[i & 1].replay()
+                    e1.record(gstream)
+                    evs.append((e0, e1))
+                gstream.synchronize()
+                iso[flushed] = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
         g_ms = reduce_max(ga.elapsed_time(gb), dist, d["q"].device)
         graph = {"value": whole_job_gbs(eff, K, world, g_ms / 1e3), "unit": "GB/s",
                  "us_per_step": 1e3 * g_ms / K,
                  "note": "host plan + upload each step (on a copy stream, two workspaces "
-                         "alternating), device work replayed from a CUDA graph"}
+                         "alternating), device work replayed from a CUDA graph",
+                 "isolated_replay_us_median": {"l2_flushed": iso[True], "unflushed": iso[False],
+                                               "flush_bytes": 256 << 20, "replays": n_iso}}
         if pkc.device_status(gws[0]) != 0 or pkc.device_status(gws[1]) != 0:
             raise RuntimeError("device status after graph replay")
     except RuntimeError:
@@ -772,9 +793,12 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n_rows, total, t, threads = cpu_oracle_sample(p, args.cpu_seconds)
         full_s = t / (n_rows / total)
+        n1, _, t1, _ = cpu_oracle_sample(p, args.cpu_seconds / 2, n_threads=1)
         cpu = {"value": eff / full_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{n_rows} of {total} (request, head) rows of one step in {t:.1f} s, "
-                         "extrapolated to the full step"}
+                         "extrapolated to the full step",
+               "single_thread": {"value": eff / (t1 / (n1 / total)) / 1e9, "unit": "GB/s", "cores": 1,
+                                 "sample": f"{n1} of {total} rows in {t1:.1f} s"}}
 
     if rank == 0:
         line = {

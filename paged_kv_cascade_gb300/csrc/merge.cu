@@ -59,6 +59,16 @@ __global__ void __launch_bounds__(256) merge2_kernel(const T* __restrict__ va, c
   for (int64_t r0 = warp * rpw; r0 < rows; r0 += nwarps * rpw) {
     const int64_t row = r0 + sub_row;
     const bool active = row < rows;
+    // With at most one 16-byte chunk per lane (head_dim 128 in any dtype),
+    // the chunk's loads go out together with the LSE loads instead of after
+    // the weights: one memory round trip per row step, not two.
+    float x1[V::N], y1[V::N];
+    const bool one = cpr <= 32 && active;
+    const int64_t off1 = (row * cpr + chunk0) * V::N;
+    if (one) {
+      V::load(va + off1, x1);
+      V::load(vb + off1, y1);
+    }
     float a = active ? sa[row] : 0.f, b = active ? sb[row] : 0.f;
     const float m = fmaxf(a, b);
     float wa = 0.f, wb = 0.f, s = neg_inf();
@@ -71,7 +81,11 @@ __global__ void __launch_bounds__(256) merge2_kernel(const T* __restrict__ va, c
       wa *= inv;
       wb *= inv;
     }
-    if (active) {
+    if (one) {
+#pragma unroll
+      for (int i = 0; i < V::N; ++i) x1[i] = x1[i] * wa + y1[i] * wb;
+      V::store(vo + off1, x1);
+    } else if (active) {
       for (int c = chunk0; c < cpr; c += cstep) {
         const int64_t off = (row * cpr + c) * V::N;
         float x[V::N], y[V::N];

@@ -37,12 +37,10 @@ WORKLOADS = {
     "paged_decode": dict(batch=64, hq=32, hkv=32, d=128, dtype="f16",
                          prefix_lens=[], prefix_groups=[],
                          suffix=("uniform", 512, 4096), page_size=16, seed=3),
-    # cascade at the long-prompt shape: prefix 32768, suffix 256, batch 128.
-    # Equal suffixes need no plan (plan=False): one decode block per
-    # (request, KV-head group) keeps every request's suffix in one piece.
+    # cascade at the long-prompt shape: prefix 32768, suffix 256, batch 128
     "cascade_long_prompt": dict(batch=128, hq=32, hkv=32, d=128, dtype="f16",
                                 prefix_lens=[32768], prefix_groups=[128],
-                                suffix=("const", 256), page_size=16, seed=4, plan=False),
+                                suffix=("const", 256), page_size=16, seed=4),
     # FP8 KV paged decode at the GQA suffix shape: 32/8 heads, fp16 q and O,
     # e4m3 cache with per-tensor scales, batch 256, lognormal lengths
     "paged_decode_fp8": dict(batch=256, hq=32, hkv=8, d=128, dtype="f16",

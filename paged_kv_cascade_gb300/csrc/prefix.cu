@@ -24,17 +24,19 @@
 // maximum exceeds it by more than 2^8 (P stays <= 256); then the row's O
 // columns are rescaled in TMEM before the next P.V.  With a stable maximum
 // nothing touches O until the end of the piece.
-// Roles: warp 0 issues TMA loads (each piece's Q tile, K/V into a 3-stage
-// ring), warp 1 allocates TMEM and issues MMAs, warps 2..9 own 16 query rows
-// each.  They read S with the 16x256b TMEM shape, four threads per row and
+// Roles: warp 0 issues TMA loads of each piece's Q tile and of K into a
+// 2-slot ring, warp 10 of V into a 2-slot ring, warp 1 allocates TMEM and
+// issues MMAs, warps 2..9 own 16 query rows each.  A K slot frees as soon as
+// QK has read it, so the K loads run ahead of the softmax; P has two buffers
+// of its own (by tile parity), so the softmax of tile j never waits for the
+// P.V of tile j - 1.  They read S with the 16x256b TMEM shape, four threads per row and
 // two rows per thread, so row maxima and sums are two shuffles and no
 // softmax warp waits for another; P goes back to shared memory with
 // stmatrix.  The exponent argument S c - m and the row sums use packed
 // two-wide fp32 FMAs.  TMEM: S double buffer (2 x 128 columns) + O
 // double buffer (2 x 128): a piece's O is read out while the next piece
-// accumulates into the other.  P_j overwrites K_j's shared memory once S_j
-// is complete.  All waits are bounded (2 s) and set PKC_ERR_TIMEOUT when
-// they run out.
+// accumulates into the other.  All waits are bounded (2 s) and set
+// PKC_ERR_TIMEOUT when they run out.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,16 +51,20 @@ namespace {
 
 constexpr int kRows = 128;       // query rows per tile (MMA M)
 constexpr int kKvTile = 128;     // tokens per KV tile (MMA N of S, K of PV)
-constexpr int kStages = 3;
+constexpr int kStagesK = 2;      // K ring: a slot frees once QK has read it
+constexpr int kStagesV = 2;      // V ring: a slot frees once P.V has read it
 constexpr int kSubTile = 16384;  // 128 rows x 128 bytes (64 elements)
 constexpr int kQBytes = 2 * kSubTile;
-constexpr int kStageBytes = 4 * kSubTile;  // K (2 sub-tiles) + V (2 sub-tiles)
-constexpr int kThreads = 320;  // TMA warp, MMA warp, 8 softmax warps
+constexpr int kTileBytes = 2 * kSubTile;  // one K or V tile (two 64-dim halves)
+constexpr int kThreads = 352;  // K/Q TMA warp, MMA warp, 8 softmax warps, V TMA warp
+constexpr int kVWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 
 struct __align__(8) Barriers {
   uint64_t q_full, q_empty;  // a piece's Q tile landed / no longer read
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kStagesK], k_empty[kStagesK];
+  uint64_t v_full[kStagesV], v_empty[kStagesV];
+  uint64_t p_free[2];        // P buffer b has been read by its last P.V
   uint64_t s_full[2], s_free[2], p_full[2], o_full;
   uint64_t o_done;           // a piece's O is final
   uint64_t o_free[2];        // O buffer b has been read out
@@ -96,11 +102,15 @@ __device__ __forceinline__ Piece piece_at(const PrefixParams& p, int x, int s1) 
   return g;
 }
 
-// Q, the K/V ring and the barriers (256 B).  The base must be 1024-byte
-// aligned for the 128B-swizzled TMA tiles; with no static shared memory it
-// is, and the kernel checks it.
-constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
+// Q, P, the K ring, the V ring and the barriers (256 B).  The base must be
+// 1024-byte aligned for the 128B-swizzled TMA tiles; with no static shared
+// memory it is, and the kernel checks it.
+constexpr int kPOffset = kQBytes;                  // two P buffers, by tile parity
+constexpr int kKOffset = kPOffset + 2 * kTileBytes;
+constexpr int kVOffset = kKOffset + kStagesK * kTileBytes;
+constexpr int kBarOffset = kVOffset + kStagesV * kTileBytes;
 constexpr int kSmemBytes = kBarOffset + 256;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -112,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const uint32_t s_q = smem_u32(smem);
-  const uint32_t s_stage0 = s_q + kQBytes;
+  const uint32_t s_p = s_q + kPOffset, s_k0 = s_q + kKOffset, s_v0 = s_q + kVOffset;
   Barriers* bars = reinterpret_cast<Barriers*>(smem + kBarOffset);
   static_assert(sizeof(Barriers) <= 256, "barrier block");
   volatile int* abort = &bars->abort;
@@ -128,10 +138,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(bars->q_full), 1);
     mbar_init(bar(bars->q_empty), 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(bars->kv_full[s]), 1);
-      mbar_init(bar(bars->kv_empty[s]), 1);
+    for (int s = 0; s < kStagesK; ++s) {
+      mbar_init(bar(bars->k_full[s]), 1);
+      mbar_init(bar(bars->k_empty[s]), 1);
     }
+    for (int s = 0; s < kStagesV; ++s) {
+      mbar_init(bar(bars->v_full[s]), 1);
+      mbar_init(bar(bars->v_empty[s]), 1);
+    }
+    mbar_init(bar(bars->p_free[0]), 1);
+    mbar_init(bar(bars->p_free[1]), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(bars->s_full[b]), 1);
       mbar_init(bar(bars->s_free[b]), 256);
@@ -159,14 +175,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    // The whole warp runs the loop; lane 0 waits on the barriers and the
-    // warp learns the result.  A contiguous tile is four boxes from lane 0; a
-    // paged tile is four boxes per page, issued by the lanes in parallel.
+  if (warp == 0 || warp == kVWarp) {
+    // ---------------- TMA producers ----------------
+    // Warp 0 loads each piece's Q tile and the K tiles into the K ring; warp
+    // 10 loads the V tiles into the V ring.  A K slot frees as soon as QK has
+    // read it and a V slot once P.V has, so the loads of later tiles never
+    // wait for this tile's softmax.  The whole warp runs the loop; lane 0
+    // waits on the barriers and the warp learns the result.  A contiguous
+    // tile is two boxes from lane 0; a paged tile is two boxes per page,
+    // issued by the lanes in parallel.
+    const bool is_v = warp == kVWarp;
+    const int n_st = is_v ? kStagesV : kStagesK;
+    const uint32_t ring0 = is_v ? s_v0 : s_k0;
+    uint64_t* full = is_v ? bars->v_full : bars->k_full;
+    uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
+    const void* tmap = is_v ? (const void*)&tm_v : (const void*)&tm_k;
     const uint64_t pol = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
-    int g = 0, q_issued = 0;  // KV tiles and Q tiles issued
+    int g = 0, q_issued = 0;  // tiles and Q tiles issued
     bool ok = true;
     auto wait0 = [&](uint64_t& b, uint32_t parity) -> bool {
       bool got = true;
@@ -176,48 +202,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = s0; ok && x < s1;) {
       const Piece pc = piece_at(p, x, s1);
       x = pc.next;
-      auto load_kv = [&](int u) -> bool {
-        const int s = g % kStages;
-        if (!wait0(bars->kv_empty[s], ((g / kStages) & 1) ^ 1)) return false;
-        const uint32_t st = s_stage0 + s * kStageBytes;
-        const uint32_t fb = bar(bars->kv_full[s]);
+      auto load_tile = [&](int u) -> bool {
+        const int s = g % n_st;
+        if (!wait0(empty[s], ((g / n_st) & 1) ^ 1)) return false;
+        const uint32_t st = ring0 + s * kTileBytes;
+        const uint32_t fb = bar(full[s]);
         const int t0 = pc.kv_lo + u * kKvTile;
-        if (lane == 0) mbar_arrive_expect_tx(fb, kStageBytes);
+        if (lane == 0) mbar_arrive_expect_tx(fb, kTileBytes);
         __syncwarp();
         if (!p.prefix_pages) {
           if (lane == 0) {
-            tma_load_3d(st, &tm_k, fb, 0, pc.kvh, t0, pol);
-            tma_load_3d(st + kSubTile, &tm_k, fb, 64, pc.kvh, t0, pol);
-            tma_load_3d(st + 2 * kSubTile, &tm_v, fb, 0, pc.kvh, t0, pol);
-            tma_load_3d(st + 3 * kSubTile, &tm_v, fb, 64, pc.kvh, t0, pol);
+            tma_load_3d(st, tmap, fb, 0, pc.kvh, t0, pol);
+            tma_load_3d(st + kSubTile, tmap, fb, 64, pc.kvh, t0, pol);
           }
         } else {
-          // Box c: page c / 4 of the tile, {K, V} x {dims 0-63, 64-127} by
-          // c % 4, {64 dims, 1 head, page_size slots}.  Pages past the group's
-          // list load from page num_pages, outside the pool: zero fill.
+          // Box c: page c / 2 of the tile, dims 0-63 or 64-127 by c % 2,
+          // {64 dims, 1 head, page_size slots}.  Pages past the group's list
+          // load from page num_pages, outside the pool: zero fill.
           const int ps = p.page_size;
           const int rel = t0 - p.kv_indptr[pc.grp];  // token offset within the group
           const int pg0 = p.page_indptr[pc.grp], n_pg = p.page_indptr[pc.grp + 1] - pg0;
-          for (int c = lane; c < 4 * (kKvTile / ps); c += 32) {
-            const int r = (c >> 2) * ps, kind = c & 3;
+          for (int c = lane; c < 2 * (kKvTile / ps); c += 32) {
+            const int r = (c >> 1) * ps, half = c & 1;
             const int pi = (rel + r) / ps;
             int32_t page = pi < n_pg ? p.prefix_pages[pg0 + pi] : (int32_t)p.num_pages;
             if (pi < n_pg && (page < 0 || page >= p.num_pages)) {
               report(p.status, PKC_ERR_BLOCK_TABLE);
               page = (int32_t)p.num_pages;  // read as zeros
             }
-            const uint32_t dst = st + (kind >> 1) * 2 * kSubTile + (kind & 1) * kSubTile + (uint32_t)r * 128;
-            tma_load_4d(dst, kind < 2 ? (const void*)&tm_k : (const void*)&tm_v, fb, (kind & 1) * 64, pc.kvh, 0,
-                        page, pol);
+            tma_load_4d(st + half * kSubTile + (uint32_t)r * 128, tmap, fb, half * 64, pc.kvh, 0, page, pol);
           }
         }
         ++g;
         return true;
       };
-      // After the first piece, the ring fills with this piece's KV tiles
-      // while the previous piece's products still read the Q buffer.
-      const int pre = q_issued > 0 ? min(pc.n, kStages) : 0;
-      for (int u = 0; ok && u < pre; ++u) ok = load_kv(u);
+      if (is_v) {
+        for (int u = 0; ok && u < pc.n; ++u) ok = load_tile(u);
+        continue;
+      }
+      // After the first piece, the K ring fills with this piece's tiles while
+      // the previous piece's products still read the Q buffer.
+      const int pre = q_issued > 0 ? min(pc.n, n_st) : 0;
+      for (int u = 0; ok && u < pre; ++u) ok = load_tile(u);
       if (!ok) break;
       if (q_issued > 0 && !wait0(bars->q_empty, (q_issued - 1) & 1)) break;
       const int b0 = p.req_begin[pc.grp] + pc.mt * (kRows / G);
@@ -227,14 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(s_q + kSubTile, &tm_q, bar(bars->q_full), 64, pc.kvh * G, b0, pol_q);
       }
       ++q_issued;
-      for (int u = pre; ok && u < pc.n; ++u) ok = load_kv(u);
+      for (int u = pre; ok && u < pc.n; ++u) ok = load_tile(u);
     }
     if (*abort && lane == 0) {
       // Let the copies already issued land before the block exits.
       volatile int no_abort = 0;
       if (q_issued > 0) mbar_wait(bar(bars->q_full), (q_issued - 1) & 1, &no_abort, p.status);
-      for (int j = g > kStages ? g - kStages : 0; j < g; ++j)
-        mbar_wait(bar(bars->kv_full[j % kStages]), (j / kStages) & 1, &no_abort, p.status);
+      for (int jt = g > n_st ? g - n_st : 0; jt < g; ++jt)
+        mbar_wait(bar(full[jt % n_st]), (jt / n_st) & 1, &no_abort, p.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -252,12 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int u = 0; ok && u <= pc.n; ++u) {
           if (u < pc.n) {
-            const int j = g + u, s = j % kStages, b = j & 1;
-            ok = mbar_wait(bar(bars->kv_full[s]), (j / kStages) & 1, abort, p.status) &&
+            const int j = g + u, s = j % kStagesK, b = j & 1;
+            ok = mbar_wait(bar(bars->k_full[s]), (j / kStagesK) & 1, abort, p.status) &&
                  mbar_wait(bar(bars->s_free[b]), ((j >> 1) & 1) ^ 1, abort, p.status);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t kb = s_stage0 + s * kStageBytes;
+            const uint32_t kb = s_k0 + s * kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t off = (kk >> 2) * kSubTile + (kk & 3) * 32;
@@ -265,11 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                          smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
             }
             tc_commit(bar(bars->s_full[b]));
+            tc_commit(bar(bars->k_empty[s]));                  // K_j read: its slot may refill
             if (u == pc.n - 1) tc_commit(bar(bars->q_empty));  // the piece's last read of Q
           }
           if (u >= 1) {
-            const int jp = g + u - 1, sp = jp % kStages, bp = jp & 1;
-            ok = mbar_wait(bar(bars->p_full[bp]), (jp >> 1) & 1, abort, p.status);
+            const int jp = g + u - 1, sv = jp % kStagesV, bp = jp & 1;
+            ok = mbar_wait(bar(bars->p_full[bp]), (jp >> 1) & 1, abort, p.status) &&
+                 mbar_wait(bar(bars->v_full[sv]), (jp / kStagesV) & 1, abort, p.status);
             // The first P.V of a piece overwrites O: the previous piece's O
             // must have been read out.
             // (O is double-buffered: piece k uses buffer k & 1, last read
@@ -277,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && u == 1 && k > 1) ok = mbar_wait(bar(bars->o_free[k & 1]), ((k >> 1) - 1) & 1, abort, p.status);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t pb = s_stage0 + sp * kStageBytes;  // P overwrote K
-            const uint32_t vb = pb + 2 * kSubTile;
+            const uint32_t pb = s_p + bp * kTileBytes;
+            const uint32_t vb = s_v0 + sv * kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {  // O accumulates over the piece's tiles
               const uint32_t a_off = (kk >> 2) * kSubTile + (kk & 3) * 32;
@@ -286,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          smem_desc_sw128(vb + kk * 2048, kSubTile, 1024), idesc_pv, (u > 1 || kk > 0) ? 1u : 0u);
             }
             tc_commit(bar(bars->o_full));
-            tc_commit(bar(bars->kv_empty[sp]));
+            tc_commit(bar(bars->v_empty[sv]));
+            tc_commit(bar(bars->p_free[bp]));
           }
         }
         if (!ok) break;
@@ -327,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t lt2 = 0ull, lb2 = 0ull;                 // packed row sums
       const uint32_t o_base = lane_base + 256 + (k & 1) * 128;  // this piece's O buffer
       for (int u = 0; u < n_kv; ++u) {
-        const int j = g + u, b = j & 1, s = j % kStages;
+        const int j = g + u, b = j & 1;
         const bool got = ok && mbar_wait(bar(bars->s_full[b]), (j >> 1) & 1, abort, p.status);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc_fence_after();
@@ -401,10 +430,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mt_ref = nt;
           mb_ref = nb;
         }
-        // P_j = exp2(S_j c - m_ref) as 16-bit pairs, stored over K_j with
-        // stmatrix: matrices (top, octet jj), (bottom, jj), (top, jj+1),
-        // (bottom, jj+1); lane l addresses row l % 8 of matrix l / 8.
-        const uint32_t pst = s_stage0 + s * kStageBytes;
+        // P_j = exp2(S_j c - m_ref) as 16-bit pairs, stored into the P buffer
+        // (once P.V of tile j-1 has read it) with stmatrix: matrices (top,
+        // octet jj), (bottom, jj), (top, jj+1), (bottom, jj+1); lane l
+        // addresses row l % 8 of matrix l / 8.
+        {
+          // buffer b was last read by P.V of tile j - 2
+          const bool free_now = mbar_wait(bar(bars->p_free[b]), ((j >> 1) & 1) ^ 1, abort, p.status);
+          if (!__all_sync(0xffffffffu, free_now)) { ok = false; break; }
+        }
+        const uint32_t pst = s_p + b * kTileBytes;
         const uint64_t nt2 = pk2(-mt_ref, -mt_ref), nb2 = pk2(-mb_ref, -mb_ref);
         const int mrow = rbase + (lane & 7) + 8 * ((lane >> 3) & 1);  // row this lane addresses
         const uint32_t mrow_addr = pst + mrow * 128;
@@ -445,8 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           p_half(std::false_type{}, sr[1], 1);
           if (p.prefix_pages) {
             // A paged prefix's last page may hold anything (even NaN) past the
-            // prefix: zero those V rows so that P = 0 meets V = 0 in P.V.
-            const uint32_t vst = s_stage0 + s * kStageBytes + 2 * kSubTile;
+            // prefix: zero those V rows (once the tile has landed) so that
+            // P = 0 meets V = 0 in P.V.
+            const int sv = j % kStagesV;
+            const bool landed = mbar_wait(bar(bars->v_full[sv]), (j / kStagesV) & 1, abort, p.status);
+            if (!__all_sync(0xffffffffu, landed)) { ok = false; break; }
+            const uint32_t vst = s_v0 + sv * kTileBytes;
             const int n_chunks = (kKvTile - vrow) * 16;  // 16-byte chunks in both 64-dim halves
             for (int c = (int)threadIdx.x - 64; c < n_chunks; c += 256) {
               const int r = vrow + (c >> 4), half = (c >> 3) & 1, ch16 = c & 7;

@@ -229,24 +229,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             tma_load_4d(kst + i * slice_bytes, &tm_k, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
             tma_load_4d(kst + kStageHalf + i * slice_bytes, &tm_v, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
           }
+          // valid rows: the HG heads of each slot inside the page and inside [kb, ke)
           const int tok0 = page_idx * ps + slot0;
-          // lanes mark the valid rows of this slice
-          for (int r = lane; r < sl * HG; r += 32) {
-            const int t = r / HG;
-            const int tok = tok0 + t;
-            if (slot0 + t < ps && tok >= kb && tok < ke) {
-              const int row = i * sl * HG + r;
-              maskw[row >> 5] |= 1u << (row & 31);
-            }
-          }
-        }
-        // combine the lanes' mask words
-#pragma unroll
-        for (int q = 0; q < kStageRows / 32; ++q) {
-          uint32_t v = maskw[q];
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
-          maskw[q] = v;
+          mask_range(maskw, (i * sl + max(kb - tok0, 0)) * HG, (i * sl + min(min(ke - tok0, sl), ps - slot0)) * HG);
         }
         sl0 += slices_per_stage;
         const bool last_stage = sl0 > last;

@@ -15,6 +15,20 @@ struct DecodeItem {
   int req, kb, ke, slot;  // request, KV range [kb, ke), partial slot or -1
 };
 
+// OR the bits [lo, hi) into a W-word mask.  A stage's valid rows are one
+// contiguous range per page slice, so the producer builds the mask with a
+// few integer operations in registers.  (Marking rows lane by lane into a
+// runtime-indexed array put the array in local memory and took an OR over
+// the warp: about 1500 cycles per stage, enough to hold the ring back.)
+template <int W>
+__device__ __forceinline__ void mask_range(uint32_t (&m)[W], int lo, int hi) {
+#pragma unroll
+  for (int q = 0; q < W; ++q) {
+    const int a = max(lo - 32 * q, 0), b = min(hi - 32 * q, 32);
+    if (b > a) m[q] |= (b - a == 32 ? 0xffffffffu : ((1u << (b - a)) - 1u)) << a;
+  }
+}
+
 // Checks of a planned item against the cache: a plan whose request length
 // (plan_len) no longer matches cache_seqlens is reported (PKC_ERR_PLAN) and
 // the range is clamped to the cache; a range past the block table is

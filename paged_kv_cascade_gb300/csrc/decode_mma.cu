@@ -232,21 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_4d(vd + half_bytes, &tm_v, bar, 64, slot0, hg * HG, pid, pol);
             }
           }
+          // valid slots: those inside the page and inside [kb, ke)
           const int tok0 = page_idx * ps + slot0;
-          for (int t = lane; t < sl; t += 32) {
-            const int tok = tok0 + t;
-            if (slot0 + t < ps && tok >= kb && tok < ke) {
-              const int st = i * sl + t;
-              maskw[st >> 5] |= 1u << (st & 31);
-            }
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < kRows / 32; ++q) {
-          uint32_t v = maskw[q];
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
-          maskw[q] = v;
+          mask_range(maskw, i * sl + max(kb - tok0, 0), i * sl + min(min(ke - tok0, sl), ps - slot0));
         }
         sl0 += slices_per_stage;
         const bool last_stage = sl0 > last;
@@ -347,24 +335,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       l0 = l1 = 0.f;
     }
     const uint32_t wm = (h.mask[(16 * cls) >> 5] >> ((16 * cls) & 31)) & 0xffffu;  // this warp's slots
+    // This warp's K and V fragments go to registers first.  With a 16-bit
+    // cache the slot is released before the dependent QK -> softmax -> PV
+    // chain, so the producer refills it that much earlier (2-3 % on the
+    // decode); the fp8 ring, 6 stages deep, was faster releasing after it.
+    constexpr int kNf = kFp8 ? 4 : 8;
+    uint32_t kf[kNf][4], vf[kNf][4];
     if (wm != 0u) {
       const uint32_t kst = s_kv + s * 2 * C::kTensor, vst = kst + C::kTensor;
+#pragma unroll
+      for (int j = 0; j < kNf; ++j) {
+        const uint32_t c = 2 * j + k_sel;
+        if constexpr (!kFp8) ldsm_x4(kst + k_off + (c >> 3) * half_bytes + (((c & 7) ^ k_key) << 4), kf[j]);
+        else ldsm_x4(kst + k_off + ((c ^ k_key) << 4), kf[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < kNf; ++j) {
+        const uint32_t c = 2 * j + v_sel;
+        if constexpr (!kFp8) ldsm_x4_t(vst + v_off + (c >> 3) * half_bytes + (((c & 7) ^ v_key) << 4), vf[j]);
+        else ldsm_x4_t(vst + v_off + ((c ^ v_key) << 4), vf[j]);
+      }
+    }
+    if constexpr (!kFp8) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    }
+    if (wm != 0u) {
       // ---- S^T = K Q^T (16 tokens x 8 heads) ----
       float sa[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (!kFp8) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t c = 2 * j + k_sel;  // 16-byte chunk of the 256-byte row
-          uint32_t a[4];
-          ldsm_x4(kst + k_off + (c >> 3) * half_bytes + (((c & 7) ^ k_key) << 4), a);
-          mma16816<T>(sa, a, qf[j][0], qf[j][1]);
-        }
+        for (int j = 0; j < 8; ++j) mma16816<T>(sa, kf[j], qf[j][0], qf[j][1]);
       } else {
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          const uint32_t c = 2 * jj + k_sel;  // 16-byte chunk = 16 dims
-          uint32_t r[4];
-          ldsm_x4(kst + k_off + ((c ^ k_key) << 4), r);
+          const uint32_t* r = kf[jj];
           const uint32_t a0[4] = {e4m3x2_lo(r[0]), e4m3x2_lo(r[1]), e4m3x2_hi(r[0]), e4m3x2_hi(r[1])};
           mma16816<T>(sa, a0, qf[2 * jj][0], qf[2 * jj][1]);
           const uint32_t a1[4] = {e4m3x2_lo(r[2]), e4m3x2_lo(r[3]), e4m3x2_hi(r[2]), e4m3x2_hi(r[3])};
@@ -409,19 +414,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (!kFp8) {
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          const uint32_t c = 2 * mt + v_sel;
-          uint32_t a[4];
-          ldsm_x4_t(vst + v_off + (c >> 3) * half_bytes + (((c & 7) ^ v_key) << 4), a);
-          a[0] &= vm_lo; a[1] &= vm_lo; a[2] &= vm_hi; a[3] &= vm_hi;
+          uint32_t a[4] = {vf[mt][0] & vm_lo, vf[mt][1] & vm_lo, vf[mt][2] & vm_hi, vf[mt][3] & vm_hi};
           mma16816<T>(o[mt], a, bh0, bh1);
           mma16816<T>(o[mt], a, bl0, bl1);
         }
       } else {
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          const uint32_t c = 2 * jj + v_sel;
-          uint32_t r[4];
-          ldsm_x4_t(vst + v_off + ((c ^ v_key) << 4), r);
+          const uint32_t* r = vf[jj];
           // r: [token 2tg: dims d, d+1][token 2tg+1: d, d+1], d = 16 c + 2 g.
           // Regroup by dim: low half (d: tokens 2tg, 2tg+1), high half (d+1).
           const uint32_t x0 = prmt(r[0] & vm_lo, 0u, 0x3120u), x1 = prmt(r[1] & vm_hi, 0u, 0x3120u);
@@ -435,8 +435,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    if constexpr (kFp8) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    }
     if (!(flags & kLast)) continue;
 
     // ---- end of a work item: row sums, then write (or merge warps) ----

@@ -176,8 +176,8 @@ int launch_merge_states(const void* v, const float* s, void* vo, float* so,
 int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype, int kv_dtype,
                         void* stream);
 int set_decode_kernel(int which);  // 0 auto, 1 CUDA cores, 2 tensor cores
-int set_decode_schedule(int dynamic);
-int launch_wait_timeout(int32_t* status, void* stream);  // diagnostics (diag.cu)  // 1 shared queue (default), 0 the plan's CTA lists
+int set_decode_schedule(int dynamic);  // 1 shared queue (default), 0 the plan's CTA lists
+int launch_wait_timeout(int32_t* status, void* stream);  // diagnostics (diag.cu)
 int launch_paged_decode_simt(const DecodeParams& p, int grid_x, int dtype,
                              void* stream);
 int launch_paged_decode_mma(const DecodeParams& p, int grid_x, int kv_kind,

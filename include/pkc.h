@@ -456,7 +456,8 @@ int pkc_cascade_decode_paged_prefix(
 /*
  * Optional timing hook for the calling thread.  When events is non-NULL,
  * the NEXT pkc_cascade_decode call on this thread records events[0] on its
- * stream before its first kernel, then events[1], events[2], events[3]
+ * stream right before its first kernel (after the host builds that kernel's
+ * TMA descriptors), then events[1], events[2], events[3]
  * after the prefix, suffix-decode and contraction kernels; the hook is then
  * cleared.  A timed call runs its stages one after the other on `stream`
  * (no side stream), so that each pair of events brackets one kernel.

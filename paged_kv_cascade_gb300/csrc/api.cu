@@ -607,21 +607,21 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   // prefix blocks fill the SMs left free and those the decode releases.
   const bool timed = ev[0] || ev[1] || ev[2] || ev[3];
   SideStream* side = timed ? nullptr : side_stream((cudaStream_t)stream);
-  auto run_prefix = [&](void* st) -> int {
-    const int r = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, st);
+  auto run_prefix = [&](void* st, cudaEvent_t start) -> int {
+    const int r = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, st, start);
     if (r == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
     if (r) return cuda_error(r, "prefix launch");
     return PKC_OK;
   };
-  mark(0);
   int e = 0;
   if (side) {
     e = (int)cudaEventRecord(side->fork, (cudaStream_t)stream);
     if (!e) e = (int)cudaStreamWaitEvent(side->side, side->fork, 0);
     if (e) return cuda_error(e, "cascade: stream fork");
   } else {
-    // 1. shared prefix: multi-query states on the tensor cores
-    if (int rc = run_prefix(stream)) return rc;
+    // 1. shared prefix: multi-query states on the tensor cores (stage event
+    // 0 is recorded right before the kernel, after its tensor maps are built)
+    if (int rc = run_prefix(stream, ev[0])) return rc;
   }
   mark(1);
   // 2. unique suffixes: paged decode states (unsplit -> suffix states)
@@ -642,7 +642,7 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   if (e) return cuda_error(e, "paged decode launch");
   if (side) {
     // 1. shared prefix, on the side stream; the caller's stream waits for it
-    if (int rc = run_prefix(side->side)) {
+    if (int rc = run_prefix(side->side, nullptr)) {
       cudaEventRecord(side->join, side->side);  // keep the fork joined
       cudaStreamWaitEvent((cudaStream_t)stream, side->join, 0);
       return rc;

@@ -191,9 +191,11 @@ int launch_append_kv(const AppendParams& p, int batch, void* stream);
 // driver entry point for tensor maps is unavailable.
 // Contiguous prefixes: k/v_prefix [prefix_tokens, Hkv, 128].  Paged
 // prefixes (p.prefix_pages set): k/v_prefix are the page pools.
+// start_event (a cudaEvent_t, or nullptr) is recorded on the stream right
+// before the kernel launch, after the host work of building the maps.
 int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix,
                   const void* v_prefix, int64_t prefix_tokens, int dtype,
-                  void* stream);
+                  void* stream, void* start_event = nullptr);
 
 int num_sms();
 

@@ -592,8 +592,12 @@ int launch_t(const PrefixParams& p, const CUtensorMap& q, const CUtensorMap& k, 
 }  // namespace
 
 int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix, const void* v_prefix,
-                  int64_t prefix_tokens, int dtype, void* stream) {
-  if (p.n_blocks <= 0 || p.total_tiles <= 0) return 0;
+                  int64_t prefix_tokens, int dtype, void* stream, void* start_event) {
+  cudaStream_t st = (cudaStream_t)stream;
+  if (p.n_blocks <= 0 || p.total_tiles <= 0) {
+    if (start_event) return (int)cudaEventRecord((cudaEvent_t)start_event, st);
+    return 0;
+  }
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, dtype, PKC_HEAD_DIM, p.hq, p.batch, p.g, kRows / p.g)) return -1;
   if (!p.prefix_pages) {
@@ -612,7 +616,9 @@ int launch_prefix(const PrefixParams& p, const void* q, const void* k_prefix, co
         !encode_tiled_map(&mv, v_prefix, dtype, 4, dims, strides, box, true))
       return -1;
   }
-  cudaStream_t st = (cudaStream_t)stream;
+  if (start_event) {  // recorded after the host work above, right before the launch
+    if (const cudaError_t e = cudaEventRecord((cudaEvent_t)start_event, st)) return (int)e;
+  }
   return dtype == PKC_BF16 ? launch_t<__nv_bfloat16>(p, mq, mk, mv, st)
                            : launch_t<__half>(p, mq, mk, mv, st);
 }

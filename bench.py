@@ -56,6 +56,10 @@ def parse_args():
     ap.add_argument("--decode-schedule", choices=["dynamic", "static"], default="dynamic",
                     help="planned decode: blocks take the plan's chunks from a shared "
                          "longest-first queue (dynamic) or run their CTA's plan list (static)")
+    ap.add_argument("--num-ctas", type=int, default=None,
+                    help="CTAs of the host plan (default: the workload's)")
+    ap.add_argument("--prefix-ctas", type=int, default=0,
+                    help="thread blocks of the prefix stage (0: automatic, pkc_set_prefix_ctas)")
     ap.add_argument("--batch", type=int, default=None,
                     help="keep only the first N requests (and their prefix groups); "
                          "a smaller case of the same workload, for profiling")
@@ -344,6 +348,8 @@ def run_aux(args):
                            "l2": "inputs larger than L2 (203 MB / 1.15 GB)"}}
     else:  # paged_decode*: non-cascade decode through the plan
         cfg = workload_cfg(args.workload)
+        if args.num_ctas is not None:
+            cfg["num_ctas"] = args.num_ctas
         p = workloads.make_problem(**cfg)
         d = to_device(p)
         fp8 = p["kv_dtype"] == "e4m3"
@@ -392,12 +398,15 @@ def run_cascade_variant(args):
     import __graft_entry__
     __graft_entry__.build()
     import paged_kv_cascade_gb300 as pkc
+    pkc.set_prefix_ctas(args.prefix_ctas)
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from pkc_testing import dev, to_device
     hbm_peak, _, peak_kind = load_peaks()
     K, W = max(args.steps, 3), max(args.warmup, 3)
     paged = args.workload == "gqa_cascade_paged_prefix"
     cfg = workload_cfg("gqa_cascade_lb" if paged else args.workload)
+    if args.num_ctas is not None:
+        cfg["num_ctas"] = args.num_ctas
     p = workloads.make_problem(**cfg)
     d = to_device(p)
     B, Hq, D = p["q"].shape
@@ -586,8 +595,11 @@ def main():
     import paged_kv_cascade_gb300 as pkc
     pkc.set_decode_kernel(args.decode_kernel)
     pkc.set_decode_schedule(args.decode_schedule)
+    pkc.set_prefix_ctas(args.prefix_ctas)
 
     cfg, p = make_workload(args.workload, args.batch)
+    if args.num_ctas is not None:
+        cfg["num_ctas"] = args.num_ctas
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from pkc_testing import to_device
     d = to_device(p, f"cuda:{local}")
@@ -818,6 +830,7 @@ def main():
                        "l2": "inputs larger than L2 (one step reads %.2f GB)" % (eff / 1e9),
                        "launch": mode, "decode_kernel": args.decode_kernel,
                        "decode_schedule": args.decode_schedule if num_ctas else None,
+                       "prefix_ctas": args.prefix_ctas or "auto",
                        "parallelism": f"replicas x{world}"},
             "direct_us_per_step": 1e3 * direct_ms_per_step,
             "hbm_fraction": value / world / hbm_peak,

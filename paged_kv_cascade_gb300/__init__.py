@@ -58,6 +58,7 @@ SIGNATURES = {
     "pkc_set_stage_events": (_I, [_c.POINTER(_P), _I]),
     "pkc_set_decode_kernel": (_I, [_I]),
     "pkc_set_decode_schedule": (_I, [_I]),
+    "pkc_set_prefix_ctas": (_I, [_I]),
     "pkc_selftest_wait_timeout": (_I, [_P, _SZ, _c.POINTER(_c.c_int32), _P]),
     "pkc_append_kv": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I64, _I, _P, _SZ, _P]),
     "pkc_cascade_decode_multilevel": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I,
@@ -348,6 +349,17 @@ def set_decode_schedule(which):
     from a shared longest-first queue; default) or "static" (each block runs
     its CTA's list of the plan); process-wide."""
     _check(lib().pkc_set_decode_schedule(DECODE_SCHEDULES[which]))
+
+
+def set_prefix_ctas(n):
+    """Thread blocks of the prefix stage: n > 0 caps them at n; 0 (default)
+    is automatic: every SM, or, in a planned cascade call whose prefix is
+    bound by the tensor pipe, the SMs the plan's CTAs leave free
+    (pkc.h, pkc_set_prefix_ctas); process-wide."""
+    n = int(n)
+    if n < 0:
+        raise ValueError(f"set_prefix_ctas: n must be >= 0 (got {n})")
+    _check(lib().pkc_set_prefix_ctas(n))
 
 
 def paged_decode_state_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, sm_scale,

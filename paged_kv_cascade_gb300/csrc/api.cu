@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
@@ -146,7 +147,7 @@ struct PrefixSetup {
 // long as the pieces of any pair fit the workspace's partial slots.
 int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_begin, const int32_t* req_end,
                  int n_prefix, int batch, int hq, int hkv, float sm_scale, uint8_t* ws, size_t ws_bytes,
-                 const WsLayout& L, int32_t* status) {
+                 const WsLayout& L, int32_t* status, int max_blocks) {
   if (n_prefix < 1 || n_prefix > PKC_MAX_PREFIX)
     return set_error(PKC_ERR_INVALID_ARG, "n_prefix must be in [1, %d] (got %d)", PKC_MAX_PREFIX, n_prefix);
   if (!kv_indptr || !req_begin || !req_end) return set_error(PKC_ERR_INVALID_ARG, "prefix arrays are NULL");
@@ -189,11 +190,37 @@ int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_be
   const size_t avail = ws_bytes > L.fixed_end ? (ws_bytes - L.fixed_end) / L.prefix_split : 0;
   if (avail < 1) return set_error(PKC_ERR_WORKSPACE, "workspace has no room for prefix partial states");
   const int max_slots = (int)std::min<size_t>(avail, PKC_MAX_PREFIX_SPLITS);
-  // One block per SM (fewer if there are fewer tiles).  Group j needs as
-  // many partial slots as the most pieces any of its pairs is cut into;
-  // groups sharing a request get disjoint slot ranges (first fit in group
-  // order), and every request's slots must fit the workspace.
-  int C = (int)std::min<int64_t>(num_sms(), T);
+  // One block per SM, or max_blocks (fewer if there are fewer tiles).
+  // Group j needs as many partial slots as the most pieces any of its pairs
+  // is cut into; groups sharing a request get disjoint slot ranges (first
+  // fit in group order), and every request's slots must fit the workspace.
+  int C = (int)std::min<int64_t>(std::max(1, std::min(max_blocks, num_sms())), T);
+  // The 128-row query tiles of one (group, KV head) read the same K/V
+  // tiles, Hkv * kvt flat tiles apart.  When that distance is a whole number
+  // of blocks' shares (D C divisible by T), block i and block i + D C / T
+  // reach the two copies of every K/V tile at the same moment and the
+  // second read hits L2; otherwise they drift apart by a fraction of a
+  // share and the second read goes to HBM (GQA prefix next to the decode:
+  // 40 or 48 blocks 296 us per step, 44 or 52 blocks 313 us).  So C is the
+  // largest count, down to 3/4 of the candidate, that aligns every group
+  // with two or more row tiles.
+  {
+    std::vector<int64_t> dist;
+    for (int j = 0; j < n_prefix; ++j) {
+      const int kvt = (kv_indptr[j + 1] - kv_indptr[j] + 127) / 128;
+      if (kvt > 0 && p.tile_indptr[j + 1] - p.tile_indptr[j] >= 2) dist.push_back((int64_t)hkv * kvt);
+    }
+    if (!dist.empty()) {
+      for (int c = C; c >= 1 && 4 * c >= 3 * C; --c) {
+        bool aligned = true;
+        for (const int64_t d : dist) aligned = aligned && (d * c) % T == 0;
+        if (aligned) {
+          C = c;
+          break;
+        }
+      }
+    }
+  }
   if (T * C >= INT32_MAX) return set_error(PKC_ERR_UNSUPPORTED, "prefix: too many KV tiles (%lld)", (long long)T);
   int slots = 0;
   std::vector<int> need(n_prefix), base(n_prefix);
@@ -248,6 +275,48 @@ int indptr_ranges(const int32_t* req_indptr, int n_prefix, int32_t* begin, int32
     end[j] = req_indptr[j + 1];
   }
   return PKC_OK;
+}
+
+// Blocks of the prefix kernel in a cascade call (pkc_set_prefix_ctas).
+std::atomic<int> g_prefix_ctas{0};
+
+// The suffix decode is bound by HBM and, with its producer's integer row
+// masks, saturates it on about 100 SMs (GQA suffix of 1.8 GB: 148 / 112 /
+// 100 CTAs take 267 / 270 / 272 us).  A prefix whose K/V tiles are each
+// read by two or more 128-row query tiles is bound by the tensor pipe
+// instead (about 5 TFLOP/s per SM measured).  Run next to a planned decode,
+// such a prefix takes only the SMs the plan leaves free, if there are at
+// least kMinPrefixSms of them and it is expected to finish well before the
+// decode: the two stages then overlap instead of queueing for SMs (GQA
+// cascade step 316 -> 291 us for decode + prefix).  Otherwise (a prefix
+// that is itself HBM-bound, a decode over every SM, a short suffix) the
+// prefix takes every SM.  A timed cascade call (stage events) runs the
+// stages one after the other but keeps the same block count.
+constexpr int kMinPrefixSms = 16;
+constexpr double kPrefixFlopsPerSm = 4.5e12;  // tensor-pipe bound prefix, per SM
+constexpr double kDecodeBytesPerS = 6.5e12;   // HBM-bound suffix decode
+int prefix_blocks(const int32_t* kv_indptr, const int32_t* req_begin, const int32_t* req_end, int n_prefix,
+                  int g, int hkv, int elem_bytes, const int32_t* plan_host, bool next_to_decode) {
+  const int sms = num_sms();
+  const int forced = g_prefix_ctas.load();
+  if (forced > 0) return std::min(forced, sms);
+  if (!next_to_decode || !plan_host) return sms;
+  const int free_sms = sms - plan_host[PKC_PLAN_NUM_CTAS];
+  if (free_sms < kMinPrefixSms) return sms;
+  double flops = 0.0;
+  for (int j = 0; j < n_prefix; ++j) {
+    const int64_t tokens = kv_indptr[j + 1] - kv_indptr[j];
+    const int64_t row_tiles = ((int64_t)(req_end[j] - req_begin[j]) * g + 127) / 128;
+    if (tokens == 0 || row_tiles == 0) continue;
+    if (row_tiles < 2) return sms;  // each K/V tile read once: HBM-bound
+    flops += 4.0 * PKC_HEAD_DIM * 128.0 * (double)row_tiles * (double)tokens * hkv;
+  }
+  int64_t suffix_tokens = 0;
+  const int32_t* kv_len = plan_host + plan_host[PKC_PLAN_OFF_UNIT_KV_LEN];
+  for (int u = 0; u < plan_host[PKC_PLAN_N_UNITS]; ++u) suffix_tokens += kv_len[u];
+  const double t_prefix = flops / (free_sms * kPrefixFlopsPerSm);
+  const double t_decode = (double)suffix_tokens * 2.0 * hkv * PKC_HEAD_DIM * elem_bytes / kDecodeBytesPerS;
+  return flops > 0.0 && t_prefix <= 0.8 * t_decode ? free_sms : sms;
 }
 
 void fill_contract_prefix(ContractParams& c, const PrefixSetup& S) {
@@ -493,6 +562,12 @@ int pkc_set_decode_schedule(int dynamic) {
   return PKC_OK;
 }
 
+int pkc_set_prefix_ctas(int n) {
+  if (n < 0) return set_error(PKC_ERR_INVALID_ARG, "set_prefix_ctas: n must be >= 0 (got %d)", n);
+  g_prefix_ctas.store(n);
+  return PKC_OK;
+}
+
 int pkc_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int32_t* gave_up_host, void* stream) {
   if (!gave_up_host) return set_error(PKC_ERR_INVALID_ARG, "selftest_wait_timeout: NULL result pointer");
   if (int rc = check_ws(workspace, workspace_bytes, PKC_STATUS_BYTES)) return rc;
@@ -525,8 +600,10 @@ int pkc_prefix_attention_state(const void* q, const void* k_prefix, const void* 
   int32_t rb[PKC_MAX_PREFIX], re[PKC_MAX_PREFIX];
   if (int rc = indptr_ranges(prefix_req_indptr_host, n_prefix, rb, re)) return rc;
   PrefixSetup S;
+  const int blocks = prefix_blocks(prefix_kv_indptr_host, rb, re, n_prefix, num_qo_heads / num_kv_heads,
+                                   num_kv_heads, 2, nullptr, false);
   if (int rc = setup_prefix(S, prefix_kv_indptr_host, rb, re, n_prefix, batch, num_qo_heads, num_kv_heads, sm_scale,
-                            ws, workspace_bytes, L, status))
+                            ws, workspace_bytes, L, status, blocks))
     return rc;
   int e = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, stream);
   if (e == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
@@ -573,9 +650,17 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
     return set_error(PKC_ERR_INVALID_ARG, "cascade_decode: tensors must be 16-byte aligned");
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
+  cudaEvent_t ev[4];
+  for (int i = 0; i < 4; ++i) ev[i] = g_stage_events[i];
+  g_stage_events[0] = g_stage_events[1] = g_stage_events[2] = g_stage_events[3] = nullptr;
+  const bool timed = ev[0] || ev[1] || ev[2] || ev[3];
   PrefixSetup S;
+  // The same block count whether or not the call is timed, so that stage
+  // events never change the result's rounding.
+  const int blocks = prefix_blocks(prefix_kv_indptr_host, req_begin, req_end, n_prefix, num_qo_heads / num_kv_heads,
+                                   num_kv_heads, 2, plan_host, true);
   if (int rc = setup_prefix(S, prefix_kv_indptr_host, req_begin, req_end, n_prefix, batch, num_qo_heads,
-                            num_kv_heads, sm_scale, ws, workspace_bytes, L, status))
+                            num_kv_heads, sm_scale, ws, workspace_bytes, L, status, blocks))
     return rc;
   if (prefix_pages) {
     if (!page_indptr) return set_error(PKC_ERR_INVALID_ARG, "paged prefix: prefix_page_indptr is NULL");
@@ -594,9 +679,6 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
     S.pp.page_size = page_size;
     S.pp.num_pages = num_pages;
   }
-  cudaEvent_t ev[4];
-  for (int i = 0; i < 4; ++i) ev[i] = g_stage_events[i];
-  g_stage_events[0] = g_stage_events[1] = g_stage_events[2] = g_stage_events[3] = nullptr;
   auto mark = [&](int i) {
     if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
   };
@@ -605,7 +687,6 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   // stream, next to the decode, and the contraction waits for both.  The
   // decode is launched first so that its blocks take the SMs first; the
   // prefix blocks fill the SMs left free and those the decode releases.
-  const bool timed = ev[0] || ev[1] || ev[2] || ev[3];
   SideStream* side = timed ? nullptr : side_stream((cudaStream_t)stream);
   auto run_prefix = [&](void* st, cudaEvent_t start) -> int {
     const int r = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, st, start);

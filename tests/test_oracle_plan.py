@@ -100,14 +100,17 @@ def test_invariants_random(seed):
 
 
 def test_invariants_at_gqa_workload():
+    # the workload's lengths over 148 CTAs (pinned values) and over the
+    # workload's own plan CTA count
     w = workloads.WORKLOADS["gqa_cascade_lb"]
     lens = workloads.suffix_lengths(w["suffix"], w["batch"],
                                     np.random.default_rng(w["seed"]))
-    p = _check_invariants([1] * w["batch"], lens.tolist(), 1, w["num_ctas"],
+    p = _check_invariants([1] * w["batch"], lens.tolist(), 1, 148,
                           w["alpha"], w["beta"])
     assert p["kv_chunk"] == 2974
     assert len(p["split_units"]) == 37
     assert max(len(p["unit_chunks"][u]) for u in range(w["batch"])) == 6
+    _check_invariants([1] * w["batch"], lens.tolist(), 1, w["num_ctas"], w["alpha"], w["beta"])
 
 
 def test_all_zero_lengths():

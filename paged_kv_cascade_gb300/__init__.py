@@ -354,8 +354,8 @@ def set_decode_schedule(which):
 def set_prefix_ctas(n):
     """Thread blocks of the prefix stage: n > 0 caps them at n; 0 (default)
     is automatic: every SM, or, in a planned cascade call whose prefix is
-    bound by the tensor pipe, the SMs the plan's CTAs leave free
-    (pkc.h, pkc_set_prefix_ctas); process-wide."""
+    bound by the tensor pipe, a quarter of the SMs next to a dynamically
+    scheduled decode on the rest (pkc.h, pkc_set_prefix_ctas); process-wide."""
     n = int(n)
     if n < 0:
         raise ValueError(f"set_prefix_ctas: n must be >= 0 (got {n})")

@@ -203,12 +203,15 @@ int setup_prefix(PrefixSetup& S, const int32_t* kv_indptr, const int32_t* req_be
   // share and the second read goes to HBM (GQA prefix next to the decode:
   // 40 or 48 blocks 296 us per step, 44 or 52 blocks 313 us).  So C is the
   // largest count, down to 3/4 of the candidate, that aligns every group
-  // with two or more row tiles.
+  // with two or more row tiles whose K/V (all heads) is larger than 16 MB;
+  // a smaller group's K/V, read by several row tiles, stays in the 126 MB L2.
   {
     std::vector<int64_t> dist;
     for (int j = 0; j < n_prefix; ++j) {
       const int kvt = (kv_indptr[j + 1] - kv_indptr[j] + 127) / 128;
-      if (kvt > 0 && p.tile_indptr[j + 1] - p.tile_indptr[j] >= 2) dist.push_back((int64_t)hkv * kvt);
+      const int64_t kv_bytes = (int64_t)(kv_indptr[j + 1] - kv_indptr[j]) * hkv * PKC_HEAD_DIM * 4;
+      if (kvt > 0 && p.tile_indptr[j + 1] - p.tile_indptr[j] >= 2 && kv_bytes > (16ll << 20))
+        dist.push_back((int64_t)hkv * kvt);
     }
     if (!dist.empty()) {
       for (int c = C; c >= 1 && 4 * c >= 3 * C; --c) {
@@ -280,43 +283,60 @@ int indptr_ranges(const int32_t* req_indptr, int n_prefix, int32_t* begin, int32
 // Blocks of the prefix kernel in a cascade call (pkc_set_prefix_ctas).
 std::atomic<int> g_prefix_ctas{0};
 
+// How a planned cascade shares the SMs between its two independent stages.
 // The suffix decode is bound by HBM and, with its producer's integer row
 // masks, saturates it on about 100 SMs (GQA suffix of 1.8 GB: 148 / 112 /
 // 100 CTAs take 267 / 270 / 272 us).  A prefix whose K/V tiles are each
 // read by two or more 128-row query tiles is bound by the tensor pipe
-// instead (about 5 TFLOP/s per SM measured).  Run next to a planned decode,
-// such a prefix takes only the SMs the plan leaves free, if there are at
-// least kMinPrefixSms of them and it is expected to finish well before the
-// decode: the two stages then overlap instead of queueing for SMs (GQA
-// cascade step 316 -> 291 us for decode + prefix).  Otherwise (a prefix
-// that is itself HBM-bound, a decode over every SM, a short suffix) the
-// prefix takes every SM.  A timed cascade call (stage events) runs the
-// stages one after the other but keeps the same block count.
+// instead (about 6 TFLOP/s per SM on SMs of its own: 34.4 GFLOP in 175 us
+// on 32 SMs, 145 us on 40; the estimate below uses 4.5, since a prefix that
+// outlasts the decode lengthens the step: the three-level GQA cascade, whose
+// prefix needs about 90 % of its decode's time on a quarter of the SMs,
+// took 317 us split against 283 us unsplit), so the two stages can overlap
+// instead of queueing for SMs.  The two grids together never exceed the SMs: which of
+// the two streams' kernels starts first is not fixed, and a prefix over
+// every SM that started first would hold the decode back.
+//  - Dynamic schedule: the decode's persistent blocks take the plan's
+//    chunks from a queue, so their number is free.  If the prefix is
+//    expected to finish before the decode on a quarter of the SMs, it gets
+//    that quarter and the decode the rest (GQA cascade step 319 -> 294 us).
+//  - Static schedule: each decode block runs one plan CTA's list; a prefix
+//    expected to finish first gets the SMs the plan leaves free (>= 16).
+// Otherwise (a prefix that is itself HBM-bound, a short suffix) the prefix
+// takes every SM and the decode one block per plan CTA.
 constexpr int kMinPrefixSms = 16;
-constexpr double kPrefixFlopsPerSm = 4.5e12;  // tensor-pipe bound prefix, per SM
+constexpr double kPrefixFlopsPerSm = 4.5e12;  // tensor-pipe bound prefix, per SM (conservative)
 constexpr double kDecodeBytesPerS = 6.5e12;   // HBM-bound suffix decode
-int prefix_blocks(const int32_t* kv_indptr, const int32_t* req_begin, const int32_t* req_end, int n_prefix,
-                  int g, int hkv, int elem_bytes, const int32_t* plan_host, bool next_to_decode) {
+struct StageSplit {
+  int prefix_blocks;  // at most this many prefix blocks (setup_prefix may use fewer)
+  int decode_blocks;  // 0: one per plan CTA; -1: the SMs the prefix leaves; else this many
+};
+StageSplit stage_split(const int32_t* kv_indptr, const int32_t* req_begin, const int32_t* req_end, int n_prefix,
+                       int g, int hkv, int elem_bytes, const int32_t* plan_host, bool next_to_decode) {
   const int sms = num_sms();
+  const bool dynamic = plan_host && decode_schedule_dynamic();
   const int forced = g_prefix_ctas.load();
-  if (forced > 0) return std::min(forced, sms);
-  if (!next_to_decode || !plan_host) return sms;
-  const int free_sms = sms - plan_host[PKC_PLAN_NUM_CTAS];
-  if (free_sms < kMinPrefixSms) return sms;
+  if (forced > 0) return {std::min(forced, sms), next_to_decode && dynamic && forced < sms ? -1 : 0};
+  const StageSplit all{sms, 0};
+  if (!next_to_decode || !plan_host) return all;
+  const int blocks = dynamic ? sms - (3 * sms) / 4 : sms - plan_host[PKC_PLAN_NUM_CTAS];
+  if (blocks < kMinPrefixSms) return all;
   double flops = 0.0;
   for (int j = 0; j < n_prefix; ++j) {
     const int64_t tokens = kv_indptr[j + 1] - kv_indptr[j];
     const int64_t row_tiles = ((int64_t)(req_end[j] - req_begin[j]) * g + 127) / 128;
     if (tokens == 0 || row_tiles == 0) continue;
-    if (row_tiles < 2) return sms;  // each K/V tile read once: HBM-bound
+    if (row_tiles < 2) return all;  // each K/V tile read once: HBM-bound
     flops += 4.0 * PKC_HEAD_DIM * 128.0 * (double)row_tiles * (double)tokens * hkv;
   }
+  if (flops <= 0.0) return all;
   int64_t suffix_tokens = 0;
   const int32_t* kv_len = plan_host + plan_host[PKC_PLAN_OFF_UNIT_KV_LEN];
   for (int u = 0; u < plan_host[PKC_PLAN_N_UNITS]; ++u) suffix_tokens += kv_len[u];
-  const double t_prefix = flops / (free_sms * kPrefixFlopsPerSm);
+  const double t_prefix = flops / (blocks * kPrefixFlopsPerSm);
   const double t_decode = (double)suffix_tokens * 2.0 * hkv * PKC_HEAD_DIM * elem_bytes / kDecodeBytesPerS;
-  return flops > 0.0 && t_prefix <= 0.8 * t_decode ? free_sms : sms;
+  if (t_prefix <= 0.8 * t_decode) return {blocks, dynamic ? -1 : 0};
+  return all;
 }
 
 void fill_contract_prefix(ContractParams& c, const PrefixSetup& S) {
@@ -600,10 +620,10 @@ int pkc_prefix_attention_state(const void* q, const void* k_prefix, const void* 
   int32_t rb[PKC_MAX_PREFIX], re[PKC_MAX_PREFIX];
   if (int rc = indptr_ranges(prefix_req_indptr_host, n_prefix, rb, re)) return rc;
   PrefixSetup S;
-  const int blocks = prefix_blocks(prefix_kv_indptr_host, rb, re, n_prefix, num_qo_heads / num_kv_heads,
-                                   num_kv_heads, 2, nullptr, false);
+  const StageSplit split = stage_split(prefix_kv_indptr_host, rb, re, n_prefix, num_qo_heads / num_kv_heads,
+                                       num_kv_heads, 2, nullptr, false);
   if (int rc = setup_prefix(S, prefix_kv_indptr_host, rb, re, n_prefix, batch, num_qo_heads, num_kv_heads, sm_scale,
-                            ws, workspace_bytes, L, status, blocks))
+                            ws, workspace_bytes, L, status, split.prefix_blocks))
     return rc;
   int e = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, stream);
   if (e == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
@@ -655,13 +675,21 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   g_stage_events[0] = g_stage_events[1] = g_stage_events[2] = g_stage_events[3] = nullptr;
   const bool timed = ev[0] || ev[1] || ev[2] || ev[3];
   PrefixSetup S;
-  // The same block count whether or not the call is timed, so that stage
-  // events never change the result's rounding.
-  const int blocks = prefix_blocks(prefix_kv_indptr_host, req_begin, req_end, n_prefix, num_qo_heads / num_kv_heads,
-                                   num_kv_heads, 2, plan_host, true);
+  // The same split whether or not the call is timed, so that stage events
+  // never change the result's rounding.
+  const StageSplit split = stage_split(prefix_kv_indptr_host, req_begin, req_end, n_prefix,
+                                       num_qo_heads / num_kv_heads, num_kv_heads, 2, plan_host, true);
   if (int rc = setup_prefix(S, prefix_kv_indptr_host, req_begin, req_end, n_prefix, batch, num_qo_heads,
-                            num_kv_heads, sm_scale, ws, workspace_bytes, L, status, blocks))
+                            num_kv_heads, sm_scale, ws, workspace_bytes, L, status, split.prefix_blocks))
     return rc;
+  // Decode blocks: one per plan CTA, or (dynamic schedule) fewer persistent
+  // blocks taking the plan's chunks from the queue; the chunks are the
+  // plan's either way.
+  int decode_blocks = plan_host ? num_ctas : batch;
+  if (plan_host && S.pp.n_blocks > 0) {
+    if (split.decode_blocks == -1) decode_blocks = std::max(1, std::min(num_ctas, num_sms() - S.pp.n_blocks));
+    else if (split.decode_blocks > 0) decode_blocks = std::min(num_ctas, split.decode_blocks);
+  }
   if (prefix_pages) {
     if (!page_indptr) return set_error(PKC_ERR_INVALID_ARG, "paged prefix: prefix_page_indptr is NULL");
     if (page_size < 8 || 128 % page_size != 0)
@@ -719,7 +747,7 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
   dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   dp.status = status;
-  e = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, dtype, stream);
+  e = launch_paged_decode(dp, decode_blocks, dtype, dtype, stream);
   if (e) return cuda_error(e, "paged decode launch");
   if (side) {
     // 1. shared prefix, on the side stream; the caller's stream waits for it

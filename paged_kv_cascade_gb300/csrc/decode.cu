@@ -695,6 +695,8 @@ int set_decode_kernel(int which) {
 // list of the plan (pkc_set_decode_schedule).
 static std::atomic<int> g_decode_dynamic{1};
 
+int decode_schedule_dynamic() { return g_decode_dynamic.load(); }
+
 int set_decode_schedule(int dynamic) {
   if (dynamic != 0 && dynamic != 1) return -1;
   g_decode_dynamic.store(dynamic);

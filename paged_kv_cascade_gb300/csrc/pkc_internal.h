@@ -177,6 +177,7 @@ int launch_paged_decode(const DecodeParams& p, int grid_x, int dtype, int kv_dty
                         void* stream);
 int set_decode_kernel(int which);  // 0 auto, 1 CUDA cores, 2 tensor cores
 int set_decode_schedule(int dynamic);  // 1 shared queue (default), 0 the plan's CTA lists
+int decode_schedule_dynamic();         // the current choice of set_decode_schedule
 int launch_wait_timeout(int32_t* status, void* stream);  // diagnostics (diag.cu)
 int launch_paged_decode_simt(const DecodeParams& p, int grid_x, int dtype,
                              void* stream);

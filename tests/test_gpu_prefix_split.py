@@ -2,12 +2,13 @@
 
 In a planned cascade call the prefix runs next to the suffix decode.  When
 its K/V tiles are shared by two or more 128-row query tiles it is bound by
-the tensor pipe, and it takes only the SMs the plan leaves free
-(pkc_set_prefix_ctas, automatic); a caller may also cap its blocks.  The
-block count changes how the flattened KV tiles are cut into pieces, so the
-states must match the oracle for every count, and a call must give the same
-bits timed (stage events, stages in order), untimed (side stream) and
-replayed from a CUDA graph."""
+the tensor pipe and gets SMs of its own (pkc_set_prefix_ctas, automatic): a
+quarter of them next to a dynamically scheduled decode on the rest, or the
+SMs a static plan leaves free; a caller may also cap its blocks.  The block
+count changes how the flattened KV tiles are cut into pieces, so the states
+must match the oracle for every count, and a call must give the same bits
+timed (stage events, stages in order), untimed (side stream) and replayed
+from a CUDA graph."""
 import pytest
 import torch
 
@@ -18,16 +19,16 @@ from pkc_testing import compare, oracle_args, to_device, workspace_for
 
 pytestmark = pytest.mark.gpu
 
-# the plan's CTAs; on a 152-SM GB300 the automatic rule gives the prefix
-# the other 40 SMs (2 row tiles per KV head, a suffix much longer than the
-# prefix's work)
-PLAN_CTAS = 112
+# the plan's CTAs (2 row tiles per KV head and a suffix much longer than the
+# prefix's work: the automatic rule splits the SMs)
+PLAN_CTAS = 148
 
 
 @pytest.fixture
 def prefix_ctas():
     yield pkc.set_prefix_ctas
     pkc.set_prefix_ctas(0)
+    pkc.set_decode_schedule("dynamic")
 
 
 @pytest.fixture(scope="module")
@@ -47,12 +48,14 @@ def _cascade(p, d, buf, ws, o=None, lse=None):
                               d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse)
 
 
+@pytest.mark.parametrize("schedule,ctas", [("dynamic", PLAN_CTAS), ("static", 112)])
 @pytest.mark.parametrize("n", [1, 5, 40, 0])
-def test_prefix_block_counts_match_oracle(prefix_ctas, gqa, n):
+def test_prefix_block_counts_match_oracle(prefix_ctas, gqa, n, schedule, ctas):
     p, d, (ref_o, ref_lse) = gqa
     prefix_ctas(n)
-    buf = pkc.plan(p["cache_seqlens"], PLAN_CTAS)
-    ws = workspace_for(pkc, p, num_ctas=PLAN_CTAS)
+    pkc.set_decode_schedule(schedule)
+    buf = pkc.plan(p["cache_seqlens"], ctas)
+    ws = workspace_for(pkc, p, num_ctas=ctas)
     pkc.plan_upload(buf, ws)
     o, lse = _cascade(p, d, buf, ws)
     torch.cuda.synchronize()

@@ -79,7 +79,8 @@ def test_static_and_dynamic_agree_bit_for_bit(schedule, which, case):
 
 def test_dynamic_cascade_gqa_workload_rows():
     """The cascade at the GQA workload shape with the default (dynamic)
-    decode against the static one: the same bits."""
+    decode against the static one: the same bits.  The prefix's SM share
+    depends on the schedule, so it is pinned to every SM here."""
     w = dict(workloads.WORKLOADS["gqa_cascade_lb"])
     p = workloads.make_problem(**dict(w, batch=64, prefix_lens=[8192], prefix_groups=[64]))
     d = to_device(p)
@@ -87,6 +88,7 @@ def test_dynamic_cascade_gqa_workload_rows():
     ws = workspace_for(pkc, p, num_ctas=148)
     pkc.plan_upload(buf, ws)
     res = {}
+    pkc.set_prefix_ctas(torch.cuda.get_device_properties(0).multi_processor_count)
     try:
         for which in ("static", "dynamic"):
             pkc.set_decode_schedule(which)
@@ -99,6 +101,7 @@ def test_dynamic_cascade_gqa_workload_rows():
             res[which] = (o.clone(), lse.clone())
     finally:
         pkc.set_decode_schedule("dynamic")
+        pkc.set_prefix_ctas(0)
     assert torch.equal(res["static"][0], res["dynamic"][0])
     assert torch.equal(res["static"][1], res["dynamic"][1])
     assert not _status_block(ws)[16:18].any()

@@ -60,16 +60,13 @@ WORKLOADS = {
                                prefix_lens=[2048] + [8192] * 4, prefix_groups=[1] * 5,
                                prefix_ranges=[(0, 256), (0, 64), (64, 128), (128, 192), (192, 256)],
                                suffix=("lognormal", 7.0, 1.0, 16, 16384),
-                               page_size=16, seed=7, num_ctas=112, alpha=1.0, beta=1.0),
+                               page_size=16, seed=7, num_ctas=148, alpha=1.0, beta=1.0),
     # GQA 32/8, bf16, batch 256; 4 prefixes x 8192 tokens, 64 requests each;
-    # suffix ~ lognormal(7, 1) clipped to [16, 16384].  The plan is over 112
-    # CTAs: the decode saturates HBM on them, and the prefix (two query row
-    # tiles per K/V tile, bound by the tensor pipe) runs next to it on the
-    # other 40 SMs of a GB300.
+    # suffix ~ lognormal(7, 1) clipped to [16, 16384]; plan over 148 CTAs
     "gqa_cascade_lb": dict(batch=256, hq=32, hkv=8, d=128, dtype="bf16",
                            prefix_lens=[8192] * 4, prefix_groups=[64] * 4,
                            suffix=("lognormal", 7.0, 1.0, 16, 16384),
-                           page_size=16, seed=5, num_ctas=112, alpha=1.0,
+                           page_size=16, seed=5, num_ctas=148, alpha=1.0,
                            beta=1.0),
 }
 

@@ -26,10 +26,13 @@ import numpy as np
 _CHUNK = 1 << 22  # elements per independently seeded generator block
 
 WORKLOADS = {
-    # batch 4, 32/32 heads, d 128, fp16; shared prefix 256, suffix 32 each
+    # batch 4, 32/32 heads, d 128, fp16; shared prefix 256, suffix 32 each.
+    # No plan: one decode block per (request, KV-head group) reads its whole
+    # suffix and writes the state directly (a plan over 148 CTAs would cut
+    # every 32-token suffix into 1-token chunks: 34 against 16 us per step).
     "tiny_cascade": dict(batch=4, hq=32, hkv=32, d=128, dtype="f16",
                          prefix_lens=[256], prefix_groups=[4],
-                         suffix=("const", 32), page_size=16, seed=1),
+                         suffix=("const", 32), page_size=16, seed=1, plan=False),
     # merge_state: 4096 tokens x 32 heads x 128, fp32 v ~ N(0,1),
     # s ~ U[-10, 10]; binary and 16-ary
     "merge": dict(tokens=4096, heads=32, d=128, n_states=16, seed=2),

@@ -42,8 +42,29 @@ template <typename H> struct Vec16 {
 template <> struct Vec<__half> : Vec16<__half> {};
 template <> struct Vec<__nv_bfloat16> : Vec16<__nv_bfloat16> {};
 
+// Binary weights of one row: (wa, wb) normalised, s the merged LSE.
+__device__ __forceinline__ void merge2_weights(float a, float b, float& wa, float& wb, float& s) {
+  const float m = fmaxf(a, b);
+  wa = 0.f;
+  wb = 0.f;
+  s = neg_inf();
+  if (m != neg_inf()) {
+    wa = ex2((a - m) * kLog2e);
+    wb = ex2((b - m) * kLog2e);
+    const float den = wa + wb;
+    s = m + lg2(den) * kLn2;
+    const float inv = 1.f / den;
+    wa *= inv;
+    wb *= inv;
+  }
+}
+
 // Rows are (token, head) pairs.  A warp covers `32 / cpr` rows at a time
 // when a row has cpr <= 32 16-byte chunks, else one row in 32-chunk steps.
+// With at most one chunk per lane (head_dim 128 in any dtype) a warp step
+// takes two row groups, a grid stride apart, and issues both groups'
+// vector and LSE loads before any arithmetic: two rows' bytes in flight per
+// warp and one memory round trip per step.
 template <typename T>
 __global__ void __launch_bounds__(256) merge2_kernel(const T* __restrict__ va, const float* sa,
                                                      const T* __restrict__ vb, const float* sb,
@@ -56,48 +77,56 @@ __global__ void __launch_bounds__(256) merge2_kernel(const T* __restrict__ va, c
   const int sub_row = cpr >= 32 ? 0 : lane / cpr;
   const int chunk0 = cpr >= 32 ? lane : lane % cpr;
   const int cstep = cpr >= 32 ? 32 : cpr;
-  for (int64_t r0 = warp * rpw; r0 < rows; r0 += nwarps * rpw) {
-    const int64_t row = r0 + sub_row;
-    const bool active = row < rows;
-    // With at most one 16-byte chunk per lane (head_dim 128 in any dtype),
-    // the chunk's loads go out together with the LSE loads instead of after
-    // the weights: one memory round trip per row step, not two.
-    float x1[V::N], y1[V::N];
-    const bool one = cpr <= 32 && active;
-    const int64_t off1 = (row * cpr + chunk0) * V::N;
-    if (one) {
-      V::load(va + off1, x1);
-      V::load(vb + off1, y1);
-    }
-    float a = active ? sa[row] : 0.f, b = active ? sb[row] : 0.f;
-    const float m = fmaxf(a, b);
-    float wa = 0.f, wb = 0.f, s = neg_inf();
-    if (m != neg_inf()) {
-      wa = ex2((a - m) * kLog2e);
-      wb = ex2((b - m) * kLog2e);
-      const float den = wa + wb;
-      s = m + lg2(den) * kLn2;
-      const float inv = 1.f / den;
-      wa *= inv;
-      wb *= inv;
-    }
-    if (one) {
+  const int64_t stride = nwarps * rpw;
+  if (cpr <= 32) {
+    for (int64_t r0 = warp * rpw; r0 < rows; r0 += 2 * stride) {
+      const int64_t row0 = r0 + sub_row, row1 = row0 + stride;
+      const bool act0 = row0 < rows, act1 = row1 < rows;
+      const int64_t off0 = (row0 * cpr + chunk0) * V::N, off1 = (row1 * cpr + chunk0) * V::N;
+      float x0[V::N], y0[V::N], x1[V::N], y1[V::N];
+      if (act0) {
+        V::load(va + off0, x0);
+        V::load(vb + off0, y0);
+      }
+      if (act1) {
+        V::load(va + off1, x1);
+        V::load(vb + off1, y1);
+      }
+      const float a0 = act0 ? sa[row0] : 0.f, b0 = act0 ? sb[row0] : 0.f;
+      const float a1 = act1 ? sa[row1] : 0.f, b1 = act1 ? sb[row1] : 0.f;
+      float wa0, wb0, s0, wa1, wb1, s1;
+      merge2_weights(a0, b0, wa0, wb0, s0);
+      merge2_weights(a1, b1, wa1, wb1, s1);
+      if (act0) {
 #pragma unroll
-      for (int i = 0; i < V::N; ++i) x1[i] = x1[i] * wa + y1[i] * wb;
-      V::store(vo + off1, x1);
-    } else if (active) {
-      for (int c = chunk0; c < cpr; c += cstep) {
-        const int64_t off = (row * cpr + c) * V::N;
-        float x[V::N], y[V::N];
-        V::load(va + off, x);
-        V::load(vb + off, y);
+        for (int i = 0; i < V::N; ++i) x0[i] = x0[i] * wa0 + y0[i] * wb0;
+        V::store(vo + off0, x0);
+        if (chunk0 == 0) so[row0] = s0;
+      }
+      if (act1) {
 #pragma unroll
-        for (int i = 0; i < V::N; ++i) x[i] = x[i] * wa + y[i] * wb;
-        V::store(vo + off, x);
+        for (int i = 0; i < V::N; ++i) x1[i] = x1[i] * wa1 + y1[i] * wb1;
+        V::store(vo + off1, x1);
+        if (chunk0 == 0) so[row1] = s1;
       }
     }
-    __syncwarp();
-    if (active && chunk0 == 0) so[row] = s;
+    return;
+  }
+  for (int64_t r0 = warp * rpw; r0 < rows; r0 += stride) {
+    const int64_t row = r0 + sub_row;
+    if (row >= rows) continue;
+    float wa, wb, s;
+    merge2_weights(sa[row], sb[row], wa, wb, s);
+    for (int c = chunk0; c < cpr; c += cstep) {
+      const int64_t off = (row * cpr + c) * V::N;
+      float x[V::N], y[V::N];
+      V::load(va + off, x);
+      V::load(vb + off, y);
+#pragma unroll
+      for (int i = 0; i < V::N; ++i) x[i] = x[i] * wa + y[i] * wb;
+      V::store(vo + off, x);
+    }
+    if (chunk0 == 0) so[row] = s;
   }
 }
 
@@ -115,6 +144,60 @@ __global__ void __launch_bounds__(256) mergen_kernel(const T* __restrict__ v, co
   const int sub_row = cpr >= 32 ? 0 : lane / cpr;
   const int chunk0 = cpr >= 32 ? lane : lane % cpr;
   const int cstep = cpr >= 32 ? 32 : cpr;
+  // Fast path: one chunk per lane and at most one state per lane of the
+  // row's lane group (cstep lanes, a power of two).  The group's lanes load
+  // the row's LSEs in parallel and reduce their maximum and sum with
+  // shuffles, while the first four states' vector loads are in flight;
+  // each lane then takes the weights from the lanes that own them.
+  const bool fast = cpr <= 32 && n_states <= cstep && (cstep & (cstep - 1)) == 0;
+  if (fast) {
+    const int base = lane - chunk0;  // first lane of this row's group
+    const unsigned gmask = cstep == 32 ? 0xffffffffu : (((1u << cstep) - 1u) << base);
+    for (int64_t r0 = warp * rpw; r0 < rows; r0 += nwarps * rpw) {
+      const int64_t row = r0 + sub_row;
+      const bool active = row < rows;
+      const int64_t t = active ? row / n_heads : 0;
+      const int h = active ? (int)(row % n_heads) : 0;
+      const T* vrow = v + ((t * n_states * n_heads + h) * cpr + chunk0) * V::N;
+      const int64_t vstride = (int64_t)n_heads * cpr * V::N;  // one state further
+      float x[4][V::N];
+      if (active) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (u < n_states) V::load(vrow + u * vstride, x[u]);
+      }
+      const float lse = active && chunk0 < n_states ? s[(t * n_states + chunk0) * n_heads + h] : neg_inf();
+      float m = lse;
+      for (int o = 1; o < cstep; o <<= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, o));
+      const float e = m == neg_inf() ? 0.f : ex2((lse - m) * kLog2e);
+      float den = e;
+      for (int o = 1; o < cstep; o <<= 1) den += __shfl_xor_sync(gmask, den, o);
+      const float w_mine = den > 0.f ? e / den : 0.f;
+      float acc[V::N];
+#pragma unroll
+      for (int k = 0; k < V::N; ++k) acc[k] = 0.f;
+      for (int i = 0; i < n_states; i += 4) {
+        if (i > 0 && active) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (i + u < n_states) V::load(vrow + (i + u) * vstride, x[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float w = __shfl_sync(gmask, w_mine, base + ((i + u) & (cstep - 1)));
+          if (i + u < n_states && m != neg_inf()) {  // an all-empty row stays 0
+#pragma unroll
+            for (int k = 0; k < V::N; ++k) acc[k] += w * x[u][k];
+          }
+        }
+      }
+      if (active) {
+        V::store(vo + (row * cpr + chunk0) * V::N, acc);
+        if (chunk0 == 0) so[row] = m == neg_inf() ? neg_inf() : m + lg2(den) * kLn2;
+      }
+    }
+    return;
+  }
   for (int64_t r0 = warp * rpw; r0 < rows; r0 += nwarps * rpw) {
     const int64_t row = r0 + sub_row;
     const bool active = row < rows;

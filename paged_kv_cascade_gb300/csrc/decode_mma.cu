@@ -362,10 +362,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (wm != 0u) {
       // ---- S^T = K Q^T (16 tokens x 8 heads) ----
-      float sa[4] = {0.f, 0.f, 0.f, 0.f};
+      // two accumulators (even / odd 16-dim steps): half the dependent MMA chain
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (!kFp8) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mma16816<T>(sa, kf[j], qf[j][0], qf[j][1]);
+        for (int j = 0; j < 8; j += 2) {
+          mma16816<T>(sa, kf[j], qf[j][0], qf[j][1]);
+          mma16816<T>(sb, kf[j + 1], qf[j + 1][0], qf[j + 1][1]);
+        }
       } else {
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -373,9 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a0[4] = {e4m3x2_lo(r[0]), e4m3x2_lo(r[1]), e4m3x2_hi(r[0]), e4m3x2_hi(r[1])};
           mma16816<T>(sa, a0, qf[2 * jj][0], qf[2 * jj][1]);
           const uint32_t a1[4] = {e4m3x2_lo(r[2]), e4m3x2_lo(r[3]), e4m3x2_hi(r[2]), e4m3x2_hi(r[3])};
-          mma16816<T>(sa, a1, qf[2 * jj + 1][0], qf[2 * jj + 1][1]);
+          mma16816<T>(sb, a1, qf[2 * jj + 1][0], qf[2 * jj + 1][1]);
         }
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sa[i] += sb[i];
       // ---- online softmax, base 2, lazy reference ----
       const bool ok_lo = (wm >> g) & 1u, ok_hi = (wm >> (g + 8)) & 1u;
       const float s0 = ok_lo ? sa[0] * p.scale_log2 : neg_inf();

@@ -517,13 +517,15 @@ int pkc_set_decode_schedule(int dynamic);
  * decode, which is bound by HBM and saturates it on about 100 SMs.  When
  * every prefix group's K/V tiles are read by two or more 128-row query
  * tiles, the prefix is bound by the tensor pipe rather than HBM, and it
- * gets SMs of its own so that the two stages overlap:
+ * gets SMs of its own so that the two stages overlap.  p_min is the SM
+ * count on which the prefix is expected (at 4.5 TFLOP/s per SM, a
+ * conservative rate, against 6.5 TB/s for the decode) to take at most 0.8
+ * of the decode's time, and at least 16:
  *   - dynamic decode schedule (pkc_set_decode_schedule): a quarter of the
- *     SMs;
- *   - static schedule: the SMs the plan's CTAs leave free, if at least 16.
- * It does so only if, on those SMs, it is expected (at 4.5 TFLOP/s per
- * SM, a conservative rate, against 6.5 TB/s for the decode) to take at
- * most 0.8 of the decode's time.
+ *     SMs, or p_min if that is more, as long as 96 SMs remain for the
+ *     decode;
+ *   - static schedule: the SMs the plan's CTAs leave free, if at least
+ *     p_min.
  * Under the dynamic schedule, with the prefix on fewer than all SMs (also
  * for n > 0), the decode runs one persistent block on each remaining SM, at
  * most one per plan CTA; the two grids together never exceed the SMs.  Those blocks take the plan's chunks from the

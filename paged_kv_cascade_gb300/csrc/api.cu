@@ -296,15 +296,20 @@ std::atomic<int> g_prefix_ctas{0};
 // instead of queueing for SMs.  The two grids together never exceed the SMs: which of
 // the two streams' kernels starts first is not fixed, and a prefix over
 // every SM that started first would hold the decode back.
+// The prefix needs p_min SMs to be expected to finish in 0.8 of the
+// decode's time.
 //  - Dynamic schedule: the decode's persistent blocks take the plan's
-//    chunks from a queue, so their number is free.  If the prefix is
-//    expected to finish before the decode on a quarter of the SMs, it gets
-//    that quarter and the decode the rest (GQA cascade step 319 -> 294 us).
-//  - Static schedule: each decode block runs one plan CTA's list; a prefix
-//    expected to finish first gets the SMs the plan leaves free (>= 16).
+//    chunks from a queue, so their number is free.  The prefix gets a
+//    quarter of the SMs or p_min if that is more, as long as the decode
+//    keeps kMinDecodeSms, and the decode the rest (GQA cascade step 319 ->
+//    294 us on 32 + 120 SMs; three-level GQA cascade 277 -> 246 us on
+//    40 + 112, where 30 prefix SMs outlasted the decode: 317 us).
+//  - Static schedule: each decode block runs one plan CTA's list; the
+//    prefix gets the SMs the plan leaves free if they are at least p_min.
 // Otherwise (a prefix that is itself HBM-bound, a short suffix) the prefix
 // takes every SM and the decode one block per plan CTA.
 constexpr int kMinPrefixSms = 16;
+constexpr int kMinDecodeSms = 96;  // 148 / 100 / 88 decode blocks: 267 / 272 / 284 us
 constexpr double kPrefixFlopsPerSm = 4.5e12;  // tensor-pipe bound prefix, per SM (conservative)
 constexpr double kDecodeBytesPerS = 6.5e12;   // HBM-bound suffix decode
 struct StageSplit {
@@ -319,8 +324,6 @@ StageSplit stage_split(const int32_t* kv_indptr, const int32_t* req_begin, const
   if (forced > 0) return {std::min(forced, sms), next_to_decode && dynamic && forced < sms ? -1 : 0};
   const StageSplit all{sms, 0};
   if (!next_to_decode || !plan_host) return all;
-  const int blocks = dynamic ? sms - (3 * sms) / 4 : sms - plan_host[PKC_PLAN_NUM_CTAS];
-  if (blocks < kMinPrefixSms) return all;
   double flops = 0.0;
   for (int j = 0; j < n_prefix; ++j) {
     const int64_t tokens = kv_indptr[j + 1] - kv_indptr[j];
@@ -333,10 +336,18 @@ StageSplit stage_split(const int32_t* kv_indptr, const int32_t* req_begin, const
   int64_t suffix_tokens = 0;
   const int32_t* kv_len = plan_host + plan_host[PKC_PLAN_OFF_UNIT_KV_LEN];
   for (int u = 0; u < plan_host[PKC_PLAN_N_UNITS]; ++u) suffix_tokens += kv_len[u];
-  const double t_prefix = flops / (blocks * kPrefixFlopsPerSm);
   const double t_decode = (double)suffix_tokens * 2.0 * hkv * PKC_HEAD_DIM * elem_bytes / kDecodeBytesPerS;
-  if (t_prefix <= 0.8 * t_decode) return {blocks, dynamic ? -1 : 0};
-  return all;
+  if (t_decode <= 0.0) return all;
+  const double need = flops / (0.8 * t_decode * kPrefixFlopsPerSm);
+  if (need > sms) return all;
+  const int p_min = std::max(kMinPrefixSms, (int)std::ceil(need));
+  if (dynamic) {
+    const int blocks = std::max(sms - (3 * sms) / 4, p_min);
+    if (blocks > sms - kMinDecodeSms) return all;
+    return {blocks, -1};
+  }
+  const int free_sms = sms - plan_host[PKC_PLAN_NUM_CTAS];
+  return free_sms >= p_min ? StageSplit{free_sms, 0} : all;
 }
 
 void fill_contract_prefix(ContractParams& c, const PrefixSetup& S) {

@@ -543,6 +543,15 @@ int pkc_set_decode_schedule(int dynamic);
  */
 int pkc_set_prefix_ctas(int n);
 
+/*
+ * Diagnostics: the thread-block counts of the prefix kernel and of the
+ * suffix decode in the calling thread's last cascade call
+ * (pkc_cascade_decode, _multilevel, _paged_prefix) that got as far as the
+ * decode launch; 0 and 0 before any.  Host only, no device work.  Returns
+ * PKC_ERR_INVALID_ARG for NULL pointers.
+ */
+int pkc_last_launch_blocks(int* prefix_blocks, int* decode_blocks);
+
 #ifdef __cplusplus
 }
 #endif

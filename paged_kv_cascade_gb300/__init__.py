@@ -59,6 +59,7 @@ SIGNATURES = {
     "pkc_set_decode_kernel": (_I, [_I]),
     "pkc_set_decode_schedule": (_I, [_I]),
     "pkc_set_prefix_ctas": (_I, [_I]),
+    "pkc_last_launch_blocks": (_I, [_c.POINTER(_c.c_int), _c.POINTER(_c.c_int)]),
     "pkc_selftest_wait_timeout": (_I, [_P, _SZ, _c.POINTER(_c.c_int32), _P]),
     "pkc_append_kv": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I64, _I, _P, _SZ, _P]),
     "pkc_cascade_decode_multilevel": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I,
@@ -360,6 +361,13 @@ def set_prefix_ctas(n):
     if n < 0:
         raise ValueError(f"set_prefix_ctas: n must be >= 0 (got {n})")
     _check(lib().pkc_set_prefix_ctas(n))
+
+
+def last_launch_blocks():
+    """(prefix blocks, decode blocks) of this thread's last cascade call."""
+    pb, db = _c.c_int(0), _c.c_int(0)
+    _check(lib().pkc_last_launch_blocks(_c.byref(pb), _c.byref(db)))
+    return pb.value, db.value
 
 
 def paged_decode_state_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, sm_scale,

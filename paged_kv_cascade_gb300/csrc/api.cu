@@ -19,6 +19,8 @@ namespace pkc {
 
 static thread_local char g_err[1024] = "";
 static thread_local cudaEvent_t g_stage_events[4] = {nullptr, nullptr, nullptr, nullptr};
+// Block counts of the calling thread's last cascade call (pkc_last_launch_blocks).
+static thread_local int g_last_prefix_blocks = 0, g_last_decode_blocks = 0;
 
 int set_error(int code, const char* fmt, ...) {
   va_list ap;
@@ -302,7 +304,7 @@ std::atomic<int> g_prefix_ctas{0};
 //    chunks from a queue, so their number is free.  The prefix gets a
 //    quarter of the SMs or p_min if that is more, as long as the decode
 //    keeps kMinDecodeSms, and the decode the rest (GQA cascade step 319 ->
-//    294 us on 32 + 120 SMs; three-level GQA cascade 277 -> 246 us on
+//    294 us on 32 + 120 SMs; three-level GQA cascade 277 -> 254 us on
 //    40 + 112, where 30 prefix SMs outlasted the decode: 317 us).
 //  - Static schedule: each decode block runs one plan CTA's list; the
 //    prefix gets the SMs the plan leaves free if they are at least p_min.
@@ -593,6 +595,13 @@ int pkc_set_decode_schedule(int dynamic) {
   return PKC_OK;
 }
 
+int pkc_last_launch_blocks(int* prefix_blocks, int* decode_blocks) {
+  if (!prefix_blocks || !decode_blocks) return set_error(PKC_ERR_INVALID_ARG, "last_launch_blocks: NULL pointer");
+  *prefix_blocks = g_last_prefix_blocks;
+  *decode_blocks = g_last_decode_blocks;
+  return PKC_OK;
+}
+
 int pkc_set_prefix_ctas(int n) {
   if (n < 0) return set_error(PKC_ERR_INVALID_ARG, "set_prefix_ctas: n must be >= 0 (got %d)", n);
   g_prefix_ctas.store(n);
@@ -758,6 +767,8 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
   dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   dp.status = status;
+  g_last_prefix_blocks = S.pp.n_blocks;
+  g_last_decode_blocks = decode_blocks;
   e = launch_paged_decode(dp, decode_blocks, dtype, dtype, stream);
   if (e) return cuda_error(e, "paged decode launch");
   if (side) {

@@ -104,6 +104,7 @@ def test_fp8_decode_and_kernel_switch_reject_bad_arguments(L):
         assert L.pkc_set_decode_schedule(bad) == 1
     for ok in (0, 1):  # leaves the dynamic schedule set
         assert L.pkc_set_decode_schedule(ok) == 0
+    assert L.pkc_last_launch_blocks(None, None) == 1
     assert L.pkc_set_prefix_ctas(-1) == 1
     for ok in (40, 0):  # leaves the automatic prefix block count set
         assert L.pkc_set_prefix_ctas(ok) == 0

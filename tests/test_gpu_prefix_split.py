@@ -61,6 +61,16 @@ def test_prefix_block_counts_match_oracle(prefix_ctas, gqa, n, schedule, ctas):
     torch.cuda.synchronize()
     assert pkc.device_status(ws) == pkc.PKC_OK
     compare(o, lse, ref_o, ref_lse)
+    # the split the library chose: this prefix (2 row tiles per K/V tile, a
+    # 4 MB K/V, work far below the suffix's) gets a quarter of the SMs next to
+    # a dynamic decode, or the SMs a static plan leaves free
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if n > 0:
+        want_p = n
+    else:
+        want_p = sms - (3 * sms) // 4 if schedule == "dynamic" else sms - ctas
+    want_d = min(ctas, sms - want_p) if schedule == "dynamic" else ctas
+    assert pkc.last_launch_blocks() == (want_p, want_d)
 
 
 def test_automatic_split_same_bits_timed_untimed_and_graph(gqa):

@@ -9,13 +9,14 @@ count changes how the flattened KV tiles are cut into pieces, so the states
 must match the oracle for every count, and a call must give the same bits
 timed (stage events, stages in order), untimed (side stream) and replayed
 from a CUDA graph."""
+import numpy as np
 import pytest
 import torch
 
 import oracle
 import paged_kv_cascade_gb300 as pkc
 import workloads
-from pkc_testing import compare, oracle_args, to_device, workspace_for
+from pkc_testing import compare, dev, oracle_args, to_device, workspace_for
 
 pytestmark = pytest.mark.gpu
 
@@ -124,6 +125,36 @@ def test_multilevel_with_capped_prefix_blocks(prefix_ctas, n):
         d["v_cache"], d["block_table"], d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf)
     torch.cuda.synchronize()
     assert pkc.device_status(ws) == pkc.PKC_OK
+    a = oracle_args(p)
+    a.pop("prefix_req_indptr")
+    ref_o, ref_lse = oracle.attention_rows(p["q"], prefix_req_ranges=ranges, **a)
+    compare(o, lse, ref_o, ref_lse)
+
+
+@pytest.mark.parametrize("n", [0, 7])
+def test_paged_prefix_with_split_blocks(prefix_ctas, n):
+    # prefixes kept in the page pool (NaN past their ends): a 700-token prompt
+    # for 40 requests x 4 heads (2 row tiles per KV head), then 150 tokens for
+    # the first half; a dynamic decode over 148 plan CTAs
+    lens = [int(x) for x in (np.random.default_rng(93).integers(0, 1500, size=40))]
+    p = workloads.make_problem(batch=40, hq=32, hkv=8, d=128, dtype="bf16",
+                               prefix_lens=[700, 150], prefix_groups=[1, 1],
+                               suffix=("list", lens), page_size=16, seed=93, poison=True)
+    kc, vc, pages, page_indptr = workloads.pool_prefixes(p, 93)
+    ranges = [(0, 40), (0, 20)]
+    prefix_ctas(n)
+    d = to_device(p)
+    buf = pkc.plan(p["cache_seqlens"], PLAN_CTAS)
+    ws = workspace_for(pkc, p, num_ctas=PLAN_CTAS)
+    pkc.plan_upload(buf, ws)
+    o, lse = pkc.cascade_decode_paged_prefix(
+        d["q"], dev(pages), page_indptr, p["prefix_kv_indptr"], ranges, dev(kc), dev(vc),
+        d["block_table"], d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf)
+    torch.cuda.synchronize()
+    assert pkc.device_status(ws) == pkc.PKC_OK
+    if n > 0:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert pkc.last_launch_blocks() == (n, min(PLAN_CTAS, sms - n))
     a = oracle_args(p)
     a.pop("prefix_req_indptr")
     ref_o, ref_lse = oracle.attention_rows(p["q"], prefix_req_ranges=ranges, **a)

@@ -832,6 +832,7 @@ def main():
                        "decode_schedule": args.decode_schedule if num_ctas else None,
                        "prefix_ctas": args.prefix_ctas or "auto",
                        "parallelism": f"replicas x{world}"},
+            "stage_split": dict(zip(("prefix_blocks", "decode_blocks"), pkc.last_launch_blocks())),
             "direct_us_per_step": 1e3 * direct_ms_per_step,
             "hbm_fraction": value / world / hbm_peak,
             "stages_us": {k: 1e3 * v for k, v in stage_ms.items()},

@@ -512,28 +512,34 @@ int pkc_set_decode_schedule(int dynamic);
  * pkc_prefix_attention_state, process-wide.
  *   - n > 0: at most n blocks (one per SM).
  *   - n = 0 (the default): automatic.
- * In automatic mode the prefix takes every SM, except in a cascade call
- * with a plan.  There the prefix runs on a side stream next to the suffix
- * decode, which is bound by HBM and saturates it on about 100 SMs.  When
- * every prefix group's K/V tiles are read by two or more 128-row query
- * tiles, the prefix is bound by the tensor pipe rather than HBM, and it
- * gets SMs of its own so that the two stages overlap.  p_min is the SM
- * count on which the prefix is expected (at 4.5 TFLOP/s per SM, a
- * conservative rate, against 6.5 TB/s for the decode) to take at most 0.8
- * of the decode's time, and at least 16:
- *   - dynamic decode schedule (pkc_set_decode_schedule): a quarter of the
- *     SMs, or p_min if that is more, as long as 96 SMs remain for the
- *     decode;
- *   - static schedule: the SMs the plan's CTAs leave free, if at least
- *     p_min.
- * Under the dynamic schedule, with the prefix on fewer than all SMs (also
- * for n > 0), the decode runs one persistent block on each remaining SM, at
- * most one per plan CTA; the two grids together never exceed the SMs.  Those blocks take the plan's chunks from the
- * shared queue, so the chunks stay those of the plan.  Any prefix block
- * count is then lowered, to no less than 3/4 of it, to the largest value
- * at which the query row tiles sharing a K/V tile are computed by different
- * blocks at the same moment, so that the second read of the tile hits L2
- * (for groups whose K/V exceeds 16 MB; smaller ones stay in L2).
+ *
+ * Automatic mode.  The prefix takes every SM, except in a cascade call with
+ * a plan.  There the prefix runs on a side stream next to the suffix decode,
+ * which is bound by HBM and saturates it on about 100 SMs.  When every
+ * prefix group's K/V tiles are read by two or more 128-row query tiles, the
+ * prefix is bound by the tensor pipe rather than HBM.  It then gets SMs of
+ * its own, so that the two stages overlap.  Let p_min be the SM count on
+ * which the prefix is expected to take at most 0.8 of the decode's time,
+ * and at least 16; the estimate uses 4.5 TFLOP/s per SM (a conservative
+ * rate) against 6.5 TB/s for the decode.
+ *   - Dynamic decode schedule (pkc_set_decode_schedule): the prefix gets a
+ *     quarter of the SMs, or p_min if that is more, as long as 96 SMs remain
+ *     for the decode.
+ *   - Static schedule: the prefix gets the SMs the plan's CTAs leave free,
+ *     if at least p_min.
+ *
+ * Decode blocks.  Under the dynamic schedule, with the prefix on fewer than
+ * all SMs (also for n > 0), the decode runs one persistent block on each
+ * remaining SM, at most one per plan CTA.  The two grids together never
+ * exceed the SMs.  Those blocks take the plan's chunks from the shared
+ * queue, so the chunks stay those of the plan.
+ *
+ * Alignment.  Any prefix block count is then lowered, to no less than 3/4
+ * of it, to the largest value at which the query row tiles sharing a K/V
+ * tile are computed by different blocks at the same moment.  The second
+ * read of each such tile then hits L2.  Only groups whose K/V exceeds 16 MB
+ * count; smaller ones stay in L2.
+ *
  * A timed call (pkc_set_stage_events) keeps the same split.  The states are
  * the same for any block count up to rounding: the prefix's pieces, and so
  * its partial states, depend on it.

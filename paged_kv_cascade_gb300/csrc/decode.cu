@@ -540,6 +540,37 @@ __global__ void __launch_bounds__(256, 4) contract_kernel(const ContractParams p
       if (in_group(j)) return j;
     return -1;
   };
+  // Pieces of group j's pair holding this row: count and first partial slot.
+  auto group_pieces = [&](int j, int& n_pref, int& base) {
+    n_pref = 0;
+    base = 0;
+    if (j < 0) return;
+    const int kvt = (p.prefix_kv_indptr[j + 1] - p.prefix_kv_indptr[j] + 127) / 128;
+    if (kvt > 0 && p.prefix_tiles > 0) {
+      const int rr = (req - p.prefix_req_begin[j]) * p.g + h % p.g;  // row within the group's rows
+      const int pair = (rr / 128) * p.hkv + h / p.g;
+      // block_of(x) = ((x + 1) C - 1) / T, in 32 bits (the host keeps T C < 2^31)
+      const int a = p.prefix_kvt_indptr[j] + pair * kvt;
+      const int T = (int)p.prefix_tiles, C = p.prefix_blocks;
+      n_pref = ((a + kvt) * C - 1) / T - ((a + 1) * C - 1) / T + 1;
+      base = p.prefix_slot_base[j];
+    }
+  };
+  auto prefix_lse = [&](int slot) { return p.prefix_lse + (int64_t)slot * p.prefix_stride_lse + row_off; };
+  auto prefix_o = [&](int slot) { return p.prefix_o + (int64_t)slot * p.prefix_stride_o + row_off * D; };
+  // The first group's first batch of prefix pieces depends on no plan word:
+  // its loads go out before the plan's words are read, so both arrive in
+  // one memory round trip.
+  int j = next_group(-1), n_pref = 0, base = 0;
+  group_pieces(j, n_pref, base);
+  float ls[kB];
+  float4 xs[kB];
+#pragma unroll
+  for (int k = 0; k < kB; ++k) {
+    const bool in = k < n_pref;
+    ls[k] = in ? *prefix_lse(base + k) : neg_inf();
+    xs[k] = in ? *reinterpret_cast<const float4*>(prefix_o(base + k) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   int suf_kind = 0, suf_begin = 0, suf_n = 0;  // 1: direct state, 2: partial slots
   if (pl) {
     const int nch = pl[p.off_unit_n_chunks + unit];       // both loads in flight together
@@ -549,42 +580,30 @@ __global__ void __launch_bounds__(256, 4) contract_kernel(const ContractParams p
   } else if (p.suffix_o) {
     suf_kind = 1; suf_n = 1;
   }
-  for (int j = next_group(-1);;) {
-    int n_pref = 0, base = 0;
-    if (j >= 0) {
-      const int kvt = (p.prefix_kv_indptr[j + 1] - p.prefix_kv_indptr[j] + 127) / 128;
-      if (kvt > 0 && p.prefix_tiles > 0) {
-        const int rr = (req - p.prefix_req_begin[j]) * p.g + h % p.g;  // row within the group's rows
-        const int pair = (rr / 128) * p.hkv + h / p.g;
-        // block_of(x) = ((x + 1) C - 1) / T, in 32 bits (the host keeps T C < 2^31)
-        const int a = p.prefix_kvt_indptr[j] + pair * kvt;
-        const int T = (int)p.prefix_tiles, C = p.prefix_blocks;
-        n_pref = ((a + kvt) * C - 1) / T - ((a + 1) * C - 1) / T + 1;
-        base = p.prefix_slot_base[j];
-      }
-    }
+  bool preloaded = true;  // ls / xs hold the first batch's prefix pieces
+  for (;;) {
     const int jn = j >= 0 ? next_group(j) : -1;
     const int n_suf = jn < 0 ? suf_n : 0;  // the last pass takes the suffix
     const int n_src = n_pref + n_suf;
     auto src_lse = [&](int i) -> const float* {
-      if (i < n_pref) return p.prefix_lse + (int64_t)(base + i) * p.prefix_stride_lse + row_off;
+      if (i < n_pref) return prefix_lse(base + i);
       if (suf_kind == 1) return p.suffix_lse + row_off;
       return p.part_lse + (int64_t)(suf_begin + i - n_pref) * p.hq + h;
     };
     auto src_o = [&](int i) -> const float* {
-      if (i < n_pref) return p.prefix_o + (int64_t)(base + i) * p.prefix_stride_o + row_off * D;
+      if (i < n_pref) return prefix_o(base + i);
       if (suf_kind == 1) return p.suffix_o + row_off * D;
       return p.part_o + ((int64_t)(suf_begin + i - n_pref) * p.hq + h) * D;
     };
     for (int i0 = 0; i0 < n_src; i0 += kB) {
-      float ls[kB];
-      float4 xs[kB];
 #pragma unroll
       for (int k = 0; k < kB; ++k) {
+        if (preloaded && k < n_pref) continue;  // loaded before the plan's words
         const bool in = i0 + k < n_src;
         ls[k] = in ? *src_lse(i0 + k) : neg_inf();
         xs[k] = in ? *reinterpret_cast<const float4*>(src_o(i0 + k) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      preloaded = false;
       float mb = m;
 #pragma unroll
       for (int k = 0; k < kB; ++k) mb = fmaxf(mb, ls[k]);
@@ -601,8 +620,10 @@ __global__ void __launch_bounds__(256, 4) contract_kernel(const ContractParams p
       }
       m = mb;
     }
+    preloaded = false;
     if (jn < 0) break;
     j = jn;
+    group_pieces(j, n_pref, base);
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;

@@ -9,7 +9,7 @@ import torch
 import oracle
 import paged_kv_cascade_gb300 as pkc
 import workloads
-from pkc_testing import compare, oracle_args, sample_rows, to_device, workspace_for
+from pkc_testing import compare, dev, oracle_args, sample_rows, to_device, workspace_for
 
 pytestmark = pytest.mark.gpu
 
@@ -120,6 +120,55 @@ def test_gqa_cascade_lb_workload_sampled():
     lens = p["cache_seqlens"]
     extra = [(int(b), 0) for b in np.argsort(-lens)[:6]]
     rows = np.unique(np.concatenate([rows, np.array(extra, np.int32)]), axis=0)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], rows=rows, **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse, rows=rows)
+
+
+def test_gqa_cascade_3level_workload_sampled():
+    """The three-level workload as the benchmark runs it: its prefix (8 and 2
+    row tiles per K/V tile) gets SMs of its own next to the decode."""
+    w = workloads.WORKLOADS["gqa_cascade_3level"]
+    p = workloads.workload("gqa_cascade_3level")
+    d = to_device(p)
+    C = w["num_ctas"]
+    buf = pkc.plan(p["cache_seqlens"], C)
+    ws = workspace_for(pkc, p, num_ctas=C)
+    pkc.plan_upload(buf, ws)
+    o, lse = pkc.cascade_decode_multilevel(
+        d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"], w["prefix_ranges"], d["k_cache"],
+        d["v_cache"], d["block_table"], d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf)
+    torch.cuda.synchronize()
+    assert pkc.device_status(ws) == pkc.PKC_OK
+    pb, db = pkc.last_launch_blocks()
+    assert pb + db <= torch.cuda.get_device_properties(0).multi_processor_count
+    B, Hq, _ = p["q"].shape
+    rows = sample_rows(B, Hq, 128, seed=7)
+    a = oracle_args(p)
+    a.pop("prefix_req_indptr")
+    ref_o, ref_lse = oracle.attention_rows(p["q"], rows=rows, prefix_req_ranges=w["prefix_ranges"], **a)
+    compare(o, lse, ref_o, ref_lse, rows=rows)
+
+
+def test_gqa_cascade_paged_prefix_workload_sampled():
+    """gqa_cascade_lb with its four 8192-token prefixes kept in the page pool
+    (NaN past their ends) and read in place, as the benchmark line runs it."""
+    w = workloads.WORKLOADS["gqa_cascade_lb"]
+    p = workloads.workload("gqa_cascade_lb")
+    kc, vc, pages, page_indptr = workloads.pool_prefixes(p, 5, poison=True)
+    d = to_device(p)
+    ind = p["prefix_req_indptr"]
+    ranges = [(int(ind[j]), int(ind[j + 1])) for j in range(len(ind) - 1)]
+    C = w["num_ctas"]
+    buf = pkc.plan(p["cache_seqlens"], C)
+    ws = workspace_for(pkc, p, num_ctas=C)
+    pkc.plan_upload(buf, ws)
+    o, lse = pkc.cascade_decode_paged_prefix(
+        d["q"], dev(pages), page_indptr, p["prefix_kv_indptr"], ranges, dev(kc), dev(vc),
+        d["block_table"], d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf)
+    torch.cuda.synchronize()
+    assert pkc.device_status(ws) == pkc.PKC_OK
+    B, Hq, _ = p["q"].shape
+    rows = sample_rows(B, Hq, 128, seed=8)
     ref_o, ref_lse = oracle.attention_rows(p["q"], rows=rows, **oracle_args(p))
     compare(o, lse, ref_o, ref_lse, rows=rows)
 

@@ -12,8 +12,16 @@ suffix lengths clip(rint(lognormal(7, 1)), 16, 16384) (440,093 tokens at
 seed 5), plan over 148 CTAs with alpha = beta = 1.  One step reads 1.94 GB,
 more than the 129 MB L2, so no flush is needed between steps.
 
-Prints one JSON line (rank 0).  `--impl reference` times the float64 CPU
-oracle instead, on bounded samples of the same workload.
+Prints one JSON line (rank 0).  Besides the headline step it carries, timed
+in the same process with their own clock records: the pages' static CTA
+assignment next to the default dynamic queue, and (`configs`) every other
+workload of the set -- the tiny cascade, the binary and 16-ary merge, the
+non-cascade paged decode, the long-prompt cascade with the non-cascade
+decode of the same problem, the fp8-KV decode, the three-level and the
+paged-prefix cascades, and a batch / prefix / suffix sweep of cascade
+against non-cascade decode.  `--workload X` prints X's entry alone.
+`--impl reference` times the float64 CPU oracle instead, on bounded samples
+of the same workload.
 """
 from __future__ import annotations
 
@@ -47,9 +55,10 @@ def parse_args():
                     choices=["gqa_cascade_lb", "cascade_long_prompt", "tiny_cascade",
                              "paged_decode", "paged_decode_gqa", "paged_decode_fp8", "merge",
                              "gqa_cascade_3level", "gqa_cascade_paged_prefix"],
-                    help="cascade workloads time the whole step; 'paged_decode*' time the "
-                         "non-cascade decode (fp16 MHA, fp16 GQA, fp8-KV GQA) and 'merge' the "
-                         "binary / 16-ary merge kernels (auxiliary lines)")
+                    help="headline cascade workload (gqa_cascade_lb, cascade_long_prompt, "
+                         "tiny_cascade), or one other workload printed alone: 'paged_decode*' "
+                         "(fp16 MHA, fp16 GQA, fp8-KV GQA), 'merge', the 3-level and "
+                         "paged-prefix cascades")
     ap.add_argument("--decode-kernel", choices=["auto", "simt", "mma"], default="auto",
                     help="paged-decode kernel for a 16-bit cache (auto: tensor cores for "
                          "grouped heads)")
@@ -67,6 +76,10 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' entries (`configs`) in the headline line")
+    ap.add_argument("--config-seconds", type=float, default=0.5,
+                    help="least timed device time per workload entry")
     return ap.parse_args()
 
 
@@ -264,15 +277,42 @@ def cpu_oracle_sample(p, target_s, rows_total_cap=None, n_threads=0):
     return n2, B * Hq, t, threads
 
 
+def line_config(name, cfg, p, num_ctas, args, world, extra=None):
+    """The `config` object of a JSON line: the same keys for both arms."""
+    B, Hq, D = p["q"].shape
+    c = {"workload": name, "batch": B, "num_qo_heads": Hq, "num_kv_heads": p["num_kv_heads"],
+         "head_dim": D, "page_size": cfg["page_size"], "prefix_lens": list(cfg["prefix_lens"]),
+         "suffix_tokens": int(p["cache_seqlens"].sum()), "num_ctas": num_ctas or None,
+         "plan": "host plan over num_ctas CTAs" if num_ctas else
+                 "none: one decode block per (request, KV-head group)",
+         "effective_bytes_per_step": workloads.effective_bytes(p),
+         "l2": ("inputs larger than L2 (one step reads %.2f GB)" % (workloads.effective_bytes(p) / 1e9)
+                if workloads.effective_bytes(p) > 129e6 else
+                "inputs fit in L2 (%.1f MB), no flush: a launch-bound workload, read in us" %
+                (workloads.effective_bytes(p) / 1e6)),
+         "parallelism": f"replicas x{world}"}
+    if extra:
+        c.update(extra)
+    return c
+
+
 def run_reference(args):
+    """The reference arm: the float64 CPU oracle, as it stands, on the host
+    cores.  Each timed step computes a bounded sample of the step's
+    (request, head) rows; `value` is the rows' share of the step's effective
+    bytes over the measured time, and `ms_per_step` the measured time of the
+    sampled step (not an extrapolation)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     import oracle
     oracle.build()
     cfg, p = make_workload(args.workload, args.batch)
+    if args.num_ctas is not None:
+        cfg["num_ctas"] = args.num_ctas
     eff = workloads.effective_bytes(p)
-    per_step_s = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    # the whole --steps/--warmup run within about 100 s of oracle time
+    per_step_s = max(0.5, min(10.0, 100.0 / max(1, args.steps + args.warmup)))
     times, fracs = [], []
     n_rows = total = threads = 0
     for i in range(args.warmup + args.steps):
@@ -280,180 +320,392 @@ def run_reference(args):
         if i >= args.warmup:
             times.append(t)
             fracs.append(n_rows / total)
-    # seconds for one full step, extrapolated from each sampled fraction
-    full = [t / f for t, f in zip(times, fracs)]
-    ms = 1e3 * sum(full) / len(full)
-    value = eff / (ms / 1e3) / 1e9
+    secs = sum(times)
+    value = sum(eff * f for f in fracs) / secs / 1e9
+    ms = 1e3 * secs / len(times)
     line = {
         "impl": "reference",
         "metric": "cascade decode effective KV throughput",
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "batch": cfg["batch"],
-                   "num_qo_heads": cfg["hq"], "num_kv_heads": cfg["hkv"], "head_dim": cfg["d"],
-                   "page_size": cfg["page_size"], "prefix_lens": cfg["prefix_lens"],
-                   "suffix_tokens": int(p["cache_seqlens"].sum()), "parallelism": "replicas"},
+        "config": line_config(args.workload, cfg, p, cfg["num_ctas"], args, world,
+                              {"step": "a sample of the step's (request, head) rows, "
+                                       "every prefix and suffix token of each"}),
+        "sample_fraction": statistics.mean(fracs),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{n_rows} of {total} (request, head) rows per step, "
-                                   "extrapolated to the full step"},
+                                   f"{args.steps} timed steps; value = the sampled rows' share "
+                                   "of the effective bytes over the measured time"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def time_region(torch, fn, steps, warmup):
-    """Mean ms of fn() over `steps` launches, CUDA events on the current stream."""
-    for _ in range(warmup):
+class GraphStepper:
+    """One step = host plan + its upload + the device work replayed from a
+    CUDA graph (how the pages run it: the plan per step on the CPU, copied
+    in asynchronously, the captured run replayed).
+
+    Two workspaces and two captured graphs alternate.  The plan of step i+1
+    is computed and uploaded (on a copy stream) while step i runs, so the
+    device never waits for the host; a workspace's plan is overwritten only
+    after the graph that read it has run, and a pinned plan buffer only
+    after its previous upload has run.  With no plan, a step is one replay.
+
+    run(workspace, plan_buf, stream) issues the device work of one step.
+    """
+
+    def __init__(self, torch, pkc, run, lens, num_ctas, cfg, ws_bytes, device):
+        self.torch, self.pkc, self.lens, self.num_ctas, self.cfg = torch, pkc, lens, num_ctas, cfg
+        self.stream, self.cstream = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        words = pkc.plan_words(len(lens), num_ctas) if num_ctas else 1
+        self.pinned = [torch.empty(words, dtype=torch.int32).pin_memory() for _ in range(2)]
+        self.plan_np = [t.numpy() for t in self.pinned]
+        self.ws = [torch.empty(ws_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+        for w in self.ws:
+            pkc.workspace_init(w)
+        self.done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.uploaded = [torch.cuda.Event(), torch.cuda.Event()]
+        self.graphs = []
+        with torch.cuda.stream(self.stream):
+            for s in range(2):
+                buf = host_plan(pkc, lens, num_ctas, cfg, out=self.plan_np[s])
+                upload_plan(pkc, buf, self.ws[s], stream=self.stream)
+                run(self.ws[s], buf, self.stream)  # eager first: kernels loaded, maps built
+                self.stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    run(self.ws[s], buf, self.stream)
+                self.graphs.append(g)
+        for e in self.done + self.uploaded:
+            e.record(self.stream)
+        self.stream.synchronize()
+        self.i = 0
+        self._prepare(0)
+
+    def _prepare(self, i):
+        if not self.num_ctas:
+            return
+        s = i & 1
+        self.uploaded[s].synchronize()
+        buf = host_plan(self.pkc, self.lens, self.num_ctas, self.cfg, out=self.plan_np[s])
+        self.cstream.wait_event(self.done[s])
+        upload_plan(self.pkc, buf, self.ws[s], stream=self.cstream)
+        self.uploaded[s].record(self.cstream)
+
+    def step(self):
+        s = self.i & 1
+        with self.torch.cuda.stream(self.stream):
+            if self.num_ctas:
+                self.stream.wait_event(self.uploaded[s])
+            self.graphs[s].replay()
+            self.done[s].record(self.stream)
+        self._prepare(self.i + 1)
+        self.i += 1
+
+    def status_ok(self):
+        return all(self.pkc.device_status(w) == 0 for w in self.ws)
+
+
+def time_loop(ctx, fn, stream, min_steps, min_seconds=None):
+    """Mean ms per call of fn() (which issues its work on `stream`), timed
+    with CUDA events on that stream over max(min_steps, enough calls for
+    min_seconds), with nvidia-smi clock samples taken meanwhile.  Warm-up
+    keeps the GPU busy for ~0.3 s first, so the samples are taken under load."""
+    torch = ctx.torch
+    min_seconds = ctx.config_seconds if min_seconds is None else min_seconds
+    sampler = ClockSampler(ctx.gpu_id)
+    sampler.start()
+    for _ in range(max(3, ctx.warmup)):
         fn()
-    torch.cuda.synchronize()
+    stream.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
+    a.record(stream)
+    fn()
+    b.record(stream)
+    stream.synchronize()
+    t1 = max(a.elapsed_time(b) / 1e3, 1e-6)
+    for _ in range(int(math.ceil(0.3 / t1))):
         fn()
-    b.record()
-    torch.cuda.synchronize()
-    return a.elapsed_time(b) / steps
+    n = max(min_steps, int(math.ceil(min_seconds / t1)))
+    a.record(stream)
+    for _ in range(n):
+        fn()
+    b.record(stream)
+    stream.synchronize()
+    clocks = sampler.stop()
+    return a.elapsed_time(b) / n, n, clocks
 
 
-def run_aux(args):
-    """Auxiliary single-kernel lines: merge kernels, non-cascade decode."""
-    import torch
-    import __graft_entry__
-    __graft_entry__.build()
-    import paged_kv_cascade_gb300 as pkc
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from pkc_testing import dev, to_device
-    hbm_peak, _, peak_kind = load_peaks()
-    K, W = max(args.steps, 3), max(args.warmup, 3)
-    if args.workload == "merge":
-        w = workloads.workload("merge")
-        va, sa, vb, sb = dev(w["v_a"]), dev(w["s_a"]), dev(w["v_b"]), dev(w["s_b"])
-        vn, sn = dev(w["v_n"]), dev(w["s_n"])
-        vo, so = torch.empty_like(va), torch.empty_like(sa)
-        T, H, D = va.shape
-        n = vn.shape[1]
-        ms2 = time_region(torch, lambda: pkc.merge_state(va, sa, vb, sb, vo, so), K, W)
-        msn = time_region(torch, lambda: pkc.merge_states(vn, sn, vo, so), K, W)
-        b2 = 3 * T * H * (D + 1) * 4       # read 2 states, write 1
-        bn = (n + 1) * T * H * (D + 1) * 4  # read n states, write 1
-        line = {"metric": "merge_state effective HBM throughput", "unit": "GB/s",
-                "value": b2 / (ms2 / 1e3) / 1e9, "us": 1e3 * ms2, "bytes": b2,
-                "frac": b2 / (ms2 / 1e3) / 1e9 / hbm_peak,
-                "n_ary": {"n": n, "value": bn / (msn / 1e3) / 1e9, "us": 1e3 * msn, "bytes": bn,
-                          "frac": bn / (msn / 1e3) / 1e9 / hbm_peak},
-                "peak": hbm_peak, "peak_source": f"{peak_kind} hbm_gbs", "steps": K, "warmup": W,
-                "dtype": "f32", "data": "synthetic",
-                "config": {"workload": "merge", "tokens": T, "heads": H, "head_dim": D,
-                           "l2": "inputs larger than L2 (203 MB / 1.15 GB)"}}
-    else:  # paged_decode*: non-cascade decode through the plan
-        cfg = workload_cfg(args.workload)
-        if args.num_ctas is not None:
-            cfg["num_ctas"] = args.num_ctas
-        p = workloads.make_problem(**cfg)
-        d = to_device(p)
-        fp8 = p["kv_dtype"] == "e4m3"
-        pkc.set_decode_kernel(args.decode_kernel)
-        pkc.set_decode_schedule(args.decode_schedule)
-        B, Hq, D = p["q"].shape
-        C = cfg["num_ctas"]
-        ws = torch.empty(pkc.workspace_size(B, Hq, C, 0), dtype=torch.uint8, device="cuda")
-        pkc.workspace_init(ws)
-        buf = pkc.plan(p["cache_seqlens"], C)
-        pkc.plan_upload(buf, ws)
-        o = torch.empty_like(d["q"])
-        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
-        if fp8:
-            call = lambda: pkc.paged_decode_state_fp8(
-                d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"],
-                p["sm_scale"], ws, k_scale=p["k_scale"], v_scale=p["v_scale"], plan_buf=buf,
-                o=o, lse=lse)
-        else:
-            call = lambda: pkc.paged_decode_state(
-                d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"],
-                p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse)
-        ms = time_region(torch, call, K, W)
-        if pkc.device_status(ws) != 0:
-            raise RuntimeError("device status not OK")
-        eff = workloads.effective_bytes(p)
-        line = {"metric": "paged decode (non-cascade) effective KV throughput", "unit": "GB/s",
-                "value": eff / (ms / 1e3) / 1e9, "us": 1e3 * ms, "bytes": eff,
-                "frac": eff / (ms / 1e3) / 1e9 / hbm_peak, "peak": hbm_peak,
-                "peak_source": f"{peak_kind} hbm_gbs", "steps": K, "warmup": W,
-                "dtype": cfg["dtype"], "data": "synthetic",
-                "config": {"workload": args.workload, "batch": B, "num_qo_heads": Hq,
-                           "num_kv_heads": p["num_kv_heads"], "kv_dtype": p["kv_dtype"],
-                           "kv_tokens": int(p["cache_seqlens"].sum()), "num_ctas": C,
-                           "decode_kernel": "mma" if fp8 else args.decode_kernel,
-                           "decode_schedule": args.decode_schedule,
-                           "launches": "decode + contraction"}}
-    print(json.dumps(line), flush=True)
+def _gbs(nbytes, ms):
+    return nbytes / (ms / 1e3) / 1e9
 
 
-def run_cascade_variant(args):
-    """Auxiliary cascade lines: the three-level cascade, and the two-level
-    cascade with its prefixes read in place from the page pool (timed beside
-    the contiguous-prefix call on the same tokens)."""
-    import torch
-    import __graft_entry__
-    __graft_entry__.build()
-    import paged_kv_cascade_gb300 as pkc
-    pkc.set_prefix_ctas(args.prefix_ctas)
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from pkc_testing import dev, to_device
-    hbm_peak, _, peak_kind = load_peaks()
-    K, W = max(args.steps, 3), max(args.warmup, 3)
-    paged = args.workload == "gqa_cascade_paged_prefix"
-    cfg = workload_cfg("gqa_cascade_lb" if paged else args.workload)
-    if args.num_ctas is not None:
-        cfg["num_ctas"] = args.num_ctas
-    p = workloads.make_problem(**cfg)
-    d = to_device(p)
-    B, Hq, D = p["q"].shape
-    C = cfg["num_ctas"]
-    ws = torch.empty(pkc.workspace_size(B, Hq, C, 64), dtype=torch.uint8, device="cuda")
-    pkc.workspace_init(ws)
-    buf = pkc.plan(p["cache_seqlens"], C)
-    pkc.plan_upload(buf, ws)
+def _entry(ctx, nbytes, ms, n, clocks, **kw):
+    e = {"us_per_step": 1e3 * ms, "value": _gbs(nbytes, ms), "unit": "GB/s",
+         "frac": _gbs(nbytes, ms) / ctx.hbm_peak, "effective_bytes": int(nbytes), "steps": n,
+         "clocks": clocks}
+    e.update(kw)
+    return e
+
+
+def cascade_call(pkc, name, p, d, extra):
+    """run(ws, plan_buf, stream) for a cascade workload, writing into
+    preallocated O / LSE."""
+    torch = extra["torch"]
+    B, Hq, _ = d["q"].shape
     o = torch.empty_like(d["q"])
-    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
-    eff = workloads.effective_bytes(p)
-    extra = {}
-    if paged:
-        kc, vc, pages, page_indptr = workloads.pool_prefixes(p, 5, poison=False)
-        kc, vc, pages = dev(kc), dev(vc), dev(pages)
-        ind = p["prefix_req_indptr"]
-        ranges = [(int(ind[j]), int(ind[j + 1])) for j in range(len(ind) - 1)]
-        call = lambda: pkc.cascade_decode_paged_prefix(
-            d["q"], pages, page_indptr, p["prefix_kv_indptr"], ranges, kc, vc, d["block_table"],
-            d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse)
-        ms_contig = time_region(torch, lambda: pkc.cascade_decode(
-            d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"], p["prefix_req_indptr"],
-            d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"], p["sm_scale"], ws,
-            plan_buf=buf, o=o, lse=lse), K, W)
-        extra = {"contiguous_prefix_us": 1e3 * ms_contig,
-                 "contiguous_prefix_value": eff / (ms_contig / 1e3) / 1e9}
-        metric = "cascade decode effective KV throughput, prefix read from the page pool"
-    else:
-        ranges = cfg["prefix_ranges"]
-        call = lambda: pkc.cascade_decode_multilevel(
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=d["q"].device)
+    if name == "gqa_cascade_3level":
+        ranges = extra["cfg"]["prefix_ranges"]
+        return lambda ws, buf, st: pkc.cascade_decode_multilevel(
             d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"], ranges, d["k_cache"],
             d["v_cache"], d["block_table"], d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf,
-            o=o, lse=lse)
-        metric = "three-level cascade decode effective KV throughput"
-    ms = time_region(torch, call, K, W)
+            o=o, lse=lse, stream=st)
+    if name == "gqa_cascade_paged_prefix":
+        pool_k, pool_v, pages, page_indptr = extra["pool"]
+        ind = p["prefix_req_indptr"]
+        ranges = [(int(ind[j]), int(ind[j + 1])) for j in range(len(ind) - 1)]
+        return lambda ws, buf, st: pkc.cascade_decode_paged_prefix(
+            d["q"], pages, page_indptr, p["prefix_kv_indptr"], ranges, pool_k, pool_v,
+            d["block_table"], d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse,
+            stream=st)
+    return lambda ws, buf, st: pkc.cascade_decode(
+        d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"], p["prefix_req_indptr"],
+        d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"], p["sm_scale"], ws,
+        plan_buf=buf, o=o, lse=lse, stream=st)
+
+
+def stage_times(ctx, run, ws, buf, steps):
+    """Per-stage times (prefix, decode, contraction), launched one after the
+    other with stage events on the current stream; plan uploaded once."""
+    torch, pkc = ctx.torch, ctx.pkc
+    stream = torch.cuda.current_stream()
+    upload_plan(pkc, buf, ws, stream=stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for _ in range(3):
+        run(ws, buf, stream)
+    for e in ev:
+        pkc.set_stage_events(e)
+        run(ws, buf, stream)
+    torch.cuda.synchronize()
     if pkc.device_status(ws) != 0:
-        raise RuntimeError("device status not OK")
-    line = {"metric": metric, "unit": "GB/s", "value": eff / (ms / 1e3) / 1e9, "us": 1e3 * ms,
-            "bytes": eff, "frac": eff / (ms / 1e3) / 1e9 / hbm_peak, "peak": hbm_peak,
-            "peak_source": f"{peak_kind} hbm_gbs", "steps": K, "warmup": W, "dtype": cfg["dtype"],
-            "data": "synthetic", "launch": "direct (prefix, decode, contraction)",
-            "config": {"workload": args.workload, "batch": B, "num_qo_heads": Hq,
-                       "num_kv_heads": p["num_kv_heads"], "prefix_lens": cfg["prefix_lens"],
-                       "prefix_ranges": ranges, "suffix_tokens": int(p["cache_seqlens"].sum()),
-                       "num_ctas": C}}
-    line.update(extra)
-    print(json.dumps(line), flush=True)
+        raise RuntimeError("device status not OK in the stage-timed run")
+    names = ("prefix_state", "paged_decode", "contraction")
+    return {k: 1e3 * statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev)
+            for i, k in enumerate(names)}
+
+
+def measure_cascade(ctx, name, stage_steps=10):
+    """A cascade workload, graph-replayed steps with the plan per step, plus
+    its stage times launched one after the other."""
+    torch, pkc = ctx.torch, ctx.pkc
+    from pkc_testing import dev, to_device
+    paged = name == "gqa_cascade_paged_prefix"
+    cfg, p = make_workload("gqa_cascade_lb" if paged else name)
+    d = to_device(p, ctx.device)
+    extra = {"torch": torch, "cfg": cfg}
+    if paged:
+        kc, vc, pages, page_indptr = workloads.pool_prefixes(p, 5, poison=False)
+        extra["pool"] = (dev(kc, ctx.device), dev(vc, ctx.device), dev(pages, ctx.device), page_indptr)
+        del kc, vc
+    run = cascade_call(pkc, name, p, d, extra)
+    B, Hq, _ = p["q"].shape
+    C = cfg["num_ctas"]
+    ws_bytes = pkc.workspace_size(B, Hq, C, 64)
+    gs = GraphStepper(torch, pkc, run, p["cache_seqlens"], C, cfg, ws_bytes, ctx.device)
+    ms, n, clocks = time_loop(ctx, gs.step, gs.stream, ctx.steps)
+    if not gs.status_ok():
+        raise RuntimeError(f"{name}: device status not OK")
+    split = dict(zip(("prefix_blocks", "decode_blocks"), pkc.last_launch_blocks()))
+    buf = host_plan(pkc, p["cache_seqlens"], C, cfg)
+    torch.cuda.synchronize()  # the stepper's last plan upload has landed
+    stages = stage_times(ctx, run, gs.ws[0], buf, stage_steps)
+    eff = workloads.effective_bytes(p)
+    kvb = kv_bytes_per_token(p)
+    entry = _entry(ctx, eff, ms, n, clocks, launch="cuda_graph (host plan + upload per step)",
+                   stages_us_serial=stages, stage_split=split, num_ctas=C or None,
+                   prefix_tokens=int(p["prefix_kv_indptr"][-1]),
+                   suffix_tokens=int(p["cache_seqlens"].sum()))
+    entry["prefix_stage_gbs_serial"] = _gbs(int(p["prefix_kv_indptr"][-1]) * kvb,
+                                            stages["prefix_state"] / 1e3)
+    entry["decode_stage_gbs_serial"] = _gbs(int(p["cache_seqlens"].sum()) * kvb,
+                                            stages["paged_decode"] / 1e3)
+    return entry, (cfg, p, d, gs)
+
+
+def noncascade_pool(torch, d, p):
+    """Device-side non-cascade form of a single-prefix cascade problem: the
+    prefix's pages appended to the cache pool (one copy, shared by every
+    request) and every block table row listing them ahead of the request's
+    own pages."""
+    ps = p["page_size"]
+    Lp = int(p["prefix_kv_indptr"][-1])
+    assert Lp % ps == 0 and len(p["prefix_kv_indptr"]) == 2
+    P0 = d["k_cache"].shape[0]
+    npre = Lp // ps
+    shape = (npre,) + tuple(d["k_cache"].shape[1:])
+    kc = torch.cat([d["k_cache"], d["k_prefix"].reshape(shape)])
+    vc = torch.cat([d["v_cache"], d["v_prefix"].reshape(shape)])
+    B = d["q"].shape[0]
+    pre = torch.arange(P0, P0 + npre, dtype=torch.int32, device=kc.device).expand(B, npre)
+    bt = torch.cat([pre, d["block_table"]], dim=1).contiguous()
+    lens = (d["cache_seqlens"] + Lp).contiguous()
+    return kc, vc, bt, lens
+
+
+def measure_noncascade(ctx, p, d, casc_ms, steps=None):
+    """The pages' non-cascade baseline on the same problem: one paged decode
+    over prefix + suffix per request (pkc_paged_decode_state), the prefix
+    pages shared through the block tables.  Plan over 148 CTAs, uploaded
+    once; direct launches."""
+    torch, pkc = ctx.torch, ctx.pkc
+    kc, vc, bt, lens = noncascade_pool(torch, d, p)
+    lens_h = lens.cpu().numpy()
+    B, Hq, _ = d["q"].shape
+    C = 148
+    buf = pkc.plan(lens_h, C)
+    ws = torch.empty(pkc.workspace_size(B, Hq, C, 0), dtype=torch.uint8, device=ctx.device)
+    pkc.workspace_init(ws)
+    pkc.plan_upload(buf, ws)
+    o = torch.empty_like(d["q"])
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=ctx.device)
+    stream = torch.cuda.current_stream()
+    call = lambda: pkc.paged_decode_state(d["q"], kc, vc, bt, lens, p["sm_scale"], ws,
+                                          plan_buf=buf, o=o, lse=lse)
+    ms, n, clocks = time_loop(ctx, call, stream, steps or ctx.steps)
+    if pkc.device_status(ws) != 0:
+        raise RuntimeError("non-cascade decode: device status not OK")
+    eff = workloads.effective_bytes(p)
+    read = int(lens_h.sum()) * kv_bytes_per_token(p)
+    del kc, vc
+    return {"us_per_step": 1e3 * ms, "value": _gbs(eff, ms), "unit": "GB/s",
+            "kv_bytes_read": read, "kv_read_gbs": _gbs(read, ms),
+            "kv_read_frac": _gbs(read, ms) / ctx.hbm_peak, "steps": n, "clocks": clocks,
+            "num_ctas": C, "launch": "direct (decode + contraction), plan uploaded once",
+            "cascade_speedup": ms / casc_ms}
+
+
+def measure_decode(ctx, name):
+    """Non-cascade paged decode of a workload through its plan (graph-replayed
+    steps with the plan per step)."""
+    torch, pkc = ctx.torch, ctx.pkc
+    from pkc_testing import to_device
+    cfg = workload_cfg(name)
+    p = workloads.make_problem(**cfg)
+    d = to_device(p, ctx.device)
+    fp8 = p["kv_dtype"] == "e4m3"
+    B, Hq, _ = p["q"].shape
+    C = cfg["num_ctas"]
+    o = torch.empty_like(d["q"])
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=ctx.device)
+    if fp8:
+        run = lambda ws, buf, st: pkc.paged_decode_state_fp8(
+            d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"],
+            p["sm_scale"], ws, k_scale=p["k_scale"], v_scale=p["v_scale"], plan_buf=buf,
+            o=o, lse=lse, stream=st)
+    else:
+        run = lambda ws, buf, st: pkc.paged_decode_state(
+            d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"],
+            p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse, stream=st)
+    gs = GraphStepper(torch, pkc, run, p["cache_seqlens"], C, cfg,
+                      pkc.workspace_size(B, Hq, C, 0), ctx.device)
+    ms, n, clocks = time_loop(ctx, gs.step, gs.stream, ctx.steps)
+    if not gs.status_ok():
+        raise RuntimeError(f"{name}: device status not OK")
+    eff = workloads.effective_bytes(p)
+    G = Hq // p["num_kv_heads"]
+    kernel = "paged_decode_mma_kernel" if (fp8 or G >= 2) else "paged_decode_kernel"
+    return _entry(ctx, eff, ms, n, clocks, launch="cuda_graph (host plan + upload per step)",
+                  kernel=kernel, kv_dtype=p["kv_dtype"], num_ctas=C,
+                  kv_tokens=int(p["cache_seqlens"].sum()), launches="decode + contraction")
+
+
+def measure_merge(ctx):
+    torch, pkc = ctx.torch, ctx.pkc
+    from pkc_testing import dev
+    w = workloads.workload("merge")
+    va, sa, vb, sb = (dev(w[k], ctx.device) for k in ("v_a", "s_a", "v_b", "s_b"))
+    vn, sn = dev(w["v_n"], ctx.device), dev(w["s_n"], ctx.device)
+    vo, so = torch.empty_like(va), torch.empty_like(sa)
+    T, H, D = va.shape
+    n = vn.shape[1]
+    stream = torch.cuda.current_stream()
+    ms2, k2, c2 = time_loop(ctx, lambda: pkc.merge_state(va, sa, vb, sb, vo, so), stream, ctx.steps)
+    msn, kn, cn = time_loop(ctx, lambda: pkc.merge_states(vn, sn, vo, so), stream, ctx.steps)
+    b2 = 3 * T * H * (D + 1) * 4
+    bn = (n + 1) * T * H * (D + 1) * 4
+    return {"binary": _entry(ctx, b2, ms2, k2, c2, kernel="merge2_kernel", launch="direct"),
+            "n_ary": _entry(ctx, bn, msn, kn, cn, kernel="mergen_kernel", n=n, launch="direct"),
+            "tokens": T, "heads": H, "head_dim": D, "dtype": "f32"}
+
+
+def measure_sweep(ctx):
+    """The pages' trend (blog "Cascade Inference", "Evaluation"): the gain of
+    the cascade over the non-cascade decode grows with the shared prefix and
+    the batch and shrinks as the unique suffix grows.  32 heads x 128, fp16,
+    page size 16, N(0,1) inputs drawn on the device; both arms planned over
+    148 CTAs with the plan uploaded once, direct launches."""
+    torch, pkc = ctx.torch, ctx.pkc
+    points = [(128, 32768, 256), (32, 32768, 256), (256, 32768, 256), (128, 2048, 256),
+              (128, 8192, 256), (128, 32768, 1024), (128, 32768, 4096)]
+    out = []
+    gen = torch.Generator(device=ctx.device)
+    H, D, ps = 32, 128, 16
+    for B, Lp, Ls in points:
+        gen.manual_seed(1000 + B + Lp + Ls)
+        npre, nsuf = Lp // ps, B * (Ls // ps)
+        pool_k = torch.randn((npre + nsuf, ps, H, D), generator=gen, device=ctx.device).half()
+        pool_v = torch.randn((npre + nsuf, ps, H, D), generator=gen, device=ctx.device).half()
+        q = torch.randn((B, H, D), generator=gen, device=ctx.device).half()
+        perm = torch.randperm(nsuf, generator=gen, device=ctx.device).to(torch.int32) + npre
+        bt_s = perm.view(B, Ls // ps).contiguous()
+        lens_s = torch.full((B,), Ls, dtype=torch.int32, device=ctx.device)
+        k_pre = pool_k[:npre].reshape(Lp, H, D)
+        v_pre = pool_v[:npre].reshape(Lp, H, D)
+        kv_ind, req_ind = np.array([0, Lp], np.int32), np.array([0, B], np.int32)
+        scale = 1.0 / math.sqrt(D)
+        C = 148
+        lens_h = np.full(B, Ls, np.int32)
+        buf = pkc.plan(lens_h, C)
+        ws = torch.empty(pkc.workspace_size(B, H, C, 64), dtype=torch.uint8, device=ctx.device)
+        pkc.workspace_init(ws)
+        pkc.plan_upload(buf, ws)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H), dtype=torch.float32, device=ctx.device)
+        stream = torch.cuda.current_stream()
+        ms_c, n_c, clk_c = time_loop(ctx, lambda: pkc.cascade_decode(
+            q, k_pre, v_pre, kv_ind, req_ind, pool_k, pool_v, bt_s, lens_s, scale, ws,
+            plan_buf=buf, o=o, lse=lse), stream, 5, 0.25)
+        bt_n = torch.cat([torch.arange(npre, dtype=torch.int32, device=ctx.device).expand(B, npre),
+                          bt_s], dim=1).contiguous()
+        lens_n = lens_s + Lp
+        buf_n = pkc.plan(np.full(B, Lp + Ls, np.int32), C)
+        ws_n = torch.empty(pkc.workspace_size(B, H, C, 0), dtype=torch.uint8, device=ctx.device)
+        pkc.workspace_init(ws_n)
+        pkc.plan_upload(buf_n, ws_n)
+        ms_n, n_n, clk_n = time_loop(ctx, lambda: pkc.paged_decode_state(
+            q, pool_k, pool_v, bt_n, lens_n, scale, ws_n, plan_buf=buf_n, o=o, lse=lse),
+            stream, 3, 0.25)
+        if pkc.device_status(ws) != 0 or pkc.device_status(ws_n) != 0:
+            raise RuntimeError("sweep: device status not OK")
+        kvb = 2 * H * D * 2
+        eff = (Lp + B * Ls) * kvb + 2 * B * H * D * 2 + B * H * 4
+        out.append({"batch": B, "prefix": Lp, "suffix": Ls, "cascade_us": 1e3 * ms_c,
+                    "cascade_gbs": _gbs(eff, ms_c), "non_cascade_us": 1e3 * ms_n,
+                    "non_cascade_kv_read_gbs": _gbs(B * (Lp + Ls) * kvb, ms_n),
+                    "speedup": ms_n / ms_c, "steps": [n_c, n_n],
+                    "sm_mhz": [c.get("sm_mhz") if c else None for c in (clk_c, clk_n)],
+                    "reasons": sorted(set((clk_c or {}).get("reasons", []) +
+                                          (clk_n or {}).get("reasons", [])))})
+        del pool_k, pool_v, q, ws, ws_n, bt_n, k_pre, v_pre
+        torch.cuda.empty_cache()
+    return out
+
+
+class Ctx:
+    pass
 
 
 def run_e2e(torch, pkc, p, d, cfg, eff, steps, num_ctas, world, dist):
@@ -569,16 +821,82 @@ def run_e2e(torch, pkc, p, d, cfg, eff, steps, num_ctas, world, dist):
                     "and copies overlap the other set's step"}
 
 
+HEADLINE_WORKLOADS = ("gqa_cascade_lb", "cascade_long_prompt", "tiny_cascade")
+
+
+def make_ctx(args, torch, pkc, local):
+    ctx = Ctx()
+    ctx.torch, ctx.pkc, ctx.args = torch, pkc, args
+    ctx.steps, ctx.warmup = max(1, args.steps), args.warmup
+    ctx.config_seconds = args.config_seconds
+    ctx.hbm_peak, ctx.tf_peak, ctx.peak_kind = load_peaks()
+    ctx.gpu_id = gpu_smi_id(torch, local)
+    ctx.device = f"cuda:{local}"
+    return ctx
+
+
+def run_single(ctx, args, world):
+    """`--workload` other than a headline cascade: that workload's entry as
+    its own line (same measurement as in the headline line's `configs`)."""
+    name = args.workload
+    if name == "merge":
+        e = measure_merge(ctx)
+        head = e["binary"]
+        metric = "merge_state effective HBM throughput"
+    elif name.startswith("paged_decode"):
+        e = head = measure_decode(ctx, name)
+        metric = "paged decode (non-cascade) effective KV throughput"
+    else:
+        e, _ = measure_cascade(ctx, name)
+        head = e
+        metric = "cascade decode effective KV throughput"
+    line = {"metric": metric, "value": head["value"], "unit": "GB/s", "n_gpus": world,
+            "steps": head["steps"], "warmup": args.warmup, "ms_per_step": head["us_per_step"] / 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "data": "synthetic", "config": {"workload": name}, "entry": e,
+            "clocks": head.get("clocks"), "peak": ctx.hbm_peak,
+            "peak_source": f"{ctx.peak_kind} hbm_gbs"}
+    print(json.dumps(line), flush=True)
+
+
+def measure_configs(ctx):
+    """Every workload of the benchmark set, each timed in this process with
+    its own clock record.  Slow to set up (host input generation), fast to
+    time."""
+    torch = ctx.torch
+    out = {}
+
+    def free():
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    e, _ = measure_cascade(ctx, "tiny_cascade")
+    out["tiny_cascade"] = e
+    free()
+    out["merge"] = measure_merge(ctx)
+    free()
+    out["paged_decode"] = measure_decode(ctx, "paged_decode")
+    free()
+    e, (cfg, p, d, gs) = measure_cascade(ctx, "cascade_long_prompt")
+    e["non_cascade"] = measure_noncascade(ctx, p, d, e["us_per_step"] / 1e3)
+    out["cascade_long_prompt"] = e
+    del cfg, p, d, gs
+    free()
+    out["paged_decode_fp8"] = measure_decode(ctx, "paged_decode_fp8")
+    free()
+    for name in ("gqa_cascade_3level", "gqa_cascade_paged_prefix"):
+        e, _ = measure_cascade(ctx, name)
+        out[name] = e
+        free()
+    out["cascade_vs_non_cascade_sweep"] = measure_sweep(ctx)
+    free()
+    return out
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
-        return
-    if args.workload in ("gqa_cascade_3level", "gqa_cascade_paged_prefix"):
-        run_cascade_variant(args)
-        return
-    if args.workload == "merge" or args.workload.startswith("paged_decode"):
-        run_aux(args)
         return
     import torch
     rank, world, local = dist_env()
@@ -596,39 +914,43 @@ def main():
     pkc.set_decode_kernel(args.decode_kernel)
     pkc.set_decode_schedule(args.decode_schedule)
     pkc.set_prefix_ctas(args.prefix_ctas)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from pkc_testing import to_device
+    ctx = make_ctx(args, torch, pkc, local)
+    if args.workload not in HEADLINE_WORKLOADS:
+        run_single(ctx, args, world)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
 
     cfg, p = make_workload(args.workload, args.batch)
     if args.num_ctas is not None:
         cfg["num_ctas"] = args.num_ctas
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from pkc_testing import to_device
-    d = to_device(p, f"cuda:{local}")
+    d = to_device(p, ctx.device)
     B, Hq, D = p["q"].shape
     num_ctas = cfg["num_ctas"]
     lens = p["cache_seqlens"]
-    ws = torch.empty(pkc.workspace_size(B, Hq, num_ctas, 64), dtype=torch.uint8, device=d["q"].device)
+    run = cascade_call(pkc, args.workload, p, d, {"torch": torch, "cfg": cfg})
+    ws_bytes = pkc.workspace_size(B, Hq, num_ctas, 64)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=ctx.device)
     pkc.workspace_init(ws)
     words = pkc.plan_words(B, num_ctas) if num_ctas else 1
     pinned = [torch.empty(words, dtype=torch.int32).pin_memory() for _ in range(2)]
     plan_np = [t.numpy() for t in pinned]
-    o = torch.empty_like(d["q"])
-    lse = torch.empty((B, Hq), dtype=torch.float32, device=d["q"].device)
 
+    # ---- directly launched steps with per-stage events (stages one after
+    # the other: the stage events keep the prefix on the caller's stream) ----
     host_plan_s = []
-    # A pinned plan buffer is rewritten only after the previous upload from
-    # it has run on the GPU (the host runs ahead of the device).
     uploaded = [torch.cuda.Event(), torch.cuda.Event()]
 
     def step(i):
-        uploaded[i & 1].synchronize()
+        uploaded[i & 1].synchronize()  # the pinned buffer's previous upload ran
         t0 = time.perf_counter()
         buf = host_plan(pkc, lens, num_ctas, cfg, out=plan_np[i & 1])
         host_plan_s.append(time.perf_counter() - t0)
         upload_plan(pkc, buf, ws)
         uploaded[i & 1].record()
-        pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
-                           p["prefix_req_indptr"], d["k_cache"], d["v_cache"], d["block_table"],
-                           d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf, o=o, lse=lse)
+        run(ws, buf, torch.cuda.current_stream())
 
     for i in range(args.warmup):
         step(i)
@@ -637,40 +959,100 @@ def main():
     if status != 0:
         raise RuntimeError(f"device status after warm-up: {pkc.STATUS_NAMES.get(status, status)}")
     host_plan_s.clear()
-
-    K = args.steps
+    K = ctx.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     for e in ev:  # torch creates the CUDA event on first record
         for x in e:
             x.record()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(gpu_smi_id(torch, local))
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
+    sampler = ClockSampler(ctx.gpu_id)
     sampler.start()
+    torch.cuda.synchronize()
     start.record()
     for i in range(K):
         pkc.set_stage_events(ev[i])
         step(i)
     end.record()
     torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    elapsed_ms = reduce_max(start.elapsed_time(end), dist, d["q"].device)
+    direct_ms_per_step = start.elapsed_time(end) / K
     status = pkc.device_status(ws)
     if status != 0:
         raise RuntimeError(f"device status after timing: {pkc.STATUS_NAMES.get(status, status)}")
-
     stage_ms = {
         "prefix_state": statistics.mean(e[0].elapsed_time(e[1]) for e in ev),
         "paged_decode": statistics.mean(e[1].elapsed_time(e[2]) for e in ev),
         "contraction": statistics.mean(e[2].elapsed_time(e[3]) for e in ev),
     }
-    eff = workloads.effective_bytes(p)
-    direct_ms_per_step = elapsed_ms / K
 
-    hbm_peak, tf_peak, peak_kind = load_peaks()
+    # ---- the headline: exactly K graph-replayed steps (host plan + upload
+    # per step, overlapping the previous step's device work) ----
+    gs = GraphStepper(torch, pkc, run, lens, num_ctas, cfg, ws_bytes, ctx.device)
+    for _ in range(max(3, args.warmup)):
+        gs.step()
+    gs.stream.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ga.record(gs.stream)
+    for _ in range(K):
+        gs.step()
+    gb.record(gs.stream)
+    gs.stream.synchronize()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    g_ms = reduce_max(ga.elapsed_time(gb), dist, d["q"].device)
+    # Single replays with and without an L2 flush (a 256 MB write) before
+    # each, timed alone: the median step with a cold L2, and with what the
+    # previous step left in it.
+    flush = torch.empty((256 << 20) // 4, dtype=torch.int32, device=ctx.device)
+    n_iso = min(max(K, 20), 50)
+    iso = {}
+    with torch.cuda.stream(gs.stream):
+        for flushed in (True, False):
+            evs = []
+            for i in range(n_iso):
+                if flushed:
+                    flush.fill_(i)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(gs.stream)
+                gs.step()
+                e1.record(gs.stream)
+                evs.append((e0, e1))
+            gs.stream.synchronize()
+            iso[flushed] = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+    del flush
+    clocks = sampler.stop()
+    if not gs.status_ok():
+        raise RuntimeError("device status after the graph-replayed steps")
+    split = dict(zip(("prefix_blocks", "decode_blocks"), pkc.last_launch_blocks()))
+
+    # ---- the pages' own CTA assignment (the plan's static CTA lists) ----
+    schedules = None
+    if num_ctas and world == 1:
+        pkc.set_decode_schedule("static" if args.decode_schedule == "dynamic" else "dynamic")
+        gs2 = GraphStepper(torch, pkc, run, lens, num_ctas, cfg, ws_bytes, ctx.device)
+        ms2, n2, clk2 = time_loop(ctx, gs2.step, gs2.stream, K)
+        if not gs2.status_ok():
+            raise RuntimeError("device status after the other schedule")
+        other = "static" if args.decode_schedule == "dynamic" else "dynamic"
+        split2 = dict(zip(("prefix_blocks", "decode_blocks"), pkc.last_launch_blocks()))
+        pkc.set_decode_schedule(args.decode_schedule)
+        ms1, n1, clk1 = time_loop(ctx, gs.step, gs.stream, K)
+        schedules = {
+            args.decode_schedule: {"us_per_step": 1e3 * ms1, "steps": n1, "clocks": clk1,
+                                   "stage_split": split},
+            other: {"us_per_step": 1e3 * ms2, "steps": n2, "clocks": clk2, "stage_split": split2},
+            "note": "graph-replayed steps timed back to back; static = each decode block runs "
+                    "its CTA's list from the host plan's min-cost priority queue; dynamic = "
+                    "blocks take the same plan's chunks from a longest-first device queue"}
+        del gs2
+
+    eff = workloads.effective_bytes(p)
+    ms_per_step = g_ms / K
+    value = whole_job_gbs(eff, 1, world, ms_per_step / 1e3)
+    hbm_peak, tf_peak, peak_kind = ctx.hbm_peak, ctx.tf_peak, ctx.peak_kind
     kvb = kv_bytes_per_token(p)
     suffix_tokens = int(lens.sum())
     prefix_tokens = int(p["prefix_kv_indptr"][-1])
@@ -683,123 +1065,21 @@ def main():
         alg_bytes = suffix_tokens * kvb
         unit_desc = f"{kvb} B per suffix token x {suffix_tokens} tokens"
     achieved = alg_bytes / (stage_ms[dominant] / 1e3) / 1e9
-    # the decode kernel the library picks (pkc_set_decode_kernel semantics)
     G = Hq // p["num_kv_heads"]
     mma = args.decode_kernel == "mma" or (args.decode_kernel == "auto" and G >= 2)
     kernel_name = {"prefix_state": "prefix_state_kernel"}.get(
         dominant, "paged_decode_mma_kernel" if mma else "paged_decode_kernel")
     tr = kernel_traffic(kernel_name, args.workload if args.batch is None else None)
-    # prefix stage on the tensor cores: FLOPs 4*D per (row, prefix token)
-    rows_per_prefix = np.diff(p["prefix_req_indptr"]) * (Hq // p["num_kv_heads"])
+    rows_per_prefix = np.diff(p["prefix_req_indptr"]) * G
     prefix_flops = float(4 * D * np.sum(rows_per_prefix * np.diff(p["prefix_kv_indptr"])) *
                          p["num_kv_heads"])
 
-    # ---- the same step with the device work replayed from a CUDA graph ----
-    # The plan still runs on the host and is uploaded every step (outside the
-    # graph); the captured cascade call reads it from its workspace.  Two
-    # workspaces and two graphs alternate, so that step i+1's plan upload (on
-    # a copy stream) overlaps step i's device work; a workspace's plan is
-    # overwritten only after the graph that read it has run.
-    graph = None
-    try:
-        gstream, cstream = torch.cuda.Stream(), torch.cuda.Stream()
-        gplan = [torch.empty(words, dtype=torch.int32).pin_memory() for _ in range(2)]
-        gplan_np = [t.numpy() for t in gplan]
-        gws = [ws, torch.empty_like(ws)]
-        pkc.workspace_init(gws[1])
-        gdone = [torch.cuda.Event(), torch.cuda.Event()]      # graph s has run
-        uploaded = [torch.cuda.Event(), torch.cuda.Event()]   # plan s is on the GPU
-        graphs = []
-        with torch.cuda.stream(gstream):
-            for sidx in range(2):
-                gbuf = host_plan(pkc, lens, num_ctas, cfg, out=gplan_np[sidx])
-
-                def g_run(sidx=sidx, gbuf=gbuf):
-                    pkc.cascade_decode(d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"],
-                                       p["prefix_req_indptr"], d["k_cache"], d["v_cache"],
-                                       d["block_table"], d["cache_seqlens"], p["sm_scale"], gws[sidx],
-                                       plan_buf=gbuf, o=o, lse=lse, stream=gstream)
-
-                upload_plan(pkc, gbuf, gws[sidx], stream=gstream)
-                g_run()
-                gstream.synchronize()
-                cg = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(cg, stream=gstream):
-                    g_run()
-                graphs.append(cg)
-            for e in gdone + uploaded:
-                e.record(gstream)
-            gstream.synchronize()
-
-            def g_step(i):
-                sidx = i & 1
-                uploaded[sidx].synchronize()  # the pinned plan buffer is free again
-                b = host_plan(pkc, lens, num_ctas, cfg, out=gplan_np[sidx])
-                cstream.wait_event(gdone[sidx])  # the graph that read this plan has run
-                upload_plan(pkc, b, gws[sidx], stream=cstream)
-                uploaded[sidx].record(cstream)
-                gstream.wait_event(uploaded[sidx])
-                graphs[sidx].replay()
-                gdone[sidx].record(gstream)
-
-            for i in range(max(3, args.warmup)):
-                g_step(i)
-            gstream.synchronize()
-            if dist is not None:
-                dist.barrier()
-            ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            ga.record(gstream)
-            for i in range(K):
-                g_step(i)
-            gb.record(gstream)
-            gstream.synchronize()
-            if dist is not None:
-                dist.barrier()
-            # Single replays with and without an L2 flush (a 256 MB write)
-            # before each, timed alone: the median step with a cold L2 and
-            # with whatever the previous step left in it.
-            flush = torch.empty((256 << 20) // 4, dtype=torch.int32, device=d["q"].device)
-            n_iso = min(K, 50)
-            iso = {}
-            for flushed in (True, False):
-                evs = []
-                for i in range(n_iso):
-                    if flushed:
-                        flush.fill_(i)
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(gstream)
-                    graphs[i & 1].replay()
-                    e1.record(gstream)
-                    evs.append((e0, e1))
-                gstream.synchronize()
-                iso[flushed] = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
-        g_ms = reduce_max(ga.elapsed_time(gb), dist, d["q"].device)
-        graph = {"value": whole_job_gbs(eff, K, world, g_ms / 1e3), "unit": "GB/s",
-                 "us_per_step": 1e3 * g_ms / K,
-                 "note": "host plan + upload each step (on a copy stream, two workspaces "
-                         "alternating), device work replayed from a CUDA graph",
-                 "isolated_replay_us_median": {"l2_flushed": iso[True], "unflushed": iso[False],
-                                               "flush_bytes": 256 << 20, "replays": n_iso}}
-        if pkc.device_status(gws[0]) != 0 or pkc.device_status(gws[1]) != 0:
-            raise RuntimeError("device status after graph replay")
-    except RuntimeError:
-        raise
-    except Exception as exc:  # graph capture unavailable: report why
-        graph = {"unavailable": str(exc)[:200]}
-    clocks = sampler.stop()
-    # Headline: the graph-replayed step (how the pages run it: plan per step
-    # on the CPU, the captured run replayed); the directly launched,
-    # event-instrumented run gives the per-stage times.
-    if graph and "us_per_step" in graph:
-        mode, ms_per_step = "cuda_graph", graph["us_per_step"] / 1e3
-    else:
-        mode, ms_per_step = "direct", direct_ms_per_step
-    value = whole_job_gbs(eff, 1, world, ms_per_step / 1e3)
-
-    # ---- e2e through host buffers ----
     e2e = None
     if args.e2e_steps > 0:
         e2e = run_e2e(torch, pkc, p, d, cfg, eff, args.e2e_steps, num_ctas, world, dist)
+    del gs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -812,6 +1092,10 @@ def main():
                "single_thread": {"value": eff / (t1 / (n1 / total)) / 1e9, "unit": "GB/s", "cores": 1,
                                  "sample": f"{n1} of {total} rows in {t1:.1f} s"}}
 
+    configs = None
+    if world == 1 and not args.no_configs and args.batch is None:
+        configs = measure_configs(ctx)
+
     if rank == 0:
         line = {
             "metric": "cascade decode effective KV throughput",
@@ -819,20 +1103,12 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": 1e3 * ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg["dtype"], "data": "synthetic",
-            "config": {"workload": args.workload, "batch": B, "num_qo_heads": Hq,
-                       "num_kv_heads": p["num_kv_heads"], "head_dim": D,
-                       "page_size": cfg["page_size"], "prefix_lens": cfg["prefix_lens"],
-                       "suffix_tokens": suffix_tokens,
-                       "num_ctas": num_ctas or None,
-                       "plan": "host plan over num_ctas CTAs" if num_ctas else
-                               "none: one decode block per (request, KV-head group)",
-                       "effective_bytes_per_step": eff,
-                       "l2": "inputs larger than L2 (one step reads %.2f GB)" % (eff / 1e9),
-                       "launch": mode, "decode_kernel": args.decode_kernel,
-                       "decode_schedule": args.decode_schedule if num_ctas else None,
-                       "prefix_ctas": args.prefix_ctas or "auto",
-                       "parallelism": f"replicas x{world}"},
-            "stage_split": dict(zip(("prefix_blocks", "decode_blocks"), pkc.last_launch_blocks())),
+            "config": line_config(args.workload, cfg, p, num_ctas, args, world, {
+                "launch": "cuda_graph", "decode_kernel": args.decode_kernel,
+                "decode_schedule": args.decode_schedule if num_ctas else None,
+                "prefix_ctas": args.prefix_ctas or "auto",
+                "step": "host plan + plan upload + prefix states + paged decode + contraction"}),
+            "stage_split": split,
             "direct_us_per_step": 1e3 * direct_ms_per_step,
             "hbm_fraction": value / world / hbm_peak,
             "stages_us": {k: 1e3 * v for k, v in stage_ms.items()},
@@ -845,11 +1121,14 @@ def main():
             "prefix_tensor": {"flops_per_launch": prefix_flops,
                               "tflops": prefix_flops / (stage_ms["prefix_state"] / 1e3) / 1e12,
                               "peak_tflops": tf_peak, "peak_source": f"{peak_kind} bf16_tflops"},
+            "graph": {"isolated_replay_us_median": {"l2_flushed": iso[True], "unflushed": iso[False],
+                                                    "flush_bytes": 256 << 20, "replays": n_iso}},
+            "decode_schedules": schedules,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "graph": graph,
             "gpu_launches": 3 * K,
             "clocks": clocks,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

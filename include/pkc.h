@@ -265,13 +265,21 @@ int pkc_paged_decode_state(const void* q, const void* k_cache,
  * spare device memory for a workspace -- e.g. code running inside another
  * framework's pre-reserved memory pool, or under a fixed memory budget.
  * The split-KV scratch (status word, uploaded plan, partial states) lives in
- * an 8 MiB array declared in device memory by the library itself; every GPU
- * that loads the library holds it until the process exits.
+ * an 8 MiB array declared in device memory by the library itself.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current.  Under CUDA's lazy
+ *     module loading (the default) that lookup is also when the driver
+ *     places the 8 MiB array in that device's memory, where it stays until
+ *     the process exits.  So make that first call before any stream
+ *     capture and before the caller's memory pool reserves the rest of the
+ *     device; a call with batch 0 (no other pointer is read) does only the
+ *     set-up.
  *   - The plan (plan_host, as in pkc_paged_decode_state, or NULL) is copied
- *     into the array by this call; no pkc_plan_upload is needed.  It needs
+ *     into the array by this call (cudaMemcpyAsync from the host buffer,
+ *     in stream order); no pkc_plan_upload is needed.  If the call is made
+ *     inside a stream capture, that copy becomes a graph node that reads
+ *     plan_host at every replay: the buffer must then stay alive, and its
+ *     contents at replay time are the plan used.  It needs
  *     256 + plan + 2 * num_ctas * num_qo_heads * 129 * 4 bytes (rounded to
  *     256-byte blocks) <= 8 MiB, else PKC_ERR_WORKSPACE with the numbers.
  *   - Every call shares the one array and leaves its contents behind; the

@@ -770,7 +770,13 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   g_last_prefix_blocks = S.pp.n_blocks;
   g_last_decode_blocks = decode_blocks;
   e = launch_paged_decode(dp, decode_blocks, dtype, dtype, stream);
-  if (e) return cuda_error(e, "paged decode launch");
+  if (e) {
+    if (side) {  // the side stream has already forked: join it before returning
+      cudaEventRecord(side->join, side->side);
+      cudaStreamWaitEvent((cudaStream_t)stream, side->join, 0);
+    }
+    return cuda_error(e, "paged decode launch");
+  }
   if (side) {
     // 1. shared prefix, on the side stream; the caller's stream waits for it
     if (int rc = run_prefix(side->side, nullptr)) {

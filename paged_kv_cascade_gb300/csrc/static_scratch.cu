@@ -7,13 +7,17 @@
 // pre-reserved memory budget.  They cannot provide the workspace that
 // pkc_paged_decode_state needs for the split-KV partial states.  This entry
 // point runs the same kernels with the workspace placed in a fixed-size
-// array that the library itself declares in device memory: every GPU that
-// loads the library holds kStaticScratchBytes (8 MiB) of it until the
-// process exits.
+// array that the library itself declares in device memory:
+// kStaticScratchBytes (8 MiB) on every GPU the entry point is first called
+// on, held until the process exits.
 //
 // The array's host-side name is only a stand-in, not a device address, so
 // the address is looked up with cudaGetSymbolAddress once per device (on the
 // first call made with that device current) and passed to the kernels.
+// With CUDA's lazy module loading (the default) that first lookup is also
+// when the driver loads this file's module and places the array in device
+// memory, so a caller whose memory pool takes the rest of the device later
+// makes one call first -- a call with batch 0 does only this.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -98,6 +102,10 @@ extern "C" int pkc_paged_decode_state_noalloc(
                      "but the built-in scratch holds %zu bytes (use fewer plan CTAs, or "
                      "pkc_paged_decode_state with a caller workspace)",
                      need, num_ctas, num_qo_heads, kStaticScratchBytes);
+  // The array is resolved (and, under lazy module loading, placed in device
+  // memory) before anything else, so that a batch-0 call pins it.
+  void* base = nullptr;
+  if (int rc = scratch_address(&base)) return rc;
   if (batch == 0) return PKC_OK;
   if (!q || !k_cache || !v_cache || !block_table || !cache_seqlens || !o || !lse)
     return set_error(PKC_ERR_INVALID_ARG, "paged_decode_state_noalloc: NULL pointer");
@@ -105,8 +113,6 @@ extern "C" int pkc_paged_decode_state_noalloc(
         reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(o)) & 15) != 0)
     return set_error(PKC_ERR_INVALID_ARG, "paged_decode_state_noalloc: q, caches and o must be 16-byte aligned");
 
-  void* base = nullptr;
-  if (int rc = scratch_address(&base)) return rc;
   uint8_t* s = static_cast<uint8_t*>(base);
   cudaStream_t st = (cudaStream_t)stream;
   // The array keeps the previous call's contents: the status word must

@@ -100,15 +100,18 @@ def compare(o_dev, lse_dev, o_ref, lse_ref, rows=None, o_tol=O_TOL, lse_tol=LSE_
     o_err = float(max(0.0, np.max(excess))) if o.size else 0.0
     fin = ~empty_ref
     lse_err = float(np.max(np.abs(lse[fin] - lse_ref[fin]))) if fin.any() else 0.0
-    assert o_err <= o_tol, (f"O max-abs error beyond output rounding {o_err:.3e} > {o_tol} "
-                            f"(raw max-abs {float(np.max(np.abs(o - o_ref))):.3e})")
+    o_raw = float(np.max(np.abs(o - o_ref))) if o.size else 0.0
+    rec = {"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
+           "rows": int(o.shape[0]), "o_raw_max_abs": o_raw, "o_err_beyond_rounding": o_err,
+           "lse_max_abs": lse_err, "o_tol": o_tol, "lse_tol": lse_tol}
+    # shown by pytest -rP / -s, and appended to PKC_PARITY_LOG when set
+    print("parity " + json.dumps(rec))
     log = os.environ.get("PKC_PARITY_LOG")
     if log:
         with open(log, "a") as f:
-            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
-                                "rows": int(o.shape[0]), "o_err_beyond_rounding": o_err,
-                                "o_raw_max_abs": float(np.max(np.abs(o - o_ref))) if o.size else 0.0,
-                                "lse_max_abs": lse_err}) + "\n")
+            f.write(json.dumps(rec) + "\n")
+    assert o_err <= o_tol, (f"O max-abs error beyond output rounding {o_err:.3e} > {o_tol} "
+                            f"(raw max-abs {o_raw:.3e})")
     assert lse_err <= lse_tol, f"LSE max-abs error {lse_err:.3e} > {lse_tol}"
     return o_err, lse_err
 

@@ -9,7 +9,7 @@ import torch
 import oracle
 import paged_kv_cascade_gb300 as pkc
 import workloads
-from pkc_testing import compare, dev, oracle_args, sample_rows, to_device, workspace_for
+from pkc_testing import compare, dev, oracle_args, to_device, workspace_for
 
 pytestmark = pytest.mark.gpu
 
@@ -101,30 +101,27 @@ def test_cascade_small(case, num_ctas):
     compare(o, lse, ref_o, ref_lse)
 
 
-def test_cascade_long_prompt_workload_sampled():
+def test_cascade_long_prompt_workload_every_row():
+    """Batch 128, 32 heads, 32768-token shared prefix + 256-token suffixes,
+    planned over 148 CTAs: all 4096 (request, head) rows against the oracle."""
     p = workloads.workload("cascade_long_prompt")
     o, lse = _cascade(p, 148)
-    B, Hq, _ = p["q"].shape
-    rows = sample_rows(B, Hq, 96, seed=4)
-    ref_o, ref_lse = oracle.attention_rows(p["q"], rows=rows, **oracle_args(p))
-    compare(o, lse, ref_o, ref_lse, rows=rows)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse)
 
 
-def test_gqa_cascade_lb_workload_sampled():
+def test_gqa_cascade_lb_workload_every_row():
+    """The load-balanced GQA cascade (batch 256, 4 prefixes x 8192 tokens,
+    lognormal suffixes, 37 split requests): all 8192 rows, so every chunk of
+    every split request reaches the comparison."""
     w = workloads.WORKLOADS["gqa_cascade_lb"]
     p = workloads.workload("gqa_cascade_lb")
     o, lse = _cascade(p, w["num_ctas"], w["alpha"], w["beta"])
-    B, Hq, _ = p["q"].shape
-    rows = sample_rows(B, Hq, 160, seed=5)
-    # include every split request's rows for head 0 and the longest request
-    lens = p["cache_seqlens"]
-    extra = [(int(b), 0) for b in np.argsort(-lens)[:6]]
-    rows = np.unique(np.concatenate([rows, np.array(extra, np.int32)]), axis=0)
-    ref_o, ref_lse = oracle.attention_rows(p["q"], rows=rows, **oracle_args(p))
-    compare(o, lse, ref_o, ref_lse, rows=rows)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse)
 
 
-def test_gqa_cascade_3level_workload_sampled():
+def test_gqa_cascade_3level_workload_every_row():
     """The three-level workload as the benchmark runs it: its prefix (8 and 2
     row tiles per K/V tile) gets SMs of its own next to the decode."""
     w = workloads.WORKLOADS["gqa_cascade_3level"]
@@ -141,15 +138,13 @@ def test_gqa_cascade_3level_workload_sampled():
     assert pkc.device_status(ws) == pkc.PKC_OK
     pb, db = pkc.last_launch_blocks()
     assert pb + db <= torch.cuda.get_device_properties(0).multi_processor_count
-    B, Hq, _ = p["q"].shape
-    rows = sample_rows(B, Hq, 128, seed=7)
     a = oracle_args(p)
     a.pop("prefix_req_indptr")
-    ref_o, ref_lse = oracle.attention_rows(p["q"], rows=rows, prefix_req_ranges=w["prefix_ranges"], **a)
-    compare(o, lse, ref_o, ref_lse, rows=rows)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], prefix_req_ranges=w["prefix_ranges"], **a)
+    compare(o, lse, ref_o, ref_lse)
 
 
-def test_gqa_cascade_paged_prefix_workload_sampled():
+def test_gqa_cascade_paged_prefix_workload_every_row():
     """gqa_cascade_lb with its four 8192-token prefixes kept in the page pool
     (NaN past their ends) and read in place, as the benchmark line runs it."""
     w = workloads.WORKLOADS["gqa_cascade_lb"]
@@ -167,10 +162,8 @@ def test_gqa_cascade_paged_prefix_workload_sampled():
         d["block_table"], d["cache_seqlens"], p["sm_scale"], ws, plan_buf=buf)
     torch.cuda.synchronize()
     assert pkc.device_status(ws) == pkc.PKC_OK
-    B, Hq, _ = p["q"].shape
-    rows = sample_rows(B, Hq, 128, seed=8)
-    ref_o, ref_lse = oracle.attention_rows(p["q"], rows=rows, **oracle_args(p))
-    compare(o, lse, ref_o, ref_lse, rows=rows)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse)
 
 
 def test_workspace_reused_across_calls_and_problems():
@@ -200,3 +193,25 @@ def test_workspace_reused_across_calls_and_problems():
         assert pkc.device_status(ws) == pkc.PKC_OK
         ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
         compare(o, lse, ref_o, ref_lse)
+
+
+def test_noncascade_decode_of_the_long_prompt_shape():
+    """The pages' non-cascade baseline: the long-prompt problem (32768-token
+    shared prefix, 256-token suffixes, 32 heads, fp16) at batch 6, decoded
+    by pkc_paged_decode_state alone with every block table listing the shared
+    prefix's pages and then the request's own.  It must give the cascade's
+    answer: attention over prefix u suffix, every row against the oracle."""
+    cfg = dict(workloads.WORKLOADS["cascade_long_prompt"], batch=6, prefix_groups=[6])
+    p = workloads.make_problem(**cfg)
+    n = workloads.noncascade_problem(p, 4)
+    d = to_device(n)
+    C = 148
+    buf = pkc.plan(n["cache_seqlens"], C)
+    ws = workspace_for(pkc, n, num_ctas=C, prefix_splits=0)
+    pkc.plan_upload(buf, ws)
+    o, lse = pkc.paged_decode_state(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                    d["cache_seqlens"], n["sm_scale"], ws, plan_buf=buf)
+    torch.cuda.synchronize()
+    assert pkc.device_status(ws) == pkc.PKC_OK
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse)

@@ -264,6 +264,47 @@ def pool_prefixes(p, seed, poison=True):
     return kc, vc, np.asarray(pages, np.int32), page_indptr
 
 
+def noncascade_problem(p, seed, poison=False):
+    """The same attention problem with no shared-prefix stage: each prefix is
+    laid into pages of the cache pool (``pool_prefixes``; the pages are shared,
+    not copied per request) and every request's block table lists its group's
+    prefix pages, then its own suffix pages; its cached length becomes prefix
+    + suffix.  Every prefix must fill whole pages (a page cannot end a prefix
+    part-way and then continue with the suffix).  Returns a problem dict
+    without prefixes."""
+    ps = p["page_size"]
+    ind = p["prefix_kv_indptr"]
+    req = p["prefix_req_indptr"]
+    lens_p = np.diff(ind).astype(np.int64)
+    if np.any(lens_p % ps):
+        raise ValueError("every prefix must be a whole number of pages")
+    kc, vc, pages, page_indptr = pool_prefixes(p, seed, poison=poison)
+    B = p["q"].shape[0]
+    bt_s = p["block_table"]
+    n_suffix_pages = (p["cache_seqlens"].astype(np.int64) + ps - 1) // ps
+    pre_of = np.full(B, -1, np.int64)
+    for j in range(len(lens_p)):
+        pre_of[int(req[j]):int(req[j + 1])] = j
+    n_pre = np.array([(page_indptr[j + 1] - page_indptr[j]) if j >= 0 else 0 for j in pre_of], np.int64)
+    width = max(1, int((n_pre + n_suffix_pages).max()) if B else 1)
+    bt = np.full((B, width), -1, np.int32)
+    lens = np.array(p["cache_seqlens"], np.int32)
+    for b in range(B):
+        j = int(pre_of[b])
+        k = 0
+        if j >= 0:
+            k = int(n_pre[b])
+            bt[b, :k] = pages[page_indptr[j]:page_indptr[j + 1]]
+            lens[b] += int(lens_p[j])
+        m = int(n_suffix_pages[b])
+        bt[b, k:k + m] = bt_s[b, :m]
+    out = dict(p)
+    out.update(k_prefix=None, v_prefix=None, prefix_kv_indptr=np.zeros(1, np.int32),
+               prefix_req_indptr=np.zeros(1, np.int32), k_cache=kc, v_cache=vc,
+               block_table=bt, cache_seqlens=lens)
+    return out
+
+
 def make_merge(*, tokens, heads, d, n_states, seed, v_dtype="f32", threads=8,
                **_ignored):
     """merge_state inputs: two states per (token, head), plus n stacked.

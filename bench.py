@@ -484,6 +484,9 @@ def stage_times(ctx, run, ws, buf, steps):
     stream = torch.cuda.current_stream()
     upload_plan(pkc, buf, ws, stream=stream)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in ev:  # torch creates the CUDA event on its first record
+        for x in e:
+            x.record(stream)
     for _ in range(3):
         run(ws, buf, stream)
     for e in ev:
@@ -866,30 +869,28 @@ def measure_configs(ctx):
     torch = ctx.torch
     out = {}
 
-    def free():
+    def long_prompt():
+        e, (cfg, p, d, gs) = measure_cascade(ctx, "cascade_long_prompt")
+        e["non_cascade"] = measure_noncascade(ctx, p, d, e["us_per_step"] / 1e3)
+        return e
+
+    jobs = [("tiny_cascade", lambda: measure_cascade(ctx, "tiny_cascade")[0]),
+            ("merge", lambda: measure_merge(ctx)),
+            ("paged_decode", lambda: measure_decode(ctx, "paged_decode")),
+            ("cascade_long_prompt", long_prompt),
+            ("paged_decode_fp8", lambda: measure_decode(ctx, "paged_decode_fp8")),
+            ("gqa_cascade_3level", lambda: measure_cascade(ctx, "gqa_cascade_3level")[0]),
+            ("gqa_cascade_paged_prefix", lambda: measure_cascade(ctx, "gqa_cascade_paged_prefix")[0]),
+            ("cascade_vs_non_cascade_sweep", lambda: measure_sweep(ctx))]
+    for name, job in jobs:
+        # A failing entry is reported as such; it does not take the headline
+        # line with it.  A device status other than OK raises inside.
+        try:
+            out[name] = job()
+        except Exception as exc:  # noqa: BLE001
+            out[name] = {"error": f"{type(exc).__name__}: {str(exc)[:300]}"}
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-
-    e, _ = measure_cascade(ctx, "tiny_cascade")
-    out["tiny_cascade"] = e
-    free()
-    out["merge"] = measure_merge(ctx)
-    free()
-    out["paged_decode"] = measure_decode(ctx, "paged_decode")
-    free()
-    e, (cfg, p, d, gs) = measure_cascade(ctx, "cascade_long_prompt")
-    e["non_cascade"] = measure_noncascade(ctx, p, d, e["us_per_step"] / 1e3)
-    out["cascade_long_prompt"] = e
-    del cfg, p, d, gs
-    free()
-    out["paged_decode_fp8"] = measure_decode(ctx, "paged_decode_fp8")
-    free()
-    for name in ("gqa_cascade_3level", "gqa_cascade_paged_prefix"):
-        e, _ = measure_cascade(ctx, name)
-        out[name] = e
-        free()
-    out["cascade_vs_non_cascade_sweep"] = measure_sweep(ctx)
-    free()
     return out
 
 

@@ -99,6 +99,22 @@ int pkc_merge_states(const void* v, const float* s, void* v_out, float* s_out,
                      int64_t n_tokens, int n_states, int n_heads, int head_dim,
                      int v_dtype, void* stream);
 
+/*
+ * The n-ary merge above with a result of another element type: float32
+ * states (v_dtype PKC_F32) merged into an fp16 or bf16 v_out (out_dtype),
+ * the weighted sum formed in float32 and rounded once (nearest even).
+ * Equal types are pkc_merge_states.  This is the last step of a KV-sharded
+ * decode ("Attention States and Recursive Attention", Applications: the
+ * states of KV subsets computed on different devices are merged in any
+ * order): the gathered float32 states [n_states, B*Hq, 128] of the shards
+ * are a [1, n_states, B*Hq, 128] input.  head_dim / 4 must divide 32 or be
+ * a multiple of 32; PKC_ERR_INVALID_ARG for other type pairs.
+ */
+int pkc_merge_states_to(const void* v, const float* s, void* v_out,
+                        float* s_out, int64_t n_tokens, int n_states,
+                        int n_heads, int head_dim, int v_dtype, int out_dtype,
+                        void* stream);
+
 /* ------------------------------------------------------------------------
  * Load-balanced plan (host only)
  * ---------------------------------------------------------------------- */
@@ -402,6 +418,25 @@ int pkc_cascade_decode(
     int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
     float sm_scale, const int32_t* plan_host, void* workspace,
     size_t workspace_bytes, void* o, float* lse, int dtype, void* stream);
+
+/*
+ * The cascade decode above returning the attention state unrounded: o is
+ * float32 [batch, num_qo_heads, 128] (every other argument as in
+ * pkc_cascade_decode, q and the caches of dtype).  For states that are
+ * merged further with (+) -- a KV-sharded decode, where each device computes
+ * the state of its part of every request's keys ("Attention States and
+ * Recursive Attention", Applications) -- so the result is rounded only once,
+ * after the last merge.
+ */
+int pkc_cascade_decode_state(
+    const void* q, const void* k_prefix, const void* v_prefix,
+    const int32_t* prefix_kv_indptr_host,
+    const int32_t* prefix_req_indptr_host, int n_prefix, const void* k_cache,
+    const void* v_cache, const int32_t* block_table, int block_table_stride,
+    const int32_t* cache_seqlens, int batch, int num_qo_heads,
+    int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+    float sm_scale, const int32_t* plan_host, void* workspace,
+    size_t workspace_bytes, float* o, float* lse, int dtype, void* stream);
 
 /*
  * Multi-level cascade decode: the cascade above with prefix groups given as

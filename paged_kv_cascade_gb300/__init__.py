@@ -41,6 +41,7 @@ SIGNATURES = {
     "pkc_last_error": (_c.c_char_p, []),
     "pkc_merge_state": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _P]),
     "pkc_merge_states": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P]),
+    "pkc_merge_states_to": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _P]),
     "pkc_plan_words": (_I, [_P, _I, _I, _I, _c.POINTER(_SZ)]),
     "pkc_plan": (_I, [_P, _P, _I, _I, _I, _D, _D, _P, _SZ]),
     "pkc_plan_upload": (_I, [_P, _P, _SZ, _P]),
@@ -68,6 +69,8 @@ SIGNATURES = {
                                              _I, _I, _I, _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
     "pkc_cascade_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                 _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
+    "pkc_cascade_decode_state": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I,
+                                      _I, _I64, _F, _P, _P, _SZ, _P, _P, _I, _P]),
 }
 
 _lib = None
@@ -216,6 +219,25 @@ def merge_states(v, s, v_out=None, s_out=None, stream=None):
     s_out = torch.empty((T, H), dtype=torch.float32, device=v.device) if s_out is None else s_out
     _check(lib().pkc_merge_states(_ptr(v), _ptr(s), _ptr(v_out), _ptr(s_out), T, n, H, D,
                                   _dtype_code(v), _stream(stream)))
+    return v_out, s_out
+
+
+def merge_states_to(v, s, out_dtype, v_out=None, s_out=None, stream=None):
+    """n-ary (+) of float32 states v [T, n, H, D], s [T, n, H] into a result
+    of out_dtype (torch.float16 / torch.bfloat16 / torch.float32), rounded
+    once."""
+    import torch
+    _expect("v", v, (torch.float32,), (None, None, None, None))
+    T, n, H, D = v.shape
+    _expect("s", s, (torch.float32,), (T, n, H), v.device)
+    if v_out is not None:
+        _expect("v_out", v_out, (out_dtype,), (T, H, D), v.device)
+    if s_out is not None:
+        _expect("s_out", s_out, (torch.float32,), (T, H), v.device)
+    v_out = torch.empty((T, H, D), dtype=out_dtype, device=v.device) if v_out is None else v_out
+    s_out = torch.empty((T, H), dtype=torch.float32, device=v.device) if s_out is None else s_out
+    _check(lib().pkc_merge_states_to(_ptr(v), _ptr(s), _ptr(v_out), _ptr(s_out), T, n, H, D, F32,
+                                     _dtype_code(v_out), _stream(stream)))
     return v_out, s_out
 
 
@@ -424,6 +446,29 @@ def cascade_decode(q, k_prefix, v_prefix, prefix_kv_indptr, prefix_req_indptr, k
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
     _check(lib().pkc_cascade_decode(
+        _ptr(q), _ptr(k_prefix), _ptr(v_prefix), _hptr(kv_ptr), _hptr(req_ptr), len(kv_ptr) - 1,
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens),
+        B, Hq, Hkv, D, ps, P, float(sm_scale), _hptr(plan_buf), _ptr(workspace),
+        workspace.numel(), _ptr(o), _ptr(lse), _dtype_code(q), _stream(stream)))
+    return o, lse
+
+
+def cascade_decode_state(q, k_prefix, v_prefix, prefix_kv_indptr, prefix_req_indptr, k_cache,
+                         v_cache, block_table, cache_seqlens, sm_scale, workspace, plan_buf=None,
+                         o=None, lse=None, stream=None):
+    """cascade_decode returning the unrounded state: O [B, Hq, 128] float32 and
+    LSE [B, Hq], for states merged further (KV sharding)."""
+    import torch
+    B, Hq, D = q.shape
+    _check_paged(q, k_cache, v_cache, block_table, cache_seqlens, workspace, None, lse, (q.dtype,))
+    _check_prefix(q, k_prefix, v_prefix, _host_i32(prefix_kv_indptr))
+    if o is not None:
+        _expect("o", o, (torch.float32,), (B, Hq, D), q.device)
+    P, ps, Hkv, _ = k_cache.shape
+    kv_ptr, req_ptr = _host_i32(prefix_kv_indptr), _host_i32(prefix_req_indptr)
+    o = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().pkc_cascade_decode_state(
         _ptr(q), _ptr(k_prefix), _ptr(v_prefix), _hptr(kv_ptr), _hptr(req_ptr), len(kv_ptr) - 1,
         _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens),
         B, Hq, Hkv, D, ps, P, float(sm_scale), _hptr(plan_buf), _ptr(workspace),

@@ -434,6 +434,28 @@ int pkc_merge_states(const void* v, const float* s, void* v_out, float* s_out, i
   return e ? cuda_error(e, "merge_states launch") : PKC_OK;
 }
 
+int pkc_merge_states_to(const void* v, const float* s, void* v_out, float* s_out, int64_t n_tokens, int n_states,
+                        int n_heads, int head_dim, int v_dtype, int out_dtype, void* stream) {
+  if (out_dtype == v_dtype)
+    return pkc_merge_states(v, s, v_out, s_out, n_tokens, n_states, n_heads, head_dim, v_dtype, stream);
+  if (v_dtype != PKC_F32 || (out_dtype != PKC_F16 && out_dtype != PKC_BF16))
+    return set_error(PKC_ERR_INVALID_ARG,
+                     "merge_states_to: fp32 states into an fp16 / bf16 result, or equal types (got %d -> %d)",
+                     v_dtype, out_dtype);
+  if (n_tokens < 0 || n_heads < 0 || n_states < 1)
+    return set_error(PKC_ERR_INVALID_ARG, "merge_states_to: bad size (n_states >= 1 required)");
+  const int cpr = head_dim / 4;  // 16-byte chunks of an fp32 row
+  if (head_dim <= 0 || head_dim % 4 != 0 || (cpr > 32 ? cpr % 32 != 0 : 32 % cpr != 0))
+    return set_error(PKC_ERR_UNSUPPORTED, "merge_states_to: head_dim/4 must divide 32 or be a multiple of 32");
+  if (n_tokens * n_heads == 0) return PKC_OK;
+  if (!v || !s || !v_out || !s_out) return set_error(PKC_ERR_INVALID_ARG, "merge_states_to: NULL pointer");
+  if (!aligned16(v) || !aligned16(v_out))
+    return set_error(PKC_ERR_INVALID_ARG, "merge_states_to: v pointers must be 16-byte aligned");
+  const int e = launch_merge_states_to(v, s, v_out, s_out, n_tokens, n_states, n_heads, head_dim, v_dtype, out_dtype,
+                                       stream);
+  return e ? cuda_error(e, "merge_states_to launch") : PKC_OK;
+}
+
 int pkc_workspace_size(int batch, int num_qo_heads, int head_dim, int num_ctas, int prefix_splits, size_t* bytes) {
   if (!bytes || batch < 0 || num_qo_heads <= 0 || head_dim <= 0 || num_ctas < 0 || prefix_splits < 0)
     return set_error(PKC_ERR_INVALID_ARG, "workspace_size: bad argument");
@@ -670,7 +692,8 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
                  int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
                  float sm_scale, const int32_t* plan_host, void* workspace, size_t workspace_bytes, void* o,
                  float* lse, int dtype, void* stream, const int32_t* prefix_pages = nullptr,
-                 const int32_t* page_indptr = nullptr) {
+                 const int32_t* page_indptr = nullptr, int o_dtype = -1) {
+  if (o_dtype < 0) o_dtype = dtype;
   if (prefix_pages) {
     k_prefix = k_cache;
     v_prefix = v_cache;
@@ -683,7 +706,12 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   const WsLayout L = ws_layout(batch, num_qo_heads, head_dim, num_ctas);
   if (int rc = check_ws(workspace, workspace_bytes, L.fixed_end)) return rc;
   if (batch == 0) return PKC_OK;
-  if (!q || !k_prefix || !v_prefix || !k_cache || !v_cache || !block_table || !cache_seqlens || !o || !lse)
+  // The prefix tensors may be NULL when no group has a prefix token (a
+  // shard of the keys that holds none of the prefixes).
+  const bool no_prefix_tokens =
+      prefix_kv_indptr_host && n_prefix >= 1 && prefix_kv_indptr_host[n_prefix] == prefix_kv_indptr_host[0];
+  if (!q || ((!k_prefix || !v_prefix) && !no_prefix_tokens) || !k_cache || !v_cache || !block_table ||
+      !cache_seqlens || !o || !lse)
     return set_error(PKC_ERR_INVALID_ARG, "cascade_decode: NULL pointer");
   if (!aligned16(q) || !aligned16(k_prefix) || !aligned16(v_prefix) || !aligned16(k_cache) ||
       !aligned16(v_cache) || !aligned16(o))
@@ -797,7 +825,7 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   cp.suffix_o = reinterpret_cast<const float*>(dp.o_direct); cp.suffix_lse = dp.lse_direct;
   cp.part_o = dp.part_o; cp.part_lse = dp.part_lse;
   fill_contract_prefix(cp, S);
-  cp.o = o; cp.lse = lse; cp.out_dtype = dtype; cp.status = status;
+  cp.o = o; cp.lse = lse; cp.out_dtype = o_dtype; cp.status = status;
   e = launch_contract(cp, batch, stream);
   if (e) return cuda_error(e, "contraction launch");
   mark(3);
@@ -819,6 +847,22 @@ int pkc_cascade_decode(const void* q, const void* k_prefix, const void* v_prefix
   return cascade_impl(q, k_prefix, v_prefix, prefix_kv_indptr_host, rb, re, n_prefix, k_cache, v_cache, block_table,
                       block_table_stride, cache_seqlens, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
                       num_pages, sm_scale, plan_host, workspace, workspace_bytes, o, lse, dtype, stream);
+}
+
+int pkc_cascade_decode_state(const void* q, const void* k_prefix, const void* v_prefix,
+                             const int32_t* prefix_kv_indptr_host, const int32_t* prefix_req_indptr_host,
+                             int n_prefix, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                             int block_table_stride, const int32_t* cache_seqlens, int batch, int num_qo_heads,
+                             int num_kv_heads, int head_dim, int page_size, int64_t num_pages, float sm_scale,
+                             const int32_t* plan_host, void* workspace, size_t workspace_bytes, float* o, float* lse,
+                             int dtype, void* stream) {
+  int32_t rb[PKC_MAX_PREFIX], re[PKC_MAX_PREFIX];
+  if (int rc = check_attn_dims(batch, num_qo_heads, num_kv_heads, head_dim, dtype)) return rc;
+  if (int rc = indptr_ranges(prefix_req_indptr_host, n_prefix, rb, re)) return rc;
+  return cascade_impl(q, k_prefix, v_prefix, prefix_kv_indptr_host, rb, re, n_prefix, k_cache, v_cache, block_table,
+                      block_table_stride, cache_seqlens, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                      num_pages, sm_scale, plan_host, workspace, workspace_bytes, o, lse, dtype, stream, nullptr,
+                      nullptr, PKC_F32);
 }
 
 int pkc_cascade_decode_paged_prefix(

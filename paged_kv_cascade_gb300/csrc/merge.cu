@@ -130,12 +130,40 @@ __global__ void __launch_bounds__(256) merge2_kernel(const T* __restrict__ va, c
   }
 }
 
-// n-ary: v [T, n, H, D], s [T, n, H] -> [T, H, D], [T, H].
-template <typename T>
+// N floats of a row written to an output of type TO at element offset off
+// (N = the input vector's width: 4 for fp32 inputs, 8 for 16-bit ones).
+template <typename TO, int N> struct Out;
+template <int N> struct Out<float, N> {
+  static __device__ __forceinline__ void store(float* o, int64_t off, const float* f) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) *reinterpret_cast<float4*>(o + off + i) = make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
+  }
+};
+template <typename H, int N> struct Out16 {
+  static __device__ __forceinline__ void store(H* o, int64_t off, const float* f) {
+    if constexpr (N == 8) {
+      uint4 u;
+      u.x = Elem<H>::from_f2(f[0], f[1]); u.y = Elem<H>::from_f2(f[2], f[3]);
+      u.z = Elem<H>::from_f2(f[4], f[5]); u.w = Elem<H>::from_f2(f[6], f[7]);
+      *reinterpret_cast<uint4*>(o + off) = u;
+    } else {
+      static_assert(N == 4, "row vector width");
+      *reinterpret_cast<uint2*>(o + off) = make_uint2(Elem<H>::from_f2(f[0], f[1]), Elem<H>::from_f2(f[2], f[3]));
+    }
+  }
+};
+template <int N> struct Out<__half, N> : Out16<__half, N> {};
+template <int N> struct Out<__nv_bfloat16, N> : Out16<__nv_bfloat16, N> {};
+
+// n-ary: v [T, n, H, D], s [T, n, H] -> [T, H, D], [T, H]; the output may
+// have another element type than the states (TO: fp32 states merged into
+// a 16-bit result, rounded once).
+template <typename T, typename TO = T>
 __global__ void __launch_bounds__(256) mergen_kernel(const T* __restrict__ v, const float* s,
-                                                     T* vo, float* so, int64_t n_tokens,
+                                                     TO* vo, float* so, int64_t n_tokens,
                                                      int n_states, int n_heads, int cpr) {
   using V = Vec<T>;
+  using W = Out<TO, V::N>;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (gridDim.x * (int64_t)blockDim.x) >> 5;
@@ -192,7 +220,7 @@ __global__ void __launch_bounds__(256) mergen_kernel(const T* __restrict__ v, co
         }
       }
       if (active) {
-        V::store(vo + (row * cpr + chunk0) * V::N, acc);
+        W::store(vo, (row * cpr + chunk0) * V::N, acc);
         if (chunk0 == 0) so[row] = m == neg_inf() ? neg_inf() : m + lg2(den) * kLn2;
       }
     }
@@ -240,7 +268,7 @@ __global__ void __launch_bounds__(256) mergen_kernel(const T* __restrict__ v, co
             for (int k = 0; k < V::N; ++k) acc[k] += w * x[k];
           }
         }
-        V::store(vo + (row * cpr + c) * V::N, acc);
+        W::store(vo, (row * cpr + c) * V::N, acc);
       }
     }
     __syncwarp();
@@ -272,6 +300,24 @@ int launch_merge_state(const void* va, const float* sa, const void* vb, const fl
   else
     merge2_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)va, sa, (const __nv_bfloat16*)vb, sb,
                                                        (__nv_bfloat16*)vo, so, rows, cpr);
+  return (int)cudaGetLastError();
+}
+
+int launch_merge_states_to(const void* v, const float* s, void* vo, float* so, int64_t n_tokens, int n_states,
+                           int n_heads, int head_dim, int dtype, int out_dtype, void* stream) {
+  if (out_dtype == dtype) return launch_merge_states(v, s, vo, so, n_tokens, n_states, n_heads, head_dim, dtype, stream);
+  if (dtype != PKC_F32) return (int)cudaErrorInvalidValue;  // 16-bit states are merged into their own type
+  const int cpr = head_dim * 4 / 16;
+  const int rpw = cpr >= 32 ? 1 : 32 / cpr;
+  const int64_t rows = n_tokens * n_heads;
+  const int grid = grid_for((rows + rpw - 1) / rpw);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (out_dtype == PKC_F16)
+    mergen_kernel<float, __half><<<grid, 256, 0, st>>>((const float*)v, s, (__half*)vo, so, n_tokens, n_states,
+                                                       n_heads, cpr);
+  else
+    mergen_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>((const float*)v, s, (__nv_bfloat16*)vo, so, n_tokens,
+                                                              n_states, n_heads, cpr);
   return (int)cudaGetLastError();
 }
 

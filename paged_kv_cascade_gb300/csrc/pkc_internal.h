@@ -170,6 +170,10 @@ int launch_merge_state(const void* va, const float* sa, const void* vb,
 int launch_merge_states(const void* v, const float* s, void* vo, float* so,
                         int64_t n_tokens, int n_states, int n_heads,
                         int head_dim, int dtype, void* stream);
+// The same with an output of out_dtype (fp32 states into a 16-bit result).
+int launch_merge_states_to(const void* v, const float* s, void* vo, float* so,
+                           int64_t n_tokens, int n_states, int n_heads,
+                           int head_dim, int dtype, int out_dtype, void* stream);
 // Paged decode: q of dtype (PKC_F16 / PKC_BF16) against a cache of
 // kv_dtype (the same, or PKC_E4M3 with an fp16 q); picks the tensor-core
 // kernel or the CUDA-core kernel.

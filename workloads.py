@@ -305,6 +305,44 @@ def noncascade_problem(p, seed, poison=False):
     return out
 
 
+def shard_problem(p, rank, world, shard_range):
+    """Rank `rank`'s part of a problem's keys when they are sharded over
+    `world` devices: for each prefix group the token slice
+    shard_range(L_j, rank, world, 1) of its prefix, and for each request the
+    page-aligned slice shard_range(len_b, rank, world, page_size) of its
+    cached suffix (its block table row cut to those pages; the page pool is
+    kept whole).  The requests, queries and prefix grouping are unchanged.
+    Returns a problem dict of the same form."""
+    ps = p["page_size"]
+    ind = p["prefix_kv_indptr"]
+    parts, new_ind = [], [0]
+    for j in range(len(ind) - 1):
+        lo, hi = shard_range(int(ind[j + 1] - ind[j]), rank, world, 1)
+        if p["k_prefix"] is not None and hi > lo:
+            parts.append((int(ind[j]) + lo, int(ind[j]) + hi))
+        new_ind.append(new_ind[-1] + (hi - lo))
+    kp = vp = None
+    if p["k_prefix"] is not None:
+        shape = (new_ind[-1],) + p["k_prefix"].shape[1:]
+        kp = np.concatenate([p["k_prefix"][a:b] for a, b in parts]) if parts else np.zeros(shape, p["k_prefix"].dtype)
+        vp = np.concatenate([p["v_prefix"][a:b] for a, b in parts]) if parts else np.zeros(shape, p["v_prefix"].dtype)
+    lens = p["cache_seqlens"]
+    B = len(lens)
+    rows, new_lens = [], np.zeros(B, np.int32)
+    for b in range(B):
+        lo, hi = shard_range(int(lens[b]), rank, world, ps)
+        rows.append(p["block_table"][b, lo // ps:(hi + ps - 1) // ps])
+        new_lens[b] = hi - lo
+    width = max(1, max((len(r) for r in rows), default=1))
+    bt = np.full((B, width), -1, np.int32)
+    for b, r in enumerate(rows):
+        bt[b, :len(r)] = r
+    out = dict(p)
+    out.update(k_prefix=kp, v_prefix=vp, prefix_kv_indptr=np.asarray(new_ind, np.int32),
+               block_table=bt, cache_seqlens=new_lens)
+    return out
+
+
 def make_merge(*, tokens, heads, d, n_states, seed, v_dtype="f32", threads=8,
                **_ignored):
     """merge_state inputs: two states per (token, head), plus n stacked.

@@ -65,6 +65,9 @@ def parse_args():
     ap.add_argument("--decode-schedule", choices=["dynamic", "static"], default="dynamic",
                     help="planned decode: blocks take the plan's chunks from a shared "
                          "longest-first queue (dynamic) or run their CTA's plan list (static)")
+    ap.add_argument("--contraction", choices=["fused", "separate"], default="fused",
+                    help="split states contracted inside the attention kernels (fused) or by a "
+                         "standalone contraction kernel after them")
     ap.add_argument("--num-ctas", type=int, default=None,
                     help="CTAs of the host plan (default: the workload's)")
     ap.add_argument("--prefix-ctas", type=int, default=0,
@@ -442,9 +445,9 @@ def _gbs(nbytes, ms):
     return nbytes / (ms / 1e3) / 1e9
 
 
-def _entry(ctx, nbytes, ms, n, clocks, **kw):
+def _entry(ctx, nbytes, ms, steps, clocks, **kw):
     e = {"us_per_step": 1e3 * ms, "value": _gbs(nbytes, ms), "unit": "GB/s",
-         "frac": _gbs(nbytes, ms) / ctx.hbm_peak, "effective_bytes": int(nbytes), "steps": n,
+         "frac": _gbs(nbytes, ms) / ctx.hbm_peak, "effective_bytes": int(nbytes), "steps": steps,
          "clocks": clocks}
     e.update(kw)
     return e
@@ -640,7 +643,7 @@ def measure_merge(ctx):
     b2 = 3 * T * H * (D + 1) * 4
     bn = (n + 1) * T * H * (D + 1) * 4
     return {"binary": _entry(ctx, b2, ms2, k2, c2, kernel="merge2_kernel", launch="direct"),
-            "n_ary": _entry(ctx, bn, msn, kn, cn, kernel="mergen_kernel", n=n, launch="direct"),
+            "n_ary": _entry(ctx, bn, msn, kn, cn, kernel="mergen_kernel", n_states=n, launch="direct"),
             "tokens": T, "heads": H, "head_dim": D, "dtype": "f32"}
 
 
@@ -915,6 +918,7 @@ def main():
     pkc.set_decode_kernel(args.decode_kernel)
     pkc.set_decode_schedule(args.decode_schedule)
     pkc.set_prefix_ctas(args.prefix_ctas)
+    pkc.set_contraction(args.contraction)
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from pkc_testing import to_device
     ctx = make_ctx(args, torch, pkc, local)
@@ -1050,6 +1054,25 @@ def main():
                     "blocks take the same plan's chunks from a longest-first device queue"}
         del gs2
 
+    # ---- where the split states are contracted: inside the attention
+    # kernels (fused) or by the standalone contraction kernel after them ----
+    contractions = None
+    if world == 1:
+        other_c = "separate" if args.contraction == "fused" else "fused"
+        pkc.set_contraction(other_c)
+        gs3 = GraphStepper(torch, pkc, run, lens, num_ctas, cfg, ws_bytes, ctx.device)
+        ms3, n3, clk3 = time_loop(ctx, gs3.step, gs3.stream, K)
+        if not gs3.status_ok():
+            raise RuntimeError("device status after the other contraction")
+        pkc.set_contraction(args.contraction)
+        ms4, n4, clk4 = time_loop(ctx, gs.step, gs.stream, K)
+        contractions = {args.contraction: {"us_per_step": 1e3 * ms4, "steps": n4, "clocks": clk4},
+                        other_c: {"us_per_step": 1e3 * ms3, "steps": n3, "clocks": clk3},
+                        "note": "graph-replayed steps timed back to back; fused = the kernel writing "
+                                "a (request, KV head)'s last source merges it (no contraction "
+                                "launch); separate = contraction kernel after both stages"}
+        del gs3
+
     eff = workloads.effective_bytes(p)
     ms_per_step = g_ms / K
     value = whole_job_gbs(eff, 1, world, ms_per_step / 1e3)
@@ -1106,6 +1129,7 @@ def main():
             "dtype": cfg["dtype"], "data": "synthetic",
             "config": line_config(args.workload, cfg, p, num_ctas, args, world, {
                 "launch": "cuda_graph", "decode_kernel": args.decode_kernel,
+                "contraction": args.contraction,
                 "decode_schedule": args.decode_schedule if num_ctas else None,
                 "prefix_ctas": args.prefix_ctas or "auto",
                 "step": "host plan + plan upload + prefix states + paged decode + contraction"}),
@@ -1125,9 +1149,10 @@ def main():
             "graph": {"isolated_replay_us_median": {"l2_flushed": iso[True], "unflushed": iso[False],
                                                     "flush_bytes": 256 << 20, "replays": n_iso}},
             "decode_schedules": schedules,
+            "contractions": contractions,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 3 * K,
+            "gpu_launches": (2 if args.contraction == "fused" else 3) * K,
             "clocks": clocks,
             "configs": configs,
         }

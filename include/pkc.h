@@ -219,8 +219,10 @@ int pkc_plan_upload(const int32_t* plan_host, void* workspace,
  * (pkc_plan_words for `batch` decode requests and num_ctas CTAs, 0 when
  * num_ctas is 0); the suffix states [batch, Hq, D+1] float32; the suffix
  * partials [2 * num_ctas, Hq, D+1] float32 (appendix D bound
- * 2 * #CTA * T_q * H * (D+1) with T_q = 1); and prefix_splits copies of
- * [batch, Hq, D+1] float32 for prefix partial states.
+ * 2 * #CTA * T_q * H * (D+1) with T_q = 1); the fused contraction's
+ * arrival counters [batch, Hq] int32 (zeroed by every call that uses them);
+ * and prefix_splits copies of [batch, Hq, D+1] float32 for prefix partial
+ * states.
  *   num_ctas: CTAs of the plan the calls will use (0 if none).
  *   prefix_splits: partial-state slots for the shared prefix (0 if no
  *                  prefix).  The prefix stage spreads the KV tiles of all
@@ -549,6 +551,28 @@ int pkc_set_decode_kernel(int which);
  * plan.  Returns PKC_ERR_INVALID_ARG for any other value.
  */
 int pkc_set_decode_schedule(int dynamic);
+
+/*
+ * Where split states are contracted into the output (process-wide):
+ *   1 = fused (default): the attention kernels do it themselves (MLSys'25
+ *       notes, A3: attention and contraction in one persistent kernel).
+ *       Every kernel that writes a state that is not yet a final output --
+ *       a chunk's partial state, a cascade's suffix state, a prefix piece --
+ *       adds one to the arrival counter of its (request, KV head) pair;
+ *       the warp whose count is the pair's last merges the pair's sources
+ *       with (+) and writes the final O and LSE.  No kernel waits for
+ *       another.  A planned pkc_paged_decode_state is then one kernel
+ *       launch, a cascade the prefix and decode kernels.  Each such call
+ *       first zeroes its counters (cudaMemsetAsync of batch * num_kv_heads
+ *       int32 in the workspace).  Cascades with more than 16 prefix groups
+ *       use the standalone kernel.
+ *   0 = a standalone contraction kernel after the attention kernels.
+ * The two give the same bits: one routine merges a row's sources in the
+ * same order either way.  pkc_prefix_attention_state and
+ * pkc_paged_decode_state_noalloc always use the standalone kernel.
+ * Returns PKC_ERR_INVALID_ARG for any other value.
+ */
+int pkc_set_contraction(int fused);
 
 /*
  * Thread blocks of the prefix stage in the cascade calls and

@@ -59,6 +59,7 @@ SIGNATURES = {
     "pkc_set_stage_events": (_I, [_c.POINTER(_P), _I]),
     "pkc_set_decode_kernel": (_I, [_I]),
     "pkc_set_decode_schedule": (_I, [_I]),
+    "pkc_set_contraction": (_I, [_I]),
     "pkc_set_prefix_ctas": (_I, [_I]),
     "pkc_last_launch_blocks": (_I, [_c.POINTER(_c.c_int), _c.POINTER(_c.c_int)]),
     "pkc_selftest_wait_timeout": (_I, [_P, _SZ, _c.POINTER(_c.c_int32), _P]),
@@ -372,6 +373,12 @@ def set_decode_schedule(which):
     from a shared longest-first queue; default) or "static" (each block runs
     its CTA's list of the plan); process-wide."""
     _check(lib().pkc_set_decode_schedule(DECODE_SCHEDULES[which]))
+
+
+def set_contraction(which):
+    """'fused' (default): the attention kernels contract split states
+    themselves; 'separate': a standalone contraction kernel after them."""
+    _check(lib().pkc_set_contraction({"fused": 1, "separate": 0}[which]))
 
 
 def set_prefix_ctas(n):

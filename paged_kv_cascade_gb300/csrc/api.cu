@@ -91,6 +91,7 @@ WsLayout ws_layout(int batch, int hq, int d, int num_ctas) {
   const size_t prow = (size_t)2 * num_ctas * hq;
   L.part_o = off;     off += al256(4 * prow * d);
   L.part_lse = off;   off += al256(4 * prow);
+  L.arrive = off;     off += al256(4 * rows);  // per (request, KV head) <= per (request, query head)
   L.fixed_end = off;
   L.prefix = off;
   L.prefix_split = al256(4 * rows * d) + al256(4 * rows);
@@ -379,6 +380,50 @@ void contract_plan_offsets(ContractParams& c, const int32_t* plan_host) {
   c.off_unit_partial_begin = plan_host[PKC_PLAN_OFF_UNIT_PARTIAL_BEGIN];
 }
 
+// Contraction fused into the attention kernels (1, default) or the
+// standalone contraction kernel after them (0): pkc_set_contraction.
+std::atomic<int> g_fused_contraction{1};
+
+// The fused contraction's view of a call: the same sources, offsets and
+// output as the standalone kernel's ContractParams (c), plus the counters.
+void fill_fuse(FuseParams& f, const ContractParams& c, int hkv, int32_t* arrive) {
+  std::memset(&f, 0, sizeof(f));
+  f.enabled = 1;
+  f.arrive = arrive;
+  f.batch = c.batch;
+  f.hq = c.hq;
+  f.hkv = hkv;
+  f.g = c.hq / hkv;
+  f.plan = c.plan;
+  f.off_unit_n_chunks = c.off_unit_n_chunks;
+  f.off_unit_partial_begin = c.off_unit_partial_begin;
+  f.suffix_o = c.suffix_o;
+  f.suffix_lse = c.suffix_lse;
+  f.part_o = c.part_o;
+  f.part_lse = c.part_lse;
+  if (c.prefix_o && c.n_prefix <= PKC_FUSE_MAX_PREFIX) {
+    f.prefix_o = c.prefix_o;
+    f.prefix_lse = c.prefix_lse;
+    f.prefix_stride_o = c.prefix_stride_o;
+    f.prefix_stride_lse = c.prefix_stride_lse;
+    f.n_prefix = c.n_prefix;
+    f.prefix_blocks = c.prefix_blocks;
+    f.prefix_tiles = c.prefix_tiles;
+    for (int j = 0; j < c.n_prefix; ++j) {
+      f.prefix_req_begin[j] = c.prefix_req_begin[j];
+      f.prefix_req_end[j] = c.prefix_req_end[j];
+      f.prefix_slot_base[j] = c.prefix_slot_base[j];
+    }
+    for (int j = 0; j <= c.n_prefix; ++j) {
+      f.prefix_kv_indptr[j] = c.prefix_kv_indptr[j];
+      f.prefix_kvt_indptr[j] = c.prefix_kvt_indptr[j];
+    }
+  }
+  f.o = c.o;
+  f.lse = c.lse;
+  f.out_dtype = c.out_dtype;
+}
+
 }  // namespace
 
 extern "C" {
@@ -537,16 +582,26 @@ int paged_decode_impl(const void* q, const void* k_cache, const void* v_cache, c
   dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
   dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   dp.status = status;
+  // Split requests' chunk partials are contracted into the output: by the
+  // decode kernel itself (fused; counters zeroed first), or by the
+  // contraction kernel after it.
+  ContractParams cp;
+  std::memset(&cp, 0, sizeof(cp));
+  cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractPlanUnits; cp.plan = dp.plan;
+  contract_plan_offsets(cp, plan_host);
+  cp.part_o = dp.part_o; cp.part_lse = dp.part_lse;
+  cp.o = o; cp.lse = lse; cp.out_dtype = dtype; cp.status = status;
+  const bool fused = plan_host && g_fused_contraction.load() != 0;
+  if (fused) {
+    int32_t* arrive = reinterpret_cast<int32_t*>(ws + L.arrive);
+    const cudaError_t me = cudaMemsetAsync(arrive, 0, 4 * (size_t)batch * num_kv_heads, (cudaStream_t)stream);
+    if (me) return cuda_error(me, "paged decode: counter reset");
+    fill_fuse(dp.fuse, cp, num_kv_heads, arrive);
+  }
   int e = launch_paged_decode(dp, plan_host ? num_ctas : batch, dtype, kv_dtype, stream);
   if (e == -1) return set_error(PKC_ERR_CUDA, "paged decode: could not build TMA tensor maps");
   if (e) return cuda_error(e, "paged decode launch");
-  if (plan_host) {
-    ContractParams cp;
-    std::memset(&cp, 0, sizeof(cp));
-    cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractPlanUnits; cp.plan = dp.plan;
-    contract_plan_offsets(cp, plan_host);
-    cp.part_o = dp.part_o; cp.part_lse = dp.part_lse;
-    cp.o = o; cp.lse = lse; cp.out_dtype = dtype; cp.status = status;
+  if (plan_host && !fused) {
     e = launch_contract(cp, batch, stream);
     if (e) return cuda_error(e, "contraction launch");
   }
@@ -621,6 +676,13 @@ int pkc_last_launch_blocks(int* prefix_blocks, int* decode_blocks) {
   if (!prefix_blocks || !decode_blocks) return set_error(PKC_ERR_INVALID_ARG, "last_launch_blocks: NULL pointer");
   *prefix_blocks = g_last_prefix_blocks;
   *decode_blocks = g_last_decode_blocks;
+  return PKC_OK;
+}
+
+int pkc_set_contraction(int fused) {
+  if (fused != 0 && fused != 1)
+    return set_error(PKC_ERR_INVALID_ARG, "set_contraction: fused must be 0 or 1 (got %d)", fused);
+  g_fused_contraction.store(fused);
   return PKC_OK;
 }
 
@@ -770,6 +832,32 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
     if (r) return cuda_error(r, "prefix launch");
     return PKC_OK;
   };
+  // 3. (planned now, launched last or fused) contraction + merge: prefix
+  // pieces (+) suffix states -> final O, LSE
+  ContractParams cp;
+  std::memset(&cp, 0, sizeof(cp));
+  cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractAllRequests;
+  cp.plan = plan_host ? reinterpret_cast<const int32_t*>(ws + L.plan) : nullptr;
+  contract_plan_offsets(cp, plan_host);
+  cp.suffix_o = reinterpret_cast<const float*>(ws + L.suffix_o);
+  cp.suffix_lse = reinterpret_cast<const float*>(ws + L.suffix_lse);
+  cp.part_o = reinterpret_cast<const float*>(ws + L.part_o);
+  cp.part_lse = reinterpret_cast<const float*>(ws + L.part_lse);
+  fill_contract_prefix(cp, S);
+  cp.o = o; cp.lse = lse; cp.out_dtype = o_dtype; cp.status = status;
+  // Fused: both stages' kernels count the sources they write, and the
+  // writer of a (request, KV head) pair's last source merges the pair; the
+  // counters are zeroed first, on the caller's stream before the fork.
+  const bool fused = g_fused_contraction.load() != 0 && n_prefix <= PKC_FUSE_MAX_PREFIX;
+  FuseParams fuse;
+  std::memset(&fuse, 0, sizeof(fuse));
+  if (fused) {
+    int32_t* arrive = reinterpret_cast<int32_t*>(ws + L.arrive);
+    const cudaError_t me = cudaMemsetAsync(arrive, 0, 4 * (size_t)batch * num_kv_heads, (cudaStream_t)stream);
+    if (me) return cuda_error(me, "cascade: counter reset");
+    fill_fuse(fuse, cp, num_kv_heads, arrive);
+    S.pp.fuse = fuse;
+  }
   int e = 0;
   if (side) {
     e = (int)cudaEventRecord(side->fork, (cudaStream_t)stream);
@@ -795,6 +883,7 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
   dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   dp.status = status;
+  dp.fuse = fuse;
   g_last_prefix_blocks = S.pp.n_blocks;
   g_last_decode_blocks = decode_blocks;
   e = launch_paged_decode(dp, decode_blocks, dtype, dtype, stream);
@@ -817,17 +906,10 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
     if (e) return cuda_error(e, "cascade: stream join");
   }
   mark(2);
-  // 3. contraction + merge: prefix splits (+) suffix chunks -> final O, LSE
-  ContractParams cp;
-  std::memset(&cp, 0, sizeof(cp));
-  cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractAllRequests; cp.plan = dp.plan;
-  contract_plan_offsets(cp, plan_host);
-  cp.suffix_o = reinterpret_cast<const float*>(dp.o_direct); cp.suffix_lse = dp.lse_direct;
-  cp.part_o = dp.part_o; cp.part_lse = dp.part_lse;
-  fill_contract_prefix(cp, S);
-  cp.o = o; cp.lse = lse; cp.out_dtype = o_dtype; cp.status = status;
-  e = launch_contract(cp, batch, stream);
-  if (e) return cuda_error(e, "contraction launch");
+  if (!fused) {
+    e = launch_contract(cp, batch, stream);
+    if (e) return cuda_error(e, "contraction launch");
+  }
   mark(3);
   return PKC_OK;
 }

@@ -36,6 +36,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "contract_common.cuh"
 #include "decode_common.cuh"
 #include "pkc_device.cuh"
 #include "pkc_internal.h"
@@ -120,7 +121,7 @@ struct HeadShift {
 template <typename T, int G, int HG>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                        const DecodeParams p) {
+                        const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<HG>;
   constexpr int kStages = Cfg::kStages;
   constexpr int kWph = Cfg::kWph;
@@ -280,6 +281,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
 
   // ------------------------------ consumers ------------------------------
+  // Fused contraction: rows that no kernel will write (empty requests) get
+  // the empty state, spread over the blocks' first consumer warps.
+  if (p.fuse.enabled && warp == 0)
+    fuse_write_empty(p.fuse, (int)(blockIdx.x + gridDim.x * blockIdx.y), (int)(gridDim.x * gridDim.y), lane);
   const int half = lane >> 4, sub = lane & 15;
   const int hh = warp % HG;       // KV head within the group
   const int cls = warp / HG;      // which pairs of rows of the stage
@@ -497,12 +502,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
       }
     }
+    // A state that is not the request's final output is one source of the
+    // fused contraction: count it; the last source's warp merges the pair.
+    if (p.fuse.enabled && (out_slot >= 0 || p.direct_f32)) fuse_arrive(p.fuse, req, kvh, lane);
   }
 }
 
-// One warp per (row, head): (+) over every state that belongs to the row,
-// lane i owning dims 4i..4i+3.
-__global__ void __launch_bounds__(256, 4) contract_kernel(const ContractParams p) {
+// One warp per (row, head): (+) over every state that belongs to the row
+// (contract_row), after the stages that wrote them.
+__global__ void __launch_bounds__(256, 4) contract_kernel(const __grid_constant__ ContractParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t row_idx = gw / p.hq;
@@ -518,126 +526,7 @@ __global__ void __launch_bounds__(256, 4) contract_kernel(const ContractParams p
     unit = pl[p.off_unit_list + row_idx];
     req = pl[p.off_unit_req + unit];
   }
-  // Running state of the merge: maximum m, denominator den, unnormalised
-  // acc.  Sources go in batches of 4 whose loads are all in flight
-  // together; the running state is rescaled between batches.  (Batches of 4
-  // keep the kernel at 56 registers, 4 blocks per SM: more rows in flight
-  // than batches of 8 at 3 blocks per SM.)
-  constexpr int kB = 4;
-  float m = neg_inf(), den = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int64_t row_off = (int64_t)req * p.hq + h;
-  // Sources: the prefix pieces of every group holding the request (one
-  // group in a two-level cascade, several in a multi-level one), then the
-  // suffix.  Group j's pair covering flat KV tiles [a, a + kvt) was computed
-  // in pieces by the prefix blocks block_of(a) .. block_of(a + kvt - 1),
-  // piece i in partial slot slot_base[j] + i.  One pass per group; the last
-  // pass also takes the suffix, so a two-level row is a single pass.
-  auto in_group = [&](int j) { return p.prefix_req_begin[j] <= req && req < p.prefix_req_end[j]; };
-  auto next_group = [&](int j) {  // first group after j holding the request, or -1
-    if (!p.prefix_o) return -1;
-    for (++j; j < p.n_prefix; ++j)
-      if (in_group(j)) return j;
-    return -1;
-  };
-  // Pieces of group j's pair holding this row: count and first partial slot.
-  auto group_pieces = [&](int j, int& n_pref, int& base) {
-    n_pref = 0;
-    base = 0;
-    if (j < 0) return;
-    const int kvt = (p.prefix_kv_indptr[j + 1] - p.prefix_kv_indptr[j] + 127) / 128;
-    if (kvt > 0 && p.prefix_tiles > 0) {
-      const int rr = (req - p.prefix_req_begin[j]) * p.g + h % p.g;  // row within the group's rows
-      const int pair = (rr / 128) * p.hkv + h / p.g;
-      // block_of(x) = ((x + 1) C - 1) / T, in 32 bits (the host keeps T C < 2^31)
-      const int a = p.prefix_kvt_indptr[j] + pair * kvt;
-      const int T = (int)p.prefix_tiles, C = p.prefix_blocks;
-      n_pref = ((a + kvt) * C - 1) / T - ((a + 1) * C - 1) / T + 1;
-      base = p.prefix_slot_base[j];
-    }
-  };
-  auto prefix_lse = [&](int slot) { return p.prefix_lse + (int64_t)slot * p.prefix_stride_lse + row_off; };
-  auto prefix_o = [&](int slot) { return p.prefix_o + (int64_t)slot * p.prefix_stride_o + row_off * D; };
-  // The first group's first batch of prefix pieces depends on no plan word:
-  // its loads go out before the plan's words are read, so both arrive in
-  // one memory round trip.
-  int j = next_group(-1), n_pref = 0, base = 0;
-  group_pieces(j, n_pref, base);
-  float ls[kB];
-  float4 xs[kB];
-#pragma unroll
-  for (int k = 0; k < kB; ++k) {
-    const bool in = k < n_pref;
-    ls[k] = in ? *prefix_lse(base + k) : neg_inf();
-    xs[k] = in ? *reinterpret_cast<const float4*>(prefix_o(base + k) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  int suf_kind = 0, suf_begin = 0, suf_n = 0;  // 1: direct state, 2: partial slots
-  if (pl) {
-    const int nch = pl[p.off_unit_n_chunks + unit];       // both loads in flight together
-    const int pbeg = pl[p.off_unit_partial_begin + unit];
-    if (nch >= 2) { suf_kind = 2; suf_begin = pbeg; suf_n = nch; }
-    else if (nch == 1 && p.suffix_o) { suf_kind = 1; suf_n = 1; }
-  } else if (p.suffix_o) {
-    suf_kind = 1; suf_n = 1;
-  }
-  bool preloaded = true;  // ls / xs hold the first batch's prefix pieces
-  for (;;) {
-    const int jn = j >= 0 ? next_group(j) : -1;
-    const int n_suf = jn < 0 ? suf_n : 0;  // the last pass takes the suffix
-    const int n_src = n_pref + n_suf;
-    auto src_lse = [&](int i) -> const float* {
-      if (i < n_pref) return prefix_lse(base + i);
-      if (suf_kind == 1) return p.suffix_lse + row_off;
-      return p.part_lse + (int64_t)(suf_begin + i - n_pref) * p.hq + h;
-    };
-    auto src_o = [&](int i) -> const float* {
-      if (i < n_pref) return prefix_o(base + i);
-      if (suf_kind == 1) return p.suffix_o + row_off * D;
-      return p.part_o + ((int64_t)(suf_begin + i - n_pref) * p.hq + h) * D;
-    };
-    for (int i0 = 0; i0 < n_src; i0 += kB) {
-#pragma unroll
-      for (int k = 0; k < kB; ++k) {
-        if (preloaded && k < n_pref) continue;  // loaded before the plan's words
-        const bool in = i0 + k < n_src;
-        ls[k] = in ? *src_lse(i0 + k) : neg_inf();
-        xs[k] = in ? *reinterpret_cast<const float4*>(src_o(i0 + k) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      preloaded = false;
-      float mb = m;
-#pragma unroll
-      for (int k = 0; k < kB; ++k) mb = fmaxf(mb, ls[k]);
-      if (mb == neg_inf()) continue;
-      const float c = ex2((m - mb) * kLog2e);  // 0 when m is -inf
-      den *= c;
-      acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
-#pragma unroll
-      for (int k = 0; k < kB; ++k) {
-        const float w = ex2((ls[k] - mb) * kLog2e);  // 0 for empty states
-        den += w;
-        acc.x = fmaf(w, xs[k].x, acc.x); acc.y = fmaf(w, xs[k].y, acc.y);
-        acc.z = fmaf(w, xs[k].z, acc.z); acc.w = fmaf(w, xs[k].w, acc.w);
-      }
-      m = mb;
-    }
-    preloaded = false;
-    if (jn < 0) break;
-    j = jn;
-    group_pieces(j, n_pref, base);
-  }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-  const int64_t row = (int64_t)req * p.hq + h;
-  if (p.out_dtype == PKC_F32) {
-    *reinterpret_cast<float4*>(static_cast<float*>(p.o) + row * D + lane * 4) = acc;
-  } else if (p.out_dtype == PKC_F16) {
-    uint2 u = make_uint2(Elem<__half>::from_f2(acc.x, acc.y), Elem<__half>::from_f2(acc.z, acc.w));
-    *reinterpret_cast<uint2*>(static_cast<__half*>(p.o) + row * D + lane * 4) = u;
-  } else {
-    uint2 u = make_uint2(Elem<__nv_bfloat16>::from_f2(acc.x, acc.y), Elem<__nv_bfloat16>::from_f2(acc.z, acc.w));
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + row * D + lane * 4) = u;
-  }
-  if (lane == 0) p.lse[row] = den > 0.f ? m + lg2(den) * kLn2 : neg_inf();
+  contract_row(p, req, unit, h, lane);
 }
 
 template <typename T, int G, int HG>

@@ -42,6 +42,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "contract_common.cuh"
 #include "decode_common.cuh"
 #include "pkc_device.cuh"
 #include "pkc_internal.h"
@@ -118,7 +119,7 @@ __device__ __forceinline__ float shfl_sum_rows(float v) {
 template <int KV, int G, int HG>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                            const DecodeParams p) {
+                            const __grid_constant__ DecodeParams p) {
   using C = Cfg<KV, HG>;
   using T = typename KvTraits<KV>::Q;
   constexpr bool kFp8 = C::kFp8;
@@ -281,6 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------ consumers ------------------------------
+  // Fused contraction: rows that no kernel will write (empty requests) get
+  // the empty state, spread over the blocks' first consumer warps.
+  if (p.fuse.enabled && warp == 0)
+    fuse_write_empty(p.fuse, (int)(blockIdx.x + gridDim.x * blockIdx.y), (int)(gridDim.x * gridDim.y), lane);
   const int hh = warp % HG;   // KV head within the group
   const int cls = warp / HG;  // which 16 slots of each stage
   const int g = lane >> 2, tg = lane & 3;  // fragment row group / thread in group
@@ -489,6 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g == 0) p.lse_direct[row] = lse;
         }
       }
+      // A state that is not the request's final output is one source of the
+      // fused contraction: count it; the last source's warp merges the pair.
+      if (p.fuse.enabled && (out_slot >= 0 || p.direct_f32)) fuse_arrive(p.fuse, req, kvh, lane);
     } else {
       // Warps of the same head meet in shared memory (bounded mbarrier wait;
       // buffers alternate between items).
@@ -546,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) p.lse_direct[row] = lse;
         }
       }
+      if (p.fuse.enabled && (out_slot >= 0 || p.direct_f32)) fuse_arrive(p.fuse, req, kvh, lane);
     }
   }
 }

@@ -30,6 +30,7 @@ PlanLayout plan_layout(int64_t n_units, int num_ctas);
 
 // Byte offsets of the workspace regions (see pkc.h, pkc_workspace_size).
 struct WsLayout {
+  size_t arrive;           // fused contraction's arrival counters [batch * hq] int32
   size_t plan;             // plan region
   size_t suffix_o, suffix_lse;
   size_t part_o, part_lse;
@@ -42,6 +43,40 @@ WsLayout ws_layout(int batch, int hq, int d, int num_ctas);
 // ---------------------------------------------------------------------------
 // Kernel parameter blocks (plain data, passed by value to the kernels)
 // ---------------------------------------------------------------------------
+
+// Prefix groups a fused contraction can follow; calls with more groups use
+// the standalone contraction kernel.
+#define PKC_FUSE_MAX_PREFIX 16
+
+// The contraction fused into the attention kernels (contract_common.cuh):
+// the sources of every (request, KV head) pair, the pair's arrival counter
+// and the final output.  Field names follow ContractParams, so one merge
+// routine serves both.
+struct FuseParams {
+  int enabled;              // 1: the kernel that writes a pair's last source merges the pair
+  int32_t* arrive;          // [batch * hkv] arrival counters, zeroed before each call
+  int batch, hq, hkv, g;
+  const int32_t* plan;      // device plan (decode plans: unit = request) or nullptr
+  int32_t off_unit_n_chunks, off_unit_partial_begin;
+  const float* suffix_o;    // direct suffix states (a cascade) or nullptr
+  const float* suffix_lse;
+  const float* part_o;      // partial states of split requests' chunks
+  const float* part_lse;
+  const float* prefix_o;    // prefix pieces [split, B, Hq, D] or nullptr
+  const float* prefix_lse;
+  int64_t prefix_stride_o, prefix_stride_lse;
+  int n_prefix;
+  int prefix_blocks;
+  int64_t prefix_tiles;
+  int32_t prefix_req_begin[PKC_FUSE_MAX_PREFIX];
+  int32_t prefix_req_end[PKC_FUSE_MAX_PREFIX];
+  int32_t prefix_slot_base[PKC_FUSE_MAX_PREFIX];
+  int32_t prefix_kv_indptr[PKC_FUSE_MAX_PREFIX + 1];
+  int32_t prefix_kvt_indptr[PKC_FUSE_MAX_PREFIX + 1];
+  void* o;                  // final O [B, Hq, D] of out_dtype, LSE [B, Hq]
+  float* lse;
+  int out_dtype;
+};
 
 struct DecodeParams {
   const void* q;
@@ -63,6 +98,7 @@ struct DecodeParams {
   float v_scale;          // V = v_scale * stored V (1 for 16-bit caches)
   int dynamic;            // 1: blocks take the plan's chunks from a shared queue
   int32_t* sched;         // the queue's two counters (in the status block)
+  FuseParams fuse;        // fused contraction (fuse.enabled) or none
 };
 
 // Element kinds of a paged KV cache.
@@ -148,6 +184,7 @@ struct PrefixParams {
   int32_t page_indptr[PKC_MAX_PREFIX + 1];
   int page_size;
   int64_t num_pages;
+  FuseParams fuse;                          // fused contraction (fuse.enabled) or none
 };
 
 struct AppendParams {

@@ -43,6 +43,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "contract_common.cuh"
 #include "pkc_device.cuh"
 #include "pkc_internal.h"
 
@@ -115,7 +116,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefix_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ PrefixParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023) != 0) {  // uniform: no thread has started yet
     if (threadIdx.x == 0) report(p.status, PKC_ERR_UNSUPPORTED);
@@ -554,6 +555,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c4 == 0) {
         if (mine_t) p.out_lse[pc.slot * p.split_stride_lse + r_t] = has_t ? (mt_ref + lg2(lt)) * kLn2 : neg_inf();
         if (mine_b) p.out_lse[pc.slot * p.split_stride_lse + r_b] = has_b ? (mb_ref + lg2(lb)) * kLn2 : neg_inf();
+      }
+      // Fused contraction: the piece is one source of every (request, KV
+      // head) pair among the warp's 16 rows (16 / G requests, whose G rows
+      // all lie here).  Lane i counts request i; the warp merges the pairs
+      // whose count was the last.
+      if (p.fuse.enabled && ok) {
+        __syncwarp();
+        const int r0 = b0 + rbase / G;
+        const int rq = r0 + lane;
+        const bool last = lane < 16 / G && rq < req_hi && fuse_count(p.fuse, rq, pc.kvh);
+        unsigned lm = __ballot_sync(0xffffffffu, last);
+        if (lm) {
+          __threadfence();  // the other writers' sources are read after the counts
+          while (lm) {
+            const int i = __ffs(lm) - 1;
+            lm &= lm - 1;
+            fuse_merge(p.fuse, r0 + i, pc.kvh, lane);
+          }
+        }
       }
     }
   }

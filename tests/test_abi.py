@@ -129,10 +129,11 @@ def test_workspace_size_matches_documented_layout(L):
         return (x + 255) // 256 * 256
     B, H, D, C, S = 7, 32, 128, 148, 3
     words = pkc.plan_words(B, C)
+    # status, plan, suffix states, chunk partials, arrival counters, prefix splits
     want = 256 + al(4 * words) + al(4 * B * H * D) + al(4 * B * H) + al(4 * 2 * C * H * D) \
-        + al(4 * 2 * C * H) + S * (al(4 * B * H * D) + al(4 * B * H))
+        + al(4 * 2 * C * H) + al(4 * B * H) + S * (al(4 * B * H * D) + al(4 * B * H))
     assert pkc.workspace_size(B, H, C, S) == want
-    assert pkc.workspace_size(B, H, 0, 0) == 256 + al(4 * B * H * D) + al(4 * B * H)
+    assert pkc.workspace_size(B, H, 0, 0) == 256 + al(4 * B * H * D) + al(4 * B * H) + al(4 * B * H)
 
 
 def _compare_plans(kv, C, T=1, qo=None, alpha=1.0, beta=1.0):

@@ -395,6 +395,8 @@ void fill_fuse(FuseParams& f, const ContractParams& c, int hkv, int32_t* arrive)
   f.hkv = hkv;
   f.g = c.hq / hkv;
   f.plan = c.plan;
+  f.off_unit_list = c.off_unit_list;
+  f.off_unit_req = c.off_unit_req;
   f.off_unit_n_chunks = c.off_unit_n_chunks;
   f.off_unit_partial_begin = c.off_unit_partial_begin;
   f.suffix_o = c.suffix_o;

@@ -50,22 +50,33 @@ __device__ __forceinline__ bool in_group(const CP& p, int j, int req) {
   return p.prefix_req_begin[j] <= req && req < p.prefix_req_end[j];
 }
 
-// One warp: (+) over every source of row (req, h), lane i owning dims
-// 4i .. 4i+3, written as the final O row (out_dtype) and LSE.  `unit` is the
-// request's unit of the plan (the request itself for decode plans).
-template <class CP>
-__device__ __forceinline__ void contract_row(const CP& p, int req, int unit, int h, int lane) {
+// One warp: (+) over every source of rows (req, h0 + r), r < nr <= R, lane i
+// owning dims 4i .. 4i+3 of each, written as the final O rows (out_dtype)
+// and LSEs.  The rows are query heads of one KV head, so they share one row
+// tile of every prefix group and the same sources; they are merged in
+// lockstep so that all their loads are in flight together, each row with
+// exactly the arithmetic it would get alone.  `unit` is the request's unit
+// of the plan (the request itself for decode plans).
+template <int R, class CP>
+__device__ __forceinline__ void contract_rows(const CP& p, int req, int unit, int h0, int nr, int lane) {
   constexpr int D = PKC_HEAD_DIM;
   const int32_t* pl = p.plan;
-  // Running state of the merge: maximum m, denominator den, unnormalised
-  // acc.  Sources go in batches of 4 whose loads are all in flight
-  // together; the running state is rescaled between batches.  (Batches of 4
-  // keep the standalone kernel at 56 registers, 4 blocks per SM: more rows
-  // in flight than batches of 8 at 3 blocks per SM.)
+  // Running state of each row's merge: maximum m, denominator den,
+  // unnormalised acc.  Sources go in batches of 4 whose loads are all in
+  // flight together; the running state is rescaled between batches.
+  // (Batches of 4 keep the standalone kernel at few registers and many rows
+  // in flight per SM: faster than batches of 8.)
   constexpr int kB = 4;
-  float m = neg_inf(), den = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int64_t row_off = (int64_t)req * p.hq + h;
+  float m[R], den[R];
+  float4 acc[R];
+  int64_t row_off[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    m[r] = neg_inf();
+    den[r] = 0.f;
+    acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    row_off[r] = (int64_t)req * p.hq + h0 + (r < nr ? r : 0);
+  }
   // Sources: the prefix pieces of every group holding the request (one
   // group in a two-level cascade, several in a multi-level one), then the
   // suffix.  One pass per group; the last pass also takes the suffix, so a
@@ -76,21 +87,23 @@ __device__ __forceinline__ void contract_row(const CP& p, int req, int unit, int
       if (in_group(p, j, req)) return j;
     return -1;
   };
-  auto prefix_lse = [&](int slot) { return p.prefix_lse + (int64_t)slot * p.prefix_stride_lse + row_off; };
-  auto prefix_o = [&](int slot) { return p.prefix_o + (int64_t)slot * p.prefix_stride_o + row_off * D; };
   // The first group's first batch of prefix pieces depends on no plan word:
   // its loads go out before the plan's words are read, so both arrive in
   // one memory round trip.
   int j = next_group(-1), base = 0;
-  int n_pref = j >= 0 ? group_pieces(p, j, req, h, base) : 0;
-  float ls[kB];
-  float4 xs[kB];
+  int n_pref = j >= 0 ? group_pieces(p, j, req, h0, base) : 0;
+  float ls[R][kB];
+  float4 xs[R][kB];
 #pragma unroll
-  for (int k = 0; k < kB; ++k) {
-    const bool in = k < n_pref;
-    ls[k] = in ? ld_cg(prefix_lse(base + k)) : neg_inf();
-    xs[k] = in ? ld_cg4(prefix_o(base + k) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const bool in = r < nr && k < n_pref;
+      const int64_t slot = base + k;
+      ls[r][k] = in ? ld_cg(p.prefix_lse + slot * p.prefix_stride_lse + row_off[r]) : neg_inf();
+      xs[r][k] = in ? ld_cg4(p.prefix_o + slot * p.prefix_stride_o + row_off[r] * D + lane * 4)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   int suf_kind = 0, suf_begin = 0, suf_n = 0;  // 1: direct state, 2: partial slots
   if (pl) {
     const int nch = pl[p.off_unit_n_chunks + unit];  // both loads in flight together
@@ -105,59 +118,73 @@ __device__ __forceinline__ void contract_row(const CP& p, int req, int unit, int
     const int jn = j >= 0 ? next_group(j) : -1;
     const int n_suf = jn < 0 ? suf_n : 0;  // the last pass takes the suffix
     const int n_src = n_pref + n_suf;
-    auto src_lse = [&](int i) -> const float* {
-      if (i < n_pref) return prefix_lse(base + i);
-      if (suf_kind == 1) return p.suffix_lse + row_off;
-      return p.part_lse + (int64_t)(suf_begin + i - n_pref) * p.hq + h;
+    // Source i of row r: its LSE and its O row.
+    auto src_lse = [&](int i, int r) -> const float* {
+      if (i < n_pref) return p.prefix_lse + (int64_t)(base + i) * p.prefix_stride_lse + row_off[r];
+      if (suf_kind == 1) return p.suffix_lse + row_off[r];
+      return p.part_lse + (int64_t)(suf_begin + i - n_pref) * p.hq + (row_off[r] - (int64_t)req * p.hq);
     };
-    auto src_o = [&](int i) -> const float* {
-      if (i < n_pref) return prefix_o(base + i);
-      if (suf_kind == 1) return p.suffix_o + row_off * D;
-      return p.part_o + ((int64_t)(suf_begin + i - n_pref) * p.hq + h) * D;
+    auto src_o = [&](int i, int r) -> const float* {
+      if (i < n_pref) return p.prefix_o + (int64_t)(base + i) * p.prefix_stride_o + row_off[r] * D;
+      if (suf_kind == 1) return p.suffix_o + row_off[r] * D;
+      return p.part_o + ((int64_t)(suf_begin + i - n_pref) * p.hq + (row_off[r] - (int64_t)req * p.hq)) * D;
     };
     for (int i0 = 0; i0 < n_src; i0 += kB) {
 #pragma unroll
-      for (int k = 0; k < kB; ++k) {
-        if (preloaded && k < n_pref) continue;  // loaded before the plan's words
-        const bool in = i0 + k < n_src;
-        ls[k] = in ? ld_cg(src_lse(i0 + k)) : neg_inf();
-        xs[k] = in ? ld_cg4(src_o(i0 + k) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+          if (preloaded && k < n_pref) continue;  // loaded before the plan's words
+          const bool in = r < nr && i0 + k < n_src;
+          ls[r][k] = in ? ld_cg(src_lse(i0 + k, r)) : neg_inf();
+          xs[r][k] = in ? ld_cg4(src_o(i0 + k, r) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       preloaded = false;
-      float mb = m;
 #pragma unroll
-      for (int k = 0; k < kB; ++k) mb = fmaxf(mb, ls[k]);
-      if (mb == neg_inf()) continue;
-      const float c = ex2((m - mb) * kLog2e);  // 0 when m is -inf
-      den *= c;
-      acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
+      for (int r = 0; r < R; ++r) {
+        float mb = m[r];
 #pragma unroll
-      for (int k = 0; k < kB; ++k) {
-        const float w = ex2((ls[k] - mb) * kLog2e);  // 0 for empty states
-        den += w;
-        acc.x = fmaf(w, xs[k].x, acc.x); acc.y = fmaf(w, xs[k].y, acc.y);
-        acc.z = fmaf(w, xs[k].z, acc.z); acc.w = fmaf(w, xs[k].w, acc.w);
+        for (int k = 0; k < kB; ++k) mb = fmaxf(mb, ls[r][k]);
+        if (mb == neg_inf()) continue;
+        // Explicitly rounded operations: the compiler may not contract them
+        // differently in different callers, so every caller gets the same bits.
+        const float c = ex2(__fmul_rn(m[r] - mb, kLog2e));  // 0 when m is -inf
+        den[r] = __fmul_rn(den[r], c);
+        acc[r].x = __fmul_rn(acc[r].x, c); acc[r].y = __fmul_rn(acc[r].y, c);
+        acc[r].z = __fmul_rn(acc[r].z, c); acc[r].w = __fmul_rn(acc[r].w, c);
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+          const float w = ex2(__fmul_rn(ls[r][k] - mb, kLog2e));  // 0 for empty states
+          den[r] = __fadd_rn(den[r], w);
+          acc[r].x = __fmaf_rn(w, xs[r][k].x, acc[r].x); acc[r].y = __fmaf_rn(w, xs[r][k].y, acc[r].y);
+          acc[r].z = __fmaf_rn(w, xs[r][k].z, acc[r].z); acc[r].w = __fmaf_rn(w, xs[r][k].w, acc[r].w);
+        }
+        m[r] = mb;
       }
-      m = mb;
     }
     preloaded = false;
     if (jn < 0) break;
     j = jn;
-    n_pref = group_pieces(p, j, req, h, base);
+    n_pref = group_pieces(p, j, req, h0, base);
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-  const int64_t row = (int64_t)req * p.hq + h;
-  if (p.out_dtype == PKC_F32) {
-    *reinterpret_cast<float4*>(static_cast<float*>(p.o) + row * D + lane * 4) = acc;
-  } else if (p.out_dtype == PKC_F16) {
-    uint2 u = make_uint2(Elem<__half>::from_f2(acc.x, acc.y), Elem<__half>::from_f2(acc.z, acc.w));
-    *reinterpret_cast<uint2*>(static_cast<__half*>(p.o) + row * D + lane * 4) = u;
-  } else {
-    uint2 u = make_uint2(Elem<__nv_bfloat16>::from_f2(acc.x, acc.y), Elem<__nv_bfloat16>::from_f2(acc.z, acc.w));
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + row * D + lane * 4) = u;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (r >= nr) continue;
+    const float inv = den[r] > 0.f ? __frcp_rn(den[r]) : 0.f;
+    float4 a = acc[r];
+    a.x = __fmul_rn(a.x, inv); a.y = __fmul_rn(a.y, inv); a.z = __fmul_rn(a.z, inv); a.w = __fmul_rn(a.w, inv);
+    const int64_t row = row_off[r];
+    if (p.out_dtype == PKC_F32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.o) + row * D + lane * 4) = a;
+    } else if (p.out_dtype == PKC_F16) {
+      uint2 u = make_uint2(Elem<__half>::from_f2(a.x, a.y), Elem<__half>::from_f2(a.z, a.w));
+      *reinterpret_cast<uint2*>(static_cast<__half*>(p.o) + row * D + lane * 4) = u;
+    } else {
+      uint2 u = make_uint2(Elem<__nv_bfloat16>::from_f2(a.x, a.y), Elem<__nv_bfloat16>::from_f2(a.z, a.w));
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + row * D + lane * 4) = u;
+    }
+    if (lane == 0) p.lse[row] = den[r] > 0.f ? __fmaf_rn(lg2(den[r]), kLn2, m[r]) : neg_inf();
   }
-  if (lane == 0) p.lse[row] = den > 0.f ? m + lg2(den) * kLn2 : neg_inf();
 }
 
 // Sources of the pair (req, kvh) that the fused kernels count: the prefix
@@ -184,46 +211,79 @@ __device__ __forceinline__ int fuse_expected(const FuseParams& f, int req, int k
   return n;
 }
 
-// One source of (req, kvh) written by this thread (and the threads it has
-// synchronised with): count it.  True for the thread whose count was the
-// pair's last; that thread's view then includes every source.
-__device__ __forceinline__ bool fuse_count(const FuseParams& f, int req, int kvh) {
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One source of (req, kvh) has been written by this thread and the threads
+// it has synchronised with: is it the pair's last?  If every other source
+// is already counted, it is, and nothing is added (no other writer is
+// left); otherwise it is counted, and the count tells.  Either way exactly
+// one writer of the pair gets true, and its view then includes every
+// source.
+__device__ __forceinline__ bool fuse_last(const FuseParams& f, int req, int kvh) {
   const int expected = fuse_expected(f, req, kvh);
+  int32_t* ctr = f.arrive + (int64_t)req * f.hkv + kvh;
+  if (ld_acquire(ctr) == expected - 1) return true;
   __threadfence();  // the sources written so far are visible before the count
-  const int before = atomicAdd(f.arrive + (int64_t)req * f.hkv + kvh, 1);
-  return before == expected - 1;
+  const bool last = atomicAdd(ctr, 1) == expected - 1;
+  if (last) __threadfence();
+  return last;
 }
 
-// (+) of the G rows of (req, kvh) into the final output, by one warp.
+// (+) of the G rows of (req, kvh) into the final output, by one warp, in
+// lockstep groups of up to 4 rows.
 __device__ __forceinline__ void fuse_merge(const FuseParams& f, int req, int kvh, int lane) {
-  for (int hd = 0; hd < f.g; ++hd) contract_row(f, req, req, kvh * f.g + hd, lane);
+  for (int hd = 0; hd < f.g; hd += 4) contract_rows<4>(f, req, req, kvh * f.g + hd, min(4, f.g - hd), lane);
 }
 
-// Warp-collective, after the warp has written its source of (req, kvh): the
-// count, and the merge if this was the pair's last source.  Not inlined:
-// it runs once per work item, and inlined into the decode loops its
-// registers would be added to theirs (which then spill).
-static __device__ __noinline__ void fuse_arrive(const FuseParams& f, int req, int kvh, int lane) {
+// Warp-collective, after the warp has written its source of (req, kvh) (a
+// chunk's partial state or a cascade's suffix state): if it was the pair's
+// last source, merge the pair.  f is the block's shared-memory copy of the
+// call's FuseParams.  Not inlined: it runs once per work item, and inlined
+// into the decode loops its registers would be added to theirs.
+static __device__ __noinline__ void fuse_arrive(const FuseParams* f, int req, int kvh, int lane) {
   __syncwarp();
   int last = 0;
-  if (lane == 0) last = fuse_count(f, req, kvh) ? 1 : 0;
+  if (lane == 0) last = fuse_last(*f, req, kvh) ? 1 : 0;
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
-  __threadfence();  // every lane reads the other writers' sources after the count
-  fuse_merge(f, req, kvh, lane);
+  __syncwarp();  // lane 0's acquire orders the other lanes' loads too
+  fuse_merge(*f, req, kvh, lane);
 }
 
-// Rows with no source at all (an empty request outside every prefix group)
-// get the empty state (0, -inf); warp `w` of `n_w` takes every n_w-th
-// request.
-static __device__ __noinline__ void fuse_write_empty(const FuseParams& f, int w, int n_w, int lane) {
+// Prefix kernel, warp-collective: the warp has written one piece's state of
+// the pairs (r0 + i, kvh), i < n (lanes i < n count one pair each); merge
+// the pairs whose last source this was.
+static __device__ __noinline__ void fuse_arrive_prefix(const FuseParams* f, int r0, int n, int kvh, int lane) {
+  __syncwarp();
+  const bool last = lane < n && fuse_last(*f, r0 + lane, kvh);
+  unsigned lm = __ballot_sync(0xffffffffu, last);
+  if (!lm) return;
+  __syncwarp();
+  while (lm) {
+    const int i = __ffs(lm) - 1;
+    lm &= lm - 1;
+    fuse_merge(*f, r0 + i, kvh, lane);
+  }
+}
+
+// Rows with no source at all get the empty state (0, -inf): the plan's
+// empty units (requests with no cached token) outside every prefix group;
+// without a plan every request has a suffix state.  Warp `w` of `n_w`
+// takes every n_w-th empty unit.
+static __device__ __noinline__ void fuse_write_empty(const FuseParams* fp, int w, int n_w, int lane) {
   constexpr int D = PKC_HEAD_DIM;
-  for (int req = w; req < f.batch; req += n_w) {
+  const FuseParams& f = *fp;
+  if (!f.plan) return;
+  const int n_split = f.plan[PKC_PLAN_N_SPLIT], n_empty = f.plan[PKC_PLAN_N_EMPTY];
+  for (int i = w; i < n_empty; i += n_w) {
+    const int unit = f.plan[f.off_unit_list + n_split + i];
+    const int req = f.plan[f.off_unit_req + unit];
     for (int kvh = 0; kvh < f.hkv; ++kvh) {
-      if (fuse_expected(f, req, kvh) != 0) continue;
-      // A planned decode writes an unsplit request itself: only empty ones here.
-      if (f.plan && f.plan[f.off_unit_n_chunks + req] != 0) continue;
-      if (!f.plan && !f.suffix_o) continue;  // not a planned call: nothing to cover
+      if (fuse_expected(f, req, kvh) != 0) continue;  // a prefix covers it
       for (int hd = 0; hd < f.g; ++hd) {
         const int64_t row = (int64_t)req * f.hq + kvh * f.g + hd;
         if (f.out_dtype == PKC_F32)
@@ -234,6 +294,14 @@ static __device__ __noinline__ void fuse_write_empty(const FuseParams& f, int w,
       }
     }
   }
+}
+
+// Copy of the call's FuseParams into shared memory (the fused helpers read
+// it there), by the threads of the block; a __syncthreads() must follow.
+__device__ __forceinline__ void fuse_params_to_smem(const FuseParams& f, FuseParams* dst) {
+  const int* src = reinterpret_cast<const int*>(&f);
+  int* d = reinterpret_cast<int*>(dst);
+  for (int i = threadIdx.x; i < (int)(sizeof(FuseParams) / 4); i += blockDim.x) d[i] = src[i];
 }
 
 }  // namespace pkc

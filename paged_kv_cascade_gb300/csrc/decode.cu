@@ -80,8 +80,17 @@ struct DecodeSmem {
 
 // Two merge buffers (alternating work items) of 8 warps x G heads x (D + 2).
 template <int G, int HG>
+constexpr int decode_merge_bytes() {
+  return DecodeCfg<HG>::kWph > 1 ? 2 * kConsumerWarps * G * (D + 2) * 4 : 0;
+}
+// ... then the block's copy of the fused contraction's parameters.
+template <int G, int HG>
+constexpr int decode_fuse_offset() {
+  return (DecodeSmem<HG>::kMerge + decode_merge_bytes<G, HG>() + 15) & ~15;
+}
+template <int G, int HG>
 constexpr int decode_smem_bytes() {
-  return DecodeSmem<HG>::kMerge + (DecodeCfg<HG>::kWph > 1 ? 2 * kConsumerWarps * G * (D + 2) * 4 : 0) + 1024;
+  return decode_fuse_offset<G, HG>() + (int)sizeof(FuseParams) + 1024;
 }
 
 // Transposed butterfly over the 16 lanes of a half-warp: in, v[i] is this
@@ -136,6 +145,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + L::kMergeBars);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
   float* merge_buf = reinterpret_cast<float*>(smem + L::kMerge);
+  FuseParams* fuse = reinterpret_cast<FuseParams*>(smem + decode_fuse_offset<G, HG>());
+  if (p.fuse.enabled) fuse_params_to_smem(p.fuse, fuse);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // Fused contraction: rows that no kernel will write (empty requests) get
   // the empty state, spread over the blocks' first consumer warps.
   if (p.fuse.enabled && warp == 0)
-    fuse_write_empty(p.fuse, (int)(blockIdx.x + gridDim.x * blockIdx.y), (int)(gridDim.x * gridDim.y), lane);
+    fuse_write_empty(fuse, (int)(blockIdx.x + gridDim.x * blockIdx.y), (int)(gridDim.x * gridDim.y), lane);
   const int half = lane >> 4, sub = lane & 15;
   const int hh = warp % HG;       // KV head within the group
   const int cls = warp / HG;      // which pairs of rows of the stage
@@ -504,7 +515,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     // A state that is not the request's final output is one source of the
     // fused contraction: count it; the last source's warp merges the pair.
-    if (p.fuse.enabled && (out_slot >= 0 || p.direct_f32)) fuse_arrive(p.fuse, req, kvh, lane);
+    if (p.fuse.enabled && (out_slot >= 0 || p.direct_f32)) fuse_arrive(fuse, req, kvh, lane);
   }
 }
 
@@ -526,7 +537,7 @@ __global__ void __launch_bounds__(256, 4) contract_kernel(const __grid_constant_
     unit = pl[p.off_unit_list + row_idx];
     req = pl[p.off_unit_req + unit];
   }
-  contract_row(p, req, unit, h, lane);
+  contract_rows<1>(p, req, unit, h, 1, lane);
 }
 
 template <typename T, int G, int HG>

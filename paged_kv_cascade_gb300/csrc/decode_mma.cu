@@ -97,8 +97,12 @@ struct Cfg {
 // Shared memory: stages, headers, barriers, abort flag, then (warps sharing
 // a KV head) two merge buffers of 8 warps x G heads x (D + 2) floats.
 template <int KV, int G, int HG>
+constexpr int mma_fuse_offset() {  // the block's copy of the fused contraction's parameters
+  return (Cfg<KV, HG>::kMerge + (Cfg<KV, HG>::kWph > 1 ? 2 * kWarps * G * (D + 2) * 4 : 0) + 15) & ~15;
+}
+template <int KV, int G, int HG>
 constexpr int mma_smem_bytes() {
-  return Cfg<KV, HG>::kMerge + (Cfg<KV, HG>::kWph > 1 ? 2 * kWarps * G * (D + 2) * 4 : 0) + 1024;
+  return mma_fuse_offset<KV, G, HG>() + (int)sizeof(FuseParams) + 1024;
 }
 static_assert(mma_smem_bytes<kKvBF16, 8, 4>() <= 227 * 1024, "shared memory");
 static_assert(mma_smem_bytes<kKvE4M3, 8, 4>() <= 227 * 1024, "shared memory");
@@ -134,6 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + C::kMergeBars);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kAbort);
   float* merge_buf = reinterpret_cast<float*>(smem + C::kMerge);
+  FuseParams* fuse = reinterpret_cast<FuseParams*>(smem + mma_fuse_offset<KV, G, HG>());
+  if (p.fuse.enabled) fuse_params_to_smem(p.fuse, fuse);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Fused contraction: rows that no kernel will write (empty requests) get
   // the empty state, spread over the blocks' first consumer warps.
   if (p.fuse.enabled && warp == 0)
-    fuse_write_empty(p.fuse, (int)(blockIdx.x + gridDim.x * blockIdx.y), (int)(gridDim.x * gridDim.y), lane);
+    fuse_write_empty(fuse, (int)(blockIdx.x + gridDim.x * blockIdx.y), (int)(gridDim.x * gridDim.y), lane);
   const int hh = warp % HG;   // KV head within the group
   const int cls = warp / HG;  // which 16 slots of each stage
   const int g = lane >> 2, tg = lane & 3;  // fragment row group / thread in group
@@ -496,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // A state that is not the request's final output is one source of the
       // fused contraction: count it; the last source's warp merges the pair.
-      if (p.fuse.enabled && (out_slot >= 0 || p.direct_f32)) fuse_arrive(p.fuse, req, kvh, lane);
+      if (p.fuse.enabled && (out_slot >= 0 || p.direct_f32)) fuse_arrive(fuse, req, kvh, lane);
     } else {
       // Warps of the same head meet in shared memory (bounded mbarrier wait;
       // buffers alternate between items).
@@ -554,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) p.lse_direct[row] = lse;
         }
       }
-      if (p.fuse.enabled && (out_slot >= 0 || p.direct_f32)) fuse_arrive(p.fuse, req, kvh, lane);
+      if (p.fuse.enabled && (out_slot >= 0 || p.direct_f32)) fuse_arrive(fuse, req, kvh, lane);
     }
   }
 }

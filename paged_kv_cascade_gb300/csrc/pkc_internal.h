@@ -57,7 +57,7 @@ struct FuseParams {
   int32_t* arrive;          // [batch * hkv] arrival counters, zeroed before each call
   int batch, hq, hkv, g;
   const int32_t* plan;      // device plan (decode plans: unit = request) or nullptr
-  int32_t off_unit_n_chunks, off_unit_partial_begin;
+  int32_t off_unit_list, off_unit_req, off_unit_n_chunks, off_unit_partial_begin;
   const float* suffix_o;    // direct suffix states (a cascade) or nullptr
   const float* suffix_lse;
   const float* part_o;      // partial states of split requests' chunks

@@ -110,7 +110,8 @@ constexpr int kPOffset = kQBytes;                  // two P buffers, by tile par
 constexpr int kKOffset = kPOffset + 2 * kTileBytes;
 constexpr int kVOffset = kKOffset + kStagesK * kTileBytes;
 constexpr int kBarOffset = kVOffset + kStagesV * kTileBytes;
-constexpr int kSmemBytes = kBarOffset + 256;
+constexpr int kFuseOffset = kBarOffset + 256;  // the block's copy of the fused contraction's parameters
+constexpr int kSmemBytes = kFuseOffset + (int)((sizeof(FuseParams) + 15) & ~size_t(15));
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 template <typename T>
@@ -125,6 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_q = smem_u32(smem);
   const uint32_t s_p = s_q + kPOffset, s_k0 = s_q + kKOffset, s_v0 = s_q + kVOffset;
   Barriers* bars = reinterpret_cast<Barriers*>(smem + kBarOffset);
+  FuseParams* fuse = reinterpret_cast<FuseParams*>(smem + kFuseOffset);
+  if (p.fuse.enabled) fuse_params_to_smem(p.fuse, fuse);
   static_assert(sizeof(Barriers) <= 256, "barrier block");
   volatile int* abort = &bars->abort;
 
@@ -561,19 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // all lie here).  Lane i counts request i; the warp merges the pairs
       // whose count was the last.
       if (p.fuse.enabled && ok) {
-        __syncwarp();
         const int r0 = b0 + rbase / G;
-        const int rq = r0 + lane;
-        const bool last = lane < 16 / G && rq < req_hi && fuse_count(p.fuse, rq, pc.kvh);
-        unsigned lm = __ballot_sync(0xffffffffu, last);
-        if (lm) {
-          __threadfence();  // the other writers' sources are read after the counts
-          while (lm) {
-            const int i = __ffs(lm) - 1;
-            lm &= lm - 1;
-            fuse_merge(p.fuse, r0 + i, pc.kvh, lane);
-          }
-        }
+        fuse_arrive_prefix(fuse, r0, max(0, min(16 / G, req_hi - r0)), pc.kvh, lane);
       }
     }
   }

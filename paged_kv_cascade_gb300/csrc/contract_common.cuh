@@ -11,7 +11,8 @@
 // rows after the stages.
 //
 // Fused (MLSys'25 notes, A3: attention and contraction in one persistent
-// kernel): the kernels that write the sources count them instead.  After a
+// kernel): the kernels that write the sources count them instead (in the
+// kernels' fused instantiations, whose other code is unchanged).  After a
 // warp has written a source of (request, KV head) it adds one to that
 // pair's arrival counter; the warp that brings the counter to the number
 // of sources the pair has merges the pair's G rows itself, so no kernel
@@ -233,40 +234,39 @@ __device__ __forceinline__ bool fuse_last(const FuseParams& f, int req, int kvh)
   return last;
 }
 
-// (+) of the G rows of (req, kvh) into the final output, by one warp, in
-// lockstep groups of up to 4 rows.
-__device__ __forceinline__ void fuse_merge(const FuseParams& f, int req, int kvh, int lane) {
-  for (int hd = 0; hd < f.g; hd += 4) contract_rows<4>(f, req, req, kvh * f.g + hd, min(4, f.g - hd), lane);
-}
-
 // Warp-collective, after the warp has written its source of (req, kvh) (a
 // chunk's partial state or a cascade's suffix state): if it was the pair's
-// last source, merge the pair.  f is the block's shared-memory copy of the
-// call's FuseParams.  Not inlined: it runs once per work item, and inlined
-// into the decode loops its registers would be added to theirs.
-static __device__ __noinline__ void fuse_arrive(const FuseParams* f, int req, int kvh, int lane) {
+// last source, merge the pair's G query-head rows, R at a time in lockstep.
+// f is the block's shared-memory copy of the call's FuseParams.  Inlined
+// into the fused instantiations of the decode kernels only.
+template <int G>
+__device__ __forceinline__ void fuse_arrive(const FuseParams* f, int req, int kvh, int lane) {
   __syncwarp();
   int last = 0;
   if (lane == 0) last = fuse_last(*f, req, kvh) ? 1 : 0;
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   __syncwarp();  // lane 0's acquire orders the other lanes' loads too
-  fuse_merge(*f, req, kvh, lane);
+  constexpr int R = G < 2 ? G : 2;
+#pragma unroll 1
+  for (int hd = 0; hd < G; hd += R) contract_rows<R>(*f, req, req, kvh * G + hd, R, lane);
 }
 
 // Prefix kernel, warp-collective: the warp has written one piece's state of
 // the pairs (r0 + i, kvh), i < n (lanes i < n count one pair each); merge
-// the pairs whose last source this was.
-static __device__ __noinline__ void fuse_arrive_prefix(const FuseParams* f, int r0, int n, int kvh, int lane) {
+// the pairs whose last source this was, one row at a time.
+__device__ __forceinline__ void fuse_arrive_prefix(const FuseParams* f, int r0, int n, int kvh, int lane) {
   __syncwarp();
   const bool last = lane < n && fuse_last(*f, r0 + lane, kvh);
   unsigned lm = __ballot_sync(0xffffffffu, last);
   if (!lm) return;
   __syncwarp();
+  const int g = f->g;
   while (lm) {
     const int i = __ffs(lm) - 1;
     lm &= lm - 1;
-    fuse_merge(*f, r0 + i, kvh, lane);
+#pragma unroll 1
+    for (int hd = 0; hd < g; ++hd) contract_rows<1>(*f, r0 + i, r0 + i, kvh * g + hd, 1, lane);
   }
 }
 
@@ -274,7 +274,7 @@ static __device__ __noinline__ void fuse_arrive_prefix(const FuseParams* f, int 
 // empty units (requests with no cached token) outside every prefix group;
 // without a plan every request has a suffix state.  Warp `w` of `n_w`
 // takes every n_w-th empty unit.
-static __device__ __noinline__ void fuse_write_empty(const FuseParams* fp, int w, int n_w, int lane) {
+__device__ __forceinline__ void fuse_write_empty(const FuseParams* fp, int w, int n_w, int lane) {
   constexpr int D = PKC_HEAD_DIM;
   const FuseParams& f = *fp;
   if (!f.plan) return;

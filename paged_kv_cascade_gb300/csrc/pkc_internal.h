@@ -224,6 +224,12 @@ int launch_paged_decode_simt(const DecodeParams& p, int grid_x, int dtype,
                              void* stream);
 int launch_paged_decode_mma(const DecodeParams& p, int grid_x, int kv_kind,
                             void* stream);
+// The instantiations with the fused contraction (p.fuse.enabled); mk, mv
+// are the CUtensorMaps of the K and V pools.
+int launch_paged_decode_mma_fused(const DecodeParams& p, int grid_x, int kv_kind, int hg,
+                                  const void* mk, const void* mv, void* stream);
+int launch_paged_decode_simt_fused(const DecodeParams& p, int grid_x, int dtype, int hg,
+                                   const void* mk, const void* mv, void* stream);
 // KV heads per block of the tensor-core kernel, or 0 if it cannot take
 // this head count and page size.
 int mma_decode_heads_per_block(int hkv, int page_size);

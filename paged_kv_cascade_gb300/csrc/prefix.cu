@@ -114,7 +114,7 @@ constexpr int kFuseOffset = kBarOffset + 256;  // the block's copy of the fused 
 constexpr int kSmemBytes = kFuseOffset + (int)((sizeof(FuseParams) + 15) & ~size_t(15));
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
-template <typename T>
+template <typename T, bool kFuse>
 __global__ void __launch_bounds__(kThreads, 1)
     prefix_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ PrefixParams p) {
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_p = s_q + kPOffset, s_k0 = s_q + kKOffset, s_v0 = s_q + kVOffset;
   Barriers* bars = reinterpret_cast<Barriers*>(smem + kBarOffset);
   FuseParams* fuse = reinterpret_cast<FuseParams*>(smem + kFuseOffset);
-  if (p.fuse.enabled) fuse_params_to_smem(p.fuse, fuse);
+  if constexpr (kFuse) fuse_params_to_smem(p.fuse, fuse);
   static_assert(sizeof(Barriers) <= 256, "barrier block");
   volatile int* abort = &bars->abort;
 
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // head) pair among the warp's 16 rows (16 / G requests, whose G rows
       // all lie here).  Lane i counts request i; the warp merges the pairs
       // whose count was the last.
-      if (p.fuse.enabled && ok) {
+      if (kFuse && ok) {
         const int r0 = b0 + rbase / G;
         fuse_arrive_prefix(fuse, r0, max(0, min(16 / G, req_hi - r0)), pc.kvh, lane);
       }
@@ -586,19 +586,25 @@ bool make_map(CUtensorMap* m, const void* base, int dtype, uint64_t d0, uint64_t
   return encode_tiled_map(m, base, dtype, 3, dims, strides, box, true);
 }
 
-template <typename T>
-int launch_t(const PrefixParams& p, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-             cudaStream_t st) {
+template <typename T, bool kFuse>
+int launch_tf(const PrefixParams& p, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+              cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefix_state_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(prefix_state_kernel<T, kFuse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kSmemBytes);
   });
   if (attr_err != cudaSuccess) return (int)attr_err;
   const dim3 grid(p.n_blocks, 1);  // one block per SM, each over an even share of the KV tiles
-  prefix_state_kernel<T><<<grid, kThreads, kSmemBytes, st>>>(q, k, v, p);
+  prefix_state_kernel<T, kFuse><<<grid, kThreads, kSmemBytes, st>>>(q, k, v, p);
   return (int)cudaGetLastError();
+}
+
+template <typename T>
+int launch_t(const PrefixParams& p, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+             cudaStream_t st) {
+  return p.fuse.enabled ? launch_tf<T, true>(p, q, k, v, st) : launch_tf<T, false>(p, q, k, v, st);
 }
 
 }  // namespace

@@ -65,7 +65,7 @@ def parse_args():
     ap.add_argument("--decode-schedule", choices=["dynamic", "static"], default="dynamic",
                     help="planned decode: blocks take the plan's chunks from a shared "
                          "longest-first queue (dynamic) or run their CTA's plan list (static)")
-    ap.add_argument("--contraction", choices=["fused", "separate"], default="fused",
+    ap.add_argument("--contraction", choices=["fused", "separate", "separate_plain"], default="separate",
                     help="split states contracted inside the attention kernels (fused) or by a "
                          "standalone contraction kernel after them")
     ap.add_argument("--num-ctas", type=int, default=None,
@@ -1058,20 +1058,24 @@ def main():
     # kernels (fused) or by the standalone contraction kernel after them ----
     contractions = None
     if world == 1:
-        other_c = "separate" if args.contraction == "fused" else "fused"
-        pkc.set_contraction(other_c)
-        gs3 = GraphStepper(torch, pkc, run, lens, num_ctas, cfg, ws_bytes, ctx.device)
-        ms3, n3, clk3 = time_loop(ctx, gs3.step, gs3.stream, K)
-        if not gs3.status_ok():
-            raise RuntimeError("device status after the other contraction")
+        contractions = {}
+        for mode in ("separate", "separate_plain", "fused"):
+            if mode == args.contraction:
+                continue
+            pkc.set_contraction(mode)
+            gs3 = GraphStepper(torch, pkc, run, lens, num_ctas, cfg, ws_bytes, ctx.device)
+            ms3, n3, clk3 = time_loop(ctx, gs3.step, gs3.stream, K)
+            if not gs3.status_ok():
+                raise RuntimeError(f"device status after contraction mode {mode}")
+            contractions[mode] = {"us_per_step": 1e3 * ms3, "steps": n3, "clocks": clk3}
+            del gs3
         pkc.set_contraction(args.contraction)
         ms4, n4, clk4 = time_loop(ctx, gs.step, gs.stream, K)
-        contractions = {args.contraction: {"us_per_step": 1e3 * ms4, "steps": n4, "clocks": clk4},
-                        other_c: {"us_per_step": 1e3 * ms3, "steps": n3, "clocks": clk3},
-                        "note": "graph-replayed steps timed back to back; fused = the kernel writing "
-                                "a (request, KV head)'s last source merges it (no contraction "
-                                "launch); separate = contraction kernel after both stages"}
-        del gs3
+        contractions[args.contraction] = {"us_per_step": 1e3 * ms4, "steps": n4, "clocks": clk4}
+        contractions["note"] = ("graph-replayed steps timed back to back; separate = contraction kernel "
+                                "after both stages, launched as the decode's programmatic dependent; "
+                                "separate_plain = the same launched plainly; fused = the kernel writing "
+                                "a (request, KV head)'s last source merges it (no contraction launch)")
 
     eff = workloads.effective_bytes(p)
     ms_per_step = g_ms / K

@@ -554,7 +554,13 @@ int pkc_set_decode_schedule(int dynamic);
 
 /*
  * Where split states are contracted into the output (process-wide):
- *   1 = fused (default): the attention kernels do it themselves (MLSys'25
+ *   0 = (default) a standalone contraction kernel after the attention
+ *       kernels, launched as a programmatic dependent of the suffix decode:
+ *       its blocks start while the decode's last blocks run, load the prefix
+ *       pieces and plan words, and wait in hardware (griddepcontrol.wait)
+ *       for the decode grid before reading the suffix states.
+ *   2 = the same kernel launched plainly after the decode (for measurement).
+ *   1 = fused: the attention kernels do it themselves (MLSys'25
  *       notes, A3: attention and contraction in one persistent kernel).
  *       Every kernel that writes a state that is not yet a final output --
  *       a chunk's partial state, a cascade's suffix state, a prefix piece --
@@ -566,13 +572,14 @@ int pkc_set_decode_schedule(int dynamic);
  *       first zeroes its counters (cudaMemsetAsync of batch * num_kv_heads
  *       int32 in the workspace).  Cascades with more than 16 prefix groups
  *       use the standalone kernel.
- *   0 = a standalone contraction kernel after the attention kernels.
- * The two give the same bits: one routine merges a row's sources in the
- * same order either way.  pkc_prefix_attention_state and
+       The standalone kernel was faster on every workload measured: the
+ *       fused merges stall decode warps that keep HBM busy.
+ * All modes give the same bits: one routine merges a row's sources in the
+ * same order.  pkc_prefix_attention_state and
  * pkc_paged_decode_state_noalloc always use the standalone kernel.
  * Returns PKC_ERR_INVALID_ARG for any other value.
  */
-int pkc_set_contraction(int fused);
+int pkc_set_contraction(int mode);
 
 /*
  * Thread blocks of the prefix stage in the cascade calls and

@@ -376,9 +376,11 @@ def set_decode_schedule(which):
 
 
 def set_contraction(which):
-    """'fused' (default): the attention kernels contract split states
-    themselves; 'separate': a standalone contraction kernel after them."""
-    _check(lib().pkc_set_contraction({"fused": 1, "separate": 0}[which]))
+    """'separate' (default): a standalone contraction kernel, launched as the
+    suffix decode's programmatic dependent; 'separate_plain': the same kernel
+    launched plainly; 'fused': the attention kernels contract split states
+    themselves (one launch fewer).  All give the same bits."""
+    _check(lib().pkc_set_contraction({"separate": 0, "fused": 1, "separate_plain": 2}[which]))
 
 
 def set_prefix_ctas(n):

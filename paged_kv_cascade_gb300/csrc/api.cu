@@ -380,9 +380,13 @@ void contract_plan_offsets(ContractParams& c, const int32_t* plan_host) {
   c.off_unit_partial_begin = plan_host[PKC_PLAN_OFF_UNIT_PARTIAL_BEGIN];
 }
 
-// Contraction fused into the attention kernels (1, default) or the
-// standalone contraction kernel after them (0): pkc_set_contraction.
-std::atomic<int> g_fused_contraction{1};
+// Contraction fused into the attention kernels (1) or the standalone
+// contraction kernel after them (0, default): pkc_set_contraction.  Fused,
+// the merges at the ends of work items stall decode warps that keep HBM
+// busy, and a prefix stage that finishes last merges whole row tiles on a
+// few blocks: measured slower on every benchmark workload (headline 296 vs
+// 293 us, long prompt 266 vs 181 us, tiny 24 vs 15 us).
+std::atomic<int> g_fused_contraction{0};
 
 // The fused contraction's view of a call: the same sources, offsets and
 // output as the standalone kernel's ContractParams (c), plus the counters.
@@ -604,7 +608,7 @@ int paged_decode_impl(const void* q, const void* k_cache, const void* v_cache, c
   if (e == -1) return set_error(PKC_ERR_CUDA, "paged decode: could not build TMA tensor maps");
   if (e) return cuda_error(e, "paged decode launch");
   if (plan_host && !fused) {
-    e = launch_contract(cp, batch, stream);
+    e = launch_contract(cp, batch, stream, true);
     if (e) return cuda_error(e, "contraction launch");
   }
   return PKC_OK;
@@ -681,10 +685,11 @@ int pkc_last_launch_blocks(int* prefix_blocks, int* decode_blocks) {
   return PKC_OK;
 }
 
-int pkc_set_contraction(int fused) {
-  if (fused != 0 && fused != 1)
-    return set_error(PKC_ERR_INVALID_ARG, "set_contraction: fused must be 0 or 1 (got %d)", fused);
-  g_fused_contraction.store(fused);
+int pkc_set_contraction(int mode) {
+  if (mode < 0 || mode > 2)
+    return set_error(PKC_ERR_INVALID_ARG, "set_contraction: mode must be 0, 1 or 2 (got %d)", mode);
+  g_fused_contraction.store(mode == 1 ? 1 : 0);
+  set_contract_pdl(mode == 0 ? 1 : 0);
   return PKC_OK;
 }
 
@@ -909,7 +914,7 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   }
   mark(2);
   if (!fused) {
-    e = launch_contract(cp, batch, stream);
+    e = launch_contract(cp, batch, stream, !timed);
     if (e) return cuda_error(e, "contraction launch");
   }
   mark(3);

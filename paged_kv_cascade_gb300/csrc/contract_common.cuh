@@ -58,7 +58,12 @@ __device__ __forceinline__ bool in_group(const CP& p, int j, int req) {
 // lockstep so that all their loads are in flight together, each row with
 // exactly the arithmetic it would get alone.  `unit` is the request's unit
 // of the plan (the request itself for decode plans).
-template <int R, class CP>
+// kWaitGrid: the standalone kernel, launched as a programmatic dependent of
+// the suffix decode, loads what the decode does not write (the prefix
+// pieces, written by a grid it fully depends on, and the plan) first and
+// waits for the decode's grid (griddepcontrol.wait) only before its suffix
+// loads.
+template <int R, class CP, bool kWaitGrid = false>
 __device__ __forceinline__ void contract_rows(const CP& p, int req, int unit, int h0, int nr, int lane) {
   constexpr int D = PKC_HEAD_DIM;
   const int32_t* pl = p.plan;
@@ -114,6 +119,7 @@ __device__ __forceinline__ void contract_rows(const CP& p, int req, int unit, in
   } else if (p.suffix_o) {
     suf_kind = 1; suf_n = 1;
   }
+  if constexpr (kWaitGrid) asm volatile("griddepcontrol.wait;" ::: "memory");
   bool preloaded = true;  // ls / xs hold the first batch's prefix pieces
   for (;;) {
     const int jn = j >= 0 ? next_group(j) : -1;

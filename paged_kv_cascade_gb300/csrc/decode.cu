@@ -3,6 +3,7 @@
 // decode_fused.cu), the standalone contraction kernel, and the dispatch
 // between the decode kernels.
 #include <atomic>
+#include <cstring>
 
 #include "decode_simt.cuh"
 
@@ -27,7 +28,7 @@ __global__ void __launch_bounds__(256, 4) contract_kernel(const __grid_constant_
     unit = pl[p.off_unit_list + row_idx];
     req = pl[p.off_unit_req + unit];
   }
-  contract_rows<1>(p, req, unit, h, 1, lane);
+  contract_rows<1, ContractParams, true>(p, req, unit, h, 1, lane);
 }
 
 }  // namespace
@@ -95,12 +96,41 @@ int launch_paged_decode(const DecodeParams& p_in, int grid_x, int dtype, int kv_
   return launch_paged_decode_simt(p, grid_x, dtype, stream);
 }
 
-int launch_contract(const ContractParams& p, int n_rows, void* stream) {
+// The contraction follows the suffix decode on the stream (after_decode).
+// Launched with programmatic stream serialization (the default), it may
+// start once every
+// decode block has signalled (griddepcontrol.launch_dependents, at each
+// decode block's start): its blocks take the SM room the decode leaves,
+// load the prefix pieces and plan words, and wait at griddepcontrol.wait
+// for the decode grid to finish before reading the suffix states.  The
+// dependency on everything else before it on the stream (the prefix stage
+// joined from its side stream, the plan upload) stays complete.
+static std::atomic<int> g_contract_pdl{1};
+int set_contract_pdl(int on) {
+  g_contract_pdl.store(on ? 1 : 0);
+  return 0;
+}
+
+int launch_contract(const ContractParams& p, int n_rows, void* stream, bool after_decode) {
   const int64_t warps = (int64_t)n_rows * p.hq;
   if (warps <= 0) return 0;
   const int blocks = (int)((warps + 7) / 8);
-  contract_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(p);
-  return (int)cudaGetLastError();
+  if (!after_decode || !g_contract_pdl.load()) {
+    contract_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(p);
+    return (int)cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, contract_kernel, p);
 }
 
 }  // namespace pkc

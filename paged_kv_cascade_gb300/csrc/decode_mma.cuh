@@ -167,6 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t half_bytes = (uint32_t)(sl * HG * kLine);  // one 64-dim half (16-bit) of a slice
   const uint32_t slice_bytes = (uint32_t)(sl * HG * C::kRowBytes);
 
+  // A contraction launched after this grid as its programmatic dependent
+  // may be scheduled from here on (it waits for this grid to finish before
+  // it reads what this grid writes).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);

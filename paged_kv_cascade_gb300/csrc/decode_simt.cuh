@@ -160,6 +160,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     w_end = pl[pl[PKC_PLAN_OFF_CTA_INDPTR] + cta + 1];
   }
 
+  // A contraction launched after this grid as its programmatic dependent
+  // may be scheduled from here on (it waits for this grid to finish before
+  // it reads what this grid writes).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);

@@ -233,7 +233,10 @@ int launch_paged_decode_simt_fused(const DecodeParams& p, int grid_x, int dtype,
 // KV heads per block of the tensor-core kernel, or 0 if it cannot take
 // this head count and page size.
 int mma_decode_heads_per_block(int hkv, int page_size);
-int launch_contract(const ContractParams& p, int n_rows, void* stream);
+// after_decode: the kernel right before it on the stream is the suffix
+// decode (it may then be launched as that grid's programmatic dependent).
+int launch_contract(const ContractParams& p, int n_rows, void* stream, bool after_decode = false);
+int set_contract_pdl(int on);  // 1: contraction as a programmatic dependent (default)
 int launch_append_kv(const AppendParams& p, int batch, void* stream);
 // q/k/v tensor maps are built inside; returns cudaError_t or -1 when the
 // driver entry point for tensor maps is unavailable.

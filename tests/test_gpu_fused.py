@@ -1,7 +1,7 @@
 """The contraction fused into the attention kernels against the standalone
 contraction kernel.
 
-Fused (the default), the kernel that writes the last source of a (request,
+Fused, the kernel that writes the last source of a (request,
 KV head) pair -- a chunk's partial state, a cascade's suffix state or a
 prefix piece -- merges the pair's sources itself.  One routine merges a
 row's sources in the same order either way, so the two must agree bit for
@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture
 def contraction():
     yield pkc.set_contraction
-    pkc.set_contraction("fused")
+    pkc.set_contraction("separate")
 
 
 def _cascade(p, num_ctas, ws=None):

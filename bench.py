@@ -81,6 +81,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other workloads' entries (`configs`) in the headline line")
+    ap.add_argument("--no-ab", action="store_true",
+                    help="skip the schedule and contraction comparisons (profiling runs)")
     ap.add_argument("--config-seconds", type=float, default=0.5,
                     help="least timed device time per workload entry")
     return ap.parse_args()
@@ -1035,7 +1037,7 @@ def main():
 
     # ---- the pages' own CTA assignment (the plan's static CTA lists) ----
     schedules = None
-    if num_ctas and world == 1:
+    if num_ctas and world == 1 and not args.no_ab:
         pkc.set_decode_schedule("static" if args.decode_schedule == "dynamic" else "dynamic")
         gs2 = GraphStepper(torch, pkc, run, lens, num_ctas, cfg, ws_bytes, ctx.device)
         ms2, n2, clk2 = time_loop(ctx, gs2.step, gs2.stream, K)
@@ -1057,7 +1059,7 @@ def main():
     # ---- where the split states are contracted: inside the attention
     # kernels (fused) or by the standalone contraction kernel after them ----
     contractions = None
-    if world == 1:
+    if world == 1 and not args.no_ab:
         contractions = {}
         for mode in ("separate", "separate_plain", "fused"):
             if mode == args.contraction:

@@ -624,6 +624,24 @@ int pkc_set_contraction(int mode);
 int pkc_set_prefix_ctas(int n);
 
 /*
+ * Small-batch cascade (process-wide; default 16).  A cascade call without a
+ * plan (pkc_cascade_decode, pkc_cascade_decode_state) whose every prefix
+ * group has at most max_rows query rows per KV head (requests x query heads
+ * per KV head), whose groups are contiguous and do not overlap, and whose
+ * prefixes (and the first prefix offset) are whole pages, runs as one
+ * CUDA-core decode launch: each request attends to its group's prefix, read
+ * as the first pages of its keys from the contiguous prefix tensors (viewed
+ * as [tokens / page_size, page_size, Hkv, 128]), then to its cached suffix,
+ * and the final state is written directly.  With so few rows per prefix the
+ * multi-query kernel has no reuse to exploit (blog "Cascade Inference",
+ * "Multi-query vs single-query kernels": the cascade pays off when many
+ * queries share the prefix), while its fixed latency and the contraction
+ * launch make up the step.  The state is the same attention state either way
+ * (up to rounding).  0 disables the path.  PKC_ERR_INVALID_ARG for n < 0.
+ */
+int pkc_set_cascade_small(int max_rows);
+
+/*
  * Diagnostics: the thread-block counts of the prefix kernel and of the
  * suffix decode in the calling thread's last cascade call
  * (pkc_cascade_decode, _multilevel, _paged_prefix) that got as far as the

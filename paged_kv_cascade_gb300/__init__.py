@@ -61,6 +61,7 @@ SIGNATURES = {
     "pkc_set_decode_schedule": (_I, [_I]),
     "pkc_set_contraction": (_I, [_I]),
     "pkc_set_prefix_ctas": (_I, [_I]),
+    "pkc_set_cascade_small": (_I, [_I]),
     "pkc_last_launch_blocks": (_I, [_c.POINTER(_c.c_int), _c.POINTER(_c.c_int)]),
     "pkc_selftest_wait_timeout": (_I, [_P, _SZ, _c.POINTER(_c.c_int32), _P]),
     "pkc_append_kv": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I64, _I, _P, _SZ, _P]),
@@ -381,6 +382,12 @@ def set_contraction(which):
     launched plainly; 'fused': the attention kernels contract split states
     themselves (one launch fewer).  All give the same bits."""
     _check(lib().pkc_set_contraction({"separate": 0, "fused": 1, "separate_plain": 2}[which]))
+
+
+def set_cascade_small(max_rows):
+    """Largest query rows per KV head of a prefix group for which an unplanned
+    cascade reads its prefixes through the decode kernel (one launch); 0 never."""
+    _check(lib().pkc_set_cascade_small(int(max_rows)))
 
 
 def set_prefix_ctas(n):

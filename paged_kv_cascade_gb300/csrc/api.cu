@@ -380,6 +380,12 @@ void contract_plan_offsets(ContractParams& c, const int32_t* plan_host) {
   c.off_unit_partial_begin = plan_host[PKC_PLAN_OFF_UNIT_PARTIAL_BEGIN];
 }
 
+// Small-batch cascade (pkc_set_cascade_small): a cascade call without a plan
+// whose every prefix group has at most this many query rows per KV head
+// (requests x G) reads its prefixes through the decode kernel, as pages of
+// the prefix tensors.  0: never.
+std::atomic<int> g_cascade_small_rows{16};
+
 // Contraction fused into the attention kernels (1) or the standalone
 // contraction kernel after them (0, default): pkc_set_contraction.  Fused,
 // the merges at the ends of work items stall decode warps that keep HBM
@@ -693,6 +699,12 @@ int pkc_set_contraction(int mode) {
   return PKC_OK;
 }
 
+int pkc_set_cascade_small(int max_rows) {
+  if (max_rows < 0) return set_error(PKC_ERR_INVALID_ARG, "set_cascade_small: max_rows must be >= 0 (got %d)", max_rows);
+  g_cascade_small_rows.store(max_rows);
+  return PKC_OK;
+}
+
 int pkc_set_prefix_ctas(int n) {
   if (n < 0) return set_error(PKC_ERR_INVALID_ARG, "set_prefix_ctas: n must be >= 0 (got %d)", n);
   g_prefix_ctas.store(n);
@@ -799,6 +811,61 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   if (int rc = setup_prefix(S, prefix_kv_indptr_host, req_begin, req_end, n_prefix, batch, num_qo_heads,
                             num_kv_heads, sm_scale, ws, workspace_bytes, L, status, split.prefix_blocks))
     return rc;
+  // Small batches: a shared prefix read by one 128-row query tile that holds
+  // a handful of rows gives the tensor cores nothing to share, and the
+  // prefix kernel's fixed latency and the contraction launch dominate such
+  // a step.  Then the decode kernel reads each request's prefix itself, as
+  // the first pages of its keys (the prefix tensors viewed as pages), and
+  // writes the final state: one launch, no partial states.  Needs no plan,
+  // contiguous non-overlapping groups of whole pages, and a contiguous
+  // prefix.
+  {
+    const int small_rows = g_cascade_small_rows.load();
+    bool small = small_rows > 0 && !plan_host && !prefix_pages && n_prefix <= PKC_FUSE_MAX_PREFIX &&
+                 prefix_kv_indptr_host[0] % page_size == 0;
+    for (int j = 0; small && j < n_prefix; ++j) {
+      small = (prefix_kv_indptr_host[j + 1] - prefix_kv_indptr_host[j]) % page_size == 0 &&
+              (req_end[j] - req_begin[j]) * (num_qo_heads / num_kv_heads) <= small_rows &&
+              (j == 0 || req_begin[j] == req_end[j - 1]);
+    }
+    if (small) {
+      DecodeParams dp;
+      std::memset(&dp, 0, sizeof(dp));
+      dp.q = q; dp.k_cache = k_cache; dp.v_cache = v_cache;
+      dp.block_table = block_table; dp.cache_seqlens = cache_seqlens;
+      dp.bt_stride = block_table_stride; dp.num_pages = num_pages;
+      dp.batch = batch; dp.hq = num_qo_heads; dp.hkv = num_kv_heads; dp.page_size = page_size;
+      dp.scale_log2 = sm_scale * 1.4426950408889634f;
+      dp.v_scale = 1.f;
+      dp.o_direct = o; dp.lse_direct = lse; dp.direct_f32 = o_dtype == PKC_F32 ? 1 : 0;
+      dp.status = status;
+      dp.prefix_as_pages = 1;
+      dp.prefix_k = k_prefix; dp.prefix_v = v_prefix;
+      dp.prefix_pages = prefix_kv_indptr_host[n_prefix] / page_size;
+      dp.pre_n = n_prefix;
+      for (int j = 0; j < n_prefix; ++j) dp.pre_req_indptr[j] = req_begin[j];
+      dp.pre_req_indptr[n_prefix] = req_end[n_prefix - 1];
+      for (int j = 0; j <= n_prefix; ++j) dp.pre_kv_indptr[j] = prefix_kv_indptr_host[j];
+      // KV heads per block: the largest of 8, 4, 2, 1 dividing Hkv that still
+      // gives every SM a block, else 1 (more blocks for a latency-bound step).
+      dp.hg = 1;
+      for (int hg = 8; hg >= 2; hg /= 2)
+        if (num_kv_heads % hg == 0 && (int64_t)batch * (num_kv_heads / hg) >= num_sms()) {
+          dp.hg = hg;
+          break;
+        }
+      for (int i = 0; i < 2; ++i)
+        if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
+      g_last_prefix_blocks = 0;
+      g_last_decode_blocks = batch * (num_kv_heads / dp.hg);
+      const int e = launch_paged_decode(dp, batch, dtype, dtype, stream);
+      if (e == -1) return set_error(PKC_ERR_CUDA, "cascade: could not build TMA tensor maps");
+      if (e) return cuda_error(e, "cascade (small batch) decode launch");
+      for (int i = 2; i < 4; ++i)
+        if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
+      return PKC_OK;
+    }
+  }
   // Decode blocks: one per plan CTA, or (dynamic schedule) fewer persistent
   // blocks taking the plan's chunks from the queue; the chunks are the
   // plan's either way.

@@ -35,21 +35,33 @@ __global__ void __launch_bounds__(256, 4) contract_kernel(const __grid_constant_
 
 int launch_paged_decode_simt(const DecodeParams& p, int grid_x, int dtype, void* stream) {
   if (grid_x <= 0) return 0;
-  // KV heads per block: the largest of 8, 4, 2, 1 that divides Hkv.
-  const int hg = p.hkv % 8 == 0 ? 8 : p.hkv % 4 == 0 ? 4 : p.hkv % 2 == 0 ? 2 : 1;
+  // KV heads per block: the largest of 8, 4, 2, 1 that divides Hkv, or the
+  // caller's choice (p.hg, which must divide Hkv).
+  const int hg = p.hg > 0 ? p.hg : p.hkv % 8 == 0 ? 8 : p.hkv % 4 == 0 ? 4 : p.hkv % 2 == 0 ? 2 : 1;
   const int sl = p.page_size < kMaxSliceRows ? p.page_size : kMaxSliceRows;
   // 4-D view [num_pages][page_size][Hkv][128]; one tile = sl slots x hg heads of a page.
   const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.hkv, (uint64_t)p.page_size,
                             (uint64_t)(p.num_pages > 0 ? p.num_pages : 1)};
   const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)D * 2 * p.hkv, (uint64_t)D * 2 * p.hkv * p.page_size};
   const uint32_t box[4] = {(uint32_t)D, (uint32_t)hg, (uint32_t)sl, 1u};
-  alignas(64) CUtensorMap mk, mv;
+  alignas(64) CUtensorMap mk, mv, mpk, mpv;
   if (!encode_tiled_map(&mk, p.k_cache, dtype, 4, dims, strides, box, false) ||
       !encode_tiled_map(&mv, p.v_cache, dtype, 4, dims, strides, box, false))
     return -1;
+  if (p.prefix_as_pages && p.prefix_pages > 0 && p.prefix_k && p.prefix_v) {
+    // the contiguous prefix tensors [prefix_pages * page_size, Hkv, 128] in the same page view
+    const uint64_t pdims[4] = {(uint64_t)D, (uint64_t)p.hkv, (uint64_t)p.page_size,
+                               (uint64_t)(p.prefix_pages > 0 ? p.prefix_pages : 1)};
+    if (!encode_tiled_map(&mpk, p.prefix_k, dtype, 4, pdims, strides, box, false) ||
+        !encode_tiled_map(&mpv, p.prefix_v, dtype, 4, pdims, strides, box, false))
+      return -1;
+  } else {
+    mpk = mk;  // not read
+    mpv = mv;
+  }
   cudaStream_t st = (cudaStream_t)stream;
-  if (p.fuse.enabled) return launch_paged_decode_simt_fused(p, grid_x, dtype, hg, &mk, &mv, st);
-  return launch_simt_mode<false>(p, grid_x, dtype, hg, mk, mv, st);
+  if (p.fuse.enabled) return launch_paged_decode_simt_fused(p, grid_x, dtype, hg, &mk, &mv, &mpk, &mpv, st);
+  return launch_simt_mode<false>(p, grid_x, dtype, hg, mk, mv, mpk, mpv, st);
 }
 
 // Kernel choice for a 16-bit cache: 0 = automatic, 1 = CUDA-core kernel,
@@ -91,7 +103,7 @@ int launch_paged_decode(const DecodeParams& p_in, int grid_x, int dtype, int kv_
     return launch_paged_decode_mma(p, grid_x, kKvE4M3, stream);
   }
   const int forced = g_decode_kernel.load();
-  const bool use_mma = mma_ok && (forced == 2 || (forced == 0 && p.hq / p.hkv >= 2));
+  const bool use_mma = mma_ok && !p.prefix_as_pages && (forced == 2 || (forced == 0 && p.hq / p.hkv >= 2));
   if (use_mma) return launch_paged_decode_mma(p, grid_x, dtype == PKC_BF16 ? kKvBF16 : kKvF16, stream);
   return launch_paged_decode_simt(p, grid_x, dtype, stream);
 }

@@ -29,6 +29,21 @@ __device__ __forceinline__ void mask_range(uint32_t (&m)[W], int lo, int hi) {
   }
 }
 
+// Small-batch cascade: the first page (in the prefix tensors' page view)
+// and the number of pages of request req's shared prefix (0 outside every
+// group).
+__device__ __forceinline__ int prefix_pages_of(const DecodeParams& p, int req, int& page0) {
+  page0 = 0;
+  if (!p.prefix_as_pages) return 0;
+  for (int j = 0; j < p.pre_n; ++j) {
+    if (p.pre_req_indptr[j] <= req && req < p.pre_req_indptr[j + 1]) {
+      page0 = p.pre_kv_indptr[j] / p.page_size;
+      return (p.pre_kv_indptr[j + 1] - p.pre_kv_indptr[j]) / p.page_size;
+    }
+  }
+  return 0;
+}
+
 // Checks of a planned item against the cache: a plan whose request length
 // (plan_len) no longer matches cache_seqlens is reported (PKC_ERR_PLAN) and
 // the range is clamped to the cache; a range past the block table is
@@ -42,9 +57,11 @@ __device__ __forceinline__ DecodeItem checked_item(const DecodeParams& p, Decode
       d.kb = min(d.kb, d.ke);
     }
   }
-  if ((int64_t)d.ke > p.bt_stride * p.page_size) {  // more tokens than table entries
+  int page0;
+  const int pre = prefix_pages_of(p, d.req, page0) * p.page_size;  // prefix tokens ahead of the cache
+  if ((int64_t)d.ke - pre > p.bt_stride * p.page_size) {  // more tokens than table entries
     report(p.status, PKC_ERR_BLOCK_TABLE);
-    d.ke = (int)(p.bt_stride * p.page_size);
+    d.ke = pre + (int)(p.bt_stride * p.page_size);
     d.kb = min(d.kb, d.ke);
   }
   return d;
@@ -58,7 +75,8 @@ __device__ __forceinline__ DecodeItem load_decode_item(const DecodeParams& p, in
   const int32_t* pl = p.plan;
   if (!pl) {
     d.req = cta;
-    d.ke = max(p.cache_seqlens[cta], 0);
+    int page0;
+    d.ke = prefix_pages_of(p, cta, page0) * p.page_size + max(p.cache_seqlens[cta], 0);
     return checked_item(p, d, 0, false);
   }
   const int w = pl[pl[PKC_PLAN_OFF_CTA_WORK] + wi];

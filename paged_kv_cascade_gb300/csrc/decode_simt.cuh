@@ -131,6 +131,7 @@ struct HeadShift {
 template <typename T, int G, int HG, bool kFuse>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CUtensorMap tm_pv,
                         const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<HG>;
   constexpr int kStages = Cfg::kStages;
@@ -184,7 +185,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int slices_per_stage = kStageRows / (sl * HG);
     const uint32_t slice_bytes = (uint32_t)(sl * HG * kRowBytes);
     const uint64_t pol = l2_policy_evict_first();
-    if (lane == 0) { prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); }
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      if (p.prefix_as_pages) { prefetch_tmap(&tm_pk); prefetch_tmap(&tm_pv); }
+    }
     int k = 0;  // stage counter
     bool ok = true;
     auto acquire = [&](int kk) -> int {
@@ -210,7 +215,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const int req = item.req, kb = item.kb, ke = item.ke, slot = item.slot;
       bool have_n = false;
       const int32_t* bt_row = p.block_table + (int64_t)req * p.bt_stride;
-      const int n_pages_used = (ke + ps - 1) / ps;
+      // Small-batch cascade: the request's first pre_pages pages are its shared
+      // prefix, page pre_page0 + i of the prefix tensors; the block table
+      // lists the rest.
+      int pre_page0;
+      const int pre_pages = prefix_pages_of(p, req, pre_page0);
+      const int n_pages_used = (ke + ps - 1) / ps - pre_pages;  // block-table entries read
       int win_base = -1 << 30;
       int32_t win_pid = -1;
       const int first = kb < ke ? (kb / ps) * spp + (kb % ps) / sl : 0;
@@ -231,20 +241,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const int sli = sl0 + i;
           const int page_idx = sli / spp;
           const int slot0 = (sli % spp) * sl;
-          if (page_idx < win_base || page_idx >= win_base + 32) {
-            win_base = page_idx;
-            const int pi = win_base + lane;
-            win_pid = pi < n_pages_used ? bt_row[pi] : -1;
+          const bool in_prefix = page_idx < pre_pages;  // uniform over the warp
+          int32_t pid;
+          if (in_prefix) {
+            pid = pre_page0 + page_idx;
+          } else {
+            const int bi = page_idx - pre_pages;  // block-table entry
+            if (bi < win_base || bi >= win_base + 32) {
+              win_base = bi;
+              const int pi = win_base + lane;
+              win_pid = pi < n_pages_used ? bt_row[pi] : -1;
+            }
+            pid = __shfl_sync(0xffffffffu, win_pid, bi - win_base);
           }
-          const int32_t pid = __shfl_sync(0xffffffffu, win_pid, page_idx - win_base);
-          if (pid < 0 || pid >= p.num_pages) {
+          if (pid < 0 || pid >= (in_prefix ? p.prefix_pages : p.num_pages)) {
             if (lane == 0) report(p.status, PKC_ERR_BLOCK_TABLE);
             continue;  // rows stay invalid, nothing is copied
           }
           if (lane == 0) {
             mbar_expect_tx(smem_u32(&full[s]), 2 * slice_bytes);  // before the copies it covers
-            tma_load_4d(kst + i * slice_bytes, &tm_k, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
-            tma_load_4d(kst + kStageHalf + i * slice_bytes, &tm_v, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
+            const CUtensorMap* mk = in_prefix ? &tm_pk : &tm_k;
+            const CUtensorMap* mv = in_prefix ? &tm_pv : &tm_v;
+            tma_load_4d(kst + i * slice_bytes, mk, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
+            tma_load_4d(kst + kStageHalf + i * slice_bytes, mv, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
           }
           // valid rows: the HG heads of each slot inside the page and inside [kb, ke)
           const int tok0 = page_idx * ps + slot0;
@@ -534,7 +553,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
 template <typename T, int G, int HG, bool kFuse>
 int launch_decode_g(const DecodeParams& p, int grid_x, const CUtensorMap& mk, const CUtensorMap& mv,
-                    cudaStream_t st) {
+                    const CUtensorMap& mpk, const CUtensorMap& mpv, cudaStream_t st) {
   constexpr int smem = decode_smem_bytes<G, HG>();
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
@@ -546,39 +565,39 @@ int launch_decode_g(const DecodeParams& p, int grid_x, const CUtensorMap& mk, co
   // one block per (planned CTA, head group); one per planned CTA when the
   // blocks take their items from the shared queue
   const dim3 grid(grid_x, p.dynamic ? 1 : p.hkv / HG);
-  paged_decode_kernel<T, G, HG, kFuse><<<grid, kDecodeThreads, smem, st>>>(mk, mv, p);
+  paged_decode_kernel<T, G, HG, kFuse><<<grid, kDecodeThreads, smem, st>>>(mk, mv, mpk, mpv, p);
   return (int)cudaGetLastError();
 }
 
 template <typename T, int HG, bool kFuse>
 int launch_decode_hg(const DecodeParams& p, int grid_x, const CUtensorMap& mk, const CUtensorMap& mv,
-                     cudaStream_t st) {
+                     const CUtensorMap& mpk, const CUtensorMap& mpv, cudaStream_t st) {
   switch (p.hq / p.hkv) {
-    case 1: return launch_decode_g<T, 1, HG, kFuse>(p, grid_x, mk, mv, st);
-    case 2: return launch_decode_g<T, 2, HG, kFuse>(p, grid_x, mk, mv, st);
-    case 4: return launch_decode_g<T, 4, HG, kFuse>(p, grid_x, mk, mv, st);
-    case 8: return launch_decode_g<T, 8, HG, kFuse>(p, grid_x, mk, mv, st);
+    case 1: return launch_decode_g<T, 1, HG, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
+    case 2: return launch_decode_g<T, 2, HG, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
+    case 4: return launch_decode_g<T, 4, HG, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
+    case 8: return launch_decode_g<T, 8, HG, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
     default: return (int)cudaErrorInvalidValue;
   }
 }
 
 template <typename T, bool kFuse>
 int launch_decode_t(const DecodeParams& p, int grid_x, int hg, const CUtensorMap& mk, const CUtensorMap& mv,
-                    cudaStream_t st) {
+                    const CUtensorMap& mpk, const CUtensorMap& mpv, cudaStream_t st) {
   switch (hg) {
-    case 8: return launch_decode_hg<T, 8, kFuse>(p, grid_x, mk, mv, st);
-    case 4: return launch_decode_hg<T, 4, kFuse>(p, grid_x, mk, mv, st);
-    case 2: return launch_decode_hg<T, 2, kFuse>(p, grid_x, mk, mv, st);
-    default: return launch_decode_hg<T, 1, kFuse>(p, grid_x, mk, mv, st);
+    case 8: return launch_decode_hg<T, 8, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
+    case 4: return launch_decode_hg<T, 4, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
+    case 2: return launch_decode_hg<T, 2, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
+    default: return launch_decode_hg<T, 1, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
   }
 }
 
 // The kernels of one contraction mode (kFuse) for a 16-bit cache.
 template <bool kFuse>
 int launch_simt_mode(const DecodeParams& p, int grid_x, int dtype, int hg, const CUtensorMap& mk,
-                     const CUtensorMap& mv, cudaStream_t st) {
-  return dtype == PKC_F16 ? launch_decode_t<__half, kFuse>(p, grid_x, hg, mk, mv, st)
-                          : launch_decode_t<__nv_bfloat16, kFuse>(p, grid_x, hg, mk, mv, st);
+                     const CUtensorMap& mv, const CUtensorMap& mpk, const CUtensorMap& mpv, cudaStream_t st) {
+  return dtype == PKC_F16 ? launch_decode_t<__half, kFuse>(p, grid_x, hg, mk, mv, mpk, mpv, st)
+                          : launch_decode_t<__nv_bfloat16, kFuse>(p, grid_x, hg, mk, mv, mpk, mpv, st);
 }
 
 }  // namespace

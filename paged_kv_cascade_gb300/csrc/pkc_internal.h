@@ -99,6 +99,20 @@ struct DecodeParams {
   int dynamic;            // 1: blocks take the plan's chunks from a shared queue
   int32_t* sched;         // the queue's two counters (in the status block)
   FuseParams fuse;        // fused contraction (fuse.enabled) or none
+  // Small-batch cascade (prefix_as_pages = 1; CUDA-core kernel, no plan):
+  // each request's keys are its group's shared prefix, read as pages of the
+  // contiguous prefix tensors (prefix_k / prefix_v viewed as
+  // [prefix_pages, page_size, Hkv, 128]), then its cached suffix.  Group j
+  // holds requests pre_req_indptr[j] .. pre_req_indptr[j+1]-1 and prefix
+  // tokens pre_kv_indptr[j] .. pre_kv_indptr[j+1]-1, whole pages.
+  int prefix_as_pages;
+  const void* prefix_k;
+  const void* prefix_v;
+  int64_t prefix_pages;
+  int pre_n;
+  int32_t pre_req_indptr[PKC_FUSE_MAX_PREFIX + 1];
+  int32_t pre_kv_indptr[PKC_FUSE_MAX_PREFIX + 1];
+  int hg;                 // CUDA-core kernel: KV heads per block (0: the largest of 8, 4, 2, 1 dividing Hkv)
 };
 
 // Element kinds of a paged KV cache.
@@ -229,7 +243,8 @@ int launch_paged_decode_mma(const DecodeParams& p, int grid_x, int kv_kind,
 int launch_paged_decode_mma_fused(const DecodeParams& p, int grid_x, int kv_kind, int hg,
                                   const void* mk, const void* mv, void* stream);
 int launch_paged_decode_simt_fused(const DecodeParams& p, int grid_x, int dtype, int hg,
-                                   const void* mk, const void* mv, void* stream);
+                                   const void* mk, const void* mv, const void* mpk, const void* mpv,
+                                   void* stream);
 // KV heads per block of the tensor-core kernel, or 0 if it cannot take
 // this head count and page size.
 int mma_decode_heads_per_block(int hkv, int page_size);

@@ -600,6 +600,7 @@ int paged_decode_impl(const void* q, const void* k_cache, const void* v_cache, c
   ContractParams cp;
   std::memset(&cp, 0, sizeof(cp));
   cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractPlanUnits; cp.plan = dp.plan;
+  cp.hkv = num_kv_heads; cp.g = num_qo_heads / num_kv_heads;
   contract_plan_offsets(cp, plan_host);
   cp.part_o = dp.part_o; cp.part_lse = dp.part_lse;
   cp.o = o; cp.lse = lse; cp.out_dtype = dtype; cp.status = status;

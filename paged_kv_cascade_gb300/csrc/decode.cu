@@ -10,13 +10,18 @@
 namespace pkc {
 namespace {
 
-// One warp per (row, head): (+) over every state that belongs to the row
-// (contract_row), after the stages that wrote them.
-__global__ void __launch_bounds__(256, 4) contract_kernel(const __grid_constant__ ContractParams p) {
+// One warp per R query heads of one KV head of a request (R divides the
+// query heads per KV head): (+) over every state that belongs to each of its
+// rows (contract_rows, the rows in lockstep so that all their loads are in
+// flight together), after the stages that wrote them.  More rows per warp
+// need more registers, so fewer blocks per SM (kMinBlocks).
+template <int R, int kMinBlocks>
+__global__ void __launch_bounds__(256, kMinBlocks) contract_kernel(const __grid_constant__ ContractParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-  const int64_t row_idx = gw / p.hq;
-  const int h = (int)(gw % p.hq);
+  const int per_row = p.hq / R;  // warps per request
+  const int64_t row_idx = gw / per_row;
+  const int h0 = (int)(gw % per_row) * R;
   const int32_t* pl = p.plan;
   // The list length changes with the lengths every step: read it from the
   // device plan (the array offsets depend only on batch and CTA count).
@@ -28,7 +33,7 @@ __global__ void __launch_bounds__(256, 4) contract_kernel(const __grid_constant_
     unit = pl[p.off_unit_list + row_idx];
     req = pl[p.off_unit_req + unit];
   }
-  contract_rows<1, ContractParams, true>(p, req, unit, h, 1, lane);
+  contract_rows<R, ContractParams, true>(p, req, unit, h0, R, lane);
 }
 
 }  // namespace
@@ -123,12 +128,13 @@ int set_contract_pdl(int on) {
   return 0;
 }
 
-int launch_contract(const ContractParams& p, int n_rows, void* stream, bool after_decode) {
-  const int64_t warps = (int64_t)n_rows * p.hq;
+template <int R, int kMinBlocks>
+int launch_contract_r(const ContractParams& p, int n_rows, cudaStream_t st, bool programmatic) {
+  const int64_t warps = (int64_t)n_rows * (p.hq / R);
   if (warps <= 0) return 0;
   const int blocks = (int)((warps + 7) / 8);
-  if (!after_decode || !g_contract_pdl.load()) {
-    contract_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(p);
+  if (!programmatic) {
+    contract_kernel<R, kMinBlocks><<<blocks, 256, 0, st>>>(p);
     return (int)cudaGetLastError();
   }
   cudaLaunchConfig_t cfg;
@@ -136,13 +142,24 @@ int launch_contract(const ContractParams& p, int n_rows, void* stream, bool afte
   cfg.gridDim = dim3(blocks);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  cfg.stream = (cudaStream_t)stream;
+  cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, contract_kernel, p);
+  return (int)cudaLaunchKernelEx(&cfg, contract_kernel<R, kMinBlocks>, p);
+}
+
+int launch_contract(const ContractParams& p, int n_rows, void* stream, bool after_decode) {
+  const bool programmatic = after_decode && g_contract_pdl.load();
+  cudaStream_t st = (cudaStream_t)stream;
+  // rows per warp: the query heads of one KV head, up to 4 (p.g is 0 where
+  // the caller did not set it: one row per warp)
+  const int g = p.g;
+  if (g >= 4 && p.hq % 4 == 0) return launch_contract_r<4, 2>(p, n_rows, st, programmatic);
+  if (g == 2 && p.hq % 2 == 0) return launch_contract_r<2, 3>(p, n_rows, st, programmatic);
+  return launch_contract_r<1, 4>(p, n_rows, st, programmatic);
 }
 
 }  // namespace pkc

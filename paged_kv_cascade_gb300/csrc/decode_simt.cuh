@@ -60,18 +60,20 @@ struct StageHdr {
   uint32_t mask[kStageRows / 32];  // valid rows (row-major: slot, head slot)
 };
 
-template <int HG>
+// Ring depth: three 64 KB stages, or two where the merge buffers of warps
+// sharing a KV head (HG < 8) at G = 8 leave no room for a third.
+template <int G, int HG>
 struct DecodeCfg {
   static constexpr int kWph = kConsumerWarps / HG;  // warps per KV head
-  static constexpr int kStages = HG == 8 ? 3 : 2;
+  static constexpr int kStages = (HG == 8 || G <= 4) ? 3 : 2;
 };
 
 // Shared memory, from a 1024-byte aligned base: the K/V stages, the stage
 // headers, the full/empty barriers, the abort flag, then (when several warps
 // share a KV head) the buffer where those warps merge their states.
-template <int HG>
+template <int G, int HG>
 struct DecodeSmem {
-  static constexpr int kStages = DecodeCfg<HG>::kStages;
+  static constexpr int kStages = DecodeCfg<G, HG>::kStages;
   static constexpr int kHdr = kStages * 2 * kStageHalf;
   static constexpr int kBars = kHdr + kStages * (int)sizeof(StageHdr);
   static constexpr int kMergeBars = kBars + 2 * kStages * 8;  // 2 merge barriers
@@ -82,17 +84,20 @@ struct DecodeSmem {
 // Two merge buffers (alternating work items) of 8 warps x G heads x (D + 2).
 template <int G, int HG>
 constexpr int decode_merge_bytes() {
-  return DecodeCfg<HG>::kWph > 1 ? 2 * kConsumerWarps * G * (D + 2) * 4 : 0;
+  return DecodeCfg<G, HG>::kWph > 1 ? 2 * kConsumerWarps * G * (D + 2) * 4 : 0;
 }
 // ... then the block's copy of the fused contraction's parameters.
 template <int G, int HG>
 constexpr int decode_fuse_offset() {
-  return (DecodeSmem<HG>::kMerge + decode_merge_bytes<G, HG>() + 15) & ~15;
+  return (DecodeSmem<G, HG>::kMerge + decode_merge_bytes<G, HG>() + 15) & ~15;
 }
 template <int G, int HG>
 constexpr int decode_smem_bytes() {
   return decode_fuse_offset<G, HG>() + (int)sizeof(FuseParams) + 1024;
 }
+static_assert(decode_smem_bytes<4, 1>() <= 227 * 1024, "shared memory");
+static_assert(decode_smem_bytes<8, 1>() <= 227 * 1024, "shared memory");
+static_assert(decode_smem_bytes<8, 8>() <= 227 * 1024, "shared memory");
 
 // Transposed butterfly over the 16 lanes of a half-warp: in, v[i] is this
 // lane's partial dot of head i; out, v[0] is the full dot of head
@@ -133,14 +138,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CUtensorMap tm_pv,
                         const __grid_constant__ DecodeParams p) {
-  using Cfg = DecodeCfg<HG>;
+  using Cfg = DecodeCfg<G, HG>;
   constexpr int kStages = Cfg::kStages;
   constexpr int kWph = Cfg::kWph;
   constexpr int kShift = HeadShift<G>::v;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_kv = smem_u32(smem);  // stage s: K at s*64KB, V at +32KB
-  using L = DecodeSmem<HG>;
+  using L = DecodeSmem<G, HG>;
   StageHdr* hdrs = reinterpret_cast<StageHdr*>(smem + L::kHdr);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* empty = full + kStages;
@@ -223,6 +228,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const int n_pages_used = (ke + ps - 1) / ps - pre_pages;  // block-table entries read
       int win_base = -1 << 30;
       int32_t win_pid = -1;
+      if (pre_pages > 0) {
+        // The first block-table window, loaded now: the load runs while the
+        // prefix pages are copied, and is waited for only at the first suffix page.
+        const int bi0 = max(kb / ps - pre_pages, 0);
+        win_base = bi0;
+        win_pid = bi0 + lane < n_pages_used ? bt_row[bi0 + lane] : -1;
+      }
       const int first = kb < ke ? (kb / ps) * spp + (kb % ps) / sl : 0;
       const int last = kb < ke ? ((ke - 1) / ps) * spp + ((ke - 1) % ps) / sl : -1;
       int sl0 = first;

@@ -143,3 +143,19 @@ def test_no_alloc_rejects_a_plan_beyond_its_scratch():
         pkc.paged_decode_state_noalloc(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
                                        d["cache_seqlens"], p["sm_scale"], plan_buf=plan_buf)
     assert e.value.code == 3 and "8388608" in str(e.value)
+
+
+def test_no_alloc_full_size_plan_matches_the_oracle():
+    """The GQA suffix shape at full size (batch 256, 32/8 heads, lognormal
+    lengths up to 16384 tokens, plan over 148 CTAs: long requests split over
+    many chunks, so the partial states fill much of the scratch array), every
+    row against the oracle."""
+    import oracle
+    from pkc_testing import compare, oracle_args
+    _set_up_call()
+    p = workloads.workload("gqa_cascade_lb", prefix_lens=[], prefix_groups=[])
+    d = to_device(p)
+    plan_buf = pkc.plan(p["cache_seqlens"], 148)
+    got_o, got_lse = _no_alloc_via_c_abi(p, d, plan_buf)
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p, prefix=False))
+    compare(got_o, got_lse, ref_o, ref_lse)

@@ -68,6 +68,9 @@ def parse_args():
     ap.add_argument("--contraction", choices=["fused", "separate", "separate_plain"], default="separate",
                     help="split states contracted inside the attention kernels (fused) or by a "
                          "standalone contraction kernel after them")
+    ap.add_argument("--cascade-small", type=int, default=16,
+                    help="largest rows per KV head of a prefix group for the one-launch "
+                         "small-batch cascade (0: never; pkc_set_cascade_small)")
     ap.add_argument("--num-ctas", type=int, default=None,
                     help="CTAs of the host plan (default: the workload's)")
     ap.add_argument("--prefix-ctas", type=int, default=0,
@@ -921,6 +924,7 @@ def main():
     pkc.set_decode_schedule(args.decode_schedule)
     pkc.set_prefix_ctas(args.prefix_ctas)
     pkc.set_contraction(args.contraction)
+    pkc.set_cascade_small(args.cascade_small)
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from pkc_testing import to_device
     ctx = make_ctx(args, torch, pkc, local)

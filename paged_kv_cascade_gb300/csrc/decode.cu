@@ -154,11 +154,10 @@ int launch_contract_r(const ContractParams& p, int n_rows, cudaStream_t st, bool
 int launch_contract(const ContractParams& p, int n_rows, void* stream, bool after_decode) {
   const bool programmatic = after_decode && g_contract_pdl.load();
   cudaStream_t st = (cudaStream_t)stream;
-  // rows per warp: the query heads of one KV head, up to 4 (p.g is 0 where
-  // the caller did not set it: one row per warp)
-  const int g = p.g;
-  if (g >= 4 && p.hq % 4 == 0) return launch_contract_r<4, 2>(p, n_rows, st, programmatic);
-  if (g == 2 && p.hq % 2 == 0) return launch_contract_r<2, 3>(p, n_rows, st, programmatic);
+  // One row per warp at 4 blocks per SM: several query heads of a KV head
+  // per warp in lockstep (4 rows at 2 blocks per SM) took longer on every
+  // cascade measured (gqa_cascade_lb contraction 12.8 -> 15.2 us): the rows
+  // in flight per SM, not the loads per warp, set its time.
   return launch_contract_r<1, 4>(p, n_rows, st, programmatic);
 }
 

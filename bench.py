@@ -337,9 +337,9 @@ def run_reference(args):
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": line_config(args.workload, cfg, p, cfg["num_ctas"], args, world,
-                              {"step": "a sample of the step's (request, head) rows, "
-                                       "every prefix and suffix token of each"}),
+        "config": line_config(args.workload, cfg, p, cfg["num_ctas"], args, world),
+        "impl_config": {"step": "a sample of the step's (request, head) rows, every prefix and "
+                                "suffix token of each, float64 on the host cores"},
         "sample_fraction": statistics.mean(fracs),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{n_rows} of {total} (request, head) rows per step, "
@@ -1137,12 +1137,13 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": 1e3 * ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg["dtype"], "data": "synthetic",
-            "config": line_config(args.workload, cfg, p, num_ctas, args, world, {
+            "config": line_config(args.workload, cfg, p, num_ctas, args, world),
+            "impl_config": {
                 "launch": "cuda_graph", "decode_kernel": args.decode_kernel,
                 "contraction": args.contraction,
                 "decode_schedule": args.decode_schedule if num_ctas else None,
                 "prefix_ctas": args.prefix_ctas or "auto",
-                "step": "host plan + plan upload + prefix states + paged decode + contraction"}),
+                "step": "host plan + plan upload + prefix states + paged decode + contraction"},
             "stage_split": split,
             "direct_us_per_step": 1e3 * direct_ms_per_step,
             "hbm_fraction": value / world / hbm_peak,

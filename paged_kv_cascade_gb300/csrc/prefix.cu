@@ -218,14 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             tma_load_3d(st, tmap, fb, 0, pc.kvh, t0, pol);
             tma_load_3d(st + kSubTile, tmap, fb, 64, pc.kvh, t0, pol);
-            // The tile a ring's length further on goes to L2 now: when its
-            // slot frees, its copy reads L2 instead of HBM, so each ring
-            // keeps about one more tile's bytes in flight than its slots
-            // hold.
-            if (u + n_st < pc.n) {
-              tma_prefetch_3d(tmap, 0, pc.kvh, t0 + n_st * kKvTile);
-              tma_prefetch_3d(tmap, 64, pc.kvh, t0 + n_st * kKvTile);
-            }
           }
         } else {
           // Box c: page c / 2 of the tile, dims 0-63 or 64-127 by c % 2,

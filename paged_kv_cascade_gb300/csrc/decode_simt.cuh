@@ -35,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <climits>
 #include <mutex>
 
 #include "contract_common.cuh"
@@ -246,40 +247,51 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         StageHdr& h = hdrs[s];
         const uint32_t kst = s_kv + s * 2 * kStageHalf;
         // Row validity: row j = i*sl*HG + t*HG + hh belongs to slice i, slot t.
+        // Lane l handles slices l, l + 32, ... of the stage: its page id, its
+        // two copies (each lane raises the stage's byte count for its own
+        // copies before issuing them; lane 0 arrives only after the warp has
+        // passed the mask reduction below, so the phase cannot complete
+        // early) and its rows of the mask.  One lane per slice instead of a
+        // loop over the slices: a stage of 8 one-head slices took 2.5 us to
+        // issue one slice after another, which a short request waits for.
         uint32_t maskw[kStageRows / 32];
 #pragma unroll
         for (int q = 0; q < kStageRows / 32; ++q) maskw[q] = 0;
-        for (int i = 0; i < n_sl; ++i) {
+        for (int i0 = 0; i0 < n_sl; i0 += 32) {
+          const int i = i0 + lane;
+          const bool mine = i < n_sl;
           const int sli = sl0 + i;
           const int page_idx = sli / spp;
           const int slot0 = (sli % spp) * sl;
-          const bool in_prefix = page_idx < pre_pages;  // uniform over the warp
-          int32_t pid;
-          if (in_prefix) {
-            pid = pre_page0 + page_idx;
-          } else {
-            const int bi = page_idx - pre_pages;  // block-table entry
-            if (bi < win_base || bi >= win_base + 32) {
-              win_base = bi;
-              const int pi = win_base + lane;
-              win_pid = pi < n_pages_used ? bt_row[pi] : -1;
-            }
-            pid = __shfl_sync(0xffffffffu, win_pid, bi - win_base);
+          const bool in_prefix = page_idx < pre_pages;
+          const int bi = page_idx - pre_pages;  // block-table entry (suffix pages)
+          const bool need = mine && !in_prefix;
+          // These slices lie on at most 32 consecutive pages: a window that
+          // starts at the first suffix page among them covers them all.
+          if (__any_sync(0xffffffffu, need && (bi < win_base || bi >= win_base + 32))) {
+            win_base = __reduce_min_sync(0xffffffffu, need ? bi : INT_MAX);
+            const int pi = win_base + lane;
+            win_pid = pi < n_pages_used ? bt_row[pi] : -1;
           }
-          if (pid < 0 || pid >= (in_prefix ? p.prefix_pages : p.num_pages)) {
-            if (lane == 0) report(p.status, PKC_ERR_BLOCK_TABLE);
-            continue;  // rows stay invalid, nothing is copied
-          }
-          if (lane == 0) {
+          int32_t pid = __shfl_sync(0xffffffffu, win_pid, need ? bi - win_base : 0);
+          if (in_prefix) pid = pre_page0 + page_idx;
+          const bool good = mine && pid >= 0 && pid < (in_prefix ? p.prefix_pages : p.num_pages);
+          if (mine && !good) report(p.status, PKC_ERR_BLOCK_TABLE);  // rows stay invalid, nothing is copied
+          uint32_t mw[kStageRows / 32];
+#pragma unroll
+          for (int q = 0; q < kStageRows / 32; ++q) mw[q] = 0;
+          if (good) {
             mbar_expect_tx(smem_u32(&full[s]), 2 * slice_bytes);  // before the copies it covers
             const CUtensorMap* mk = in_prefix ? &tm_pk : &tm_k;
             const CUtensorMap* mv = in_prefix ? &tm_pv : &tm_v;
             tma_load_4d(kst + i * slice_bytes, mk, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
             tma_load_4d(kst + kStageHalf + i * slice_bytes, mv, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
+            // valid rows: the HG heads of each slot inside the page and inside [kb, ke)
+            const int tok0 = page_idx * ps + slot0;
+            mask_range(mw, (i * sl + max(kb - tok0, 0)) * HG, (i * sl + min(min(ke - tok0, sl), ps - slot0)) * HG);
           }
-          // valid rows: the HG heads of each slot inside the page and inside [kb, ke)
-          const int tok0 = page_idx * ps + slot0;
-          mask_range(maskw, (i * sl + max(kb - tok0, 0)) * HG, (i * sl + min(min(ke - tok0, sl), ps - slot0)) * HG);
+#pragma unroll
+          for (int q = 0; q < kStageRows / 32; ++q) maskw[q] |= __reduce_or_sync(0xffffffffu, mw[q]);
         }
         sl0 += slices_per_stage;
         const bool last_stage = sl0 > last;

@@ -374,6 +374,7 @@ void fill_contract_prefix(ContractParams& c, const PrefixSetup& S) {
 // Copy the plan-array offsets the contraction kernel needs.
 void contract_plan_offsets(ContractParams& c, const int32_t* plan_host) {
   if (!plan_host) return;
+  c.plan_words = plan_host[PKC_PLAN_TOTAL_WORDS];
   c.off_unit_list = plan_host[PKC_PLAN_OFF_UNIT_LIST];
   c.off_unit_req = plan_host[PKC_PLAN_OFF_UNIT_REQ];
   c.off_unit_n_chunks = plan_host[PKC_PLAN_OFF_UNIT_N_CHUNKS];
@@ -405,6 +406,7 @@ void fill_fuse(FuseParams& f, const ContractParams& c, int hkv, int32_t* arrive)
   f.hkv = hkv;
   f.g = c.hq / hkv;
   f.plan = c.plan;
+  f.plan_words = c.plan_words;
   f.off_unit_list = c.off_unit_list;
   f.off_unit_req = c.off_unit_req;
   f.off_unit_n_chunks = c.off_unit_n_chunks;
@@ -590,6 +592,7 @@ int paged_decode_impl(const void* q, const void* k_cache, const void* v_cache, c
   dp.scale_log2 = sm_scale * k_scale * 1.4426950408889634f;
   dp.v_scale = v_scale;
   dp.plan = plan_host ? reinterpret_cast<const int32_t*>(ws + L.plan) : nullptr;
+  dp.plan_words = plan_host ? plan_host[PKC_PLAN_TOTAL_WORDS] : 0;
   dp.o_direct = o; dp.lse_direct = lse; dp.direct_f32 = 0;
   dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
   dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
@@ -954,6 +957,7 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
   dp.v_scale = 1.f;
   dp.plan = plan_host ? reinterpret_cast<const int32_t*>(ws + L.plan) : nullptr;
+  dp.plan_words = plan_host ? plan_host[PKC_PLAN_TOTAL_WORDS] : 0;
   dp.o_direct = ws + L.suffix_o; dp.lse_direct = reinterpret_cast<float*>(ws + L.suffix_lse); dp.direct_f32 = 1;
   dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
   dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);

@@ -23,6 +23,10 @@ __global__ void __launch_bounds__(256, kMinBlocks) contract_kernel(const __grid_
   const int64_t row_idx = gw / per_row;
   const int h0 = (int)(gw % per_row) * R;
   const int32_t* pl = p.plan;
+  if (pl && !device_plan_ok(pl, p.plan_words, p.batch)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(p.status, PKC_ERR_PLAN);
+    return;
+  }
   // The list length changes with the lengths every step: read it from the
   // device plan (the array offsets depend only on batch and CTA count).
   const int64_t n_rows =

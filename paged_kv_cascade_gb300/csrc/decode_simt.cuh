@@ -161,6 +161,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // Head groups of this block: blockIdx.y, blockIdx.y + gridDim.y, ...
   const int n_hg_mine = (p.hkv / HG - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
   const int32_t* pl = p.plan;
+  if (pl && !device_plan_ok(pl, p.plan_words, p.batch)) {  // uniform: before any barrier
+    if (threadIdx.x == 0) report(p.status, PKC_ERR_PLAN);
+    return;
+  }
   int w_begin = 0, w_end = 1;
   if (pl) {
     w_begin = pl[pl[PKC_PLAN_OFF_CTA_INDPTR] + cta];

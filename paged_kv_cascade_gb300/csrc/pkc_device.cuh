@@ -21,6 +21,18 @@ __device__ __forceinline__ void report(int32_t* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// The device copy of a plan (the workspace's plan words, written by
+// pkc_plan_upload) against the call's host plan: magic word, total words and
+// request count.  A plan that was never uploaded leaves whatever the
+// workspace held in those words; the kernels that read a plan check it first
+// and report PKC_ERR_PLAN instead of following its offsets.  (A stale plan
+// of the same batch and CTA count is a whole plan: its offsets stay inside
+// it, and its lengths are checked against cache_seqlens item by item.)
+__device__ __forceinline__ bool device_plan_ok(const int32_t* pl, int32_t words, int batch) {
+  return pl[PKC_PLAN_MAGIC] == PKC_PLAN_MAGIC_VALUE && pl[PKC_PLAN_TOTAL_WORDS] == words &&
+         pl[PKC_PLAN_N_REQ] == batch;
+}
+
 // Hardware base-2 exponent / logarithm (MUFU), flush-to-zero.
 __device__ __forceinline__ float ex2(float x) {
   float y;

@@ -57,6 +57,7 @@ struct FuseParams {
   int32_t* arrive;          // [batch * hkv] arrival counters, zeroed before each call
   int batch, hq, hkv, g;
   const int32_t* plan;      // device plan (decode plans: unit = request) or nullptr
+  int32_t plan_words;       // the host plan's total words (the device copy must match)
   int32_t off_unit_list, off_unit_req, off_unit_n_chunks, off_unit_partial_begin;
   const float* suffix_o;    // direct suffix states (a cascade) or nullptr
   const float* suffix_lse;
@@ -89,6 +90,7 @@ struct DecodeParams {
   int batch, hq, hkv, page_size;
   float scale_log2;       // sm_scale * log2(e)
   const int32_t* plan;    // device copy of the plan, or nullptr
+  int32_t plan_words;     // the host plan's total words (the device copy must match)
   void* o_direct;         // unsplit outputs: [B, Hq, D] (dtype or f32)
   float* lse_direct;      // [B, Hq]
   int direct_f32;         // 1: o_direct is float32 (suffix states)
@@ -147,6 +149,7 @@ struct ContractParams {
   int batch, hq;
   int mode;
   const int32_t* plan;      // device plan or nullptr
+  int32_t plan_words;       // the host plan's total words (the device copy must match)
   // Word offsets of the plan arrays, copied from the host plan (they depend
   // only on batch and CTA count) so the kernel's first loads are the arrays.
   int32_t off_unit_list, off_unit_req, off_unit_n_chunks, off_unit_partial_begin;

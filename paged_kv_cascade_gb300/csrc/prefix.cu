@@ -123,6 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) report(p.status, PKC_ERR_UNSUPPORTED);
     return;
   }
+  if (kFuse && p.fuse.plan && !device_plan_ok(p.fuse.plan, p.fuse.plan_words, p.fuse.batch)) {
+    if (threadIdx.x == 0) report(p.status, PKC_ERR_PLAN);  // the fused merges would follow its offsets
+    return;
+  }
   const uint32_t s_q = smem_u32(smem);
   const uint32_t s_p = s_q + kPOffset, s_k0 = s_q + kKOffset, s_v0 = s_q + kVOffset;
   Barriers* bars = reinterpret_cast<Barriers*>(smem + kBarOffset);

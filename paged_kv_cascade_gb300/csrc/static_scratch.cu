@@ -132,6 +132,7 @@ extern "C" int pkc_paged_decode_state_noalloc(
   dp.scale_log2 = sm_scale * 1.4426950408889634f;
   dp.v_scale = 1.f;
   dp.plan = plan_host ? reinterpret_cast<const int32_t*>(s + off_plan) : nullptr;
+  dp.plan_words = plan_host ? plan_host[PKC_PLAN_TOTAL_WORDS] : 0;
   dp.o_direct = o; dp.lse_direct = lse; dp.direct_f32 = 0;
   dp.part_o = reinterpret_cast<float*>(s + off_po);
   dp.part_lse = reinterpret_cast<float*>(s + off_pl);
@@ -142,6 +143,7 @@ extern "C" int pkc_paged_decode_state_noalloc(
     ContractParams cp;
     std::memset(&cp, 0, sizeof(cp));
     cp.batch = batch; cp.hq = num_qo_heads; cp.mode = kContractPlanUnits; cp.plan = dp.plan;
+    cp.plan_words = plan_host[PKC_PLAN_TOTAL_WORDS];
     cp.off_unit_list = plan_host[PKC_PLAN_OFF_UNIT_LIST];
     cp.off_unit_req = plan_host[PKC_PLAN_OFF_UNIT_REQ];
     cp.off_unit_n_chunks = plan_host[PKC_PLAN_OFF_UNIT_N_CHUNKS];

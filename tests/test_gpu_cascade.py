@@ -215,3 +215,33 @@ def test_noncascade_decode_of_the_long_prompt_shape():
     assert pkc.device_status(ws) == pkc.PKC_OK
     ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
     compare(o, lse, ref_o, ref_lse)
+
+
+@pytest.mark.parametrize("contraction", ["separate", "fused"])
+def test_cascade_plan_never_uploaded_is_reported(contraction):
+    """A planned cascade on a workspace that never received the plan (its
+    plan words are zeros here): every kernel that reads the plan (decode,
+    contraction, and the prefix kernel when it merges) checks the device
+    plan's header against the call's host plan and reports PKC_ERR_PLAN.
+    Once the plan is uploaded the same call matches the oracle."""
+    p = workloads.make_problem(batch=12, hq=16, hkv=4, d=128, dtype="bf16", prefix_lens=[300],
+                               prefix_groups=[12], suffix=("uniform", 1, 200), page_size=16,
+                               seed=41)
+    d = to_device(p)
+    plan_buf = pkc.plan(p["cache_seqlens"], 8)
+    nbytes = pkc.workspace_size(12, 16, 8, 64)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    args = (d["q"], d["k_prefix"], d["v_prefix"], p["prefix_kv_indptr"], p["prefix_req_indptr"],
+            d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"], p["sm_scale"], ws)
+    pkc.set_contraction(contraction)
+    try:
+        pkc.cascade_decode(*args, plan_buf=plan_buf)
+        assert pkc.device_status(ws) == 7  # PKC_ERR_PLAN
+        pkc.plan_upload(plan_buf, ws)
+        o, lse = pkc.cascade_decode(*args, plan_buf=plan_buf)
+        torch.cuda.synchronize()
+        assert pkc.device_status(ws) == pkc.PKC_OK
+    finally:
+        pkc.set_contraction("separate")
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p))
+    compare(o, lse, ref_o, ref_lse)

@@ -116,3 +116,27 @@ def test_decode_plan_that_does_not_match_lengths_is_reported():
     pkc.paged_decode_state(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
                            d["cache_seqlens"], p["sm_scale"], ws, plan_buf=plan_buf)
     assert pkc.device_status(ws) == 7
+
+
+@pytest.mark.parametrize("hq", [4, 8])  # G = 1: CUDA-core decode; G = 2: tensor-core decode
+def test_decode_plan_never_uploaded_is_reported(hq):
+    """A planned call on a workspace that never received the plan (no
+    pkc_plan_upload; its plan words are zeros here): the decode and the
+    contraction compare the device plan's header with the call's host plan
+    and report PKC_ERR_PLAN instead of following the words.  Once the plan
+    is uploaded the same call is exact."""
+    p = workloads.make_problem(batch=3, hq=hq, hkv=4, d=128, dtype="f16", prefix_lens=[],
+                               prefix_groups=[], suffix=("list", [40, 20, 5]), page_size=16,
+                               seed=3)
+    d = to_device(p)
+    plan_buf = pkc.plan([40, 20, 5], 4)
+    ws = torch.zeros(pkc.workspace_size(3, hq, 4, 0), dtype=torch.uint8, device="cuda")
+    args = (d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["cache_seqlens"], p["sm_scale"], ws)
+    pkc.paged_decode_state(*args, plan_buf=plan_buf)
+    assert pkc.device_status(ws) == 7  # PKC_ERR_PLAN
+    pkc.plan_upload(plan_buf, ws)
+    o, lse = pkc.paged_decode_state(*args, plan_buf=plan_buf)
+    torch.cuda.synchronize()
+    assert pkc.device_status(ws) == pkc.PKC_OK
+    ref_o, ref_lse = oracle.attention_rows(p["q"], **oracle_args(p, prefix=False))
+    compare(o, lse, ref_o, ref_lse)

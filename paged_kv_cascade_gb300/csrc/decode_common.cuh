@@ -113,34 +113,46 @@ struct DecodeItemWindow {
 // workspace's status block.  Ticket t is chunk t / n_hg of the plan's
 // longest-first order (its 16-byte record) for head group t % n_hg, so the
 // blocks that run ahead take the short chunks at the end and the blocks
-// finish together.  Each block counts itself out once the queue is empty;
-// the last one resets both counters for the next launch (every block
-// reaches that point, on the error paths too).
+// finish together.  Block b's first ticket is ticket b, taken without the
+// counter; the counter hands out the rest (tickets gridDim + 0, 1, ...).
+// Each block counts itself out once the queue is empty; the last one resets
+// both counters for the next launch (every block reaches that point, on the
+// error paths too).
 struct DecodeQueue {
-  int32_t* ctr;     // [0] next ticket, [1] blocks finished
+  int32_t* ctr;     // [0] tickets handed out by the counter, [1] blocks finished
   const int4* rec;  // order_rec of the plan
   const int32_t* plan_len;
   int n_total, n_hg;
-  __device__ __forceinline__ DecodeQueue(const DecodeParams& p, int hg_per_block, bool active) {
+  bool first;       // the block's own first ticket is still to be taken
+  // Warp-collective.  hw: word `lane` of the plan's header, which the warp
+  // has loaded (the queue's offsets and sizes are header words).
+  __device__ __forceinline__ DecodeQueue(const DecodeParams& p, int hg_per_block, bool active, int32_t hw) {
     ctr = nullptr;
     rec = nullptr;
     plan_len = nullptr;
     n_total = 0;
     n_hg = 1;
+    first = true;
     if (!active) return;
     const int32_t* pl = p.plan;
     ctr = p.sched;
-    rec = reinterpret_cast<const int4*>(pl + pl[PKC_PLAN_OFF_ORDER_REC]);
-    plan_len = pl + pl[PKC_PLAN_OFF_UNIT_KV_LEN];
+    rec = reinterpret_cast<const int4*>(pl + __shfl_sync(0xffffffffu, hw, PKC_PLAN_OFF_ORDER_REC));
+    plan_len = pl + __shfl_sync(0xffffffffu, hw, PKC_PLAN_OFF_UNIT_KV_LEN);
     n_hg = p.hkv / hg_per_block;
-    n_total = pl[PKC_PLAN_N_WORK] * n_hg;
+    n_total = __shfl_sync(0xffffffffu, hw, PKC_PLAN_N_WORK) * n_hg;
   }
   // The next ticket's item (all lanes get it), or false once the queue is
   // empty.  A decode plan's unit is its request.
   __device__ __forceinline__ bool take(const DecodeParams& p, int lane, DecodeItem& d, int& hg) {
-    int t = 0;
-    if (lane == 0) t = atomicAdd(ctr, 1);
-    t = __shfl_sync(0xffffffffu, t, 0);
+    int t;
+    if (first) {
+      first = false;
+      t = (int)(blockIdx.x + gridDim.x * blockIdx.y);
+    } else {
+      int a = 0;
+      if (lane == 0) a = atomicAdd(ctr, 1);
+      t = __shfl_sync(0xffffffffu, a, 0) + (int)(gridDim.x * gridDim.y);
+    }
     if (t < 0 || t >= n_total) return false;
     const int4 r = rec[t / n_hg];
     hg = t % n_hg;

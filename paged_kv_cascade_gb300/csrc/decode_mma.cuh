@@ -157,14 +157,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cta = blockIdx.x;
   const int n_hg_mine = (p.hkv / HG - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
   const int32_t* pl = p.plan;
-  if (pl && !device_plan_ok(pl, p.plan_words, p.batch)) {  // uniform: before any barrier
+  // Word `lane` of the plan's header, one load per lane: the device-plan
+  // check and the producer's set-up read the header from here, so a block's
+  // first item costs one round trip less.
+  const int32_t hw = pl ? pl[lane] : 0;
+  if (pl && !device_plan_header_ok(hw, p.plan_words, p.batch)) {  // uniform: before any barrier
     if (threadIdx.x == 0) report(p.status, PKC_ERR_PLAN);
     return;
   }
   int w_begin = 0, w_end = 1;
-  if (pl) {
-    w_begin = pl[pl[PKC_PLAN_OFF_CTA_INDPTR] + cta];
-    w_end = pl[pl[PKC_PLAN_OFF_CTA_INDPTR] + cta + 1];
+  if (pl && !p.dynamic) {  // the static schedule's CTA list
+    const int32_t* cta_indptr = pl + __shfl_sync(0xffffffffu, hw, PKC_PLAN_OFF_CTA_INDPTR);
+    w_begin = cta_indptr[cta];
+    w_end = cta_indptr[cta + 1];
   }
   const int ps = p.page_size;
   const int sl = ps < kMaxSl ? ps : kMaxSl;             // slots per slice
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool dyn = p.dynamic && pl;
     const int n_w = w_end - w_begin;
     DecodeItemWindow items;
-    DecodeQueue queue(p, HG, dyn);
+    DecodeQueue queue(p, HG, dyn, hw);
     DecodeItem item{0, 0, 0, -1}, item_n{0, 0, 0, -1};
     int hg = (int)blockIdx.y, hg_n = 0, it = 0;
     bool have = dyn ? queue.take(p, lane, item, hg) : n_hg_mine * n_w > 0;

@@ -32,6 +32,13 @@ __device__ __forceinline__ bool device_plan_ok(const int32_t* pl, int32_t words,
   return pl[PKC_PLAN_MAGIC] == PKC_PLAN_MAGIC_VALUE && pl[PKC_PLAN_TOTAL_WORDS] == words &&
          pl[PKC_PLAN_N_REQ] == batch;
 }
+// The same check, warp-collective, from the header words the warp holds one
+// per lane (lane l: word l of the plan's PKC_PLAN_HEADER_WORDS = 32).
+__device__ __forceinline__ bool device_plan_header_ok(int32_t hw, int32_t words, int batch) {
+  return __shfl_sync(0xffffffffu, hw, PKC_PLAN_MAGIC) == PKC_PLAN_MAGIC_VALUE &&
+         __shfl_sync(0xffffffffu, hw, PKC_PLAN_TOTAL_WORDS) == words &&
+         __shfl_sync(0xffffffffu, hw, PKC_PLAN_N_REQ) == batch;
+}
 
 // Hardware base-2 exponent / logarithm (MUFU), flush-to-zero.
 __device__ __forceinline__ float ex2(float x) {

@@ -204,7 +204,9 @@ int pkc_plan(const int32_t* qo_len_host, const int32_t* kv_len_host, int n,
 
 /*
  * Copy a plan into the plan region of a workspace (cudaMemcpyAsync on
- * `stream`).  plan_host must stay valid until the copy has run.
+ * `stream`).  plan_host must stay valid until the copy has run.  Every
+ * planned call reads the plan from the workspace: it must have been
+ * uploaded there (pkc_workspace_init clears only the status block).
  */
 int pkc_plan_upload(const int32_t* plan_host, void* workspace,
                     size_t workspace_bytes, void* stream);
@@ -262,7 +264,10 @@ int pkc_device_status(void* workspace, void* stream, int32_t* status);
  *   cache_seqlens [batch] int32 >= 0
  *   plan_host: NULL, or a plan of these lengths (tile_q 1) that was
  *            uploaded into this workspace with pkc_plan_upload.  NULL runs
- *            one chunk per request.
+ *            one chunk per request.  The kernels compare the workspace's
+ *            copy (magic word, total words, request count) with plan_host
+ *            before reading it: a plan never uploaded is reported as
+ *            PKC_ERR_PLAN on the device, and nothing is computed.
  *   o        [batch, num_qo_heads, 128] of dtype; lse [batch, num_qo_heads]
  *            float32 natural log.  A request with 0 tokens gets (0, -inf).
  */

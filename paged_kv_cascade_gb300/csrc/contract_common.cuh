@@ -68,11 +68,12 @@ __device__ __forceinline__ void contract_rows(const CP& p, int req, int unit, in
   constexpr int D = PKC_HEAD_DIM;
   const int32_t* pl = p.plan;
   // Running state of each row's merge: maximum m, denominator den,
-  // unnormalised acc.  Sources go in batches of 4 whose loads are all in
-  // flight together; the running state is rescaled between batches.
-  // (Batches of 4 keep the standalone kernel at few registers and many rows
-  // in flight per SM: faster than batches of 8.)
-  constexpr int kB = 4;
+  // unnormalised acc.  Sources go in batches (4 per row for one row, 2 per
+  // row for two rows in lockstep: 4 loads in flight per warp either way)
+  // whose loads are all in flight together; the running state is rescaled
+  // between batches.  (Small batches keep the standalone kernel at few
+  // registers and many rows in flight per SM: faster than batches of 8.)
+  constexpr int kB = R >= 2 ? 2 : 4;
   float m[R], den[R];
   float4 acc[R];
   int64_t row_off[R];

@@ -158,10 +158,13 @@ int launch_contract_r(const ContractParams& p, int n_rows, cudaStream_t st, bool
 int launch_contract(const ContractParams& p, int n_rows, void* stream, bool after_decode) {
   const bool programmatic = after_decode && g_contract_pdl.load();
   cudaStream_t st = (cudaStream_t)stream;
-  // One row per warp at 4 blocks per SM: several query heads of a KV head
-  // per warp in lockstep (4 rows at 2 blocks per SM) took longer on every
-  // cascade measured (gqa_cascade_lb contraction 12.8 -> 15.2 us): the rows
-  // in flight per SM, not the loads per warp, set its time.
+  // The rows in flight per SM, not the loads per warp, set the kernel's
+  // time: 4 rows per warp at 2 blocks per SM took longer than 1 row at 4
+  // blocks (gqa_cascade_lb contraction 12.8 -> 15.2 us), while 2 rows at 4
+  // blocks fit the headline's rows in one wave of resident blocks (step
+  // 290.1 -> 288.5 us).  The two rows are query heads of one KV head
+  // (G >= 2), which share their prefix pieces; G = 1 keeps one row per warp.
+  if (p.g >= 2 && p.hq % 2 == 0) return launch_contract_r<2, 4>(p, n_rows, st, programmatic);
   return launch_contract_r<1, 4>(p, n_rows, st, programmatic);
 }
 

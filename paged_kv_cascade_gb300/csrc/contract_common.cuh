@@ -68,12 +68,17 @@ __device__ __forceinline__ void contract_rows(const CP& p, int req, int unit, in
   constexpr int D = PKC_HEAD_DIM;
   const int32_t* pl = p.plan;
   // Running state of each row's merge: maximum m, denominator den,
-  // unnormalised acc.  Sources go in batches (4 per row for one row, 2 per
-  // row for two rows in lockstep: 4 loads in flight per warp either way)
-  // whose loads are all in flight together; the running state is rescaled
-  // between batches.  (Small batches keep the standalone kernel at few
-  // registers and many rows in flight per SM: faster than batches of 8.)
+  // unnormalised acc.  Sources go in batches whose loads are all in flight
+  // together; the running state is rescaled between batches, so the
+  // batch size is part of the result's rounding.  It follows the call's G
+  // (2 sources per batch when G >= 2, where the standalone kernel takes two
+  // rows per warp, else 4), never the rows per warp: every kernel that
+  // merges a call's rows then gets the same bits.  kB sizes the arrays; a
+  // slot past kb holds the empty state (-inf, 0), which adds exact zeros.
+  // (Small batches keep the standalone kernel at few registers and many
+  // rows in flight per SM: faster than batches of 8.)
   constexpr int kB = R >= 2 ? 2 : 4;
+  const int kb = p.g >= 2 ? 2 : kB;
   float m[R], den[R];
   float4 acc[R];
   int64_t row_off[R];
@@ -105,7 +110,7 @@ __device__ __forceinline__ void contract_rows(const CP& p, int req, int unit, in
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int k = 0; k < kB; ++k) {
-      const bool in = r < nr && k < n_pref;
+      const bool in = r < nr && k < kb && k < n_pref;
       const int64_t slot = base + k;
       ls[r][k] = in ? ld_cg(p.prefix_lse + slot * p.prefix_stride_lse + row_off[r]) : neg_inf();
       xs[r][k] = in ? ld_cg4(p.prefix_o + slot * p.prefix_stride_o + row_off[r] * D + lane * 4)
@@ -137,13 +142,13 @@ __device__ __forceinline__ void contract_rows(const CP& p, int req, int unit, in
       if (suf_kind == 1) return p.suffix_o + row_off[r] * D;
       return p.part_o + ((int64_t)(suf_begin + i - n_pref) * p.hq + (row_off[r] - (int64_t)req * p.hq)) * D;
     };
-    for (int i0 = 0; i0 < n_src; i0 += kB) {
+    for (int i0 = 0; i0 < n_src; i0 += kb) {
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int k = 0; k < kB; ++k) {
-          if (preloaded && k < n_pref) continue;  // loaded before the plan's words
-          const bool in = r < nr && i0 + k < n_src;
+          if (preloaded && k < kb && k < n_pref) continue;  // loaded before the plan's words
+          const bool in = r < nr && k < kb && i0 + k < n_src;
           ls[r][k] = in ? ld_cg(src_lse(i0 + k, r)) : neg_inf();
           xs[r][k] = in ? ld_cg4(src_o(i0 + k, r) + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
         }

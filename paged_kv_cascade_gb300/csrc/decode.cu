@@ -53,7 +53,8 @@ int launch_paged_decode_simt(const DecodeParams& p, int grid_x, int dtype, void*
                             (uint64_t)(p.num_pages > 0 ? p.num_pages : 1)};
   const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)D * 2 * p.hkv, (uint64_t)D * 2 * p.hkv * p.page_size};
   const uint32_t box[4] = {(uint32_t)D, (uint32_t)hg, (uint32_t)sl, 1u};
-  alignas(64) CUtensorMap mk, mv, mpk, mpv;
+  alignas(64) CUtensorMap mk, mv;
+  alignas(64) PrefixMaps pm;
   if (!encode_tiled_map(&mk, p.k_cache, dtype, 4, dims, strides, box, false) ||
       !encode_tiled_map(&mv, p.v_cache, dtype, 4, dims, strides, box, false))
     return -1;
@@ -61,16 +62,22 @@ int launch_paged_decode_simt(const DecodeParams& p, int grid_x, int dtype, void*
     // the contiguous prefix tensors [prefix_pages * page_size, Hkv, 128] in the same page view
     const uint64_t pdims[4] = {(uint64_t)D, (uint64_t)p.hkv, (uint64_t)p.page_size,
                                (uint64_t)(p.prefix_pages > 0 ? p.prefix_pages : 1)};
-    if (!encode_tiled_map(&mpk, p.prefix_k, dtype, 4, pdims, strides, box, false) ||
-        !encode_tiled_map(&mpv, p.prefix_v, dtype, 4, pdims, strides, box, false))
+    // ... and as tokens, one box per stage: 128 / hg tokens x hg heads
+    const uint64_t tdims[3] = {(uint64_t)D, (uint64_t)p.hkv, (uint64_t)p.prefix_pages * (uint64_t)p.page_size};
+    const uint64_t tstrides[2] = {(uint64_t)D * 2, (uint64_t)D * 2 * p.hkv};
+    const uint32_t tbox[3] = {(uint32_t)D, (uint32_t)hg, (uint32_t)(kStageRows / hg)};
+    if (!encode_tiled_map(&pm.pk, p.prefix_k, dtype, 4, pdims, strides, box, false) ||
+        !encode_tiled_map(&pm.pv, p.prefix_v, dtype, 4, pdims, strides, box, false) ||
+        !encode_tiled_map(&pm.pk3, p.prefix_k, dtype, 3, tdims, tstrides, tbox, false) ||
+        !encode_tiled_map(&pm.pv3, p.prefix_v, dtype, 3, tdims, tstrides, tbox, false))
       return -1;
   } else {
-    mpk = mk;  // not read
-    mpv = mv;
+    pm.pk = pm.pk3 = mk;  // not read
+    pm.pv = pm.pv3 = mv;
   }
   cudaStream_t st = (cudaStream_t)stream;
-  if (p.fuse.enabled) return launch_paged_decode_simt_fused(p, grid_x, dtype, hg, &mk, &mv, &mpk, &mpv, st);
-  return launch_simt_mode<false>(p, grid_x, dtype, hg, mk, mv, mpk, mpv, st);
+  if (p.fuse.enabled) return launch_paged_decode_simt_fused(p, grid_x, dtype, hg, &mk, &mv, &pm, st);
+  return launch_simt_mode<false>(p, grid_x, dtype, hg, mk, mv, pm, st);
 }
 
 // Kernel choice for a 16-bit cache: 0 = automatic, 1 = CUDA-core kernel,

@@ -5,10 +5,10 @@
 namespace pkc {
 
 int launch_paged_decode_simt_fused(const DecodeParams& p, int grid_x, int dtype, int hg, const void* mk,
-                                   const void* mv, const void* mpk, const void* mpv, void* stream) {
+                                   const void* mv, const void* prefix_maps, void* stream) {
   return launch_simt_mode<true>(p, grid_x, dtype, hg, *static_cast<const CUtensorMap*>(mk),
-                                *static_cast<const CUtensorMap*>(mv), *static_cast<const CUtensorMap*>(mpk),
-                                *static_cast<const CUtensorMap*>(mpv), (cudaStream_t)stream);
+                                *static_cast<const CUtensorMap*>(mv), *static_cast<const PrefixMaps*>(prefix_maps),
+                                (cudaStream_t)stream);
 }
 
 }  // namespace pkc

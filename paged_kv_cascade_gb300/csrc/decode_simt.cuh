@@ -56,6 +56,17 @@ constexpr int kMaxSliceRows = 16;          // slots per slice
 
 enum : int { kFirst = 1, kLast = 2, kDone = 4 };
 
+// Small-batch cascade: the contiguous prefix tensors [prefix tokens, Hkv,
+// 128] seen as pages of the cache (pk, pv: one box per page slice, like the
+// cache's maps), and as tokens with one box per stage (pk3, pv3: 128 / HG
+// tokens x HG heads, the stage's rows in its (slot, head) order).  A stage
+// that lies wholly inside the prefix takes one copy per tensor instead of
+// one per page slice: the TMA unit issues 4 KB slices one after another, and
+// a one-head stage of 8 slices took it about 0.9 us.
+struct PrefixMaps {
+  CUtensorMap pk, pv, pk3, pv3;
+};
+
 struct StageHdr {
   int32_t flags, req, slot, n_rows, hg, pad0, pad1, pad2;
   uint32_t mask[kStageRows / 32];  // valid rows (row-major: slot, head slot)
@@ -137,7 +148,7 @@ struct HeadShift {
 template <typename T, int G, int HG, bool kFuse>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                        const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CUtensorMap tm_pv,
+                        const __grid_constant__ PrefixMaps pm,
                         const __grid_constant__ DecodeParams p) {
   using Cfg = DecodeCfg<G, HG>;
   constexpr int kStages = Cfg::kStages;
@@ -203,7 +214,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      if (p.prefix_as_pages) { prefetch_tmap(&tm_pk); prefetch_tmap(&tm_pv); }
+      if (p.prefix_as_pages) { prefetch_tmap(&pm.pk); prefetch_tmap(&pm.pv); prefetch_tmap(&pm.pk3); prefetch_tmap(&pm.pv3); }
     }
     int k = 0;  // stage counter
     bool ok = true;
@@ -266,6 +277,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         uint32_t maskw[kStageRows / 32];
 #pragma unroll
         for (int q = 0; q < kStageRows / 32; ++q) maskw[q] = 0;
+        // A full stage wholly inside the prefix: one stage-sized box per
+        // tensor from the prefix's token view (its rows are the stage's rows
+        // in order; every page of it was checked when the call was set up).
+        const bool whole_prefix = n_sl == slices_per_stage && (sl0 + n_sl - 1) / spp < pre_pages;
+        if (whole_prefix && lane == 0) {
+          const int z = (pre_page0 + sl0 / spp) * ps + (sl0 % spp) * sl;  // its first prefix token
+          mbar_expect_tx(smem_u32(&full[s]), 2 * kStageHalf);
+          tma_load_3d(kst, &pm.pk3, smem_u32(&full[s]), 0, hg * HG, z, pol);
+          tma_load_3d(kst + kStageHalf, &pm.pv3, smem_u32(&full[s]), 0, hg * HG, z, pol);
+        }
         for (int i0 = 0; i0 < n_sl; i0 += 32) {
           const int i = i0 + lane;
           const bool mine = i < n_sl;
@@ -290,11 +311,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
           for (int q = 0; q < kStageRows / 32; ++q) mw[q] = 0;
           if (good) {
-            mbar_expect_tx(smem_u32(&full[s]), 2 * slice_bytes);  // before the copies it covers
-            const CUtensorMap* mk = in_prefix ? &tm_pk : &tm_k;
-            const CUtensorMap* mv = in_prefix ? &tm_pv : &tm_v;
-            tma_load_4d(kst + i * slice_bytes, mk, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
-            tma_load_4d(kst + kStageHalf + i * slice_bytes, mv, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
+            if (!whole_prefix) {
+              mbar_expect_tx(smem_u32(&full[s]), 2 * slice_bytes);  // before the copies it covers
+              const CUtensorMap* mk = in_prefix ? &pm.pk : &tm_k;
+              const CUtensorMap* mv = in_prefix ? &pm.pv : &tm_v;
+              tma_load_4d(kst + i * slice_bytes, mk, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
+              tma_load_4d(kst + kStageHalf + i * slice_bytes, mv, smem_u32(&full[s]), 0, hg * HG, slot0, pid, pol);
+            }
             // valid rows: the HG heads of each slot inside the page and inside [kb, ke)
             const int tok0 = page_idx * ps + slot0;
             mask_range(mw, (i * sl + max(kb - tok0, 0)) * HG, (i * sl + min(min(ke - tok0, sl), ps - slot0)) * HG);
@@ -586,7 +609,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
 template <typename T, int G, int HG, bool kFuse>
 int launch_decode_g(const DecodeParams& p, int grid_x, const CUtensorMap& mk, const CUtensorMap& mv,
-                    const CUtensorMap& mpk, const CUtensorMap& mpv, cudaStream_t st) {
+                    const PrefixMaps& pm, cudaStream_t st) {
   constexpr int smem = decode_smem_bytes<G, HG>();
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
@@ -598,39 +621,39 @@ int launch_decode_g(const DecodeParams& p, int grid_x, const CUtensorMap& mk, co
   // one block per (planned CTA, head group); one per planned CTA when the
   // blocks take their items from the shared queue
   const dim3 grid(grid_x, p.dynamic ? 1 : p.hkv / HG);
-  paged_decode_kernel<T, G, HG, kFuse><<<grid, kDecodeThreads, smem, st>>>(mk, mv, mpk, mpv, p);
+  paged_decode_kernel<T, G, HG, kFuse><<<grid, kDecodeThreads, smem, st>>>(mk, mv, pm, p);
   return (int)cudaGetLastError();
 }
 
 template <typename T, int HG, bool kFuse>
 int launch_decode_hg(const DecodeParams& p, int grid_x, const CUtensorMap& mk, const CUtensorMap& mv,
-                     const CUtensorMap& mpk, const CUtensorMap& mpv, cudaStream_t st) {
+                     const PrefixMaps& pm, cudaStream_t st) {
   switch (p.hq / p.hkv) {
-    case 1: return launch_decode_g<T, 1, HG, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
-    case 2: return launch_decode_g<T, 2, HG, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
-    case 4: return launch_decode_g<T, 4, HG, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
-    case 8: return launch_decode_g<T, 8, HG, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
+    case 1: return launch_decode_g<T, 1, HG, kFuse>(p, grid_x, mk, mv, pm, st);
+    case 2: return launch_decode_g<T, 2, HG, kFuse>(p, grid_x, mk, mv, pm, st);
+    case 4: return launch_decode_g<T, 4, HG, kFuse>(p, grid_x, mk, mv, pm, st);
+    case 8: return launch_decode_g<T, 8, HG, kFuse>(p, grid_x, mk, mv, pm, st);
     default: return (int)cudaErrorInvalidValue;
   }
 }
 
 template <typename T, bool kFuse>
 int launch_decode_t(const DecodeParams& p, int grid_x, int hg, const CUtensorMap& mk, const CUtensorMap& mv,
-                    const CUtensorMap& mpk, const CUtensorMap& mpv, cudaStream_t st) {
+                    const PrefixMaps& pm, cudaStream_t st) {
   switch (hg) {
-    case 8: return launch_decode_hg<T, 8, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
-    case 4: return launch_decode_hg<T, 4, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
-    case 2: return launch_decode_hg<T, 2, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
-    default: return launch_decode_hg<T, 1, kFuse>(p, grid_x, mk, mv, mpk, mpv, st);
+    case 8: return launch_decode_hg<T, 8, kFuse>(p, grid_x, mk, mv, pm, st);
+    case 4: return launch_decode_hg<T, 4, kFuse>(p, grid_x, mk, mv, pm, st);
+    case 2: return launch_decode_hg<T, 2, kFuse>(p, grid_x, mk, mv, pm, st);
+    default: return launch_decode_hg<T, 1, kFuse>(p, grid_x, mk, mv, pm, st);
   }
 }
 
 // The kernels of one contraction mode (kFuse) for a 16-bit cache.
 template <bool kFuse>
 int launch_simt_mode(const DecodeParams& p, int grid_x, int dtype, int hg, const CUtensorMap& mk,
-                     const CUtensorMap& mv, const CUtensorMap& mpk, const CUtensorMap& mpv, cudaStream_t st) {
-  return dtype == PKC_F16 ? launch_decode_t<__half, kFuse>(p, grid_x, hg, mk, mv, mpk, mpv, st)
-                          : launch_decode_t<__nv_bfloat16, kFuse>(p, grid_x, hg, mk, mv, mpk, mpv, st);
+                     const CUtensorMap& mv, const PrefixMaps& pm, cudaStream_t st) {
+  return dtype == PKC_F16 ? launch_decode_t<__half, kFuse>(p, grid_x, hg, mk, mv, pm, st)
+                          : launch_decode_t<__nv_bfloat16, kFuse>(p, grid_x, hg, mk, mv, pm, st);
 }
 
 }  // namespace

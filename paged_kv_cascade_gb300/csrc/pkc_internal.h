@@ -246,7 +246,7 @@ int launch_paged_decode_mma(const DecodeParams& p, int grid_x, int kv_kind,
 int launch_paged_decode_mma_fused(const DecodeParams& p, int grid_x, int kv_kind, int hg,
                                   const void* mk, const void* mv, void* stream);
 int launch_paged_decode_simt_fused(const DecodeParams& p, int grid_x, int dtype, int hg,
-                                   const void* mk, const void* mv, const void* mpk, const void* mpv,
+                                   const void* mk, const void* mv, const void* prefix_maps,
                                    void* stream);
 // KV heads per block of the tensor-core kernel, or 0 if it cannot take
 // this head count and page size.

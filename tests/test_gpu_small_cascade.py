@@ -37,6 +37,13 @@ SMALL = [
     (32, 8, "bf16", [160, 0, 48], [2, 1, 3], [5, 0, 300, 16, 17, 2, 9], 16),  # G = 4, an empty prefix, one request outside
     (16, 2, "f16", [64, 96], [1, 2], [100, 7, 64], 32),             # G = 8, page size 32
     (8, 4, "bf16", [16], [5], [1, 15, 16, 31, 0], 16),              # G = 2
+    # stages wholly inside a prefix (one box per tensor) next to stages that
+    # mix prefix and suffix pages:
+    (16, 8, "f16", [320], [4], [10, 40, 0, 3], 32),                 # page size 32: two slices per page
+    (32, 32, "bf16", [208, 96], [12, 12],                           # 24 requests: 4 KV heads per block
+     [3, 50, 0, 17, 1, 64, 9, 33, 2, 80, 5, 16, 7, 0, 41, 12, 1, 30, 6, 72, 15, 8, 3, 20], 16),
+    (32, 32, "f16", [304, 64, 160], [16, 16, 16],                   # 48 requests: 8 KV heads per block
+     [int(x) for x in np.random.default_rng(7).integers(0, 90, 48)], 16),
 ]
 
 

@@ -408,13 +408,12 @@ int pkc_prefix_attention_state(
  * num_qo_heads] float32, equal to attention over prefix u suffix.
  * Arguments as in the two calls above; cache_seqlens counts suffix tokens
  * only; plan_host as in pkc_paged_decode_state.
- * The prefix and suffix stages do not depend on each other: the prefix
- * kernel runs on a library-owned side stream (one per host thread and
- * device) forked from `stream` after the work already queued there, next to
- * the suffix decode, and joined back before the contraction.  To the caller
- * the call stays ordered on `stream`, under CUDA-graph capture too (the
- * side stream is created on the first call made outside a capture; a
- * captured first call runs the stages one after the other).
+ * The prefix and suffix stages do not depend on each other: the three
+ * kernels go on `stream` as a chain of programmatic dependents, so that the
+ * suffix decode runs next to the prefix kernel and each waits in hardware
+ * for the grid before it (the decode only before its blocks exit).  The call
+ * stays ordered on `stream` after the work already queued there, under
+ * CUDA-graph capture too; the library creates no stream.
  */
 int pkc_cascade_decode(
     const void* q, const void* k_prefix, const void* v_prefix,
@@ -510,7 +509,8 @@ int pkc_cascade_decode_paged_prefix(
  * TMA descriptors), then events[1], events[2], events[3]
  * after the prefix, suffix-decode and contraction kernels; the hook is then
  * cleared.  A timed call runs its stages one after the other on `stream`
- * (no side stream), so that each pair of events brackets one kernel.
+ * (the decode does not overlap the prefix), so that each pair of events
+ * brackets one kernel.
  * events: n_events >= 4 cudaEvent_t handles created by the caller; NULL
  * clears the hook.
  */
@@ -593,7 +593,7 @@ int pkc_set_contraction(int mode);
  *   - n = 0 (the default): automatic.
  *
  * Automatic mode.  The prefix takes every SM, except in a cascade call with
- * a plan.  There the prefix runs on a side stream next to the suffix decode,
+ * a plan.  There the prefix runs next to the suffix decode,
  * which is bound by HBM and saturates it on about 100 SMs.  When every
  * prefix group's K/V tiles are read by two or more 128-row query tiles, the
  * prefix is bound by the tensor pipe rather than HBM.  It then gets SMs of

@@ -30,37 +30,6 @@ int set_error(int code, const char* fmt, ...) {
   return code;
 }
 
-// A side stream per (host thread, device) on which the cascade runs its
-// prefix stage next to the suffix decode, with the two events that fork it
-// from and join it to the caller's stream.  Created on first use outside a
-// stream capture; while one is being captured before that, the stages run
-// one after the other on the caller's stream.
-struct SideStream {
-  cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-
-static SideStream* side_stream(cudaStream_t caller) {
-  static thread_local SideStream per_dev[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  SideStream& s = per_dev[dev];
-  if (s.side) return &s;
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
-  if (cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking) != cudaSuccess) {
-    s.side = nullptr;
-    return nullptr;
-  }
-  if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) {
-    cudaStreamDestroy(s.side);
-    s.side = nullptr;
-    return nullptr;
-  }
-  return &s;
-}
-
 int cuda_error(int e, const char* what) {
   if (e == -1) return set_error(PKC_ERR_CUDA, "%s: TMA tensor map encoding failed", what);
   return set_error(PKC_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)e));
@@ -898,12 +867,16 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   auto mark = [&](int i) {
     if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
   };
-  // The prefix and suffix stages are independent: unless per-stage timing
-  // is asked for, the prefix runs on a side stream forked from the caller's
-  // stream, next to the decode, and the contraction waits for both.  The
-  // decode is launched first so that its blocks take the SMs first; the
-  // prefix blocks fill the SMs left free and those the decode releases.
-  SideStream* side = timed ? nullptr : side_stream((cudaStream_t)stream);
+  // The prefix and suffix stages are independent.  Unless per-stage timing
+  // is asked for, all three launches go on the caller's stream as a chain of
+  // programmatic dependents: the decode starts as soon as every prefix block
+  // has started (on the SMs the prefix leaves, or those it releases) and
+  // waits for the prefix grid only before its blocks exit; the contraction
+  // starts once every decode block has, and waits for the decode grid (and
+  // so the prefix's) before it reads either stage's states.  (With the
+  // prefix on a side stream joined before the contraction, the join
+  // serialised the contraction behind the decode: it started 2.5-3 us after
+  // the decode's last block.)  Timed, the stages run one after the other.
   auto run_prefix = [&](void* st, cudaEvent_t start) -> int {
     const int r = launch_prefix(S.pp, q, k_prefix, v_prefix, S.tokens, dtype, st, start);
     if (r == -1) return set_error(PKC_ERR_CUDA, "prefix: could not build TMA tensor maps");
@@ -925,7 +898,7 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   cp.o = o; cp.lse = lse; cp.out_dtype = o_dtype; cp.status = status;
   // Fused: both stages' kernels count the sources they write, and the
   // writer of a (request, KV head) pair's last source merges the pair; the
-  // counters are zeroed first, on the caller's stream before the fork.
+  // counters are zeroed first, on the caller's stream before the prefix.
   const bool fused = g_fused_contraction.load() != 0 && n_prefix <= PKC_FUSE_MAX_PREFIX;
   FuseParams fuse;
   std::memset(&fuse, 0, sizeof(fuse));
@@ -937,15 +910,9 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
     S.pp.fuse = fuse;
   }
   int e = 0;
-  if (side) {
-    e = (int)cudaEventRecord(side->fork, (cudaStream_t)stream);
-    if (!e) e = (int)cudaStreamWaitEvent(side->side, side->fork, 0);
-    if (e) return cuda_error(e, "cascade: stream fork");
-  } else {
-    // 1. shared prefix: multi-query states on the tensor cores (stage event
-    // 0 is recorded right before the kernel, after its tensor maps are built)
-    if (int rc = run_prefix(stream, ev[0])) return rc;
-  }
+  // 1. shared prefix: multi-query states on the tensor cores (stage event 0
+  // is recorded right before the kernel, after its tensor maps are built)
+  if (int rc = run_prefix(stream, ev[0])) return rc;
   mark(1);
   // 2. unique suffixes: paged decode states (unsplit -> suffix states)
   DecodeParams dp;
@@ -963,29 +930,15 @@ int cascade_impl(const void* q, const void* k_prefix, const void* v_prefix, cons
   dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   dp.status = status;
   dp.fuse = fuse;
+  // the prefix's programmatic dependent, when this call launched a prefix grid
+  dp.after_prefix = !timed && S.pp.n_blocks > 0 && S.pp.total_tiles > 0 ? 1 : 0;
   g_last_prefix_blocks = S.pp.n_blocks;
   g_last_decode_blocks = decode_blocks;
   e = launch_paged_decode(dp, decode_blocks, dtype, dtype, stream);
-  if (e) {
-    if (side) {  // the side stream has already forked: join it before returning
-      cudaEventRecord(side->join, side->side);
-      cudaStreamWaitEvent((cudaStream_t)stream, side->join, 0);
-    }
-    return cuda_error(e, "paged decode launch");
-  }
-  if (side) {
-    // 1. shared prefix, on the side stream; the caller's stream waits for it
-    if (int rc = run_prefix(side->side, nullptr)) {
-      cudaEventRecord(side->join, side->side);  // keep the fork joined
-      cudaStreamWaitEvent((cudaStream_t)stream, side->join, 0);
-      return rc;
-    }
-    e = (int)cudaEventRecord(side->join, side->side);
-    if (!e) e = (int)cudaStreamWaitEvent((cudaStream_t)stream, side->join, 0);
-    if (e) return cuda_error(e, "cascade: stream join");
-  }
+  if (e) return cuda_error(e, "paged decode launch");
   mark(2);
   if (!fused) {
+    cp.prefix_after_wait = dp.after_prefix;  // prefix pieces only after the contraction's wait
     e = launch_contract(cp, batch, stream, !timed);
     if (e) return cuda_error(e, "contraction launch");
   }

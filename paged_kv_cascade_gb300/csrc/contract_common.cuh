@@ -104,6 +104,16 @@ __device__ __forceinline__ void contract_rows(const CP& p, int req, int unit, in
   // one memory round trip.
   int j = next_group(-1), base = 0;
   int n_pref = j >= 0 ? group_pieces(p, j, req, h0, base) : 0;
+  // Launched next to a prefix stage that may still run (a cascade's
+  // contraction whose decode followed the prefix as its programmatic
+  // dependent), the prefix pieces are ready only once the wait returns.
+  bool waited = false;
+  if constexpr (kWaitGrid) {
+    if (p.prefix_after_wait) {
+      grid_wait_prerequisites();
+      waited = true;
+    }
+  }
   float ls[R][kB];
   float4 xs[R][kB];
 #pragma unroll
@@ -125,7 +135,9 @@ __device__ __forceinline__ void contract_rows(const CP& p, int req, int unit, in
   } else if (p.suffix_o) {
     suf_kind = 1; suf_n = 1;
   }
-  if constexpr (kWaitGrid) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if constexpr (kWaitGrid) {
+    if (!waited) grid_wait_prerequisites();
+  }
   bool preloaded = true;  // ls / xs hold the first batch's prefix pieces
   for (;;) {
     const int jn = j >= 0 ? next_group(j) : -1;

@@ -129,10 +129,12 @@ int launch_paged_decode(const DecodeParams& p_in, int grid_x, int dtype, int kv_
 // start once every
 // decode block has signalled (griddepcontrol.launch_dependents, at each
 // decode block's start): its blocks take the SM room the decode leaves,
-// load the prefix pieces and plan words, and wait at griddepcontrol.wait
+// load the plan words (and, unless the decode itself follows the prefix
+// kernel as a dependent, the prefix pieces), and wait at griddepcontrol.wait
 // for the decode grid to finish before reading the suffix states.  The
-// dependency on everything else before it on the stream (the prefix stage
-// joined from its side stream, the plan upload) stays complete.
+// dependency on everything else before the decode on the stream (the plan
+// upload, and the prefix grid, which every decode block waits for before it
+// exits) stays complete.
 static std::atomic<int> g_contract_pdl{1};
 int set_contract_pdl(int on) {
   g_contract_pdl.store(on ? 1 : 0);

@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t hw = pl ? pl[lane] : 0;
   if (pl && !device_plan_header_ok(hw, p.plan_words, p.batch)) {  // uniform: before any barrier
     if (threadIdx.x == 0) report(p.status, PKC_ERR_PLAN);
+    grid_wait_prerequisites();  // as at every exit of this kernel
     return;
   }
   int w_begin = 0, w_end = 1;
@@ -309,6 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(smem_u32(&full[kk % kStages]), (kk / kStages) & 1, &no_abort, p.status);
     }
     if (dyn) queue.finish(lane);
+    // A cascade's decode runs next to the prefix stage (launched as its
+    // programmatic dependent): no block of this grid finishes before that
+    // grid has, so the contraction that waits for this grid sees the prefix
+    // pieces too.  (At once when the decode was launched normally.)
+    grid_wait_prerequisites();
     return;
   }
 
@@ -594,6 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  grid_wait_prerequisites();  // see the producer's exit
 }
 
 template <int KV, int G, int HG, bool kFuse>
@@ -607,6 +614,19 @@ int launch_mma_g(const DecodeParams& p, int grid_x, const CUtensorMap& mk, const
   });
   if (attr != cudaSuccess) return (int)attr;
   const dim3 grid(grid_x, p.dynamic ? 1 : p.hkv / HG);
+  if (p.after_prefix) {  // next to the prefix stage: see the kernel's exits
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&cfg, paged_decode_mma_kernel<KV, G, HG, kFuse>, mk, mv, p);
+  }
   paged_decode_mma_kernel<KV, G, HG, kFuse><<<grid, kThreads, smem, st>>>(mk, mv, p);
   return (int)cudaGetLastError();
 }

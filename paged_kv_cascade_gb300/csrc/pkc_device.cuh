@@ -263,6 +263,18 @@ __device__ __forceinline__ bool bar_and_sync(bool v, int count) {
   return out != 0;
 }
 
+// ---- programmatic dependent launch ----
+// Let the grid launched after this one as its programmatic dependent start
+// (its blocks then wait at their own griddepcontrol.wait).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one depends on (programmatically) have completed
+// and their writes are visible; returns at once if there are none.
+__device__ __forceinline__ void grid_wait_prerequisites() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- fences ----
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -91,6 +91,7 @@ struct DecodeParams {
   float scale_log2;       // sm_scale * log2(e)
   const int32_t* plan;    // device copy of the plan, or nullptr
   int32_t plan_words;     // the host plan's total words (the device copy must match)
+  int after_prefix;       // launched as the prefix kernel's programmatic dependent (cascade)
   void* o_direct;         // unsplit outputs: [B, Hq, D] (dtype or f32)
   float* lse_direct;      // [B, Hq]
   int direct_f32;         // 1: o_direct is float32 (suffix states)
@@ -150,6 +151,7 @@ struct ContractParams {
   int mode;
   const int32_t* plan;      // device plan or nullptr
   int32_t plan_words;       // the host plan's total words (the device copy must match)
+  int prefix_after_wait;    // the prefix stage may still run until griddepcontrol.wait returns
   // Word offsets of the plan arrays, copied from the host plan (they depend
   // only on batch and CTA count) so the kernel's first loads are the arrays.
   int32_t off_unit_list, off_unit_req, off_unit_n_chunks, off_unit_partial_begin;

@@ -123,6 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) report(p.status, PKC_ERR_UNSUPPORTED);
     return;
   }
+  // A decode launched after this grid as its programmatic dependent may start
+  // now, next to it (it reads nothing this grid writes, and waits for this
+  // grid before it exits).
+  grid_launch_dependents();
   if (kFuse && p.fuse.plan && !device_plan_ok(p.fuse.plan, p.fuse.plan_words, p.fuse.batch)) {
     if (threadIdx.x == 0) report(p.status, PKC_ERR_PLAN);  // the fused merges would follow its offsets
     return;

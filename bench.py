@@ -539,11 +539,35 @@ def measure_cascade(ctx, name, stage_steps=10):
                    stages_us_serial=stages, stage_split=split, num_ctas=C or None,
                    prefix_tokens=int(p["prefix_kv_indptr"][-1]),
                    suffix_tokens=int(p["cache_seqlens"].sum()))
+    if not C:  # an unplanned step is one launch: also time it among others in one graph
+        entry["in_multi_call_graph"] = multi_call_graph_time(ctx, run, gs.ws[0], 20)
     entry["prefix_stage_gbs_serial"] = _gbs(int(p["prefix_kv_indptr"][-1]) * kvb,
                                             stages["prefix_state"] / 1e3)
     entry["decode_stage_gbs_serial"] = _gbs(int(p["cache_seqlens"].sum()) * kvb,
                                             stages["paged_decode"] / 1e3)
     return entry, (cfg, p, d, gs)
+
+
+def multi_call_graph_time(ctx, run, ws, calls):
+    """µs per call with `calls` unplanned calls captured in one CUDA graph,
+    the way a model's per-layer attention calls are captured into one
+    decode-step graph: the kernel with its launch gap inside a graph,
+    without the cost of launching a graph per call.  Same inputs and outputs
+    every call."""
+    torch = ctx.torch
+    st = torch.cuda.Stream(ctx.device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        run(ws, None, st)
+        st.synchronize()
+        with torch.cuda.graph(g, stream=st):
+            for _ in range(calls):
+                run(ws, None, st)
+        ms, n, clocks = time_loop(ctx, g.replay, st, max(10, ctx.steps // calls))
+    if ctx.pkc.device_status(ws) != 0:
+        raise RuntimeError("multi-call graph: device status not OK")
+    return {"calls_per_graph": calls, "us_per_call": 1e3 * ms / calls, "graph_replays": n,
+            "clocks": clocks}
 
 
 def noncascade_pool(torch, d, p):

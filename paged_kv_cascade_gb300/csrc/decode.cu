@@ -3,7 +3,6 @@
 // decode_fused.cu), the standalone contraction kernel, and the dispatch
 // between the decode kernels.
 #include <atomic>
-#include <cstring>
 
 #include "decode_simt.cuh"
 
@@ -150,18 +149,7 @@ int launch_contract_r(const ContractParams& p, int n_rows, cudaStream_t st, bool
     contract_kernel<R, kMinBlocks><<<blocks, 256, 0, st>>>(p);
     return (int)cudaGetLastError();
   }
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(blocks);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return (int)cudaLaunchKernelEx(&cfg, contract_kernel<R, kMinBlocks>, p);
+  return launch_programmatic(contract_kernel<R, kMinBlocks>, dim3(blocks), dim3(256), 0, st, p);
 }
 
 int launch_contract(const ContractParams& p, int n_rows, void* stream, bool after_decode) {

@@ -614,19 +614,8 @@ int launch_mma_g(const DecodeParams& p, int grid_x, const CUtensorMap& mk, const
   });
   if (attr != cudaSuccess) return (int)attr;
   const dim3 grid(grid_x, p.dynamic ? 1 : p.hkv / HG);
-  if (p.after_prefix) {  // next to the prefix stage: see the kernel's exits
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return (int)cudaLaunchKernelEx(&cfg, paged_decode_mma_kernel<KV, G, HG, kFuse>, mk, mv, p);
-  }
+  if (p.after_prefix)  // next to the prefix stage: see the kernel's exits
+    return launch_programmatic(paged_decode_mma_kernel<KV, G, HG, kFuse>, grid, dim3(kThreads), smem, st, mk, mv, p);
   paged_decode_mma_kernel<KV, G, HG, kFuse><<<grid, kThreads, smem, st>>>(mk, mv, p);
   return (int)cudaGetLastError();
 }

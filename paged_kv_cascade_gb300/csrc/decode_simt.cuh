@@ -628,19 +628,9 @@ int launch_decode_g(const DecodeParams& p, int grid_x, const CUtensorMap& mk, co
   // one block per (planned CTA, head group); one per planned CTA when the
   // blocks take their items from the shared queue
   const dim3 grid(grid_x, p.dynamic ? 1 : p.hkv / HG);
-  if (p.after_prefix) {  // next to the prefix stage: see the kernel's exits
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kDecodeThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return (int)cudaLaunchKernelEx(&cfg, paged_decode_kernel<T, G, HG, kFuse>, mk, mv, pm, p);
-  }
+  if (p.after_prefix)  // next to the prefix stage: see the kernel's exits
+    return launch_programmatic(paged_decode_kernel<T, G, HG, kFuse>, grid, dim3(kDecodeThreads), smem, st, mk, mv,
+                               pm, p);
   paged_decode_kernel<T, G, HG, kFuse><<<grid, kDecodeThreads, smem, st>>>(mk, mv, pm, p);
   return (int)cudaGetLastError();
 }

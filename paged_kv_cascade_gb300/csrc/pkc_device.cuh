@@ -274,6 +274,25 @@ __device__ __forceinline__ void grid_launch_dependents() {
 __device__ __forceinline__ void grid_wait_prerequisites() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+// Host side: launch `kernel` as the programmatic dependent of the grid
+// launched before it on `st`.  Its blocks may be scheduled once every block
+// of that grid has executed griddepcontrol.launch_dependents (or exited),
+// and each waits for that grid at its own griddepcontrol.wait.
+template <class... KArgs, class... Args>
+inline int launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem, cudaStream_t st,
+                               Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = la;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 // ---- fences ----
 __device__ __forceinline__ void fence_proxy_async_smem() {

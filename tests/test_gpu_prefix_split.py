@@ -7,8 +7,9 @@ quarter of them next to a dynamically scheduled decode on the rest, or the
 SMs a static plan leaves free; a caller may also cap its blocks.  The block
 count changes how the flattened KV tiles are cut into pieces, so the states
 must match the oracle for every count, and a call must give the same bits
-timed (stage events, stages in order), untimed (side stream) and replayed
-from a CUDA graph."""
+timed (stage events, stages in order), untimed (the decode launched as the
+prefix kernel's programmatic dependent, next to it) and replayed from a CUDA
+graph."""
 import numpy as np
 import pytest
 import torch
@@ -90,7 +91,7 @@ def test_automatic_split_same_bits_timed_untimed_and_graph(gqa):
     timed = (o.clone(), lse.clone())
     assert all(ev[i].elapsed_time(ev[i + 1]) > 0 for i in range(3))
     o.zero_()
-    _cascade(p, d, buf, ws, o, lse)  # prefix on a side stream next to the decode
+    _cascade(p, d, buf, ws, o, lse)  # the decode next to the prefix (launch chain)
     torch.cuda.synchronize()
     assert torch.equal(o, timed[0]) and torch.equal(lse, timed[1])
     s = torch.cuda.Stream()
